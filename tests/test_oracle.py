@@ -1,0 +1,69 @@
+"""The oracle against its pins (CPU only)."""
+import numpy as np
+import pytest
+
+import oracle_pins as P
+import torch_gpt2
+from stream_decode_gb300 import synth
+
+
+@pytest.mark.parametrize("check", P.FAST_CHECKS, ids=lambda c: c.__name__)
+def test_pin(oracle, check):
+    check(oracle)
+
+
+def test_forward_vs_torch_plain(oracle):
+    P.check_forward_vs_torch(oracle, variant="plain")
+
+
+def test_forward_vs_torch_small_shape(oracle):
+    P.check_forward_vs_torch(oracle, shape=P.SMALL, seed=P.SEED_SMALL, variant="rich", n=16)
+
+
+def test_124m_forward_vs_torch(oracle, w124m_rich):
+    """Full GPT-2 124M shapes: 4 positions against the float64 restatement."""
+    s = synth.GPT2_124M
+    m = oracle.model(s, w124m_rich)
+    toks = synth.tokens(s.vocab, 4)
+    logits, _, cache = m.session(list(toks), 4)
+    ref, K, V = torch_gpt2.forward(s, w124m_rich, toks)
+    assert np.abs(logits - ref).max() < 1e-4
+    c = cache.reshape(4, s.n_layer, 2, s.d_model)
+    assert np.abs(c[:, :, 0, :].transpose(1, 0, 2) - K).max() < 1e-4
+    assert np.abs(c[:, :, 1, :].transpose(1, 0, 2) - V).max() < 1e-4
+    m.close()
+
+
+def test_124m_validation(oracle, w124m):
+    s = synth.GPT2_124M
+    row = oracle.cache_words_per_position(s)
+    assert row * 4 == 12 * 1536 * 4
+    st, lg, co = oracle.cached_step(s, w124m, np.zeros(row, np.float32), s.vocab, 1)
+    assert st == "token" and lg.size == 0 and co.size == 0
+    st, lg, co = oracle.cached_step(s, w124m, np.zeros(0, np.float32), 1, 128)
+    assert st == "position"
+    st, lg = oracle.infer(s, w124m, np.zeros(129, "<u4").tobytes())
+    assert st == "tokens_len"
+
+
+def test_long_context_config_accepts_position_1023(oracle):
+    """max_pos = 1024 accepts every stored position row (tiny analogue:
+    max_pos = n_pos = 16 accepts position 15 and rejects 16)."""
+    s = synth.GPT2_TINY
+    w = synth.checkpoint(s, synth.SEED_TINY)
+    row = oracle.cache_words_per_position(s)
+    assert oracle.cached_step(s, w, np.zeros(15 * row, np.float32), 1, 15)[0] == "ok"
+    assert oracle.cached_step(s, w, np.zeros(16 * row, np.float32), 1, 16)[0] == "position"
+
+
+def test_int8_session_runs(oracle):
+    s = synth.GPT2_TINY
+    w = synth.checkpoint(s, synth.SEED_TINY, "rich")
+    mq = oracle.model(s, w, quant=1)
+    toks = synth.tokens(s.vocab, 8)
+    lq, ch, cache = mq.session(list(toks) + [-1] * 8, 16)
+    assert np.isfinite(lq).all() and cache.size == 16 * oracle.cache_words_per_position(s)
+    # cached and full-prefix agree bit for bit in the int8 model too
+    full = np.concatenate([toks, ch[7:15]]).astype(np.uint32)
+    st, li = mq.infer(full)
+    assert st == "ok" and np.array_equal(li.view(np.uint32), lq[-1].view(np.uint32))

@@ -1,0 +1,72 @@
+"""Plant plausible mistakes in copies of the oracle and require that the pins
+catch every one.  The mistakes are planted in a temporary copy of the C
+source, on the CPU; the oracle in the repository is never modified."""
+import os
+import tempfile
+
+import pytest
+
+import oracle_pins as P
+from oracle import Oracle, build, _SRC
+
+# (name, exact text in gpt2_ref.c, replacement)
+MUTANTS = [
+    ("drop_qkv_bias", "project(m, 4 * l + 0, a, b->w_qkv, b->b_qkv, d, 3 * d, qkv);",
+     "project(m, 4 * l + 0, a, b->w_qkv, NULL, d, 3 * d, qkv);"),
+    ("unbiased_variance", "float var = sq / (float)n;", "float var = sq / (float)(n - 1);"),
+    ("wrong_eps", "#define REF_LN_EPS 1e-5f", "#define REF_LN_EPS 1e-3f"),
+    ("ln_gain_dropped", "y[i] = (x[i] - mean) / den * g[i] + b[i];", "y[i] = (x[i] - mean) / den + b[i];"),
+    ("score_scale_1_over_dh", "float scale_den = sqrtf((float)dh);", "float scale_den = (float)dh;"),
+    ("head_slice_offset", "const float *k0 = cache + (size_t)l * 2 * d + h * dh;",
+     "const float *k0 = cache + (size_t)l * 2 * d + h;"),
+    ("keys_from_values", "mine[i] = qkv[d + i];", "mine[i] = qkv[2 * d + i];"),
+    ("gelu_constant", "0.044715f", "0.44715f"),
+    ("no_position_embedding", "x[i] = m->wte[(size_t)token * d + i] + m->wpe[(size_t)pos * d + i];",
+     "x[i] = m->wte[(size_t)token * d + i];"),
+    ("transposed_projection", "y[j] += xi * row[j];", "y[j] += xi * w[(size_t)j * n_in + i];"),
+    ("mlp_residual_dropped", "project(m, 4 * l + 3, u, b->w_p, b->b_p, f, d, y);\n        for (int i = 0; i < d; i++) x[i] = x[i] + y[i];",
+     "project(m, 4 * l + 3, u, b->w_p, b->b_p, f, d, y);\n        for (int i = 0; i < d; i++) x[i] = y[i];"),
+    ("softmax_no_normalise", "for (int j = 0; j < n_src; j++) e[j] = e[j] / z;", ""),
+    ("argmax_last_tie", "if (x[i] > x[best]) best = i;", "if (x[i] >= x[best]) best = i;"),
+    ("argmax_accepts_inf", "if (!isfinite(x[i])) {", "if (isnan(x[i])) {"),
+    ("round_half_away", "if (s != 0.0f) r = rintf(x[i] / s);", "if (s != 0.0f) r = roundf(x[i] / s);"),
+    ("no_saturation", "if (r > 127.0f) r = 127.0f;", "if (r > 128.0f) r = 127.0f;"),
+    ("scale_over_128", "return m / 127.0f;", "return m / 128.0f;"),
+    ("first_group_scale_only", "sum += ((float)acc[g] * xs[g]) * ws[(size_t)j * ng + g];",
+     "sum += ((float)acc[g] * xs[g]) * ws[(size_t)j * ng];"),
+    ("embedding_group0_scale",
+     "float w = (float)e->q[(size_t)token * d + i] * e->s[(size_t)token * ng + i / REF_GROUP];",
+     "float w = (float)e->q[(size_t)token * d + i] * e->s[(size_t)token * ng];"),
+    ("infer_positions_zero", "forward_token(m, work, load_le_u32(tb + 4 * t), (uint32_t)t,",
+     "forward_token(m, work, load_le_u32(tb + 4 * t), (uint32_t)0,"),
+    ("cache_prefix_not_returned", "for (size_t i = 0; i < ((size_t)position + 1) * row; i++) store_le_f32",
+     "for (size_t i = (size_t)position * row; i < ((size_t)position + 1) * row; i++) store_le_f32"),
+    ("position_bound_off_by_one", "if (position >= c->max_pos) return REF_ERR_POSITION;",
+     "if (position > c->max_pos) return REF_ERR_POSITION;"),
+    ("token_bound_off_by_one", "if (token >= c->vocab) return REF_ERR_TOKEN;",
+     "if (token > c->vocab) return REF_ERR_TOKEN;"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(_SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(source, name, old, new):
+    assert source.count(old) == 1, f"mutation site for {name} must be unique"
+    with tempfile.TemporaryDirectory() as td:
+        src = os.path.join(td, "mutant.c")
+        with open(src, "w") as f:
+            f.write(source.replace(old, new))
+        lib = build(src, os.path.join(td, "mutant.so"))
+        o = Oracle(lib)
+        caught = []
+        for check in P.FAST_CHECKS:
+            try:
+                check(o)
+            except (AssertionError, ValueError, RuntimeError) as e:  # noqa: PERF203
+                caught.append(check.__name__)
+        assert caught, f"no pin caught mutant {name}"
