@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Benchmark: GPT-2 124M cachedStep decode tokens/s on one GB300, and the
+achieved HBM bandwidth of the step kernel against the measured peak.
+
+Workload (one bench step): GPT-2 124M shapes, binary32 packed checkpoint with
+N(0, 0.02) weights from a fixed seed (synthetic: no pretrained weights exist
+here); 16 uniform random prompt tokens fill positions 0..15 once; each bench
+step rewinds the session to position 16 and runs 112 greedy cachedStep
+decode steps (positions 16..127) as ONE persistent kernel launch, the next
+token chosen on the device.  The weights (495 MB per token) are larger than
+the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quant f32|int8]
+
+Multi-GPU runs (torchrun) are independent replicas: one session per GPU, no
+data exchange; value = all tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GPT-2 124M cachedStep tokens/s on 1 GB300; achieved HBM GB/s vs peak"
+PROMPT, DECODE = 16, 112
+KV_ROW_BYTES = 12 * 1536 * 4  # one cached position (README cachedStep paragraph)
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def step_bytes(shape, quant: str, p: int) -> int:
+    """Algorithmic HBM bytes of one cachedStep at position p: every weight the
+    step needs once (block matrices, LayerNorm parameters, biases, the tied
+    vocabulary matrix, one position row), the KV cache read at positions
+    0..p-1, this position's KV write and the logits write."""
+    d, F, L, V = shape.d_model, shape.d_ff, shape.n_layer, shape.vocab
+    params = L * (2 * d + 3 * d + d + 2 * d + F + d) + 2 * d + d  # LN, biases, final LN, one wpe row
+    if quant == "f32":
+        mats = L * (d * 3 * d + d * d + d * F + F * d) + V * d
+        weights = 4 * (mats + params)
+    else:
+        rb = lambda K: K + (K // 64) * 4
+        mats = L * (3 * d * rb(d) + d * rb(d) + F * rb(d) + d * rb(F)) + V * rb(d)
+        weights = mats + 4 * params
+    return weights + KV_ROW_BYTES * p + KV_ROW_BYTES + 4 * V
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.rows = []
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                self.rows.append(f)
+
+    def summary(self):
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def oracle_decode_rate(shape, w, toks, quant: int, n_decode: int):
+    """Times the oracle (single-threaded C) on the decode workload: the prompt
+    cache is built untimed, then n_decode teacher-forced steps are timed."""
+    from oracle import Oracle
+    om = Oracle().model(shape, w, quant=quant)
+    _, ch, cache = om.session(list(toks), PROMPT)
+    tok = int(ch[-1])
+    t0 = time.perf_counter()
+    for i in range(n_decode):
+        st, lg, cache = om.cached_step(cache, tok, PROMPT + i)
+        tok = int(np.argmax(lg))
+    dt = time.perf_counter() - t0
+    om.close()
+    return n_decode / dt, dt
+
+
+def reference_arm(args, shape, w, toks):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    quant = 1 if args.quant == "int8" else 0
+    per_step = 2
+    from oracle import Oracle
+    om = Oracle().model(shape, w, quant=quant)
+    _, ch, cache0 = om.session(list(toks), PROMPT)
+    tok0 = int(ch[-1])
+
+    def one_step():
+        cache, tok = cache0, tok0
+        for i in range(per_step):
+            st, lg, cache = om.cached_step(cache, tok, PROMPT + i)
+            tok = int(np.argmax(lg))
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    sample = f"{per_step} teacher-free greedy oracle steps at positions 16..{16 + per_step - 1} per bench step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if quant == 0 else "int8", "data": "synthetic",
+            "config": workload_config(args),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args):
+    return {"workload": f"gpt2-124m {args.quant} cachedStep greedy decode, 16-token prompt then 112 steps "
+                        "(positions 16..127), one persistent launch per 112 steps",
+            "tokens_per_step": DECODE, "positions": "16..127", "model_shape": "12x768, 12 heads, ffn 3072, "
+            "vocab 50257", "l2": "inputs larger than L2 (weights 495 MB f32 / 132 MB int8 per token)",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+def traffic_from_profiles(kernel_src_hash: str, quant: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t.get(quant)
+        if e and e.get("kernel_sha256") == kernel_src_hash:
+            return e["dram_bytes_per_launch_112_steps"]
+    except Exception:
+        pass
+    return None
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "gpt2_dev.cuh"):
+        with open(os.path.join(ROOT, "stream_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measure_decode(g, torch, shape, w, toks, quant: str, args, rank_sync):
+    """Returns (ms per bench step, launches, session) after W warm-ups and K timed steps."""
+    q = g.INT8_G64 if quant == "int8" else g.F32
+    model = g.Model(shape, w, quant=q)
+    sess = g.Session(model)
+    V = shape.vocab
+    stream = torch.cuda.current_stream()
+    d_prompt = torch.tensor(np.asarray(toks, np.int32), device="cuda")
+    tout = torch.empty(DECODE, dtype=torch.int32, device="cuda")
+    assert sess.run(d_prompt, PROMPT, None, 0, tout) == "ok"
+    assert sess.sync() == "ok"
+    first = int(tout[PROMPT - 1].item())
+    tin = torch.full((DECODE,), -1, dtype=torch.int32, device="cuda")
+    tin[0] = first
+    logits = torch.empty(V, dtype=torch.float32, device="cuda")
+
+    def one():
+        assert sess.rewind(PROMPT) == "ok"
+        assert sess.run(tin, DECODE, logits, 0, tout, stream) == "ok"
+
+    for _ in range(args.warmup):
+        one()
+    assert sess.sync() == "ok"
+    torch.cuda.synchronize()
+    rank_sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id(torch)) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    rank_sync()
+    st = sess.sync()
+    assert st == "ok", st
+    ms = e0.elapsed_time(e1) / args.steps
+    return ms, args.steps, model, sess, first, clk.summary()
+
+
+def gpu_id(torch) -> str:
+    """nvidia-smi --id of the current device (its UUID when torch knows it)."""
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(torch.cuda.current_device())
+
+
+def measure_e2e(g, sess, shape, first, n_steps):
+    """Host buffers through the C ABI: every token goes in as a call argument,
+    every step's logits (pinned host memory) and greedy choice come back."""
+    import torch
+    host = torch.empty(shape.vocab, dtype=torch.float32, pin_memory=True)
+    nxt = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        assert sess.rewind(PROMPT) == "ok"
+        tok = first
+        for i in range(DECODE):
+            st = sess.step_host(tok, host, nxt)
+            assert st == "ok", st
+            tok = int(nxt.item()) & 0xFFFFFFFF
+    dt = time.perf_counter() - t0
+    return DECODE * n_steps / dt, dt
+
+
+def long_context(g, torch, w, reps=20):
+    """µs per cachedStep at p = 128, 512, 1023 over a cache of uniform random
+    tokens (the long-context configuration)."""
+    from stream_decode_gb300 import synth
+    s = synth.GPT2_124M_LONG
+    model = g.Model(s, w)
+    sess = g.Session(model)
+    toks = synth.tokens(s.vocab, 1024, seed=1234)
+    d = torch.tensor(toks.astype(np.int32), device="cuda")
+    assert sess.run(d, 1023, None, 0, None) == "ok"
+    assert sess.sync() == "ok"
+    out = {}
+    stream = torch.cuda.current_stream()
+    for p in (128, 512, 1023):
+        tin = d[p:p + 1]
+        for _ in range(3):
+            sess.rewind(p)
+            sess.run(tin, 1, None, 0, None, stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            sess.rewind(p)
+            sess.run(tin, 1, None, 0, None, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert sess.sync() == "ok"
+        us = 1e3 * e0.elapsed_time(e1) / reps
+        by = step_bytes(s, "f32", p)
+        out[f"p{p}"] = {"us_per_step": us, "GB_per_s": by / us * 1e-3, "bytes": by}
+    sess.close()
+    model.close()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quant", choices=["f32", "int8"], default="f32")
+    ap.add_argument("--no-extra", action="store_true", help="skip the int8 and long-context extras")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from stream_decode_gb300 import synth
+    shape = synth.GPT2_124M
+    w = synth.checkpoint(shape, synth.SEED_124M)
+    toks = synth.tokens(shape.vocab, PROMPT)
+
+    if args.impl == "reference":
+        reference_arm(args, shape, w, toks)
+        return
+
+    import torch
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        rank_sync = dist.barrier
+    else:
+        rank_sync = lambda: None
+    from stream_decode_gb300 import gpt2 as g
+
+    ms, launches, model, sess, first, clocks = measure_decode(g, torch, shape, w, toks, args.quant, args, rank_sync)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * DECODE / (ms * 1e-3)
+
+    peak, peak_kind = _peaks()
+    launch_bytes = sum(step_bytes(shape, args.quant, p) for p in range(PROMPT, PROMPT + DECODE))
+    achieved = launch_bytes / (ms * 1e-3) / 1e9
+    traffic = traffic_from_profiles(kernel_hash(), args.quant)
+
+    e2e_rate, _ = measure_e2e(g, sess, shape, first, 2)
+    sess.close()
+    model.close()
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        if args.quant == "f32":
+            ms8, _, m8, s8, _, _ = measure_decode(g, torch, shape, w, toks, "int8", args, lambda: None)
+            b8 = sum(step_bytes(shape, "int8", p) for p in range(PROMPT, PROMPT + DECODE))
+            extra["int8_decode"] = {"tokens_per_s": DECODE / (ms8 * 1e-3), "ms_per_step": ms8,
+                                    "GB_per_s": b8 / (ms8 * 1e-3) / 1e9,
+                                    "frac_of_peak": b8 / (ms8 * 1e-3) / 1e9 / peak}
+            s8.close()
+            m8.close()
+        extra["long_context_f32"] = long_context(g, torch, w)
+
+    cpu = None
+    if rank == 0:
+        n_dec = 16
+        rate, dt = oracle_decode_rate(shape, w, toks, 1 if args.quant == "int8" else 0, n_dec)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n_dec} greedy decode steps at positions 16..31 after an untimed 16-token prompt "
+                         f"({dt:.1f} s of single-threaded C on {cpu_cores()} available host cores)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": args.quant, "data": "synthetic (seeded N(0,0.02) weights, "
+                "uniform random prompt tokens)", "config": workload_config(args),
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": traffic,
+                             "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                             "algorithmic_bytes_per_launch": launch_bytes},
+                "cpu_baseline": cpu,
+                "e2e": {"value": ws * e2e_rate, "unit": "tokens/s", "h2d_bytes_per_step": 4 * DECODE,
+                        "d2h_bytes_per_step": DECODE * (4 * shape.vocab + 4)},
+                "gpu_launches": launches, "clocks": clocks, "extra": extra}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

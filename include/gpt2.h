@@ -1,0 +1,194 @@
+/*
+ * gpt2.h -- C ABI of the GB300 GPT-2 decode library (libgpt2gb.so).
+ *
+ * The library computes the GPT-2 124M forward pass described in the LeanExe
+ * GPT-2 README (model description paragraph): token plus position embedding;
+ * per block LayerNorm, query/key/value projection, causal attention, output
+ * projection and residual, LayerNorm, GELU feed-forward network and residual;
+ * final LayerNorm and the tied vocabulary projection.  It also provides the
+ * int8 group-64 variant of "Quantized GPT-2 Inference with Exact WebAssembly
+ * Proofs" (abstract).  All arithmetic runs in this library's CUDA kernels
+ * (sm_103a); there is no CPU fallback.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_host are host memory owned by the caller; pointers
+ *    named d_* are device memory owned by the caller; handles own their own
+ *    device memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *  - On a validation failure an entry returns its status, writes 0 to every
+ *    output length and launches no device work (LeanExe GPT-2 README: invalid
+ *    inputs return empty byte arrays).
+ *  - Device-side failures of asynchronous calls (an invalid device-resident
+ *    token, non-finite logits, a wait that timed out) are recorded in the
+ *    session and returned by the next gpt2_session_sync().
+ */
+#ifndef GPT2_GB300_H
+#define GPT2_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Model dimensions.  max_pos is the number of accepted positions (positions
+ * 0..max_pos-1): 128 for the README's entry points ("accepts positions zero
+ * through 127"), up to n_pos (1024 stored position rows) for long contexts.
+ * Supported shapes: (d_model, d_ff, d_model/n_head) = (768, 3072, 64),
+ * (192, 384, 64) and (64, 256, 16). */
+typedef struct gpt2_config {
+    uint32_t n_layer, d_model, n_head, d_ff, vocab, n_pos, max_pos;
+} gpt2_config;
+
+typedef enum gpt2_status {
+    GPT2_OK = 0,
+    GPT2_ERR_WEIGHTS_LEN = 1, /* weights_len != 4 * checkpoint words */
+    GPT2_ERR_TOKEN = 2,       /* a token id >= vocab */
+    GPT2_ERR_POSITION = 3,    /* position >= max_pos (or a run would pass it) */
+    GPT2_ERR_CACHE_LEN = 4,   /* cache_len != position * n_layer * 2 * d_model * 4 */
+    GPT2_ERR_TOKENS_LEN = 5,  /* token array empty, not a multiple of 4 bytes, or > max_pos ids */
+    GPT2_ERR_NONFINITE = 6,   /* a step produced a NaN or infinite logit */
+    GPT2_ERR_CONFIG = 7,      /* unsupported shape, quantization or grid */
+    GPT2_ERR_NOMEM = 8,       /* a device or host allocation failed */
+    GPT2_ERR_TIMEOUT = 9,     /* a device-side wait exceeded its limit; the run was abandoned */
+    GPT2_ERR_CUDA = 10,       /* a CUDA runtime call failed */
+    GPT2_ERR_ARG = 11         /* a NULL pointer or an out-of-range argument */
+} gpt2_status;
+
+typedef enum gpt2_quant {
+    GPT2_F32 = 0,     /* binary32 weights and arithmetic */
+    GPT2_INT8_G64 = 1 /* int8 weights and projection inputs, scales per 64 inputs, int32 sums */
+} gpt2_quant;
+
+/* In a device token array: use the previous step's greedy choice. */
+#define GPT2_TOKEN_GREEDY 0xFFFFFFFFu
+
+typedef struct gpt2_model gpt2_model;
+typedef struct gpt2_session gpt2_session;
+
+/* Packed checkpoint size in 32-bit words (LeanExe GPT-2 README, packed
+ * checkpoint paragraph: wte, all stored position rows, the blocks, the final
+ * normalization; 124,439,808 words for GPT-2 124M).  0 for a NULL config. */
+size_t gpt2_weight_words(const gpt2_config* cfg);
+
+/* Words of one cached position: n_layer * 2 * d_model (README, cachedStep
+ * paragraph: 12 x 1536 for GPT-2 124M). */
+size_t gpt2_cache_words_per_position(const gpt2_config* cfg);
+
+/* ---------------------------------------------------------------------
+ * Byte-level entries with the README's semantics (host buffers; each call
+ * uploads the checkpoint, runs on the GPU and copies results back; slow by
+ * design, use the session API for decoding).
+ * ------------------------------------------------------------------- */
+
+/* infer (README, infer paragraph): weights = packed little-endian binary32
+ * checkpoint; tokens = 1..max_pos little-endian u32 ids.  Writes the final
+ * row's vocab logits to logits_out_host (capacity vocab floats) and
+ * *logits_out_len = vocab.  Checks, in order: weights_len, tokens_len, each
+ * token. */
+gpt2_status gpt2_infer(const gpt2_config* cfg, const void* weights_host, size_t weights_len,
+                       const void* tokens_host, size_t tokens_len, float* logits_out_host,
+                       size_t* logits_out_len);
+
+/* cachedStep (README, cachedStep paragraph): one token at `position`, given a
+ * cache of position*n_layer*2*d_model little-endian binary32 words ordered by
+ * prior position, then layer, then d_model keys and d_model values (word
+ * (source*n_layer + layer)*2*d_model + offset).  Writes vocab logits and the
+ * cache with this position's rows appended (cache_out_host capacity
+ * cache_len + n_layer*2*d_model*4 bytes; it may be the same buffer as
+ * cache_host).  Checks, in order: weights_len, token, position, cache_len. */
+gpt2_status gpt2_cached_step(const gpt2_config* cfg, const void* weights_host, size_t weights_len,
+                             const void* cache_host, size_t cache_len, uint32_t token, uint32_t position,
+                             float* logits_out_host, size_t* logits_out_len, void* cache_out_host,
+                             size_t* cache_out_len);
+
+/* ---------------------------------------------------------------------
+ * Device-resident model and session (the measured path).
+ * ------------------------------------------------------------------- */
+
+/* Uploads the packed checkpoint and builds the device weight streams
+ * (K-major copies of the block matrices; for GPT2_INT8_G64 the int8 copies
+ * of the 48 block matrices and the tied wte with their group scales).
+ * grid_ctas: CTAs of the persistent step kernel, 0 = one per SM.
+ * Synchronous.  Checks weights_len, the shape and the quantization. */
+gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights_host, size_t weights_len, int quant,
+                              int grid_ctas, gpt2_model** out);
+void gpt2_model_destroy(gpt2_model* model);
+
+/* Copies back one int8 matrix of the model as q[out][in] (int8) and
+ * s[out][in/64] (float): index 4*layer + {0: qkv, 1: out-proj, 2: fc,
+ * 3: mlp-proj}, or 4*n_layer for the tied wte.  GPT2_ERR_CONFIG for a
+ * binary32 model. */
+gpt2_status gpt2_model_read_q8(gpt2_model* model, int index, int8_t* q_host, float* s_host);
+
+/* A session owns a device KV cache of max_pos positions and the step
+ * kernel's scratch; it starts empty at position 0.  Synchronous. */
+gpt2_status gpt2_session_create(gpt2_model* model, gpt2_session** out);
+void gpt2_session_destroy(gpt2_session* session);
+
+/* Current position (= number of cached positions), as enqueued. */
+uint32_t gpt2_session_position(const gpt2_session* session);
+
+/* Replaces the cache with cache_len bytes in the boundary layout above and
+ * sets the position to cache_len / (n_layer*2*d_model*4).  Synchronous.
+ * GPT2_ERR_CACHE_LEN unless cache_len is a whole number of positions below
+ * max_pos. */
+gpt2_status gpt2_session_load_cache(gpt2_session* session, const void* cache_host, size_t cache_len);
+
+/* Truncates the session to its first `position` cached positions (the
+ * cache words beyond are overwritten by later steps) and clears the greedy
+ * history, stream-ordered on the session's last stream.  GPT2_ERR_POSITION
+ * if position exceeds the current position. */
+gpt2_status gpt2_session_rewind(gpt2_session* session, uint32_t position);
+
+/* Copies the cache (position positions, boundary layout) to cache_host
+ * (capacity bytes).  Synchronous; waits for queued runs. */
+gpt2_status gpt2_session_read_cache(gpt2_session* session, void* cache_host, size_t capacity, size_t* len);
+
+/* Enqueues n_steps cached steps at positions position..position+n_steps-1 as
+ * ONE persistent kernel launch on `stream`.  d_tokens_in: device array of
+ * n_steps token ids; GPT2_TOKEN_GREEDY takes the previous step's greedy
+ * choice (for step 0: the session's last choice).  d_logits (may be NULL):
+ * device output, step s written at d_logits + s*logits_stride floats
+ * (logits_stride 0 = every step overwrites one row).  d_tokens_out (may be
+ * NULL): device array receiving each step's greedy choice (argmax, lowest
+ * index on ties; 0xFFFFFFFF if a logit was not finite).  Host-side checks:
+ * n_steps >= 1 and position + n_steps <= max_pos.  The position advances
+ * when the call returns. */
+gpt2_status gpt2_session_run(gpt2_session* session, const uint32_t* d_tokens_in, uint32_t n_steps,
+                             float* d_logits, size_t logits_stride, uint32_t* d_tokens_out, void* stream);
+
+/* One step with a host token; outputs as in gpt2_session_run.  Asynchronous. */
+gpt2_status gpt2_session_step(gpt2_session* session, uint32_t token, float* d_logits, uint32_t* d_next_token,
+                              void* stream);
+
+/* One step with host buffers end to end: the token goes in as a kernel
+ * argument, the logits (vocab floats) and greedy choice are copied back to
+ * host memory, and the call waits for them.  Returns any device status. */
+gpt2_status gpt2_session_step_host(gpt2_session* session, uint32_t token, float* logits_host,
+                                   uint32_t* next_token_host);
+
+/* Waits for the session's queued work and returns (and clears) the first
+ * device-side failure recorded since the last sync. */
+gpt2_status gpt2_session_sync(gpt2_session* session);
+
+/* Debug: enqueue the next run with an activation trace.  d_trace receives,
+ * for step 0 of that run only, per layer: x_in[d], LN1(x)[d], qkv[3d],
+ * attention output[d], x_mid[d], LN2(x_mid)[d], gelu output[d_ff]; then
+ * x_final[d], LN_f(x_final)[d].  Pass NULL to stop tracing. */
+gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
+
+/* Debug/test: make the next run's CTA 0 skip publishing one phase so that
+ * the other CTAs' bounded waits expire and the run ends with
+ * GPT2_ERR_TIMEOUT (no GPU fault, no hang).  wait_limit_ns bounds every
+ * device-side wait of that run. */
+gpt2_status gpt2_session_inject_stall(gpt2_session* session, uint32_t phase, uint64_t wait_limit_ns);
+
+/* Human-readable status name ("ok", "token", ...). */
+const char* gpt2_status_name(gpt2_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_GB300_H */

@@ -1,0 +1,173 @@
+// gpt2_dev.cuh -- device-side definitions shared by the library's kernels:
+// the step plan, the device weight-stream geometry and inline-PTX wrappers
+// (mbarrier, bulk copies, release/acquire flags).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gpt2 {
+
+// ---------------------------------------------------------------- constants
+constexpr int kGroup = 64;          // int8 group size (quantized GPT-2 abstract)
+constexpr int kConsumerWarps = 8;   // warps that compute
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kSlotBytes = 12288;   // one ring slot (one 3072-float row)
+constexpr int kSlots = 16;          // ring depth: 192 KiB of weights in flight per SM
+constexpr float kLnEps = 1e-5f;
+
+// status words written by the device
+enum DevStatus : int {
+    kDevOk = 0,
+    kDevToken = 2,
+    kDevNonfinite = 6,
+    kDevTimeout = 9,
+};
+
+// Matrix kinds in the per-layer weight stream, in stream order.
+enum Mat : int { kQKV = 0, kO = 1, kFC = 2, kP = 3, kVocab = 4 };
+
+// Packed-checkpoint word offsets of the small per-layer tensors the step
+// reads directly (LayerNorm parameters and biases).
+struct LayerParams {
+    uint64_t ln1_g, ln1_b, b_qkv, b_o, ln2_g, ln2_b, b_fc, b_p;
+};
+
+constexpr int kMaxLayers = 16;
+
+// Everything one launch of the step kernel needs.  Passed by value.
+struct StepPlan {
+    // shape
+    int L, D, H, FF, V, n_pos, max_pos;
+    int G;  // CTAs in the grid
+    // weights
+    const float* packed;        // packed checkpoint on the device
+    const uint8_t* wstream;     // per layer: qkv[3D] rows, o[D], fc[FF], p[D] (K-major rows)
+    uint64_t layer_bytes;       // bytes of one layer in wstream
+    uint64_t mat_off[4];        // byte offset of each matrix inside a layer
+    const uint8_t* vocab;       // vocab rows (fp32: wte in the packed checkpoint; int8: q rows + scales)
+    uint64_t wte_off, wpe_off, lnf_g, lnf_b;  // word offsets in packed
+    LayerParams lp[kMaxLayers];
+    // session buffers
+    float* cache;               // [max_pos][L][2D]
+    float* xa;                  // [D] residual stream after a block
+    float* xb;                  // [D] residual stream after attention
+    float* qkv;                 // [3D]
+    float* u;                   // [FF]
+    float* attn_part;           // [H * S][2 + DH]
+    float* arg_part;            // [G][4]
+    unsigned* flags;            // [G] published phase numbers
+    unsigned epoch;             // phase numbers of this run start above this
+    int* status;                // sticky device status
+    int* abort_flag;            // set by any CTA that gives up
+    uint32_t* last_token;       // the session's last greedy choice
+    // the run
+    int p0, n_steps;
+    const uint32_t* tokens_in;  // [n_steps]
+    uint32_t token0;            // used when tokens_in == nullptr (single host-token step)
+    uint32_t* tokens_out;       // [n_steps] or null
+    float* logits;              // or null
+    uint64_t logits_stride;     // floats between steps' logits
+    float* trace;               // or null
+    // robustness
+    uint64_t wait_limit_ns;     // bound of every spin-wait
+    int stall_phase;            // test: CTA 0 skips publishing this phase (-1 = none)
+    int prefetch_chunks;        // L2 bulk prefetch distance in chunks (0 = off)
+};
+
+// Bytes of one K-major weight row in the device stream.
+__host__ __device__ constexpr int row_bytes(int K, bool q8) {
+    return q8 ? K + ((K / kGroup) * 4 + 15) / 16 * 16 : K * 4;
+}
+
+// --------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int ld_volatile_int(const int* p) {
+    return *reinterpret_cast<const volatile int*>(p);
+}
+
+// Named barrier over the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// int8 quantization rule shared by activations and weights: nearest-even,
+// saturate to [-127, 127], a zero scale or a NaN quotient gives 0.
+__device__ __forceinline__ int quantize_one(float x, float s) {
+    float r = 0.0f;
+    if (s != 0.0f) r = rintf(__fdiv_rn(x, s));
+    if (r != r) r = 0.0f;
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+}  // namespace gpt2

@@ -1,0 +1,86 @@
+// repack.cu -- load-time construction of the device weight streams.
+//
+// The packed checkpoint stores block matrices [in][out] (gpt2.s page,
+// weight-layout paragraph).  The step kernel wants each output's weights
+// contiguous (K-major rows) so that a CTA's share of outputs is one byte
+// range.  binary32 models get a transposed copy; int8 models get, per output
+// row, K int8 codes followed by the K/64 group scales (padded to 16 bytes),
+// quantized with the rule of the quantized GPT-2 abstract: scale =
+// maxabs/127 over 64 consecutive inputs of the row, nearest-even, saturate.
+#include <cuda_runtime.h>
+
+#include "gpt2_dev.cuh"
+
+namespace gpt2 {
+
+// src [K][N] row-major -> dst rows of N outputs, each K floats (row pitch rb bytes).
+__global__ void transpose_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int K, int N, int rb) {
+    __shared__ float tile[32][33];
+    const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+        const int k = k0 + dy, n = n0 + threadIdx.x;
+        tile[dy][threadIdx.x] = (k < K && n < N) ? src[(size_t)k * N + n] : 0.0f;
+    }
+    __syncthreads();
+    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+        const int n = n0 + dy, k = k0 + threadIdx.x;
+        if (n < N && k < K) reinterpret_cast<float*>(dst + (size_t)n * rb)[k] = tile[threadIdx.x][dy];
+    }
+}
+
+// One thread per (output n, group g): weights W[64g .. 64g+63][n] of a [K][N] matrix.
+__global__ void quantize_in_out_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int K, int N,
+                                       int rb) {
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    const int g = blockIdx.y;
+    if (n >= N) return;
+    float m = 0.0f;
+    for (int t = 0; t < kGroup; ++t) {
+        const float a = fabsf(src[(size_t)(g * kGroup + t) * N + n]);
+        if (a > m) m = a;
+    }
+    const float s = __fdiv_rn(m, 127.0f);
+    int8_t* q = reinterpret_cast<int8_t*>(dst + (size_t)n * rb);
+    for (int t = 0; t < kGroup; ++t) q[g * kGroup + t] = (int8_t)quantize_one(src[(size_t)(g * kGroup + t) * N + n], s);
+    reinterpret_cast<float*>(dst + (size_t)n * rb + K)[g] = s;
+}
+
+// One thread per (row n, group g) of an [N][K] matrix (the tied wte).
+__global__ void quantize_out_in_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int K, int N,
+                                       int rb) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int ng = K / kGroup;
+    if (i >= (long long)N * ng) return;
+    const int n = (int)(i / ng), g = (int)(i % ng);
+    const float* row = src + (size_t)n * K + g * kGroup;
+    float m = 0.0f;
+    for (int t = 0; t < kGroup; ++t) {
+        const float a = fabsf(row[t]);
+        if (a > m) m = a;
+    }
+    const float s = __fdiv_rn(m, 127.0f);
+    int8_t* q = reinterpret_cast<int8_t*>(dst + (size_t)n * rb);
+    for (int t = 0; t < kGroup; ++t) q[g * kGroup + t] = (int8_t)quantize_one(row[t], s);
+    reinterpret_cast<float*>(dst + (size_t)n * rb + K)[g] = s;
+}
+
+cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, bool q8, cudaStream_t st) {
+    const int rb = row_bytes(K, q8);
+    if (!q8) {
+        dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
+        transpose_kernel<<<grid, block, 0, st>>>(src_in_out, dst, K, N, rb);
+    } else {
+        dim3 grid((N + 127) / 128, K / kGroup), block(128);
+        quantize_in_out_kernel<<<grid, block, 0, st>>>(src_in_out, dst, K, N, rb);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, cudaStream_t st) {
+    const int rb = row_bytes(K, true);
+    const long long n = (long long)N * (K / kGroup);
+    quantize_out_in_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src_out_in, dst, K, N, rb);
+    return cudaGetLastError();
+}
+
+}  // namespace gpt2

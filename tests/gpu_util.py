@@ -1,0 +1,43 @@
+"""Helpers for the GPU tests: device token arrays, one-launch sessions, and
+the oracle side of each comparison."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+GREEDY = -1  # int32 view of 0xFFFFFFFF
+
+# The tolerance the spec states for binary32 logits (max |delta|) and the
+# greedy agreement rate it requires.
+LOGIT_TOL = 2e-3
+AGREE_MIN = 0.99
+
+
+def dev_tokens(seq) -> torch.Tensor:
+    a = np.asarray(seq, dtype=np.int64)
+    a = np.where(a < 0, -1, a).astype(np.int32)
+    return torch.tensor(a, dtype=torch.int32, device="cuda")
+
+
+def run(sess, seq, n_steps, want_logits=True):
+    """One persistent launch of n_steps; returns (logits[n][V] or None, choices[n] as int64 u32)."""
+    V = sess.model.shape.vocab
+    tin = dev_tokens(seq)
+    logits = torch.empty(n_steps, V, dtype=torch.float32, device="cuda") if want_logits else None
+    tout = torch.full((n_steps,), -7, dtype=torch.int32, device="cuda")
+    st = sess.run(tin, n_steps, logits, V if want_logits else 0, tout)
+    assert st == "ok", st
+    st = sess.sync()
+    assert st == "ok", st
+    ch = tout.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    return (logits.cpu().numpy() if want_logits else None), ch
+
+
+def oracle_teacher_forced(omodel, seq_tokens, p0=0, cache=None):
+    """Oracle logits for an explicit token sequence (no greedy feedback)."""
+    return omodel.session([int(t) for t in seq_tokens], len(seq_tokens), p0=p0, cache=cache)
+
+
+def greedy_agreement(oracle_logits, gpu_choices) -> float:
+    o = np.argmax(oracle_logits, axis=1)
+    return float(np.mean(o == gpu_choices))
