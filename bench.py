@@ -32,7 +32,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GPT-2 124M cachedStep tokens/s on 1 GB300; achieved HBM GB/s vs peak"
-PROMPT, DECODE = 16, 112
+PROMPT = 16
+DECODE = 112  # decode positions per bench step (--decode-steps)
 KV_ROW_BYTES = 12 * 1536 * 4  # one cached position (README cachedStep paragraph)
 
 
@@ -176,9 +177,9 @@ def reference_arm(args, shape, w, toks):
 
 
 def workload_config(args):
-    return {"workload": f"gpt2-124m {args.quant} cachedStep greedy decode, 16-token prompt then 112 steps "
-                        "(positions 16..127), one persistent launch per 112 steps",
-            "tokens_per_step": DECODE, "positions": "16..127", "model_shape": "12x768, 12 heads, ffn 3072, "
+    return {"workload": f"gpt2-124m {args.quant} cachedStep greedy decode, 16-token prompt then {DECODE} steps "
+                        f"(positions 16..{15 + DECODE}), one persistent launch per {DECODE} steps",
+            "tokens_per_step": DECODE, "positions": f"16..{15 + DECODE}", "model_shape": "12x768, 12 heads, ffn 3072, "
             "vocab 50257", "l2": "inputs larger than L2 (weights 495 MB f32 / 132 MB int8 per token)",
             "parallelism": f"replicas x{args.gpus}"}
 
@@ -315,8 +316,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quant", choices=["f32", "int8"], default="f32")
     ap.add_argument("--no-extra", action="store_true", help="skip the int8 and long-context extras")
+    ap.add_argument("--decode-steps", type=int, default=112,
+                    help="decode positions per bench step (112 = positions 16..127)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    global DECODE
+    DECODE = max(1, min(112, args.decode_steps))
 
     from stream_decode_gb300 import synth
     shape = synth.GPT2_124M

@@ -150,7 +150,7 @@ def test_nonfinite_logits_reported(g):
     tout = torch.zeros(3, dtype=torch.int32, device="cuda")
     assert sess.run(dev_tokens([1, 2, 3]), 3, None, 0, tout) == "ok"
     assert sess.sync() == "nonfinite"
-    assert (tout.cpu().numpy()[0] & 0xFFFFFFFF) == 0xFFFFFFFF
+    assert (int(tout.cpu().numpy()[0]) & 0xFFFFFFFF) == 0xFFFFFFFF
 
 
 def test_stalled_phase_times_out_and_session_recovers(g):
