@@ -215,7 +215,7 @@ def measure_decode(g, torch, shape, w, toks, quant: str, args, rank_sync):
     V = shape.vocab
     stream = torch.cuda.current_stream()
     d_prompt = torch.tensor(np.asarray(toks, np.int32), device="cuda")
-    tout = torch.empty(DECODE, dtype=torch.int32, device="cuda")
+    tout = torch.empty(max(PROMPT, DECODE), dtype=torch.int32, device="cuda")  # the prompt run writes PROMPT ids
     assert sess.run(d_prompt, PROMPT, None, 0, tout) == "ok"
     assert sess.sync() == "ok"
     first = int(tout[PROMPT - 1].item())

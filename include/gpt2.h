@@ -185,6 +185,21 @@ gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
  * device-side wait of that run. */
 gpt2_status gpt2_session_inject_stall(gpt2_session* session, uint32_t phase, uint64_t wait_limit_ns);
 
+/* Test hook: applies projection `index` of the model (index convention of
+ * gpt2_model_read_q8; the vocabulary projection has no bias) to the device
+ * vector d_x (its input width in floats) and writes d_y (its output width),
+ * using the step kernel's own device routines: for int8 models the per-64
+ * activation quantizer, the dp4a group sums and the fixed-order rescale; for
+ * binary32 models the float4 dot products.  Enqueued on `stream`. */
+gpt2_status gpt2_debug_project(gpt2_model* model, int index, const float* d_x, float* d_y, void* stream);
+
+/* Test hook: the step kernel's greedy-choice routine over d_values[n]:
+ * *d_index = index of the largest value (lowest index on ties), and
+ * *d_nonfinite = 1 with *d_index = 0xFFFFFFFF if any value is NaN or
+ * infinite.  Enqueued on `stream`. */
+gpt2_status gpt2_debug_argmax(const float* d_values, uint32_t n, uint32_t* d_index, int* d_nonfinite,
+                              void* stream);
+
 /* Human-readable status name ("ok", "token", ...). */
 const char* gpt2_status_name(gpt2_status status);
 

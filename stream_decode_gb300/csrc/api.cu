@@ -17,6 +17,9 @@ int step_max_ctas(int D, int FF, int DH, bool q8, int max_pos);
 bool step_shape_supported(int D, int FF, int DH);
 cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, bool q8, cudaStream_t st);
 cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, cudaStream_t st);
+cudaError_t launch_project(const uint8_t* rows, int K, int N, bool q8, const float* x, const float* bias, float* y,
+                           cudaStream_t st);
+cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfinite, cudaStream_t st);
 }  // namespace gpt2
 
 using namespace gpt2;
@@ -448,6 +451,36 @@ gpt2_status gpt2_session_inject_stall(gpt2_session* s, uint32_t phase, uint64_t 
     s->stall_phase = (int)phase;
     s->wait_limit_ns = wait_limit_ns;
     return GPT2_OK;
+}
+
+gpt2_status gpt2_debug_project(gpt2_model* m, int index, const float* d_x, float* d_y, void* stream) {
+    if (!m || !d_x || !d_y) return GPT2_ERR_ARG;
+    const int D = (int)m->cfg.d_model, FF = (int)m->cfg.d_ff, L = (int)m->cfg.n_layer;
+    if (index < 0 || index > 4 * L) return GPT2_ERR_ARG;
+    const bool q8 = m->quant == GPT2_INT8_G64;
+    int K, N;
+    const uint8_t* rows;
+    const float* bias = nullptr;
+    if (index == 4 * L) {
+        K = D;
+        N = (int)m->cfg.vocab;
+        rows = q8 ? m->d_vocab_q8 : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
+    } else {
+        const int l = index / 4, k = index % 4;
+        K = (k == kP) ? FF : D;
+        N = (k == kQKV) ? 3 * D : (k == kFC ? FF : D);
+        rows = m->d_wstream + (uint64_t)l * m->layer_bytes + m->mat_off[k];
+        const LayerParams& lp = m->lp[l];
+        const uint64_t b = (k == kQKV) ? lp.b_qkv : (k == kO ? lp.b_o : (k == kFC ? lp.b_fc : lp.b_p));
+        bias = m->d_packed + b;
+    }
+    return cuda_status(launch_project(rows, K, N, q8, d_x, bias, d_y, (cudaStream_t)stream));
+}
+
+gpt2_status gpt2_debug_argmax(const float* d_values, uint32_t n, uint32_t* d_index, int* d_nonfinite,
+                              void* stream) {
+    if (!d_values || !d_index || !d_nonfinite || n == 0) return GPT2_ERR_ARG;
+    return cuda_status(launch_argmax(d_values, n, d_index, d_nonfinite, (cudaStream_t)stream));
 }
 
 // ------------------------------------------------------- byte-level entries

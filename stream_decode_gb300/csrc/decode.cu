@@ -155,6 +155,36 @@ __device__ __forceinline__ bool arg_better(float v, unsigned i, float bv, unsign
     return v > bv || (v == bv && i < bi);
 }
 
+// Running greedy choice: best finite value (lowest index on ties) and a
+// flag for any NaN or infinite value seen.
+struct ArgBest {
+    float v;
+    unsigned i;
+    int nf;
+};
+
+__device__ __forceinline__ ArgBest arg_init() { return ArgBest{-INFINITY, 0xFFFFFFFFu, 0}; }
+
+__device__ __forceinline__ void arg_update(ArgBest& b, float v, unsigned j) {
+    if (!isfinite(v)) b.nf = 1;
+    else if (arg_better(v, j, b.v, b.i)) { b.v = v; b.i = j; }
+}
+
+__device__ __forceinline__ void arg_merge(ArgBest& b, float v, unsigned i, int nf) {
+    b.nf |= nf;
+    if (arg_better(v, i, b.v, b.i)) { b.v = v; b.i = i; }
+}
+
+__device__ __forceinline__ void arg_warp_reduce(ArgBest& b) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, b.v, o);
+        const unsigned oi = __shfl_xor_sync(0xffffffffu, b.i, o);
+        const int onf = __shfl_xor_sync(0xffffffffu, b.nf, o);
+        arg_merge(b, ov, oi, onf);
+    }
+}
+
 // LayerNorm of x (smem, N values) into y (smem); biased variance, eps 1e-5.
 template <int N>
 __device__ __forceinline__ void layernorm(const float* x, const float* __restrict__ g, const float* __restrict__ b,
@@ -671,58 +701,41 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             trace_vec(L * trace_layer, xs, D);
             trace_vec(L * trace_layer + D, vin, D);
         }
-        float bv = -INFINITY;
-        unsigned bi = 0xFFFFFFFFu;
-        int nf = 0;
+        ArgBest best = arg_init();
         {
             float* lg = P.logits ? P.logits + (uint64_t)s * P.logits_stride : nullptr;
             auto epi = [&](int j, float acc) {
                 if (lg) lg[j] = acc;
-                if (!isfinite(acc)) nf = 1;
-                else if (arg_better(acc, (unsigned)j, bv, bi)) { bv = acc; bi = (unsigned)j; }
+                arg_update(best, acc, (unsigned)j);
             };
             if (!gemv(4 * L, 0, epi)) break;
         }
         // reduce the per-lane choices of this CTA
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const unsigned oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            nf |= __shfl_xor_sync(0xffffffffu, nf, o);
-            if (arg_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
+        arg_warp_reduce(best);
         if (lane == 0) {
-            s_arg[warp * 3 + 0] = bv;
-            s_arg[warp * 3 + 1] = __uint_as_float(bi);
-            s_arg[warp * 3 + 2] = (float)nf;
+            s_arg[warp * 3 + 0] = best.v;
+            s_arg[warp * 3 + 1] = __uint_as_float(best.i);
+            s_arg[warp * 3 + 2] = (float)best.nf;
         }
         consumers_sync();
         if (tid == 0) {
-            for (int w = 1; w < kConsumerWarps; ++w) {
-                const float ov = s_arg[w * 3 + 0];
-                const unsigned oi = __float_as_uint(s_arg[w * 3 + 1]);
-                nf |= (s_arg[w * 3 + 2] != 0.0f);
-                if (arg_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-            }
+            for (int w = 1; w < kConsumerWarps; ++w)
+                arg_merge(best, s_arg[w * 3 + 0], __float_as_uint(s_arg[w * 3 + 1]), s_arg[w * 3 + 2] != 0.0f);
             float* ap = P.arg_part + (size_t)cta * 4;
-            ap[0] = bv;
-            ap[1] = __uint_as_float(bi);
-            ap[2] = (float)nf;
+            ap[0] = best.v;
+            ap[1] = __uint_as_float(best.i);
+            ap[2] = (float)best.nf;
         }
         publish();
         if (!grid_wait(P.epoch + phase_no)) break;
         if (tid == 0) {
-            float gv = -INFINITY;
-            unsigned gidx = 0xFFFFFFFFu;
-            int gnf = 0;
+            ArgBest gb = arg_init();
             for (int c = 0; c < P.G; ++c) {
                 const float* ap = P.arg_part + (size_t)c * 4;
-                const float ov = __ldcg(ap);
-                const unsigned oi = __float_as_uint(__ldcg(ap + 1));
-                gnf |= (__ldcg(ap + 2) != 0.0f);
-                if (arg_better(ov, oi, gv, gidx)) { gv = ov; gidx = oi; }
+                arg_merge(gb, __ldcg(ap), __float_as_uint(__ldcg(ap + 1)), __ldcg(ap + 2) != 0.0f);
             }
-            const unsigned choice = gnf ? 0xFFFFFFFFu : gidx;
+            const int gnf = gb.nf;
+            const unsigned choice = gnf ? 0xFFFFFFFFu : gb.i;
             *s_tok = choice;
             *s_nf = gnf;
             if (cta == 0) {
@@ -737,6 +750,76 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     }
     // Make the producer stop if the consumers left early.
     if (tid == 0) *s_abort = 1;
+}
+
+// ------------------------------------------------------------ test hooks
+// One projection of the model on a given input vector, with the step
+// kernel's own routines (activation quantizer, chunk dot products,
+// epilogue bias add).  Block: 8 warps over 64 output rows.
+template <int K, bool Q8>
+__global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint8_t* __restrict__ rows, int N,
+                                                                      const float* __restrict__ x,
+                                                                      const float* __restrict__ bias,
+                                                                      float* __restrict__ y) {
+    __shared__ __align__(16) float vin[K];
+    __shared__ __align__(16) int8_t vq[K];
+    __shared__ float vs[K / kGroup];
+    __shared__ float scr[kConsumerWarps * kRescalePerWarp];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < K; i += blockDim.x) vin[i] = x[i];
+    __syncthreads();
+    if constexpr (Q8) quantize_vec<K>(vin, vq, vs, warp, lane);
+    __syncthreads();
+    auto epi = [&](int j, float acc) { y[j] = bias ? __fadd_rn(acc, bias[j]) : acc; };
+    const int rb = row_bytes(K, Q8);
+    const int r0 = blockIdx.x * 64 + warp * 8;
+    const int n = min(8, N - r0);
+    if (n <= 0) return;
+    if constexpr (Q8) chunk_q8<K>(rows + (size_t)r0 * rb, n, vq, vs, lane, scr + warp * kRescalePerWarp, r0, epi);
+    else chunk_f32<K>(reinterpret_cast<const float*>(rows + (size_t)r0 * rb), n, vin, lane, r0, epi);
+}
+
+// The step kernel's greedy-choice routine over n values (one block).
+__global__ void __launch_bounds__(kConsumerWarps * 32) argmax_kernel(const float* __restrict__ v, unsigned n,
+                                                                     uint32_t* idx, int* nonfinite) {
+    __shared__ float s_arg[kConsumerWarps * 3];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    ArgBest b = arg_init();
+    for (unsigned j = tid; j < n; j += blockDim.x) arg_update(b, v[j], j);
+    arg_warp_reduce(b);
+    if (lane == 0) {
+        s_arg[warp * 3 + 0] = b.v;
+        s_arg[warp * 3 + 1] = __uint_as_float(b.i);
+        s_arg[warp * 3 + 2] = (float)b.nf;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < kConsumerWarps; ++w)
+            arg_merge(b, s_arg[w * 3 + 0], __float_as_uint(s_arg[w * 3 + 1]), s_arg[w * 3 + 2] != 0.0f);
+        *idx = b.nf ? 0xFFFFFFFFu : b.i;
+        *nonfinite = b.nf;
+    }
+}
+
+template <int K, bool Q8>
+static cudaError_t project_t(const uint8_t* rows, int N, const float* x, const float* bias, float* y,
+                             cudaStream_t st) {
+    project_kernel<K, Q8><<<(N + 63) / 64, kConsumerWarps * 32, 0, st>>>(rows, N, x, bias, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_project(const uint8_t* rows, int K, int N, bool q8, const float* x, const float* bias, float* y,
+                           cudaStream_t st) {
+#define GPT2_PROJ(KK)                                                                             \
+    if (K == KK) return q8 ? project_t<KK, true>(rows, N, x, bias, y, st) : project_t<KK, false>(rows, N, x, bias, y, st);
+    GPT2_PROJ(64) GPT2_PROJ(192) GPT2_PROJ(256) GPT2_PROJ(384) GPT2_PROJ(768) GPT2_PROJ(3072)
+#undef GPT2_PROJ
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfinite, cudaStream_t st) {
+    argmax_kernel<<<1, kConsumerWarps * 32, 0, st>>>(v, n, idx, nonfinite);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ launcher

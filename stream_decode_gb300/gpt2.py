@@ -57,6 +57,8 @@ _SIGS = {
     "gpt2_session_sync": ([_vp], _i32),
     "gpt2_session_set_trace": ([_vp, _vp], _i32),
     "gpt2_session_inject_stall": ([_vp, _u32, C.c_uint64], _i32),
+    "gpt2_debug_project": ([_vp, _i32, _vp, _vp, _vp], _i32),
+    "gpt2_debug_argmax": ([_vp, _u32, _vp, _vp, _vp], _i32),
     "gpt2_status_name": ([_i32], C.c_char_p),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -146,6 +148,10 @@ class Model:
         _check("gpt2_model_read_q8", lib.gpt2_model_read_q8(self.h, index, q.ctypes.data, sc.ctypes.data))
         return q, sc
 
+    def debug_project(self, index: int, x, y, stream=None) -> str:
+        """Test hook: projection `index` of x (CUDA tensor) into y (CUDA tensor)."""
+        return STATUS[lib.gpt2_debug_project(self.h, index, _ptr(x), _ptr(y), _stream(stream))]
+
     def close(self):
         if getattr(self, "h", None):
             lib.gpt2_model_destroy(self.h)
@@ -215,6 +221,12 @@ class Session:
 
     def __del__(self):
         self.close()
+
+
+def debug_argmax(values, index, nonfinite, stream=None) -> str:
+    """Test hook: the step kernel's greedy choice over a CUDA float tensor."""
+    return STATUS[lib.gpt2_debug_argmax(_ptr(values), values.numel(), _ptr(index), _ptr(nonfinite),
+                                        _stream(stream))]
 
 
 def trace_words(shape) -> int:

@@ -178,3 +178,12 @@ def uniform_f32(seed: int, count: int, lo: float = -1.0, hi: float = 1.0) -> np.
     r = splitmix64(seed, 0, count)
     u = (r >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
     return (lo + (hi - lo) * u).astype(np.float32)
+
+
+def cache(s: Shape, positions: int, seed: int, scale: float = 0.5) -> np.ndarray:
+    """A KV cache of `positions` positions in the boundary layout (word
+    (source*n_layer + layer)*2*d + offset), every word ~ N(0, scale^2): the
+    magnitude of keys and values that N(0, 0.02) weights produce from a
+    LayerNorm output (sqrt(768) * 0.02 ~ 0.55)."""
+    n = positions * s.n_layer * 2 * s.d_model
+    return (scale * normals(seed, 0, n)).astype(np.float32)

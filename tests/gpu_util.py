@@ -41,3 +41,34 @@ def oracle_teacher_forced(omodel, seq_tokens, p0=0, cache=None):
 def greedy_agreement(oracle_logits, gpu_choices) -> float:
     o = np.argmax(oracle_logits, axis=1)
     return float(np.mean(o == gpu_choices))
+
+
+def disagreements_are_near_ties(oracle_logits, gpu_choices, tol) -> bool:
+    """Where the greedy choices differ, the oracle's logits of the two tokens
+    must lie within `tol` of each other: a near tie, where either token is a
+    correct greedy choice given the stated logit tolerance."""
+    n = len(gpu_choices)
+    o = np.argmax(oracle_logits, axis=1)
+    ch = np.asarray(gpu_choices, np.int64)
+    if np.any(ch >= oracle_logits.shape[1]):
+        return False
+    gap = oracle_logits[np.arange(n), o] - oracle_logits[np.arange(n), ch]
+    return bool(np.all((o == ch) | (gap <= tol)))
+
+
+def oracle_greedy(omodel, prompt, n_steps):
+    """The oracle's own greedy session: prompt tokens, then its own choices.
+    Returns (token sequence fed at each position, logits, choices, cache)."""
+    logits, ch, cache = omodel.session(list(prompt) + [-1] * (n_steps - len(prompt)), n_steps)
+    seq = np.concatenate([np.asarray(prompt, np.int64), ch[len(prompt) - 1:n_steps - 1]])
+    return seq, logits, ch, cache
+
+
+def int8_tolerance(logits_q8, logits_f32) -> float:
+    """End-to-end int8 logit tolerance: the oracle's own int8-vs-binary32
+    distance on the same tokens.  Two correct int8 realizations differ by
+    activation-code flips (a float rounding difference before a quantizer
+    moves a code by one step), and a code step is the quantization error the
+    method already accepts; so the GPU's distance from the int8 oracle is
+    bounded by the method's distance from binary32."""
+    return max(LOGIT_TOL, float(np.abs(logits_q8 - logits_f32).max()))

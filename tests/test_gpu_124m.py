@@ -1,5 +1,8 @@
 """GPU parity at the full GPT-2 124M shapes, in the launch configuration the
-benchmark times (one persistent launch per decode run, one CTA per SM)."""
+benchmark times (one persistent launch per decode run, one CTA per SM).
+
+The oracle runs first, on seeded inputs only; the GPU is then fed the same
+inputs (the oracle's greedy token sequence, seeded synthetic caches)."""
 import numpy as np
 import pytest
 
@@ -7,7 +10,8 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-from gpu_util import AGREE_MIN, GREEDY, LOGIT_TOL, run  # noqa: E402
+from gpu_util import (AGREE_MIN, GREEDY, LOGIT_TOL, disagreements_are_near_ties,  # noqa: E402
+                      greedy_agreement, int8_tolerance, oracle_greedy, run)
 from stream_decode_gb300 import synth  # noqa: E402
 
 
@@ -19,59 +23,81 @@ def g():
     return gpt2
 
 
-def _decode_run(g, oracle, w, quant):
-    """16 uniform random prompt tokens through cachedStep at positions 0..15,
-    then 112 greedy steps up to position 127, all in one launch; the oracle
-    recomputes every step on the GPU's token sequence."""
+@pytest.fixture(scope="module")
+def ref_f32(oracle, w124m):
+    """The oracle's greedy session: 16 uniform random prompt tokens at
+    positions 0..15, then 112 greedy steps up to position 127."""
     s = synth.GPT2_124M
-    toks = synth.tokens(s.vocab, 16)
-    model = g.Model(s, w, quant=quant)
-    sess = g.Session(model)
-    logits, ch = run(sess, list(toks) + [GREEDY] * 112, 128)
-    seq = np.concatenate([toks, ch[15:127]])
-    om = oracle.model(s, w, quant=quant)
-    ref, ref_ch, ref_cache = om.session(list(seq), 128)
-    cache = sess.read_cache()
+    om = oracle.model(s, w124m)
+    out = oracle_greedy(om, synth.tokens(s.vocab, 16), 128)
     om.close()
-    return logits, ch, ref, cache, ref_cache
+    return out
 
 
-def test_124m_f32_decode_128_positions(g, oracle, w124m):
-    logits, ch, ref, cache, ref_cache = _decode_run(g, oracle, w124m, 0)
+def test_124m_f32_decode_128_positions(g, w124m, ref_f32):
+    s = synth.GPT2_124M
+    seq, ref, ref_ch, ref_cache = ref_f32
+    model = g.Model(s, w124m)
+    logits, ch = run(g.Session(model), list(seq), 128)
     err = np.abs(logits - ref).max(axis=1)
     assert err.max() <= LOGIT_TOL, err.max()
-    assert np.mean(np.argmax(ref, 1) == ch) >= AGREE_MIN
+    assert greedy_agreement(ref, ch) >= AGREE_MIN
+    assert disagreements_are_near_ties(ref, ch, LOGIT_TOL)
+    sess = g.Session(model)
+    run(sess, list(seq), 128, want_logits=False)
+    cache = sess.read_cache()
     assert cache.size == 128 * 12 * 1536 and np.abs(cache - ref_cache).max() <= LOGIT_TOL
+    # device-side greedy feedback from the same prompt follows the oracle
+    _, gch = run(g.Session(model), list(seq[:16]) + [GREEDY] * 112, 128, want_logits=False)
+    d = np.nonzero(gch != ref_ch)[0]
+    if d.size:
+        top2 = np.sort(ref[d[0]])[-2:]
+        assert top2[1] - top2[0] <= LOGIT_TOL, f"greedy run left the oracle's path at step {d[0]}"
 
 
-def test_124m_int8_decode_128_positions(g, oracle, w124m):
-    logits, ch, ref, cache, ref_cache = _decode_run(g, oracle, w124m, 1)
+def test_124m_int8_decode_128_positions(g, oracle, w124m, ref_f32):
+    s = synth.GPT2_124M
+    om = oracle.model(s, w124m, quant=1)
+    seq, ref, ref_ch, _ = oracle_greedy(om, synth.tokens(s.vocab, 16), 128)
+    om.close()
+    of = oracle.model(s, w124m)
+    ref_f32_same, _, _ = of.session(list(seq), 128)
+    of.close()
+    tol = int8_tolerance(ref, ref_f32_same)
+    logits, ch = run(g.Session(g.Model(s, w124m, quant=1)), list(seq), 128)
     err = np.abs(logits - ref).max(axis=1)
-    assert err.max() <= LOGIT_TOL, err.max()
-    assert np.mean(np.argmax(ref, 1) == ch) >= AGREE_MIN
+    assert err.max() <= tol, (err.max(), tol)
+    assert disagreements_are_near_ties(ref, ch, tol)
+    print(f"int8: max|gpu-oracle| {err.max():.4g}, tolerance {tol:.4g}, "
+          f"greedy agreement {greedy_agreement(ref, ch):.3f}")
 
 
-def test_124m_long_context_positions(g, oracle, w124m):
-    """Cache of 1023 prior positions from 1023 uniform random tokens (built by
-    one GPU launch), then single steps at p = 128, 512, 1023 compared with the
-    oracle given the same cache prefix."""
+@pytest.mark.parametrize("quant", [0, 1], ids=["f32", "int8"])
+def test_124m_projections_on_identical_inputs(g, oracle, w124m, quant):
+    from test_gpu_decode import check_projections
+    L = 12
+    check_projections(g, oracle, synth.GPT2_124M, w124m, quant, [0, 1, 2, 3, 4 * 5 + 2, 4 * 11 + 3, 4 * L])
+
+
+@pytest.mark.parametrize("p", [128, 512, 1023])
+def test_124m_long_context_positions(g, oracle, w124m, p):
+    """A seeded synthetic cache of p prior positions (keys/values ~ N(0, 0.25),
+    the magnitude N(0,0.02) weights give), then one step at position p with
+    token = the p-th uniform random token, on both sides."""
     s = synth.GPT2_124M_LONG
-    toks = synth.tokens(s.vocab, 1024, seed=1234)
+    row = g.cache_words_per_position(s)
+    cache = synth.cache(s, p, seed=4242 + p)
+    tok = int(synth.tokens(s.vocab, 1024, seed=1234)[p])
+    om = oracle.model(s, w124m)
+    st, ol, ocache = om.cached_step(cache, tok, p)
+    om.close()
+    assert st == "ok"
     model = g.Model(s, w124m)
     sess = g.Session(model)
-    run(sess, list(toks[:1023]), 1023, want_logits=False)
-    full = sess.read_cache()
-    row = g.cache_words_per_position(s)
-    om = oracle.model(s, w124m)
-    for p in (128, 512, 1023):
-        prefix = full[:p * row]
-        st, ol, ocache = om.cached_step(prefix, int(toks[p]), p)
-        assert st == "ok"
-        s2 = g.Session(model)
-        assert s2.load_cache(prefix) == "ok"
-        lg, ch = run(s2, [int(toks[p])], 1)
-        assert np.abs(lg[0] - ol).max() <= LOGIT_TOL, p
-        assert ch[0] == np.argmax(ol) or abs(np.sort(ol)[-1] - np.sort(ol)[-2]) < LOGIT_TOL
-        newrow = s2.read_cache()[p * row:]
-        assert np.abs(newrow - ocache[p * row:]).max() <= LOGIT_TOL
-    om.close()
+    assert sess.load_cache(cache) == "ok"
+    lg, ch = run(sess, [tok], 1)
+    assert np.abs(lg[0] - ol).max() <= LOGIT_TOL
+    assert disagreements_are_near_ties(ol[None], ch, LOGIT_TOL)
+    out = sess.read_cache()
+    assert np.array_equal(out[:p * row].view(np.uint32), cache.view(np.uint32))
+    assert np.abs(out[p * row:] - ocache[p * row:]).max() <= LOGIT_TOL
