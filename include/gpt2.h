@@ -53,7 +53,8 @@ typedef enum gpt2_status {
     GPT2_ERR_NOMEM = 8,       /* a device or host allocation failed */
     GPT2_ERR_TIMEOUT = 9,     /* a device-side wait exceeded its limit; the run was abandoned */
     GPT2_ERR_CUDA = 10,       /* a CUDA runtime call failed */
-    GPT2_ERR_ARG = 11         /* a NULL pointer or an out-of-range argument */
+    GPT2_ERR_ARG = 11,        /* a NULL pointer or an out-of-range argument */
+    GPT2_ERR_SCRATCH = 12     /* the call needs more scratch than gpt2_cached_step_noalloc's static area */
 } gpt2_status;
 
 typedef enum gpt2_quant {
@@ -184,6 +185,39 @@ gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
  * GPT2_ERR_TIMEOUT (no GPU fault, no hang).  wait_limit_ns bounds every
  * device-side wait of that run. */
 gpt2_status gpt2_session_inject_stall(gpt2_session* session, uint32_t phase, uint64_t wait_limit_ns);
+
+/* gpt2_cached_step_noalloc -- one cached step that allocates nothing.
+ * The pages have no counterpart: this entry exists for callers that may not
+ * allocate device memory while they run steps.  Examples are a plug-in or
+ * embedded runtime whose host framework owns every device allocation within
+ * a fixed budget, and a latency-critical loop that cannot afford cudaMalloc,
+ * which may synchronise the device.  The caller still passes every input and
+ * output:
+ *   model         created once beforehand with gpt2_model_create;
+ *   d_cache       caller-owned device KV cache in the cachedStep layout
+ *                 above, holding positions 0..position-1, with room for
+ *                 position+1 positions; this step's keys and values are
+ *                 written at position `position`;
+ *   token         this step's token id (< vocab; GPT2_TOKEN_GREEDY is
+ *                 rejected);
+ *   d_logits      device output of vocab floats, or NULL;
+ *   d_next_token  device output of the greedy choice, or NULL; it reads
+ *                 0xFFFFFFFF after the step if a logit was not finite or the
+ *                 step gave up on a device-side wait.
+ * The step kernel's scratch is a file-scope static device array of 256 KiB
+ * (GPT-2 124M on 152 CTAs uses about 70 KB).  Every GPU that loads the
+ * library holds it until the process exits.  A model whose scratch would
+ * not fit is rejected with GPT2_ERR_SCRATCH before any device work.  The
+ * first call on each device looks the array's device address up (once, with
+ * that device current); make that first call before any stream capture.
+ * No call allocates: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  All calls share the one array, and it keeps the previous call's
+ * contents.  Each call clears, on `stream`, what must start at zero (phase
+ * flags, status words).  Calls that overlap on the GPU race on the array:
+ * order them on one stream, or otherwise serialize them.  Enqueued on
+ * `stream`; host-side checks: model, d_cache, token, position < max_pos. */
+gpt2_status gpt2_cached_step_noalloc(const gpt2_model* model, float* d_cache, uint32_t position, uint32_t token,
+                                     float* d_logits, uint32_t* d_next_token, void* stream);
 
 /* Test hook: applies projection `index` of the model (index convention of
  * gpt2_model_read_q8; the vocabulary projection has no bias) to the device

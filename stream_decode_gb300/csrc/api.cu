@@ -10,6 +10,7 @@
 
 #include "../../include/gpt2.h"
 #include "gpt2_dev.cuh"
+#include "model_internal.h"
 
 namespace gpt2 {
 cudaError_t launch_step(const StepPlan& P, bool q8, cudaStream_t stream);
@@ -23,19 +24,6 @@ cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfin
 }  // namespace gpt2
 
 using namespace gpt2;
-
-struct gpt2_model {
-    gpt2_config cfg;
-    int quant;
-    int G;
-    float* d_packed;
-    uint8_t* d_wstream;
-    uint8_t* d_vocab_q8;
-    uint64_t layer_bytes;
-    uint64_t mat_off[4];
-    uint64_t wte_off, wpe_off, lnf_g, lnf_b;
-    LayerParams lp[kMaxLayers];
-};
 
 struct gpt2_session {
     gpt2_model* m;
@@ -187,6 +175,7 @@ const char* gpt2_status_name(gpt2_status st) {
         case GPT2_ERR_TIMEOUT: return "timeout";
         case GPT2_ERR_CUDA: return "cuda";
         case GPT2_ERR_ARG: return "arg";
+        case GPT2_ERR_SCRATCH: return "scratch";
     }
     return "unknown";
 }

@@ -1,0 +1,20 @@
+// model_internal.h -- the device-resident model handle shared by the
+// library's translation units.
+#pragma once
+#include <cstdint>
+
+#include "../../include/gpt2.h"
+#include "gpt2_dev.cuh"
+
+struct gpt2_model {
+    gpt2_config cfg;
+    int quant;
+    int G;
+    float* d_packed;
+    uint8_t* d_wstream;
+    uint8_t* d_vocab_q8;
+    uint64_t layer_bytes;
+    uint64_t mat_off[4];
+    uint64_t wte_off, wpe_off, lnf_g, lnf_b;
+    gpt2::LayerParams lp[gpt2::kMaxLayers];
+};

@@ -1,0 +1,158 @@
+// noalloc.cu -- gpt2_cached_step_noalloc: one cached decode step that
+// allocates no device memory.
+//
+// Who needs it: callers that may not allocate device memory while they run
+// steps.  Some host frameworks own every device allocation themselves (a
+// plug-in or an embedded runtime with a fixed, pre-reserved memory budget).
+// Some latency-critical loops cannot afford cudaMalloc, which may
+// synchronise the device and has no latency bound.  Such a caller creates
+// the model once at start-up, keeps its own KV-cache, logits and token
+// buffers, and steps with this entry point, which needs nothing else.
+//
+// The step kernel's scratch (activation vectors, attention partials, greedy
+// partials, per-CTA phase flags, status words) lives in the file-scope
+// array `g_step_scratch` below, of kScratchMax bytes; every GPU that loads
+// the library holds that array until the process exits.  Host code may not
+// pass the symbol itself to a kernel: on the host it names a stand-in, not
+// the device array, so a kernel given it would fault or, where the GPU can
+// reach host memory, silently use the wrong memory.  The device address is
+// fetched once per device with cudaGetSymbolAddress, with that device
+// current, on the first call made on it.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gpt2.h"
+#include "gpt2_dev.cuh"
+#include "model_internal.h"
+
+namespace gpt2 {
+cudaError_t launch_step(const StepPlan& P, bool q8, cudaStream_t stream);
+}
+
+using namespace gpt2;
+
+namespace {
+
+// Largest scratch one call may use (GPT-2 124M on 152 CTAs needs about 70 KB).
+constexpr size_t kScratchMax = 256 * 1024;
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __align__(256) unsigned char g_step_scratch[kScratchMax];
+
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte offsets of the step kernel's scratch inside one contiguous area.
+struct Carve {
+    size_t xa, xb, qkv, u, attn_part, arg_part, flags, words, last_token, total;
+};
+
+Carve carve(const gpt2_config& c, int G) {
+    const size_t D = c.d_model, FF = c.d_ff, H = c.n_head, DH = D / H;
+    const size_t S = (size_t)G >= H ? (size_t)G / H : 1;
+    Carve k{};
+    size_t o = 0;
+    k.flags = o; o = up256(o + 4 * (size_t)G);
+    k.words = o; o = up256(o + 4 * 4);
+    k.last_token = o; o = up256(o + 4 * 2);
+    k.xa = o; o = up256(o + 4 * D);
+    k.xb = o; o = up256(o + 4 * D);
+    k.qkv = o; o = up256(o + 4 * 3 * D);
+    k.u = o; o = up256(o + 4 * FF);
+    k.attn_part = o; o = up256(o + 4 * H * S * (DH + 2));
+    k.arg_part = o; o = up256(o + 4 * 4 * (size_t)G);
+    k.total = o;
+    return k;
+}
+
+// Device address of g_step_scratch on the current device (set up once per device).
+gpt2_status scratch_base(unsigned char** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return GPT2_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_step_scratch);
+        if (e != cudaSuccess || !p) return GPT2_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(g_scratch_addr[dev]);
+    return GPT2_OK;
+}
+
+}  // namespace
+
+extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_cache, uint32_t position,
+                                                uint32_t token, float* d_logits, uint32_t* d_next_token,
+                                                void* stream) {
+    if (!m || !d_cache) return GPT2_ERR_ARG;
+    const gpt2_config& c = m->cfg;
+    if (token >= c.vocab) return GPT2_ERR_TOKEN;
+    if (position >= c.max_pos) return GPT2_ERR_POSITION;
+    const Carve k = carve(c, m->G);
+    if (k.total > kScratchMax) return GPT2_ERR_SCRATCH;
+    unsigned char* base = nullptr;
+    gpt2_status st = scratch_base(&base);
+    if (st != GPT2_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // The array keeps the previous call's contents: phase flags and status
+    // words must start at zero, the greedy history empty.
+    cudaError_t e = cudaMemsetAsync(base + k.flags, 0, k.last_token - k.flags, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + k.last_token, 0xFF, 8, s);
+    if (e == cudaSuccess && d_next_token) e = cudaMemsetAsync(d_next_token, 0xFF, 4, s);
+    if (e != cudaSuccess) return GPT2_ERR_CUDA;
+
+    StepPlan P;
+    memset(&P, 0, sizeof(P));
+    P.L = (int)c.n_layer;
+    P.D = (int)c.d_model;
+    P.H = (int)c.n_head;
+    P.FF = (int)c.d_ff;
+    P.V = (int)c.vocab;
+    P.n_pos = (int)c.n_pos;
+    P.max_pos = (int)c.max_pos;
+    P.G = m->G;
+    P.packed = m->d_packed;
+    P.wstream = m->d_wstream;
+    P.layer_bytes = m->layer_bytes;
+    for (int i = 0; i < 4; ++i) P.mat_off[i] = m->mat_off[i];
+    P.vocab = m->quant ? m->d_vocab_q8 : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
+    P.wte_off = m->wte_off;
+    P.wpe_off = m->wpe_off;
+    P.lnf_g = m->lnf_g;
+    P.lnf_b = m->lnf_b;
+    for (uint32_t l = 0; l < c.n_layer; ++l) P.lp[l] = m->lp[l];
+    P.cache = d_cache;
+    P.xa = reinterpret_cast<float*>(base + k.xa);
+    P.xb = reinterpret_cast<float*>(base + k.xb);
+    P.qkv = reinterpret_cast<float*>(base + k.qkv);
+    P.u = reinterpret_cast<float*>(base + k.u);
+    P.attn_part = reinterpret_cast<float*>(base + k.attn_part);
+    P.arg_part = reinterpret_cast<float*>(base + k.arg_part);
+    P.flags = reinterpret_cast<unsigned*>(base + k.flags);
+    P.status = reinterpret_cast<int*>(base + k.words);
+    P.abort_flag = reinterpret_cast<int*>(base + k.words) + 1;
+    P.last_token = reinterpret_cast<uint32_t*>(base + k.last_token);
+    P.epoch = 0;
+    P.p0 = (int)position;
+    P.n_steps = 1;
+    P.tokens_in = nullptr;
+    P.token0 = token;
+    P.tokens_out = d_next_token;
+    P.logits = d_logits;
+    P.logits_stride = 0;
+    P.trace = nullptr;
+    P.wait_limit_ns = kWaitNs;
+    P.stall_phase = -1;
+    P.prefetch_chunks = 0;
+    e = launch_step(P, m->quant == GPT2_INT8_G64, s);
+    return e == cudaSuccess ? GPT2_OK : (e == cudaErrorMemoryAllocation ? GPT2_ERR_NOMEM : GPT2_ERR_CUDA);
+}

@@ -23,7 +23,7 @@ lib = C.CDLL(_LIB_PATH)
 GREEDY = 0xFFFFFFFF
 F32, INT8_G64 = 0, 1
 STATUS = {0: "ok", 1: "weights_len", 2: "token", 3: "position", 4: "cache_len", 5: "tokens_len",
-          6: "nonfinite", 7: "config", 8: "nomem", 9: "timeout", 10: "cuda", 11: "arg"}
+          6: "nonfinite", 7: "config", 8: "nomem", 9: "timeout", 10: "cuda", 11: "arg", 12: "scratch"}
 
 
 class Config(C.Structure):
@@ -59,6 +59,7 @@ _SIGS = {
     "gpt2_session_inject_stall": ([_vp, _u32, C.c_uint64], _i32),
     "gpt2_debug_project": ([_vp, _i32, _vp, _vp, _vp], _i32),
     "gpt2_debug_argmax": ([_vp, _u32, _vp, _vp, _vp], _i32),
+    "gpt2_cached_step_noalloc": ([_vp, _vp, _u32, _u32, _vp, _vp, _vp], _i32),
     "gpt2_status_name": ([_i32], C.c_char_p),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -151,6 +152,14 @@ class Model:
     def debug_project(self, index: int, x, y, stream=None) -> str:
         """Test hook: projection `index` of x (CUDA tensor) into y (CUDA tensor)."""
         return STATUS[lib.gpt2_debug_project(self.h, index, _ptr(x), _ptr(y), _stream(stream))]
+
+    def cached_step_noalloc(self, cache, position: int, token: int, logits=None, next_token=None,
+                            stream=None) -> str:
+        """One step that allocates nothing (gpt2_cached_step_noalloc): `cache`
+        is a caller-owned CUDA tensor in the cachedStep layout with room for
+        position + 1 positions; logits / next_token are CUDA tensors or None."""
+        return STATUS[lib.gpt2_cached_step_noalloc(self.h, _ptr(cache), position, token, _ptr(logits),
+                                                   _ptr(next_token), _stream(stream))]
 
     def close(self):
         if getattr(self, "h", None):

@@ -1,0 +1,89 @@
+"""gpt2_cached_step_noalloc: the cached step for callers that may not
+allocate device memory while stepping (their host framework owns every
+device allocation, or the loop cannot afford cudaMalloc's device-wide
+synchronisation).  Its scratch lives in a static device array inside the
+library; the caller passes the model, its own KV cache and output buffers.
+
+The check: several calls in a row through the C ABI give the same logits,
+greedy choices and cache as the session entry point (gpt2_session_step)
+within the logit tolerance the other tests use.  This file is collected last
+so that a failure here comes after every other test has run; it also passes
+alone in a fresh process.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+from gpu_util import LOGIT_TOL  # noqa: E402
+from stream_decode_gb300 import synth  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from stream_decode_gb300 import gpt2
+    return gpt2
+
+
+def _compare(g, shape, w, quant, n_calls=4):
+    model = g.Model(shape, w, quant=quant)
+    V, row = shape.vocab, g.cache_words_per_position(shape)
+    toks = [int(t) for t in synth.tokens(V, n_calls, seed=77)]
+
+    # existing entry point: a session, one gpt2_session_step per position
+    sess = g.Session(model)
+    ref_logits, ref_next = [], []
+    d_logits = torch.empty(V, dtype=torch.float32, device="cuda")
+    d_next = torch.empty(1, dtype=torch.int32, device="cuda")
+    for t in toks:
+        assert sess.step(t, d_logits, d_next) == "ok"
+        assert sess.sync() == "ok"
+        ref_logits.append(d_logits.cpu().numpy().copy())
+        ref_next.append(int(d_next.item()) & 0xFFFFFFFF)
+    ref_cache = sess.read_cache()
+
+    # the no-allocation entry point, caller-owned buffers, calls in a row
+    cache = torch.zeros(shape.max_pos * row, dtype=torch.float32, device="cuda")
+    out = torch.empty(V, dtype=torch.float32, device="cuda")
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    for p, t in enumerate(toks):
+        out.fill_(float("nan"))
+        assert model.cached_step_noalloc(cache, p, t, out, nxt) == "ok"
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        assert np.abs(got - ref_logits[p]).max() <= LOGIT_TOL, f"call {p}"
+        assert (int(nxt.item()) & 0xFFFFFFFF) == ref_next[p], f"call {p}"
+    got_cache = cache[:n_calls * row].cpu().numpy()
+    assert np.abs(got_cache - ref_cache).max() <= LOGIT_TOL
+    sess.close()
+    model.close()
+
+
+def test_noalloc_matches_session_step_tiny(g):
+    shape = synth.GPT2_TINY
+    _compare(g, shape, synth.checkpoint(shape, synth.SEED_TINY, "rich"), g.F32)
+
+
+def test_noalloc_matches_session_step_124m(g, w124m):
+    _compare(g, synth.GPT2_124M, w124m, g.F32, n_calls=3)
+
+
+def test_noalloc_matches_session_step_int8(g):
+    shape = synth.GPT2_TINY
+    _compare(g, shape, synth.checkpoint(shape, synth.SEED_TINY, "rich"), g.INT8_G64)
+
+
+def test_noalloc_rejects_bad_arguments(g):
+    shape = synth.GPT2_TINY
+    model = g.Model(shape, synth.checkpoint(shape, synth.SEED_TINY))
+    row = g.cache_words_per_position(shape)
+    cache = torch.zeros(shape.max_pos * row, dtype=torch.float32, device="cuda")
+    assert model.cached_step_noalloc(cache, 0, g.GREEDY) == "token"
+    assert model.cached_step_noalloc(cache, 0, shape.vocab) == "token"
+    assert model.cached_step_noalloc(cache, shape.max_pos, 1) == "position"
+    assert g.STATUS[g.lib.gpt2_cached_step_noalloc(model.h, None, 0, 1, None, None, None)] == "arg"
+    model.close()
