@@ -180,6 +180,16 @@ gpt2_status gpt2_session_sync(gpt2_session* session);
  * x_final[d], LN_f(x_final)[d].  Pass NULL to stop tracing. */
 gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
 
+/* Profiling: enqueue the next run with phase timestamps.  d_stamps
+ * (device, (5*n_layer+1) * grid_ctas * 8 u64) receives, for step 0 of that
+ * run, per phase and CTA: the device globaltimer (ns) when the CTA started
+ * the phase, when its inputs were complete and when its outputs were stored;
+ * then the SM's clock64 at the start, at inputs complete, when its input
+ * transform (LayerNorm / head merge) was done, when its first weight chunk of
+ * the phase had landed, and when its outputs were stored.  Pass NULL to
+ * stop. */
+gpt2_status gpt2_session_set_timing(gpt2_session* session, uint64_t* d_stamps);
+
 /* Debug/test: make the next run's CTA 0 skip publishing one phase so that
  * the other CTAs' bounded waits expire and the run ends with
  * GPT2_ERR_TIMEOUT (no GPU fault, no hang).  wait_limit_ns bounds every
@@ -233,6 +243,10 @@ gpt2_status gpt2_debug_project(gpt2_model* model, int index, const float* d_x, f
  * infinite.  Enqueued on `stream`. */
 gpt2_status gpt2_debug_argmax(const float* d_values, uint32_t n, uint32_t* d_index, int* d_nonfinite,
                               void* stream);
+
+/* The CUDA runtime error behind the most recent GPT2_ERR_CUDA / NOMEM of
+ * this process (0 if none), and its name (e.g. "cudaErrorIllegalAddress"). */
+int gpt2_last_cuda_error(const char** name);
 
 /* Human-readable status name ("ok", "token", ...). */
 const char* gpt2_status_name(gpt2_status status);

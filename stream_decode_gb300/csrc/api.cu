@@ -28,9 +28,8 @@ using namespace gpt2;
 struct gpt2_session {
     gpt2_model* m;
     float* d_cache;
-    float* d_scratch;
-    float *xa, *xb, *qkv, *u, *attn_part, *arg_part;
-    unsigned* d_flags;
+    unsigned char* d_scratch;  // ScratchLayout: status words, last token, tagged exchange buffers
+    ScratchLayout lay;
     int* d_words;  // [0] status, [1] abort
     uint32_t* d_last_token;
     float* d_logits;       // session-owned logits for gpt2_session_step_host
@@ -40,6 +39,7 @@ struct gpt2_session {
     unsigned epoch;
     uint32_t position;
     float* trace_next;
+    uint64_t* timing_next;
     int stall_phase;
     uint64_t wait_limit_ns;
 };
@@ -64,8 +64,11 @@ bool config_ok(const gpt2_config* c) {
     return step_shape_supported((int)c->d_model, (int)c->d_ff, (int)(c->d_model / c->n_head));
 }
 
+int g_last_cuda_error = 0;
+
 gpt2_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return GPT2_OK;
+    g_last_cuda_error = (int)e;
     if (e == cudaErrorMemoryAllocation) return GPT2_ERR_NOMEM;
     return GPT2_ERR_CUDA;
 }
@@ -102,13 +105,12 @@ void fill_plan(const gpt2_session* s, StepPlan& P) {
     P.lnf_b = m->lnf_b;
     for (uint32_t l = 0; l < c.n_layer; ++l) P.lp[l] = m->lp[l];
     P.cache = s->d_cache;
-    P.xa = s->xa;
-    P.xb = s->xb;
-    P.qkv = s->qkv;
-    P.u = s->u;
-    P.attn_part = s->attn_part;
-    P.arg_part = s->arg_part;
-    P.flags = s->d_flags;
+    P.xa = reinterpret_cast<uint64_t*>(s->d_scratch + s->lay.xa);
+    P.xb = reinterpret_cast<uint64_t*>(s->d_scratch + s->lay.xb);
+    P.qkv = reinterpret_cast<uint64_t*>(s->d_scratch + s->lay.qkv);
+    P.u = reinterpret_cast<uint64_t*>(s->d_scratch + s->lay.u);
+    P.attn_part = reinterpret_cast<uint64_t*>(s->d_scratch + s->lay.attn);
+    P.arg_part = reinterpret_cast<uint64_t*>(s->d_scratch + s->lay.arg);
     P.status = s->d_words;
     P.abort_flag = s->d_words + 1;
     P.last_token = s->d_last_token;
@@ -126,7 +128,8 @@ gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t t
     fill_plan(s, P);
     const unsigned need = n_steps * phases_per_step(s->m);
     if (s->epoch > (1u << 30)) {
-        cudaError_t e = cudaMemsetAsync(s->d_flags, 0, sizeof(unsigned) * s->m->G, stream);
+        // tags restart: clear every exchanged word so no stale tag can match
+        cudaError_t e = cudaMemsetAsync(s->d_scratch + s->lay.xa, 0, s->lay.total - s->lay.xa, stream);
         if (e != cudaSuccess) return cuda_status(e);
         s->epoch = 0;
     }
@@ -139,6 +142,7 @@ gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t t
     P.logits = d_logits;
     P.logits_stride = stride;
     P.trace = s->trace_next;
+    P.timing = s->timing_next;
     P.stall_phase = s->stall_phase;
     if (s->stall_phase >= 0) P.wait_limit_ns = s->wait_limit_ns;
     const char* pf = getenv("GPT2_PREFETCH_CHUNKS");
@@ -146,6 +150,7 @@ gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t t
     cudaError_t e = launch_step(P, s->m->quant == GPT2_INT8_G64, stream);
     if (e != cudaSuccess) return cuda_status(e);
     s->trace_next = nullptr;
+    s->timing_next = nullptr;
     s->stall_phase = -1;
     s->epoch += need;
     s->position += n_steps;
@@ -160,6 +165,11 @@ extern "C" {
 size_t gpt2_weight_words(const gpt2_config* cfg) { return cfg ? words_of(cfg) : 0; }
 
 size_t gpt2_cache_words_per_position(const gpt2_config* cfg) { return cfg ? row_words(cfg) : 0; }
+
+int gpt2_last_cuda_error(const char** name) {
+    if (name) *name = cudaGetErrorName((cudaError_t)g_last_cuda_error);
+    return g_last_cuda_error;
+}
 
 const char* gpt2_status_name(gpt2_status st) {
     switch (st) {
@@ -300,24 +310,13 @@ gpt2_status gpt2_session_create(gpt2_model* m, gpt2_session** out) {
     s->stall_phase = -1;
     {
         const gpt2_config& c = m->cfg;
-        const size_t D = c.d_model, FF = c.d_ff, H = c.n_head, DH = D / H;
-        const size_t S = (size_t)m->G >= H ? (size_t)m->G / H : 1;
-        const size_t n_scratch = D + D + 3 * D + FF + H * S * (DH + 2) + (size_t)m->G * 4;
+        s->lay = scratch_layout((int)c.d_model, (int)c.n_head, (int)c.d_ff, m->G);
         CK(cudaMalloc(&s->d_cache, sizeof(float) * row_words(&c) * c.max_pos));
         CK(cudaMemset(s->d_cache, 0, sizeof(float) * row_words(&c) * c.max_pos));
-        CK(cudaMalloc(&s->d_scratch, sizeof(float) * n_scratch));
-        CK(cudaMemset(s->d_scratch, 0, sizeof(float) * n_scratch));
-        s->xa = s->d_scratch;
-        s->xb = s->xa + D;
-        s->qkv = s->xb + D;
-        s->u = s->qkv + 3 * D;
-        s->attn_part = s->u + FF;
-        s->arg_part = s->attn_part + H * S * (DH + 2);
-        CK(cudaMalloc(&s->d_flags, sizeof(unsigned) * m->G));
-        CK(cudaMemset(s->d_flags, 0, sizeof(unsigned) * m->G));
-        CK(cudaMalloc(&s->d_words, sizeof(int) * 4));
-        CK(cudaMemset(s->d_words, 0, sizeof(int) * 4));
-        CK(cudaMalloc(&s->d_last_token, sizeof(uint32_t) * 2));
+        CK(cudaMalloc(&s->d_scratch, s->lay.total));
+        CK(cudaMemset(s->d_scratch, 0, s->lay.total));
+        s->d_words = reinterpret_cast<int*>(s->d_scratch + s->lay.words);
+        s->d_last_token = reinterpret_cast<uint32_t*>(s->d_scratch + s->lay.last_token);
         CK(cudaMemset(s->d_last_token, 0xFF, sizeof(uint32_t) * 2));
         CK(cudaMalloc(&s->d_logits, sizeof(float) * c.vocab));
         CK(cudaMalloc(&s->d_next, sizeof(uint32_t)));
@@ -336,9 +335,6 @@ void gpt2_session_destroy(gpt2_session* s) {
     if (s->last) cudaStreamSynchronize(s->last);
     cudaFree(s->d_cache);
     cudaFree(s->d_scratch);
-    cudaFree(s->d_flags);
-    cudaFree(s->d_words);
-    cudaFree(s->d_last_token);
     cudaFree(s->d_logits);
     cudaFree(s->d_next);
     if (s->own) cudaStreamDestroy(s->own);
@@ -356,9 +352,9 @@ gpt2_status gpt2_session_sync(gpt2_session* s) {
     e = cudaMemcpy(words, s->d_words, sizeof(words), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_status(e);
     if (words[0] == 0 && words[1] == 0) return GPT2_OK;
-    // A failed run leaves the flags mid-sequence: start a fresh epoch.
+    // A failed run leaves exchanged words mid-sequence: clear them and restart the tags.
     e = cudaMemset(s->d_words, 0, sizeof(int) * 4);
-    if (e == cudaSuccess) e = cudaMemset(s->d_flags, 0, sizeof(unsigned) * s->m->G);
+    if (e == cudaSuccess) e = cudaMemset(s->d_scratch + s->lay.xa, 0, s->lay.total - s->lay.xa);
     if (e != cudaSuccess) return cuda_status(e);
     s->epoch = 0;
     return words[0] ? (gpt2_status)words[0] : GPT2_ERR_TIMEOUT;
@@ -432,6 +428,12 @@ gpt2_status gpt2_session_step_host(gpt2_session* s, uint32_t token, float* logit
 gpt2_status gpt2_session_set_trace(gpt2_session* s, float* d_trace) {
     if (!s) return GPT2_ERR_ARG;
     s->trace_next = d_trace;
+    return GPT2_OK;
+}
+
+gpt2_status gpt2_session_set_timing(gpt2_session* s, uint64_t* d_stamps) {
+    if (!s) return GPT2_ERR_ARG;
+    s->timing_next = d_stamps;
     return GPT2_OK;
 }
 

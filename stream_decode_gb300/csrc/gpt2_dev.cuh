@@ -1,6 +1,6 @@
 // gpt2_dev.cuh -- device-side definitions shared by the library's kernels:
-// the step plan, the device weight-stream geometry and inline-PTX wrappers
-// (mbarrier, bulk copies, release/acquire flags).
+// the step plan, the device weight-stream geometry, the scratch layout and
+// inline-PTX wrappers (mbarrier, bulk copies, tagged words).
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -10,7 +10,11 @@ namespace gpt2 {
 
 // ---------------------------------------------------------------- constants
 constexpr int kGroup = 64;          // int8 group size (quantized GPT-2 abstract)
-constexpr int kConsumerWarps = 8;   // warps that compute
+// Seven consumer warps plus the producer: at most two warps per SM
+// sub-partition, so every thread may hold up to 255 registers (three warps
+// on one sub-partition would cap it at 168 and spill into local memory,
+// which has almost no L1 left beside the 220+ KB of shared memory).
+constexpr int kConsumerWarps = 7;   // warps that compute
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kSlotBytes = 12288;   // one ring slot (one 3072-float row)
 constexpr int kSlots = 16;          // ring depth: 192 KiB of weights in flight per SM
@@ -35,6 +39,47 @@ struct LayerParams {
 
 constexpr int kMaxLayers = 16;
 
+constexpr int kMaxSplits = 8;   // key-axis splits per attention head
+constexpr int kMaxGrid = kConsumerWarps * 32;  // CTAs of the step kernel (one per SM on GB300: 152)
+
+// Key-axis splits per head for a grid of G CTAs and H heads.
+__host__ __device__ inline int attn_splits(int G, int H) {
+    int s = G >= H ? G / H : 1;
+    return s > kMaxSplits ? kMaxSplits : s;
+}
+
+// Splits used at a given number of keys: one per 56 keys (the two passes of
+// 7 warps x 4 keys that a unit loads before waiting for q), at most `cap`.
+constexpr int kKeysPerSplit = 56;
+__host__ __device__ inline int attn_splits_for(int keys, int cap) {
+    const int s = (keys + kKeysPerSplit - 1) / kKeysPerSplit;
+    return s < 1 ? 1 : (s > cap ? cap : s);
+}
+
+// Scratch of one step-kernel run, as byte offsets in one contiguous area.
+// Every exchanged value is a 64-bit tagged word (float bits | tag << 32).
+struct ScratchLayout {
+    size_t words, last_token, xa, xb, qkv, u, attn, arg, total;
+};
+
+__host__ __device__ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline ScratchLayout scratch_layout(int D, int H, int FF, int G) {
+    const size_t DH = (size_t)(D / H), units = (size_t)H * attn_splits(G, H);
+    ScratchLayout k{};
+    size_t o = 0;
+    k.words = o; o = up256(o + 4 * 4);
+    k.last_token = o; o = up256(o + 4 * 2);
+    k.xa = o; o = up256(o + 8 * (size_t)D);
+    k.xb = o; o = up256(o + 8 * (size_t)D);
+    k.qkv = o; o = up256(o + 8 * 3 * (size_t)D);
+    k.u = o; o = up256(o + 8 * (size_t)FF);
+    k.attn = o; o = up256(o + 8 * units * (DH + 2));
+    k.arg = o; o = up256(o + 8 * 2 * (size_t)G);
+    k.total = o;
+    return k;
+}
+
 // Everything one launch of the step kernel needs.  Passed by value.
 struct StepPlan {
     // shape
@@ -48,16 +93,15 @@ struct StepPlan {
     const uint8_t* vocab;       // vocab rows (fp32: wte in the packed checkpoint; int8: q rows + scales)
     uint64_t wte_off, wpe_off, lnf_g, lnf_b;  // word offsets in packed
     LayerParams lp[kMaxLayers];
-    // session buffers
+    // session buffers (tagged words: value bits | tag << 32)
     float* cache;               // [max_pos][L][2D]
-    float* xa;                  // [D] residual stream after a block
-    float* xb;                  // [D] residual stream after attention
-    float* qkv;                 // [3D]
-    float* u;                   // [FF]
-    float* attn_part;           // [H * S][2 + DH]
-    float* arg_part;            // [G][4]
-    unsigned* flags;            // [G] published phase numbers
-    unsigned epoch;             // phase numbers of this run start above this
+    uint64_t* xa;               // [D] residual stream after a block
+    uint64_t* xb;               // [D] residual stream after attention
+    uint64_t* qkv;              // [3D]
+    uint64_t* u;                // [FF]
+    uint64_t* attn_part;        // [H * S][2 + DH]: max, sum, unnormalised o
+    uint64_t* arg_part;         // [G][2]: best value, index | nonfinite << 31
+    unsigned epoch;             // tags of this run start above this
     int* status;                // sticky device status
     int* abort_flag;            // set by any CTA that gives up
     uint32_t* last_token;       // the session's last greedy choice
@@ -69,6 +113,7 @@ struct StepPlan {
     float* logits;              // or null
     uint64_t logits_stride;     // floats between steps' logits
     float* trace;               // or null
+    uint64_t* timing;           // or null: [phase of step 0][G][3] globaltimer stamps
     // robustness
     uint64_t wait_limit_ns;     // bound of every spin-wait
     int stall_phase;            // test: CTA 0 skips publishing this phase (-1 = none)
@@ -148,6 +193,31 @@ __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Tagged words: one single-copy-atomic 64-bit access carries a value and
+// the number of the phase that produced it.
+__device__ __forceinline__ uint64_t tag_pack(unsigned tag, float v) {
+    return ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+}
+__device__ __forceinline__ unsigned tag_of(uint64_t w) { return (unsigned)(w >> 32); }
+__device__ __forceinline__ float val_of(uint64_t w) { return __uint_as_float((unsigned)w); }
+
+__device__ __forceinline__ void st_tagged(uint64_t* p, unsigned tag, float v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(tag_pack(tag, v)) : "memory");
+}
+__device__ __forceinline__ void st_tagged_release(uint64_t* p, uint64_t w) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t ld_tagged_acquire(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 

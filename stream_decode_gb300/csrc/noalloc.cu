@@ -10,7 +10,7 @@
 // buffers, and steps with this entry point, which needs nothing else.
 //
 // The step kernel's scratch (activation vectors, attention partials, greedy
-// partials, per-CTA phase flags, status words) lives in the file-scope
+// partials as tagged exchange words, status words) lives in the file-scope
 // array `g_step_scratch` below, of kScratchMax bytes; every GPU that loads
 // the library holds that array until the process exits.  Host code may not
 // pass the symbol itself to a kernel: on the host it names a stand-in, not
@@ -45,31 +45,6 @@ __device__ __align__(256) unsigned char g_step_scratch[kScratchMax];
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
-size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// Byte offsets of the step kernel's scratch inside one contiguous area.
-struct Carve {
-    size_t xa, xb, qkv, u, attn_part, arg_part, flags, words, last_token, total;
-};
-
-Carve carve(const gpt2_config& c, int G) {
-    const size_t D = c.d_model, FF = c.d_ff, H = c.n_head, DH = D / H;
-    const size_t S = (size_t)G >= H ? (size_t)G / H : 1;
-    Carve k{};
-    size_t o = 0;
-    k.flags = o; o = up256(o + 4 * (size_t)G);
-    k.words = o; o = up256(o + 4 * 4);
-    k.last_token = o; o = up256(o + 4 * 2);
-    k.xa = o; o = up256(o + 4 * D);
-    k.xb = o; o = up256(o + 4 * D);
-    k.qkv = o; o = up256(o + 4 * 3 * D);
-    k.u = o; o = up256(o + 4 * FF);
-    k.attn_part = o; o = up256(o + 4 * H * S * (DH + 2));
-    k.arg_part = o; o = up256(o + 4 * 4 * (size_t)G);
-    k.total = o;
-    return k;
-}
-
 // Device address of g_step_scratch on the current device (set up once per device).
 gpt2_status scratch_base(unsigned char** out) {
     int dev = 0;
@@ -96,16 +71,18 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     const gpt2_config& c = m->cfg;
     if (token >= c.vocab) return GPT2_ERR_TOKEN;
     if (position >= c.max_pos) return GPT2_ERR_POSITION;
-    const Carve k = carve(c, m->G);
+    const ScratchLayout k = scratch_layout((int)c.d_model, (int)c.n_head, (int)c.d_ff, m->G);
     if (k.total > kScratchMax) return GPT2_ERR_SCRATCH;
     unsigned char* base = nullptr;
     gpt2_status st = scratch_base(&base);
     if (st != GPT2_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // The array keeps the previous call's contents: phase flags and status
-    // words must start at zero, the greedy history empty.
-    cudaError_t e = cudaMemsetAsync(base + k.flags, 0, k.last_token - k.flags, s);
+    // The array keeps the previous call's contents.  Every call numbers its
+    // phases from the same start, so the status words and every tagged
+    // exchange word must start at zero (no stale tag may match); the greedy
+    // history starts empty.
+    cudaError_t e = cudaMemsetAsync(base, 0, k.total, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + k.last_token, 0xFF, 8, s);
     if (e == cudaSuccess && d_next_token) e = cudaMemsetAsync(d_next_token, 0xFF, 4, s);
     if (e != cudaSuccess) return GPT2_ERR_CUDA;
@@ -131,13 +108,12 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     P.lnf_b = m->lnf_b;
     for (uint32_t l = 0; l < c.n_layer; ++l) P.lp[l] = m->lp[l];
     P.cache = d_cache;
-    P.xa = reinterpret_cast<float*>(base + k.xa);
-    P.xb = reinterpret_cast<float*>(base + k.xb);
-    P.qkv = reinterpret_cast<float*>(base + k.qkv);
-    P.u = reinterpret_cast<float*>(base + k.u);
-    P.attn_part = reinterpret_cast<float*>(base + k.attn_part);
-    P.arg_part = reinterpret_cast<float*>(base + k.arg_part);
-    P.flags = reinterpret_cast<unsigned*>(base + k.flags);
+    P.xa = reinterpret_cast<uint64_t*>(base + k.xa);
+    P.xb = reinterpret_cast<uint64_t*>(base + k.xb);
+    P.qkv = reinterpret_cast<uint64_t*>(base + k.qkv);
+    P.u = reinterpret_cast<uint64_t*>(base + k.u);
+    P.attn_part = reinterpret_cast<uint64_t*>(base + k.attn);
+    P.arg_part = reinterpret_cast<uint64_t*>(base + k.arg);
     P.status = reinterpret_cast<int*>(base + k.words);
     P.abort_flag = reinterpret_cast<int*>(base + k.words) + 1;
     P.last_token = reinterpret_cast<uint32_t*>(base + k.last_token);

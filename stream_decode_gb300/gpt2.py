@@ -57,10 +57,12 @@ _SIGS = {
     "gpt2_session_sync": ([_vp], _i32),
     "gpt2_session_set_trace": ([_vp, _vp], _i32),
     "gpt2_session_inject_stall": ([_vp, _u32, C.c_uint64], _i32),
+    "gpt2_session_set_timing": ([_vp, _vp], _i32),
     "gpt2_debug_project": ([_vp, _i32, _vp, _vp, _vp], _i32),
     "gpt2_debug_argmax": ([_vp, _u32, _vp, _vp, _vp], _i32),
     "gpt2_cached_step_noalloc": ([_vp, _vp, _u32, _u32, _vp, _vp, _vp], _i32),
     "gpt2_status_name": ([_i32], C.c_char_p),
+    "gpt2_last_cuda_error": ([C.POINTER(C.c_char_p)], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -220,6 +222,10 @@ class Session:
     def set_trace(self, trace) -> str:
         return STATUS[lib.gpt2_session_set_trace(self.h, _ptr(trace))]
 
+    def set_timing(self, stamps) -> str:
+        """Profiling: next run records (phase, CTA, 3) globaltimer stamps into a CUDA int64 tensor."""
+        return STATUS[lib.gpt2_session_set_timing(self.h, _ptr(stamps))]
+
     def inject_stall(self, phase: int, wait_limit_ns: int) -> str:
         return STATUS[lib.gpt2_session_inject_stall(self.h, phase, wait_limit_ns)]
 
@@ -236,6 +242,13 @@ def debug_argmax(values, index, nonfinite, stream=None) -> str:
     """Test hook: the step kernel's greedy choice over a CUDA float tensor."""
     return STATUS[lib.gpt2_debug_argmax(_ptr(values), values.numel(), _ptr(index), _ptr(nonfinite),
                                         _stream(stream))]
+
+
+def last_cuda_error() -> tuple[int, str]:
+    """(code, name) of the CUDA error behind the last 'cuda' / 'nomem' status."""
+    name = C.c_char_p()
+    code = lib.gpt2_last_cuda_error(C.byref(name))
+    return code, (name.value or b"").decode()
 
 
 def trace_words(shape) -> int:

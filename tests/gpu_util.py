@@ -28,6 +28,9 @@ def run(sess, seq, n_steps, want_logits=True):
     st = sess.run(tin, n_steps, logits, V if want_logits else 0, tout)
     assert st == "ok", st
     st = sess.sync()
+    if st == "cuda":
+        from stream_decode_gb300 import gpt2
+        st = f"cuda {gpt2.last_cuda_error()}"
     assert st == "ok", st
     ch = tout.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
     return (logits.cpu().numpy() if want_logits else None), ch
