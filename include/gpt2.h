@@ -181,13 +181,14 @@ gpt2_status gpt2_session_sync(gpt2_session* session);
 gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
 
 /* Profiling: enqueue the next run with phase timestamps.  d_stamps
- * (device, (5*n_layer+1) * grid_ctas * 8 u64) receives, for step 0 of that
- * run, per phase and CTA: the device globaltimer (ns) when the CTA started
- * the phase, when its inputs were complete and when its outputs were stored;
- * then the SM's clock64 at the start, at inputs complete, when its input
- * transform (LayerNorm / head merge) was done, when its first weight chunk of
- * the phase had landed, and when its outputs were stored.  Pass NULL to
- * stop. */
+ * (device, (5*n_layer+1) * grid_ctas * 8 u64, phase-major) receives, for
+ * step 0 of that run, per phase and CTA: [0..2] the device globaltimer (ns)
+ * when the CTA started the phase, when its inputs were complete and when
+ * its outputs were stored; [3..6] the SM's clock64 when its inputs were
+ * complete, when its projection started (after LayerNorm / head merge /
+ * quantization), when thread 0's projection work ended and when its outputs
+ * were stored; [7] clock64 when the phase's first weight chunk was known to
+ * have landed.  Attention phases fill [0..6] only.  Pass NULL to stop. */
 gpt2_status gpt2_session_set_timing(gpt2_session* session, uint64_t* d_stamps);
 
 /* Debug/test: make the next run's CTA 0 skip publishing one phase so that
@@ -232,9 +233,11 @@ gpt2_status gpt2_cached_step_noalloc(const gpt2_model* model, float* d_cache, ui
 /* Test hook: applies projection `index` of the model (index convention of
  * gpt2_model_read_q8; the vocabulary projection has no bias) to the device
  * vector d_x (its input width in floats) and writes d_y (its output width),
- * using the step kernel's own device routines: for int8 models the per-64
- * activation quantizer, the dp4a group sums and the fixed-order rescale; for
- * binary32 models the float4 dot products.  Enqueued on `stream`. */
+ * using the step kernel's own device routines and the path it takes for that
+ * matrix (rows spread over warps for block matrices, one warp per ring chunk
+ * for the vocabulary): for int8 models the per-64 activation quantizer, the
+ * dp4a group sums and the fixed-order rescale; for binary32 models the float4
+ * dot products.  Enqueued on `stream`. */
 gpt2_status gpt2_debug_project(gpt2_model* model, int index, const float* d_x, float* d_y, void* stream);
 
 /* Test hook: the step kernel's greedy-choice routine over d_values[n]:

@@ -19,7 +19,7 @@ bool step_shape_supported(int D, int FF, int DH);
 cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, bool q8, cudaStream_t st);
 cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, cudaStream_t st);
 cudaError_t launch_project(const uint8_t* rows, int K, int N, bool q8, const float* x, const float* bias, float* y,
-                           cudaStream_t st);
+                           int stream, cudaStream_t st);
 cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfinite, cudaStream_t st);
 }  // namespace gpt2
 
@@ -117,6 +117,7 @@ void fill_plan(const gpt2_session* s, StepPlan& P) {
     P.wait_limit_ns = s->wait_limit_ns;
     P.stall_phase = -1;
     P.prefetch_chunks = 0;
+    P.pace_ns = kDefaultPaceNs;
 }
 
 unsigned phases_per_step(const gpt2_model* m) { return 5u * m->cfg.n_layer + 1u; }
@@ -147,6 +148,8 @@ gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t t
     if (s->stall_phase >= 0) P.wait_limit_ns = s->wait_limit_ns;
     const char* pf = getenv("GPT2_PREFETCH_CHUNKS");
     if (pf) P.prefetch_chunks = atoi(pf);
+    const char* pace = getenv("GPT2_PACE_NS");
+    if (pace) P.pace_ns = (uint32_t)atoi(pace);
     cudaError_t e = launch_step(P, s->m->quant == GPT2_INT8_G64, stream);
     if (e != cudaSuccess) return cuda_status(e);
     s->trace_next = nullptr;
@@ -465,7 +468,8 @@ gpt2_status gpt2_debug_project(gpt2_model* m, int index, const float* d_x, float
         const uint64_t b = (k == kQKV) ? lp.b_qkv : (k == kO ? lp.b_o : (k == kFC ? lp.b_fc : lp.b_p));
         bias = m->d_packed + b;
     }
-    return cuda_status(launch_project(rows, K, N, q8, d_x, bias, d_y, (cudaStream_t)stream));
+    // the path the step kernel takes for this matrix at one CTA per SM: streaming for the vocabulary
+    return cuda_status(launch_project(rows, K, N, q8, d_x, bias, d_y, index == 4 * L ? 1 : 0, (cudaStream_t)stream));
 }
 
 gpt2_status gpt2_debug_argmax(const float* d_values, uint32_t n, uint32_t* d_index, int* d_nonfinite,

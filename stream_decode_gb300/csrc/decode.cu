@@ -42,7 +42,7 @@ namespace gpt2 {
 
 // ----------------------------------------------------------- smem layout
 struct SmemLayout {
-    uint32_t ring, full, empty, xs, vin, vq, vs, red, ored, qh, rsc, stage, bias, geot, misc, total;
+    uint32_t ring, full, empty, xs, vin, vq, vs, red, ored, qh, rsc, stage, bias, geot, misc, plan, total;
 };
 
 __host__ __device__ constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -52,8 +52,9 @@ __host__ __device__ constexpr uint32_t align16(uint32_t x) { return (x + 15u) & 
 // attention unit (2 * 12 heads * kMaxSplits), and the per-CTA greedy choices
 // [256 + kMaxGrid].
 constexpr int kStageFloats = 640;
-// int8 rescale terms of one window: [32 rows][48 groups] at most.
-constexpr int kCoopTaskFloats = 32 * 48;
+// int8 rescale terms, per consumer warp: [rows][groups] of one pass.
+constexpr int kWarpScratch = 192;
+constexpr int kCoopTaskFloats = kConsumerWarps * kWarpScratch;
 static_assert(kConsumerWarps * 8 * (2 + 8) <= kStageFloats, "attention warp merge fits in stage");
 static_assert(2 * 16 * kMaxSplits <= kStageFloats, "unit (max, sum) pairs fit in stage");
 static_assert(256 + kMaxGrid <= kStageFloats, "greedy choices fit in stage");
@@ -78,6 +79,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D, int FF, bool q8, int ma
     s.bias = o; o = align16(o + kConsumerWarps * 32 * 4);
     s.geot = o; o = align16(o + 5 * 32);  // GeoRow table
     s.misc = o; o = align16(o + 64 * 4);
+    s.plan = o; o = align16(o + (uint32_t)sizeof(StepPlan));  // the launch's plan, copied once
     s.total = o;
     return s;
 }
@@ -149,29 +151,6 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Deterministic sum over the 256 consumer threads (fixed order).
-__device__ __forceinline__ float block_sum(float v, float* red, int tid) {
-    v = warp_sum(v);
-    if ((tid & 31) == 0) red[tid >> 5] = v;
-    consumers_sync();
-    float t = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) t += red[w];
-    consumers_sync();
-    return t;
-}
-
-__device__ __forceinline__ float block_max(float v, float* red, int tid) {
-    v = warp_max(v);
-    if ((tid & 31) == 0) red[tid >> 5] = v;
-    consumers_sync();
-    float t = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) t = fmaxf(t, red[w]);
-    consumers_sync();
-    return t;
-}
-
 __device__ __forceinline__ float gelu_tanh(float x) {
     float inner = 0.7978845608f * (x + 0.044715f * x * x * x);
     return 0.5f * x * (1.0f + tanhf(inner));
@@ -217,26 +196,9 @@ __device__ __forceinline__ void arg_warp_reduce(ArgBest& b) {
     }
 }
 
-// LayerNorm of x (smem, N values) into y (smem); biased variance, eps 1e-5.
-template <int N>
-__device__ __forceinline__ void layernorm(const float* x, const float* __restrict__ g, const float* __restrict__ b,
-                                          float* y, float* red, int tid) {
-    float s = 0.0f;
-    for (int i = tid; i < N; i += kConsumerWarps * 32) s += x[i];
-    const float mean = block_sum(s, red, tid) / (float)N;
-    float q = 0.0f;
-    for (int i = tid; i < N; i += kConsumerWarps * 32) {
-        float t = x[i] - mean;
-        q += t * t;
-    }
-    const float var = block_sum(q, red, tid) / (float)N;
-    const float den = sqrtf(var + kLnEps);
-    for (int i = tid; i < N; i += kConsumerWarps * 32) y[i] = (x[i] - mean) / den * __ldg(g + i) + __ldg(b + i);
-}
-
 // Quantize v[0..N) per group of 64 into q/s (int8 path).  Warp w owns groups
-// w, w + warps, ...; its groups are loaded, reduced and quantized together
-// so the shuffles and divisions of different groups overlap.
+// w, w + warps, ...; its groups are loaded, reduced and quantized together so
+// the shuffles and divisions of different groups overlap.
 template <int N>
 __device__ __forceinline__ void quantize_vec(const float* v, int8_t* q, float* s, int warp, int lane) {
     constexpr int NG = N / kGroup;
@@ -289,104 +251,206 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[N], int lane) {
     return v[0];
 }
 
-// Rows per ring chunk and per window for input width K.  A window is a run
-// of whole chunks (at most 8, at most 32 rows; 8 rows for binary32 K = 3072,
-// which keeps the accumulators in registers) that all warps compute together.
+// ---------------------------------------------------------- projection cores
+// A phase share (this CTA's rows of one matrix, input width K) arrives in
+// ring chunks of RPC rows of RB bytes; chunk c of the ring sequence sits in
+// slot c % kSlots.
+//
+// Spread shares (all chunks fit in half the ring, at most kSpreadRows rows)
+// are computed cooperatively by the whole CTA once every chunk has landed:
+// each weight byte is read from shared memory once and every thread works.
+// Longer shares (the vocabulary) stream: one warp per chunk, chunks
+// released as they are used.
 template <int K, bool Q8>
-struct WinGeo {
-    static constexpr int RB = row_bytes(K, Q8);
+struct Rows {
+    static constexpr int RB = row_bytes(K, Q8);                               // bytes per row
     static constexpr int RPC0 = kSlotBytes / RB;
     static constexpr int RPC = RPC0 > kMaxChunkRows ? kMaxChunkRows : RPC0;  // rows per chunk
-    static constexpr int MAXW = (!Q8 && K > 2048) ? 8 : 32;                  // rows per window, at most
-    static constexpr int CPW0 = MAXW / RPC < 1 ? 1 : MAXW / RPC;
-    static constexpr int CPW = CPW0 > 8 ? 8 : CPW0;                          // chunks per window
-    static constexpr int WR = CPW * RPC;                                      // rows per window
-    static constexpr int MR = WR > 8 ? 32 : 8;                                // padded for the transpose-sum
+    static constexpr int NG = K / kGroup;                                     // int8 groups per row
 };
 
-// binary32 window: thread t covers float4 columns t, t + NT, ... of every
-// row; the warps' partial sums meet through wpart.  Thread r < wn returns
-// row r's dot product with x.  Window row r lives in chunk c0 + r / RPC.
-template <int K>
-__device__ __forceinline__ float win_f32(const uint8_t* ring, uint32_t c0, int wn, const float* x, float* wpart,
-                                         int tid, int lane, int warp) {
-    using W = WinGeo<K, false>;
+constexpr int kSpreadRows = 32;
+
+__host__ __device__ constexpr bool share_spread(int nchunks, int nrows, int K, bool q8) {
+    return nchunks <= kSlots / 2 && nrows <= kSpreadRows && (!q8 || nrows * (K / kGroup) <= kCoopTaskFloats);
+}
+
+// binary32, cooperative: thread t takes float4 columns t, t + NT, ... of
+// rows 0..nrows-1 (NR >= nrows accumulators); a warp transpose-reduction
+// leaves the warp's partial of row r on lane r, stored to part[warp][r].
+template <int K, int NR>
+__device__ __forceinline__ void coop_f32_part(const uint8_t* ring, uint32_t c0, int nrows, const float* x, float* part,
+                                              int tid) {
+    using R = Rows<K, false>;
     constexpr int NT = kConsumerWarps * 32;
-    constexpr int NV = K / 4;
-    constexpr int FPT = (NV + NT - 1) / NT;
+    constexpr int NV = K / 4;                  // float4 columns per row
+    constexpr int NC = (NV + NT - 1) / NT;     // columns per thread
+    const int warp = tid >> 5, lane = tid & 31;
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    float4 xv[FPT];
+    float acc[NR];
 #pragma unroll
-    for (int i = 0; i < FPT; ++i) {
-        const int f = tid + NT * i;
-        xv[i] = f < NV ? x4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float acc[W::MR];
+    for (int i = 0; i < NR; ++i) acc[i] = 0.0f;
 #pragma unroll
-    for (int r = 0; r < W::MR; ++r) {
-        acc[r] = 0.0f;
-        // a compiler-only fence every 8 rows bounds the shared loads in flight
-        if ((r & 7) == 0) asm volatile("" ::: "memory");
-        if (r < wn) {
-            const int c = r / W::RPC, rr = r - c * W::RPC;
-            const float4* w4 = reinterpret_cast<const float4*>(ring + (size_t)((c0 + c) % kSlots) * kSlotBytes +
-                                                              (size_t)rr * W::RB);
+    for (int cc = 0; cc < NC; ++cc) {
+        const int col = tid + NT * cc;
+        if ((NV % NT) == 0 || col < NV) {
+            const float4 xv = x4[col];
 #pragma unroll
-            for (int i = 0; i < FPT; ++i) {
-                const int f = tid + NT * i;
-                if (f < NV) {
-                    const float4 wv = w4[f];
-                    acc[r] = fmaf(xv[i].x, wv.x, acc[r]);
-                    acc[r] = fmaf(xv[i].y, wv.y, acc[r]);
-                    acc[r] = fmaf(xv[i].z, wv.z, acc[r]);
-                    acc[r] = fmaf(xv[i].w, wv.w, acc[r]);
+            for (int i = 0; i < NR; ++i) {
+                if (i < nrows) {
+                    // row i: chunk c0 + i / RPC, byte (i % RPC) * RB of its slot (constants but c0)
+                    const uint32_t off = ((c0 + (uint32_t)(i / R::RPC)) % kSlots) * (uint32_t)kSlotBytes +
+                                         (uint32_t)((i % R::RPC) * R::RB);
+                    const float4 wv = *reinterpret_cast<const float4*>(ring + off + 16u * (uint32_t)col);
+                    acc[i] = fmaf(xv.x, wv.x, acc[i]);
+                    acc[i] = fmaf(xv.y, wv.y, acc[i]);
+                    acc[i] = fmaf(xv.z, wv.z, acc[i]);
+                    acc[i] = fmaf(xv.w, wv.w, acc[i]);
                 }
             }
         }
     }
-    const float tot = warp_transpose_sum<W::MR>(acc, lane);
-    if (lane < W::MR) wpart[warp * 32 + lane] = tot;
+    const float t = warp_transpose_sum<NR>(acc, lane);
+    if (lane < NR && lane < nrows) part[warp * kSpreadRows + lane] = t;
+}
+
+// Rows 0..nrows-1 of a spread share against x; thread r < nrows returns
+// row r's total (the warps' partials summed in warp order), others 0.
+// Contains a barrier over the consumer warps: every consumer thread calls it.
+template <int K>
+__device__ __forceinline__ float coop_f32(const uint8_t* ring, uint32_t c0, int nrows, const float* x, float* part,
+                                          int tid) {
+    // a spread share has at most kSlots / 2 chunks of RPC rows
+    constexpr int MAXR = (kSlots / 2) * Rows<K, false>::RPC;
+    if (MAXR > 16 && nrows > 16) coop_f32_part<K, (MAXR > 16 ? 32 : 8)>(ring, c0, nrows, x, part, tid);
+    else if (MAXR > 8 && nrows > 8) coop_f32_part<K, (MAXR > 8 ? 16 : 8)>(ring, c0, nrows, x, part, tid);
+    else coop_f32_part<K, 8>(ring, c0, nrows, x, part, tid);
     consumers_sync();
     float y = 0.0f;
-    if (tid < wn)
+    if (tid < nrows) {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) y += wpart[w * 32 + tid];
+        for (int w = 0; w < kConsumerWarps; ++w) y += part[w * kSpreadRows + tid];
+    }
     return y;
 }
 
-// int8 window: (row, group) tasks over all warps give the exact int32 group
-// sums; t_g = ((float)acc_g * s_x[g]) * s_w[g] is parked in tsm, and thread
-// r < wn returns its row's terms summed in ascending group order from 0.0f
-// (the fixed rescale order), explicitly rounded so nothing is fused.
-template <int K>
-__device__ __forceinline__ float win_q8(const uint8_t* ring, uint32_t c0, int wn, const int8_t* xq, const float* xs,
-                                        float* tsm, int tid) {
-    using W = WinGeo<K, true>;
-    constexpr int NT = kConsumerWarps * 32;
-    constexpr int NG = K / kGroup;
-    const int tasks = wn * NG;
-    for (int tk = tid; tk < tasks; tk += NT) {
-        const int r = tk / NG, g = tk - r * NG;
-        const int c = r / W::RPC, rr = r - c * W::RPC;
-        const uint8_t* row = ring + (size_t)((c0 + c) % kSlots) * kSlotBytes + (size_t)rr * W::RB;
-        const int4* wv = reinterpret_cast<const int4*>(row + g * kGroup);
-        const int4* xv = reinterpret_cast<const int4*>(xq + g * kGroup);
-        int acc = 0;
+// Exact int32 sum of the 64 products of one group (two independent dp4a
+// chains; integer addition is exact in any order).
+__device__ __forceinline__ int group_dot(const uint8_t* w, const int8_t* x) {
+    const int4* wv = reinterpret_cast<const int4*>(w);
+    const int4* xv = reinterpret_cast<const int4*>(x);
+    int a0 = 0, a1 = 0;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int4 a = wv[v], b = xv[v];
-            acc = __dp4a(a.x, b.x, acc);
-            acc = __dp4a(a.y, b.y, acc);
-            acc = __dp4a(a.z, b.z, acc);
-            acc = __dp4a(a.w, b.w, acc);
+    for (int v = 0; v < 4; v += 2) {
+        const int4 p = wv[v], q = xv[v], r = wv[v + 1], s = xv[v + 1];
+        a0 = __dp4a(p.x, q.x, a0);
+        a1 = __dp4a(r.x, s.x, a1);
+        a0 = __dp4a(p.y, q.y, a0);
+        a1 = __dp4a(r.y, s.y, a1);
+        a0 = __dp4a(p.z, q.z, a0);
+        a1 = __dp4a(r.z, s.z, a1);
+        a0 = __dp4a(p.w, q.w, a0);
+        a1 = __dp4a(r.w, s.w, a1);
+    }
+    return a0 + a1;
+}
+
+// The rescale term of one (row, group): ((float)acc * s_x[g]) * s_w[g],
+// explicitly rounded.
+__device__ __forceinline__ float group_term(const uint8_t* row, int g, int K, const int8_t* xq, const float* xs) {
+    const int acc = group_dot(row + g * kGroup, xq + g * kGroup);
+    return __fmul_rn(__fmul_rn(__int2float_rn(acc), xs[g]), reinterpret_cast<const float*>(row + K)[g]);
+}
+
+// Ordered rescale sum of one row: t[0] + t[1] + ... from 0.0f, explicitly
+// rounded (the fixed int8 rescale order).
+template <int NG>
+__device__ __forceinline__ float ordered_sum(const float* t) {
+    float sum = 0.0f;
+    if constexpr ((NG & 3) == 0) {
+#pragma unroll
+        for (int g = 0; g < NG; g += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(t + g);
+            sum = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(sum, v.x), v.y), v.z), v.w);
         }
-        const float sw = reinterpret_cast<const float*>(row + K)[g];
-        tsm[tk] = __fmul_rn(__fmul_rn(__int2float_rn(acc), xs[g]), sw);
+    } else {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) sum = __fadd_rn(sum, t[g]);
+    }
+    return sum;
+}
+
+// int8, cooperative: the (row, group) tasks of the share are spread over
+// every consumer thread; task terms go to scr[row][group]; thread r < nrows
+// returns row r's ordered sum, others 0.  Contains a barrier over the
+// consumer warps.
+template <int K>
+__device__ __forceinline__ float coop_q8(const uint8_t* ring, uint32_t c0, int nrows, const int8_t* xq,
+                                         const float* xs, float* scr, int tid) {
+    using R = Rows<K, true>;
+    constexpr int NT = kConsumerWarps * 32;
+    for (int tk = tid; tk < nrows * R::NG; tk += NT) {
+        const int i = tk / R::NG, g = tk - i * R::NG;
+        const uint8_t* row = ring + (size_t)((c0 + (uint32_t)(i / R::RPC)) % kSlots) * kSlotBytes +
+                             (size_t)((i % R::RPC) * R::RB);
+        scr[tk] = group_term(row, g, K, xq, xs);
     }
     consumers_sync();
-    float sum = 0.0f;
-    if (tid < wn)
-        for (int g = 0; g < NG; ++g) sum = __fadd_rn(sum, tsm[tid * NG + g]);
+    return tid < nrows ? ordered_sum<R::NG>(scr + tid * R::NG) : 0.0f;
+}
+
+// Rows one streaming call covers: binary32 keeps four accumulators per
+// lane; int8 is bounded by the warp's rescale scratch.
+template <int K, bool Q8>
+__host__ __device__ constexpr int dot_rows() {
+    return !Q8 ? 4 : ((kWarpScratch / (K / kGroup)) < 32 ? (kWarpScratch / (K / kGroup)) : 32);
+}
+
+// binary32, streaming: m <= 4 consecutive rows at w against x[0..K); lane
+// i < m returns row i's total.  Lanes stride float4 columns; one butterfly
+// transpose per call.
+template <int K>
+__device__ __forceinline__ float dot_f32(const uint8_t* w, int m, const float* x, int lane) {
+    using R = Rows<K, false>;
+    constexpr int NV = K / 4, T = (NV + 31) / 32, S4 = R::RB / 16;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 2
+    for (int t = 0; t < T; ++t) {
+        const int idx = lane + 32 * t;
+        if ((NV % 32) == 0 || idx < NV) {
+            const float4 xv = x4[idx];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < m) {
+                    const float4 wv = w4[i * S4 + idx];
+                    acc[i] = fmaf(xv.x, wv.x, acc[i]);
+                    acc[i] = fmaf(xv.y, wv.y, acc[i]);
+                    acc[i] = fmaf(xv.z, wv.z, acc[i]);
+                    acc[i] = fmaf(xv.w, wv.w, acc[i]);
+                }
+            }
+        }
+    }
+    return warp_transpose_sum<4>(acc, lane);
+}
+
+// int8, streaming: m consecutive rows at w (m * K/64 <= kWarpScratch);
+// lanes take (row, group) tasks; lane i < m returns row i's ordered sum.
+// scr: this warp's scratch.
+template <int K>
+__device__ __forceinline__ float dot_q8(const uint8_t* w, int m, const int8_t* xq, const float* xs, float* scr,
+                                        int lane) {
+    using R = Rows<K, true>;
+#pragma unroll 2
+    for (int tk = lane; tk < m * R::NG; tk += 32) {
+        const int i = tk / R::NG, g = tk - i * R::NG;
+        scr[tk] = group_term(w + (size_t)i * R::RB, g, K, xq, xs);
+    }
+    __syncwarp();
+    const float sum = lane < m ? ordered_sum<R::NG>(scr + lane * R::NG) : 0.0f;
+    __syncwarp();
     return sum;
 }
 
@@ -397,6 +461,12 @@ __device__ __forceinline__ float win_q8(const uint8_t* ring, uint32_t c0, int wn
 // reloaded together, so one round costs one L2 round trip.  Returns false
 // when the run is abandoned (another CTA gave up, or the wait exceeded its
 // limit).
+// Every spin-wait reads the grid's abort word only once it has lasted
+// kAbortCheckNs: one word polled by every thread of every CTA makes a hot L2
+// line that slows every exchange; no wait of a healthy run lasts this long.
+constexpr uint64_t kAbortCheckNs = 20000;
+__device__ __forceinline__ bool waited_long(uint64_t elapsed_ns) { return elapsed_ns > kAbortCheckNs; }
+
 template <int MAXC, typename Addr>
 __device__ __forceinline__ bool tagged_wait(uint64_t (&w)[MAXC], uint64_t pending, unsigned tag, Addr addr,
                                             const StepPlan& P) {
@@ -410,9 +480,9 @@ __device__ __forceinline__ bool tagged_wait(uint64_t (&w)[MAXC], uint64_t pendin
         for (int k = 0; k < MAXC; ++k)
             if (((pending >> k) & 1ull) && tag_of(w[k]) == tag) pending &= ~(1ull << k);
         if (pending && (++rounds & 7u) == 0) {
-            if (ld_volatile_int(P.abort_flag)) return false;
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) t0 = now;
+            else if (waited_long(now - t0) && ld_volatile_int(P.abort_flag)) return false;
             else if (now - t0 > P.wait_limit_ns) {
                 record_error(P, kDevTimeout);
                 return false;
@@ -446,40 +516,55 @@ __device__ __forceinline__ bool gather_vec(const uint64_t* src, int N, unsigned 
     return ok;
 }
 
-// LayerNorm with this thread's gains/shifts already in registers (loaded
-// before the wait for x, so their latency hides behind it).
+// Gathers this thread's words tid + NT*k (k < PN, tid + NT*k < N) of a
+// tagged N-word vector into registers once each carries `tag`.
+template <int PN>
+__device__ __forceinline__ bool gather_vals(const uint64_t* src, int N, unsigned tag, float (&v)[PN], int tid,
+                                            const StepPlan& P) {
+    constexpr int NT = kConsumerWarps * 32;
+    uint64_t w[PN];
+    const bool ok = tagged_wait<PN>(w, own_words<PN>(N, tid), tag, [&](int k) { return src + tid + NT * k; }, P);
+#pragma unroll
+    for (int k = 0; k < PN; ++k) v[k] = (tid + NT * k < N) ? val_of(w[k]) : 0.0f;
+    return ok;
+}
+
+// LayerNorm of this thread's coordinates v[k] = x[tid + NT*k] into y
+// (shared memory), with the gains/shifts already in registers (loaded before
+// the wait for x, so their latency hides behind it).  One block reduction of
+// (sum x, sum x^2); biased variance E[x^2] - mean^2; eps 1e-5.
 template <int N, int PN>
-__device__ __forceinline__ void layernorm_regs(const float* x, const float (&g)[PN], const float (&b)[PN], float* y,
-                                               float* red, int tid) {
-    // one block reduction of (sum x, sum x^2); var = E[x^2] - mean^2 (biased)
+__device__ __forceinline__ void layernorm_vals(const float (&v)[PN], const float (&g)[PN], const float (&b)[PN],
+                                               float* y, float* red, int tid) {
     constexpr int NT = kConsumerWarps * 32;
     float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
     for (int k = 0; k < PN; ++k)
         if (tid + NT * k < N) {
-            const float v = x[tid + NT * k];
-            s1 += v;
-            s2 = fmaf(v, v, s2);
+            s1 += v[k];
+            s2 = fmaf(v[k], v[k], s2);
         }
-    s1 = warp_sum(s1);
-    s2 = warp_sum(s2);
-    if ((tid & 31) == 0) {
-        red[tid >> 5] = s1;
-        red[32 + (tid >> 5)] = s2;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
     }
+    if ((tid & 31) == 0) reinterpret_cast<float2*>(red)[tid >> 5] = make_float2(s1, s2);
     consumers_sync();
     float t1 = 0.0f, t2 = 0.0f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-        t1 += red[w];
-        t2 += red[32 + w];
+        const float2 r = reinterpret_cast<const float2*>(red)[w];
+        t1 += r.x;
+        t2 += r.y;
     }
-    const float mean = t1 / (float)N;
-    const float var = fmaxf(t2 / (float)N - mean * mean, 0.0f);
-    const float den = sqrtf(var + kLnEps);
+    constexpr float inv_n = 1.0f / (float)N;
+    const float mean = t1 * inv_n;
+    const float var = fmaxf(fmaf(t2, inv_n, -mean * mean), 0.0f);
+    const float rstd = rsqrtf(var + kLnEps);
 #pragma unroll
     for (int k = 0; k < PN; ++k)
-        if (tid + NT * k < N) y[tid + NT * k] = (x[tid + NT * k] - mean) / den * g[k] + b[k];
+        if (tid + NT * k < N) y[tid + NT * k] = fmaf((v[k] - mean) * rstd, g[k], b[k]);
 }
 
 template <int N, int PN>
@@ -493,10 +578,36 @@ __device__ __forceinline__ void load_ln(const float* g, const float* b, float (&
     }
 }
 
+// Phase kinds of a step, in order: per layer LN1 + QKV, attention,
+// out-projection, LN2 + FC, MLP projection; then LN_f + vocabulary.
+enum PhaseKind : int { kPhQKV = 0, kPhAtt = 1, kPhO = 2, kPhFC = 3, kPhP = 4, kPhVocab = 5 };
+
+// Profiling stamps per (phase of step 0, CTA): globaltimer at phase start,
+// inputs complete, outputs stored; clock64 at inputs complete, projection
+// start, warp 0's last row stored, outputs stored, warp 0's first weight
+// chunk landed.
+constexpr int kStamps = 8;
+
+// The consumer side is one loop over the phases of a step with a runtime
+// dispatch on the phase kind, so that every routine (gather, LayerNorm, head
+// merge, quantizer, dot products, epilogue, attention) exists once in the
+// binary: a layer executes far more code than an SM's instruction cache
+// holds when each phase carries inlined copies of its own.
 template <int D, int FF, int DH, bool Q8>
-__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepPlan P) {
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepPlan plan) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemLayout lay = smem_layout(D, FF, Q8, P.max_pos);
+    const SmemLayout lay = smem_layout(D, FF, Q8, plan.max_pos);
+    // Every field of the plan is read from a shared-memory copy: kernel
+    // parameters live in the constant bank, whose cache misses cost an L2
+    // round trip in the middle of a phase's critical path.
+    {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&plan);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(smem + lay.plan);
+        static_assert(sizeof(StepPlan) % 4 == 0, "plan copies as words");
+        for (int i = threadIdx.x; i < (int)(sizeof(StepPlan) / 4); i += blockDim.x) dst[i] = src[i];
+        __syncthreads();
+    }
+    const StepPlan& P = *reinterpret_cast<const StepPlan*>(smem + lay.plan);
     uint8_t* ring = smem + lay.ring;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
@@ -547,7 +658,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         // L2 prefetch cursor: walks the same chunk sequence prefetch_chunks ahead.
         int pf_s = 0, pf_ph = 0, pf_k = 0;
         Geo pf_g = geo_of(P, geot, 0);
-        uint32_t pf_issued = 0;
         auto pf_advance = [&]() {
             // issue one prefetch at the cursor, then move it
             while (pf_s < P.n_steps && pf_k >= pf_g.nchunks) {
@@ -560,12 +670,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             const int n = min(pf_g.rpc, pf_g.nrows - r);
             bulk_prefetch_l2(pf_g.base + (uint64_t)r * pf_g.rb, (uint32_t)(n * pf_g.rb));
             ++pf_k;
-            ++pf_issued;
         };
         for (int i = 0; i < P.prefetch_chunks; ++i) pf_advance();
+        // Pacing: the chunks of the block matrices are issued at least pace_ns
+        // apart, so that the refills released together at a phase boundary do
+        // not saturate HBM while the next phase exchanges its activations
+        // (loaded memory raises the latency of every exchange).  The
+        // vocabulary streams unpaced.
+        uint64_t next_issue = 0;
         for (int s = 0; s < P.n_steps && !stop; ++s) {
             for (int ph = 0; ph < phases_per_step && !stop; ++ph) {
                 const Geo g = geo_of(P, geot, ph);
+                const bool paced = P.pace_ns != 0 && ph != phases_per_step - 1;
                 for (int k = 0; k < g.nchunks; ++k) {
                     const int slot = gi % kSlots;
                     const uint32_t fill = gi / kSlots;
@@ -587,6 +703,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                             }
                         }
                         if (stop) break;
+                    }
+                    if (paced) {
+                        uint64_t now = globaltimer_ns();
+                        while (now < next_issue && !*s_abort) {
+                            __nanosleep(64);
+                            now = globaltimer_ns();
+                        }
+                        next_issue = (now > next_issue ? now : next_issue) + P.pace_ns;
                     }
                     const int r = k * g.rpc;
                     const int n = min(g.rpc, g.nrows - r);
@@ -613,40 +737,29 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 }
             }
         }
-        (void)pf_issued;
         return;
     }
-
 
     // ================================================= consumer warps
     constexpr int NT = kConsumerWarps * 32;
     constexpr int PD = (D + NT - 1) / NT;      // D-vector words per thread
     constexpr int PF = (FF + NT - 1) / NT;     // FF-vector words per thread
     constexpr int P3 = (3 * D + NT - 1) / NT;  // qkv words per thread (trace)
+    constexpr int PV = PF > P3 ? PF : P3;      // words per thread of any gathered vector
     constexpr int PM = PD * kMaxSplits;        // attention partial words per thread (merge)
-    static_assert(PM <= 64 && PF <= 64 && P3 <= 64, "tagged gathers hold at most 64 words per thread");
+    static_assert(PM <= 64 && PV <= 64, "tagged gathers hold at most 64 words per thread");
     uint32_t gi = 0;  // chunks consumed (same sequence as the producer)
+    using KD = std::integral_constant<int, D>;
+    using KF = std::integral_constant<int, FF>;
+    static_assert(kSlots / 2 <= 32, "a spread share's chunks are released by one warp's lanes");
     const int S = attn_splits(P.G, P.H);  // splits the scratch holds per head
-    const unsigned per_step = 5u * (unsigned)L + 1u;
+    const int nph = 5 * L + 1;
+    const unsigned per_step = (unsigned)nph;
     const bool tracer = (P.trace != nullptr) && cta == 0;
     const int trace_layer = 8 * D + FF;
-    // Profiling hook: globaltimer stamps of step 0, per (phase, CTA): phase
-    // start, inputs ready, outputs stored.
-    int tph = 0;
-    // per (phase, CTA): globaltimer at start / inputs ready / outputs stored,
-    // then SM clock64 at start / ready / transform done / first chunk in / stored
-    // (10 slots: + clock64 after warp 0's first chunk body, after its last chunk)
-    constexpr int kStamps = 10;
-    auto stamp = [&](int s_now, int point) {
-        if (P.timing && s_now == 0 && tid == 0) {
-            uint64_t* e = P.timing + ((size_t)tph * P.G + cta) * kStamps;
-            const int ci = point == 0 ? 3 : point == 1 ? 4 : point == 3 ? 5 : point == 4 ? 6 : 9;
-            e[ci] = (uint64_t)clock64();
-            if (point <= 2) e[point] = globaltimer_ns();
-        }
-        if (point == 2) ++tph;
-    };
-    bool stamp_chunk = false;  // warp 0 stamps point 4 when its first chunk of the phase has landed
+    uint64_t* stp = nullptr;  // this phase's stamps (thread 0, step 0, when profiling)
+    auto gstamp = [&](int k) { if (stp) stp[k] = globaltimer_ns(); };
+    auto cstamp = [&](int k) { if (stp) stp[k] = (uint64_t)clock64(); };
     // Test hook: CTA 0 tags one phase's outputs one too low, so nobody accepts them.
     const unsigned stall_tag = P.stall_phase >= 0 ? P.epoch + (unsigned)P.stall_phase : 0u;
     auto out_tag = [&](unsigned t) -> unsigned { return (cta == 0 && t == stall_tag) ? t - 1u : t; };
@@ -663,106 +776,261 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         return *slot == 0;
     };
 
-    // Epilogue of one output row j (run by the thread that owns the row):
-    // QKV: + bias, tagged store, KV append; O and P: + bias + residual; FC:
-    // + bias, GELU; vocabulary: logits and the running greedy choice.
-    struct Epi {
-        int kind;
-        unsigned tag;
-        uint64_t bias;   // word offset of the bias in the packed checkpoint (unused for the vocabulary)
-        float* kv_row;   // QKV: this position's cache row
-        float* logits;   // vocabulary: this step's logits or null
+    // Lane i < n of a warp waits (bounded) until ring chunk c0 + i has
+    // landed.  The caller's next CTA barrier orders the observed copies
+    // before every consumer thread's reads.  Warp-uniform result.
+    auto wait_chunks = [&](uint32_t c0, int n) -> bool {
+        const uint32_t cc = c0 + (uint32_t)lane;
+        uint64_t t0 = 0;
+        uint32_t spins = 0;
+        while (!__all_sync(0xffffffffu, lane >= n || mbar_try_wait(&full[cc % kSlots], (cc / kSlots) & 1))) {
+            if ((++spins & 255) == 0) {
+                int give_up = 0;
+                const uint64_t now = globaltimer_ns();
+                if (t0 == 0) t0 = now;
+                else if (waited_long(now - t0) && ld_volatile_int(P.abort_flag)) give_up = 1;
+                if (t0 != now && now - t0 > P.wait_limit_ns) {
+                    if (lane == 0) record_error(P, kDevTimeout);
+                    give_up = 1;
+                }
+                if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+            }
+        }
+        return true;
     };
+
     ArgBest best = arg_init();
-    auto apply_epi = [&](const Epi& e, const Geo& g, int j, float acc) {
-        if (e.kind == kVocab) {
-            if (e.logits) e.logits[j] = acc;
-            arg_update(best, acc, (unsigned)j);
-            return;
-        }
-        const float b = g.nrows <= NT ? bias_s[j - g.r0] : __ldg(P.packed + e.bias + j);
-        const float y = __fadd_rn(acc, b);
-        if (e.kind == kQKV) {
-            st_tagged(P.qkv + j, e.tag, y);
-            if (j >= D) e.kv_row[j - D] = y;
-        } else if (e.kind == kO) {
-            st_tagged(P.xb + j, e.tag, __fadd_rn(xs[j], y));
-        } else if (e.kind == kFC) {
-            st_tagged(P.u + j, e.tag, gelu_tanh(y));
-        } else {
-            st_tagged(P.xa + j, e.tag, __fadd_rn(xs[j], y));
-        }
-    };
-    // Runs weight phase `ph` over this CTA's rows, one window of whole ring
-    // chunks at a time (all warps on every row of the window); the producer
-    // fills the next window's slots meanwhile.  Returns false if a chunk
-    // never arrived (the run is then abandoned at the next agreement).
-    auto run_phase = [&](auto kk, int ph, const Epi& e) -> bool {
+    // One projection phase over this CTA's share of rows (input width KK),
+    // with the epilogue of each output row j run by the thread that holds it:
+    // QKV: + bias, tagged store, KV append; O and P: + bias + residual; FC:
+    // + bias, GELU; vocabulary: logits and the running greedy choice.  A
+    // spread share's slots are released by the caller after the phase's
+    // agreement barrier (*release = its chunk count); a streamed share's
+    // chunks are released by the warp that used them, with a named barrier
+    // per round of chunks so warp skew stays below one ring length.
+    auto run_gemv = [&](auto kk, int kind, int mat, unsigned tag, uint64_t boff, float* kv_row, float* lg,
+                        int* release) -> bool {
         constexpr int KK = decltype(kk)::value;
-        using W = WinGeo<KK, Q8>;
-        const Geo g = geo_of(P, geot, ph);
+        using R = Rows<KK, Q8>;
+        const Geo g = geo_of(P, geot, mat);
+        auto epilogue = [&](int j, float y) {
+            if (kind == kPhVocab) {
+                if (lg) lg[j] = y;
+                arg_update(best, y, (unsigned)j);
+                return;
+            }
+            const float b = g.nrows <= NT ? bias_s[j - g.r0] : __ldg(P.packed + boff + j);
+            const float v = __fadd_rn(y, b);
+            if (kind == kPhQKV) {
+                st_tagged(P.qkv + j, tag, v);
+                if (j >= D) kv_row[j - D] = v;
+            } else if (kind == kPhFC) {
+                st_tagged(P.u + j, tag, gelu_tanh(v));
+            } else {
+                st_tagged((kind == kPhO ? P.xb : P.xa) + j, tag, __fadd_rn(xs[j], v));
+            }
+        };
+        *release = 0;
         bool ok = true;
-        for (int w0 = 0; w0 < g.nrows; w0 += W::WR) {
-            const int wn = min(W::WR, g.nrows - w0);
-            const uint32_t c0 = gi + (uint32_t)(w0 / W::RPC);
-            const int nc = (wn + W::RPC - 1) / W::RPC;
-            for (int c = 0; c < nc && ok; ++c) {
-                const uint32_t cc = c0 + c;
-                const int slot = cc % kSlots;
-                uint64_t t0 = 0;
-                uint32_t spins = 0;
-                // every lane observes the completed phase (acquire) before reading the slot
-                while (!__all_sync(0xffffffffu, mbar_try_wait(&full[slot], (cc / kSlots) & 1))) {
-                    if ((++spins & 255) == 0) {
-                        int give_up = 0;
-                        if (ld_volatile_int(P.abort_flag)) give_up = 1;
-                        const uint64_t now = globaltimer_ns();
-                        if (t0 == 0) t0 = now;
-                        else if (now - t0 > P.wait_limit_ns) {
-                            if (lane == 0) record_error(P, kDevTimeout);
-                            give_up = 1;
-                        }
-                        if (__shfl_sync(0xffffffffu, give_up, 0)) { ok = false; break; }
+        if (share_spread(g.nchunks, g.nrows, KK, Q8)) {
+            if (warp == 0) ok = wait_chunks(gi, g.nchunks);
+            cstamp(7);
+            if (!agree(ok)) return false;  // the cooperative body has barriers: all warps or none
+            float y;
+            if constexpr (Q8) y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
+            else y = coop_f32<KK>(ring, gi, g.nrows, vin, stage, tid);
+            if (tid < g.nrows) epilogue(g.r0 + tid, y);
+            cstamp(5);
+            *release = g.nchunks;
+            return true;
+        }
+        constexpr int MR = dot_rows<KK, Q8>();
+        static_assert(2 * kConsumerWarps <= kSlots, "a round must stay within one ring length");
+        for (int k0 = 0; k0 < g.nchunks; k0 += kConsumerWarps) {
+            const int k = k0 + warp;
+            if (ok && k < g.nchunks) {
+                const uint32_t c = gi + (uint32_t)k;
+                ok = wait_chunks(c, 1);
+                __syncwarp();
+                if (k0 == 0) cstamp(7);
+                if (ok) {
+                    const uint8_t* w = ring + (size_t)(c % kSlots) * kSlotBytes;
+                    const int n = min(R::RPC, g.nrows - k * R::RPC);
+                    for (int q = 0; q < n; q += MR) {
+                        const int m = min(MR, n - q);
+                        float y;
+                        if constexpr (Q8)
+                            y = dot_q8<KK>(w + (size_t)q * R::RB, m, vq, vs, rsc + warp * kWarpScratch, lane);
+                        else
+                            y = dot_f32<KK>(w + (size_t)q * R::RB, m, vin, lane);
+                        if (lane < m) epilogue(g.r0 + k * R::RPC + q + lane, y);
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[c % kSlots]);
                 }
             }
-            const bool st0 = w0 == 0 && stamp_chunk && P.timing && tid == 0 && tph < (int)per_step;
-            if (st0) P.timing[((size_t)tph * P.G + cta) * kStamps + 6] = (uint64_t)clock64();
-            float y;
-            if constexpr (Q8) y = win_q8<KK>(ring, c0, wn, vq, vs, rsc, tid);
-            else y = win_f32<KK>(ring, c0, wn, vin, stage, tid, lane, warp);
-            if (st0) P.timing[((size_t)tph * P.G + cta) * kStamps + 7] = (uint64_t)clock64();
-            if (ok && tid < wn) apply_epi(e, g, g.r0 + w0 + tid, y);
-            consumers_sync();  // the window's slots are read and its scratch is free again
-            if (tid == 0)
-                for (int c = 0; c < nc; ++c) mbar_arrive(&empty[(c0 + c) % kSlots]);
+            if (k0 + kConsumerWarps < g.nchunks) consumers_sync();
         }
-        stamp_chunk = false;
-        if (P.timing && tid == 0 && tph < (int)per_step)
-            P.timing[((size_t)tph * P.G + cta) * kStamps + 8] = (uint64_t)clock64();
+        cstamp(5);
         gi += g.nchunks;
         return ok;
     };
-    using KD = std::integral_constant<int, D>;
-    using KF = std::integral_constant<int, FF>;
-    // Bias rows of this CTA's share of a phase: loaded into a register before
-    // the phase's wait, parked in shared memory after it.
-    auto bias_prefetch = [&](const Geo& g, uint64_t off) -> float {
-        return (g.nrows <= NT && tid < g.nrows) ? __ldg(P.packed + off + g.r0 + tid) : 0.0f;
-    };
-    auto bias_park = [&](const Geo& g, float v) {
-        if (g.nrows <= NT && tid < g.nrows) bias_s[tid] = v;
-    };
-    auto trace_vec = [&](int offset, const float* v, int n) {
-        for (int i = tid; i < n; i += NT) P.trace[offset + i] = v[i];
-    };
-    auto quantize_in = [&](int n) {
-        if constexpr (Q8) {
-            if (n == FF) quantize_vec<FF>(vin, vq, vs, warp, lane);
-            else quantize_vec<D>(vin, vq, vs, warp, lane);
+
+    // Attention of layer l over positions 0..p, split along the key axis.
+    // Unit (head h, split sp) covers keys [k0, k1).  A warp takes KPW keys
+    // per pass (LPK lanes per key, DPL dims per lane) and every lane keeps an
+    // online softmax (running max, sum, weighted values).  Keys and values of
+    // positions < p do not depend on this step, so a warp's first two passes
+    // are loaded before waiting for q; position p's key and value come from
+    // this step's tagged qkv words.  Each unit stores an unnormalised partial
+    // (max, sum, o[DH]) as tagged words.
+    auto attention = [&](int l, int p, int S_eff, unsigned tag) -> bool {
+        constexpr int LPK = DH >= 32 ? 8 : 4;    // lanes per key
+        constexpr int KPW = 32 / LPK;            // keys per warp per pass
+        constexpr int DPL = DH / LPK;            // dims per lane
+        constexpr int F4 = DPL / 4;              // float4 per lane per row
+        constexpr int KPP = kConsumerWarps * KPW;  // keys per pass over the CTA
+        static_assert(DPL % 4 == 0, "a lane holds whole float4s of a head row");
+        const unsigned tin = tag - 1u, tg = out_tag(tag);
+        const int ks = lane / LPK, dc = lane % LPK;
+        const int n = p + 1;
+        const float den = sqrtf((float)DH);
+        const uint64_t kv_stride = (uint64_t)L * 2 * D;  // floats between positions in the cache
+        bool first = true;
+        for (int u = cta; u < P.H * S_eff; u += P.G) {
+            const int h = u / S_eff, sp = u - h * S_eff;
+            const int k0 = (int)(((long long)sp * n) / S_eff), k1 = (int)(((long long)(sp + 1) * n) / S_eff);
+            const bool has_p = (k1 == n);  // the last split holds this position's key
+            const float* kv0 = P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL;
+            auto fetch = [&](int j, float4 (&kk)[F4], float4 (&vv)[F4]) {
+                if (j < k1 && j < p) {
+                    const float4* row = reinterpret_cast<const float4*>(kv0 + (uint64_t)j * kv_stride);
+#pragma unroll
+                    for (int f = 0; f < F4; ++f) {
+                        kk[f] = __ldcg(row + f);
+                        vv[f] = __ldcg(row + D / 4 + f);
+                    }
+                }
+            };
+            int j = k0 + warp * KPW + ks;  // this lane's key in the current pass
+            float4 ka[F4], va[F4], kb[F4], vb[F4];
+            fetch(j, ka, va);
+            fetch(j + KPP, kb, vb);
+            // q_h (threads 0..DH-1); k_p, v_p (DH..3DH-1) when this unit holds key p
+            uint64_t mine = 0;
+            const uint64_t* src = nullptr;
+            if (tid < DH) src = P.qkv + h * DH + tid;
+            else if (has_p && tid < 2 * DH) src = P.qkv + D + h * DH + (tid - DH);
+            else if (has_p && tid < 3 * DH) src = P.qkv + 2 * D + h * DH + (tid - 2 * DH);
+            if (src) mine = 1;
+            uint64_t wq[1];
+            const bool got = tagged_wait<1>(wq, mine, tin, [&](int) { return src; }, P);
+            if (src) qh[tid] = val_of(wq[0]);
+            if (!agree(got)) return false;
+            if (first) {
+                gstamp(1);
+                cstamp(3);
+                cstamp(4);
+            }
+            first = false;
+            const float4* q4 = reinterpret_cast<const float4*>(qh + dc * DPL);
+            float m = -INFINITY, z = 0.0f;
+            float acc[DPL];
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) acc[d] = 0.0f;
+            for (int jb = k0 + warp * KPW; jb < k1; jb += KPP, j += KPP) {
+                if (j == p) {
+#pragma unroll
+                    for (int f = 0; f < F4; ++f) {
+                        ka[f] = reinterpret_cast<const float4*>(qh + DH + dc * DPL)[f];
+                        va[f] = reinterpret_cast<const float4*>(qh + 2 * DH + dc * DPL)[f];
+                    }
+                }
+                float dot = 0.0f;
+#pragma unroll
+                for (int f = 0; f < F4; ++f) {
+                    const float4 qf = q4[f];
+                    dot += qf.x * ka[f].x + qf.y * ka[f].y + qf.z * ka[f].z + qf.w * ka[f].w;
+                }
+#pragma unroll
+                for (int o = 1; o < LPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                if (j < k1) {
+                    const float sc = dot / den;
+                    const float mn = fmaxf(m, sc);
+                    const float corr = expf(m - mn);  // 0 while m is -inf
+                    const float e = expf(sc - mn);
+                    z = fmaf(z, corr, e);
+#pragma unroll
+                    for (int f = 0; f < F4; ++f) {
+                        acc[4 * f + 0] = fmaf(acc[4 * f + 0], corr, e * va[f].x);
+                        acc[4 * f + 1] = fmaf(acc[4 * f + 1], corr, e * va[f].y);
+                        acc[4 * f + 2] = fmaf(acc[4 * f + 2], corr, e * va[f].z);
+                        acc[4 * f + 3] = fmaf(acc[4 * f + 3], corr, e * va[f].w);
+                    }
+                    m = mn;
+                }
+#pragma unroll
+                for (int f = 0; f < F4; ++f) {
+                    ka[f] = kb[f];
+                    va[f] = vb[f];
+                }
+                fetch(j + 2 * KPP, kb, vb);
+            }
+            // merge the key slots of the warp (lanes with the same dc)
+#pragma unroll
+            for (int o = LPK; o < 32; o <<= 1) {
+                const float om = __shfl_xor_sync(0xffffffffu, m, o);
+                const float oz = __shfl_xor_sync(0xffffffffu, z, o);
+                const float mn = fmaxf(m, om);
+                const float c1 = (m == -INFINITY) ? 0.0f : expf(m - mn);
+                const float c2 = (om == -INFINITY) ? 0.0f : expf(om - mn);
+                z = z * c1 + oz * c2;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) {
+                    const float oa = __shfl_xor_sync(0xffffffffu, acc[d], o);
+                    acc[d] = acc[d] * c1 + oa * c2;
+                }
+                m = mn;
+            }
+            // then the warps: stage[w][dc][2 + DPL]
+            if (ks == 0) {
+                float* st = stage + (warp * LPK + dc) * (2 + DPL);
+                st[0] = m;
+                st[1] = z;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) st[2 + d] = acc[d];
+            }
+            consumers_sync();
+            if (tid < DH) {
+                const int c = tid / DPL, d = tid - c * DPL;
+                float M = -INFINITY;
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stage[(w * LPK + c) * (2 + DPL)]);
+                float Z = 0.0f, O = 0.0f;
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float* st = stage + (w * LPK + c) * (2 + DPL);
+                    if (st[0] == -INFINITY) continue;
+                    const float cw = expf(st[0] - M);
+                    Z = fmaf(st[1], cw, Z);
+                    O = fmaf(st[2 + d], cw, O);
+                }
+                uint64_t* part = P.attn_part + (size_t)u * (DH + 2);
+                st_tagged(part + 2 + tid, tg, O);
+                if (tid == 0) {
+                    st_tagged(part, tg, M);
+                    st_tagged(part + 1, tg, Z);
+                }
+            }
             consumers_sync();
         }
+        if (first) {
+            gstamp(1);
+            cstamp(3);
+            cstamp(4);
+        }
+        cstamp(5);
+        return true;
     };
+
     // The previous step's per-CTA greedy choices (tag `tag`), reduced here.
     // The acquire pairs with each CTA's release of its choice, so the KV rows
     // that step wrote are visible to this step's attention.
@@ -775,9 +1043,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             uint64_t w0 = ld_tagged_acquire(ap);
             while (tag_of(w0) != tag) {
                 if ((++rounds & 7u) == 0) {
-                    if (ld_volatile_int(P.abort_flag)) { ok = false; break; }
                     const uint64_t now = globaltimer_ns();
                     if (t0 == 0) t0 = now;
+                    else if (waited_long(now - t0) && ld_volatile_int(P.abort_flag)) { ok = false; break; }
                     else if (now - t0 > P.wait_limit_ns) {
                         record_error(P, kDevTimeout);
                         ok = false;
@@ -842,223 +1110,48 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             alive = false;
             break;
         }
-        for (int l = 0; l < L && alive; ++l) {
-            const LayerParams& lp = P.lp[l];
-            const unsigned tQKV = base + 5u * (unsigned)l + 1u, tATT = tQKV + 1u, tO = tQKV + 2u, tFC = tQKV + 3u,
-                           tP = tQKV + 4u;
-            // ---------------- LN1 + QKV (+ KV append)
-            {
-                stamp(s, 0);
-                float gr[PD], br[PD];
-                load_ln<D>(P.packed + lp.ln1_g, P.packed + lp.ln1_b, gr, br, tid);
-                const Geo g = geo_of(P, geot, 4 * l + kQKV);
-                const float bv = bias_prefetch(g, lp.b_qkv);
-                bool ok = true;
-                if (l == 0) {
-                    for (int i = tid; i < D; i += NT) {
-                        const float pe = __ldg(P.packed + P.wpe_off + (uint64_t)p * D + i);
-                        if constexpr (Q8) {
-                            const uint8_t* row = P.vocab + (uint64_t)tok * row_bytes(D, true);
-                            const float qv = (float)reinterpret_cast<const int8_t*>(row)[i];
-                            const float sv = reinterpret_cast<const float*>(row + D)[i / kGroup];
-                            xs[i] = __fadd_rn(__fmul_rn(qv, sv), pe);
-                        } else {
-                            xs[i] = __fadd_rn(__ldg(P.packed + P.wte_off + (uint64_t)tok * D + i), pe);
-                        }
-                    }
-                } else {
-                    ok = gather_vec<PD>(P.xa, D, tQKV - 1u, xs, tid, P);
-                }
-                bias_park(g, bv);
-                if (!agree(ok)) { alive = false; break; }
-                stamp(s, 1);
-                layernorm_regs<D>(xs, gr, br, vin, red, tid);
-                consumers_sync();
-                quantize_in(D);
-                if (trace_step) {
-                    trace_vec(l * trace_layer, xs, D);
-                    trace_vec(l * trace_layer + D, vin, D);
-                }
-                const Epi e{kQKV, out_tag(tQKV), lp.b_qkv, P.cache + ((uint64_t)p * L + l) * 2 * D, nullptr};
-                stamp(s, 3);
-                stamp_chunk = (s == 0);
-                if (!agree(run_phase(KD{}, 4 * l + kQKV, e))) { alive = false; break; }
-                stamp(s, 2);
+        const int S_eff = attn_splits_for(p + 1, S);
+        for (int ph = 0; ph < nph; ++ph) {
+            const int kind = ph == nph - 1 ? (int)kPhVocab : ph % 5;
+            const int l = ph / 5;  // L for the vocabulary phase
+            const unsigned tag = base + (unsigned)ph + 1u;  // this phase's outputs; its inputs carry tag - 1
+            stp = (P.timing && s == 0 && tid == 0) ? P.timing + ((size_t)ph * P.G + cta) * kStamps : nullptr;
+            gstamp(0);
+            if (kind == kPhAtt) {
+                if (!attention(l, p, S_eff, tag)) { alive = false; break; }
+                gstamp(2);
+                cstamp(6);
+                continue;
             }
-            // ---------------- attention over positions 0..p, split along keys
-            // Unit (head h, split sp) covers keys [k0, k1).  A warp takes 8 keys
-            // per pass (4 lanes per key, DH/4 dims per lane) and every lane keeps
-            // an online softmax (running max, sum, weighted values).  Keys and
-            // values of positions < p do not depend on this step, so the first
-            // passes are loaded before waiting for q; position p's key and value
-            // come from this step's tagged qkv words.
-            const int S_eff = attn_splits_for(p + 1, S);
-            {
-                stamp(s, 0);
-                const unsigned tg = out_tag(tATT);
-                bool ok = true;
-                bool first_unit = true;
-                constexpr int LPK = DH >= 32 ? 8 : 4;    // lanes per key
-                constexpr int KPW = 32 / LPK;            // keys per warp per pass
-                constexpr int DPL = DH / LPK;            // dims per lane
-                constexpr int F4 = DPL / 4;              // float4 per lane per row
-                constexpr int KPP = kConsumerWarps * KPW;  // keys per pass over the CTA
-                constexpr int PRE = 2;                   // passes loaded before the wait for q
-                static_assert(DPL % 4 == 0, "a lane holds whole float4s of a head row");
-                const int ks = lane / LPK, dc = lane % LPK;
-                for (int u = cta; u < P.H * S_eff; u += P.G) {
-                    const int h = u / S_eff, sp = u - h * S_eff;
-                    const int n = p + 1;
-                    const int k0 = (int)(((long long)sp * n) / S_eff), k1 = (int)(((long long)(sp + 1) * n) / S_eff);
-                    const bool has_p = (k1 == n);  // the last split holds this position's key
-                    float4 kr[PRE][F4], vr[PRE][F4];
-#pragma unroll
-                    for (int ps = 0; ps < PRE; ++ps) {
-                        const int j = k0 + (ps * kConsumerWarps + warp) * KPW + ks;
-                        if (j < k1 && j < p) {
-                            const float* row = P.cache + ((uint64_t)j * L + l) * 2 * D + h * DH + dc * DPL;
-#pragma unroll
-                            for (int f = 0; f < F4; ++f) {
-                                kr[ps][f] = __ldcg(reinterpret_cast<const float4*>(row) + f);
-                                vr[ps][f] = __ldcg(reinterpret_cast<const float4*>(row + D) + f);
-                            }
-                        }
-                    }
-                    // q_h (threads 0..DH-1); k_p, v_p (DH..3DH-1) when this unit holds key p
-                    uint64_t mine = 0;
-                    const uint64_t* src = nullptr;
-                    if (tid < DH) src = P.qkv + h * DH + tid;
-                    else if (has_p && tid < 2 * DH) src = P.qkv + D + h * DH + (tid - DH);
-                    else if (has_p && tid < 3 * DH) src = P.qkv + 2 * D + h * DH + (tid - 2 * DH);
-                    if (src) mine = 1;
-                    uint64_t wq[1];
-                    const bool got = tagged_wait<1>(wq, mine, tQKV, [&](int) { return src; }, P);
-                    if (src) qh[tid] = val_of(wq[0]);
-                    if (!agree(got)) { ok = false; break; }
-                    if (first_unit) stamp(s, 1);
-                    first_unit = false;
-                    const float4* q4 = reinterpret_cast<const float4*>(qh + dc * DPL);  // read from smem per key
-                    const float den = sqrtf((float)DH);
-                    float m = -INFINITY, z = 0.0f;
-                    float acc[DPL];
-#pragma unroll
-                    for (int d = 0; d < DPL; ++d) acc[d] = 0.0f;
-                    auto consume = [&](int j, const float4 (&kk)[F4], const float4 (&vv)[F4]) {
-                        float dot = 0.0f;
-#pragma unroll
-                        for (int f = 0; f < F4; ++f) {
-                            const float4 qf = q4[f];
-                            dot += qf.x * kk[f].x + qf.y * kk[f].y + qf.z * kk[f].z + qf.w * kk[f].w;
-                        }
-#pragma unroll
-                        for (int o = 1; o < LPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                        if (j < k1) {
-                            const float sc = dot / den;
-                            const float mn = fmaxf(m, sc);
-                            const float corr = expf(m - mn);  // 0 while m is -inf
-                            const float e = expf(sc - mn);
-                            z = fmaf(z, corr, e);
-#pragma unroll
-                            for (int f = 0; f < F4; ++f) {
-                                acc[4 * f + 0] = fmaf(acc[4 * f + 0], corr, e * vv[f].x);
-                                acc[4 * f + 1] = fmaf(acc[4 * f + 1], corr, e * vv[f].y);
-                                acc[4 * f + 2] = fmaf(acc[4 * f + 2], corr, e * vv[f].z);
-                                acc[4 * f + 3] = fmaf(acc[4 * f + 3], corr, e * vv[f].w);
-                            }
-                            m = mn;
-                        }
-                    };
-                    auto fetch = [&](int j, float4 (&kk)[F4], float4 (&vv)[F4]) {
-                        if (j < k1) {
-                            if (j < p) {
-                                const float* row = P.cache + ((uint64_t)j * L + l) * 2 * D + h * DH + dc * DPL;
-#pragma unroll
-                                for (int f = 0; f < F4; ++f) {
-                                    kk[f] = __ldcg(reinterpret_cast<const float4*>(row) + f);
-                                    vv[f] = __ldcg(reinterpret_cast<const float4*>(row + D) + f);
-                                }
-                            } else {
-#pragma unroll
-                                for (int f = 0; f < F4; ++f) {
-                                    kk[f] = reinterpret_cast<const float4*>(qh + DH + dc * DPL)[f];
-                                    vv[f] = reinterpret_cast<const float4*>(qh + 2 * DH + dc * DPL)[f];
-                                }
-                            }
-                        }
-                    };
-#pragma unroll
-                    for (int ps = 0; ps < PRE; ++ps) {
-                        const int j = k0 + (ps * kConsumerWarps + warp) * KPW + ks;
-                        if (j == p && j < k1) fetch(j, kr[ps], vr[ps]);
-                        consume(j, kr[ps], vr[ps]);
-                    }
-                    for (int jb = k0 + PRE * KPP + warp * KPW; jb < k1; jb += KPP) {
-                        float4 kk[F4], vv[F4];
-                        fetch(jb + ks, kk, vv);
-                        consume(jb + ks, kk, vv);
-                    }
-                    // merge the key slots of the warp (lanes with the same dc)
-#pragma unroll
-                    for (int o = LPK; o < 32; o <<= 1) {
-                        const float om = __shfl_xor_sync(0xffffffffu, m, o);
-                        const float oz = __shfl_xor_sync(0xffffffffu, z, o);
-                        const float mn = fmaxf(m, om);
-                        const float c1 = (m == -INFINITY) ? 0.0f : expf(m - mn);
-                        const float c2 = (om == -INFINITY) ? 0.0f : expf(om - mn);
-                        z = z * c1 + oz * c2;
-#pragma unroll
-                        for (int d = 0; d < DPL; ++d) {
-                            const float oa = __shfl_xor_sync(0xffffffffu, acc[d], o);
-                            acc[d] = acc[d] * c1 + oa * c2;
-                        }
-                        m = mn;
-                    }
-                    // then the warps: stage[w][dc][2 + DPL]
-                    if (ks == 0) {
-                        float* st = stage + (warp * LPK + dc) * (2 + DPL);
-                        st[0] = m;
-                        st[1] = z;
-#pragma unroll
-                        for (int d = 0; d < DPL; ++d) st[2 + d] = acc[d];
-                    }
-                    consumers_sync();
-                    if (tid < DH) {
-                        const int c = tid / DPL, d = tid - c * DPL;
-                        float M = -INFINITY;
-                        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stage[(w * LPK + c) * (2 + DPL)]);
-                        float Z = 0.0f, O = 0.0f;
-                        for (int w = 0; w < kConsumerWarps; ++w) {
-                            const float* st = stage + (w * LPK + c) * (2 + DPL);
-                            if (st[0] == -INFINITY) continue;
-                            const float cw = expf(st[0] - M);
-                            Z = fmaf(st[1], cw, Z);
-                            O = fmaf(st[2 + d], cw, O);
-                        }
-                        uint64_t* part = P.attn_part + (size_t)u * (DH + 2);
-                        st_tagged(part + 2 + tid, tg, O);
-                        if (tid == 0) {
-                            st_tagged(part, tg, M);
-                            st_tagged(part + 1, tg, Z);
-                        }
-                    }
-                    consumers_sync();
-                }
-                if (!ok) { alive = false; break; }
-                if (first_unit) stamp(s, 1);
-                stamp(s, 3);
-                stamp(s, 2);
+            const LayerParams& lp = P.lp[kind == kPhVocab ? 0 : l];
+            const int mat = kind == kPhVocab ? 4 * L
+                                             : 4 * l + (kind == kPhQKV ? (int)kQKV
+                                                        : kind == kPhO ? (int)kO
+                                                        : kind == kPhFC ? (int)kFC : (int)kP);
+            const int K = kind == kPhP ? FF : D;
+            // LayerNorm parameters (QKV: ln_1, FC: ln_2, vocabulary: ln_f) and
+            // this CTA's bias rows are loaded before the wait for the inputs.
+            const bool has_ln = kind == kPhQKV || kind == kPhFC || kind == kPhVocab;
+            float gr[PD], br[PD];
+            if (has_ln) {
+                const uint64_t go = kind == kPhQKV ? lp.ln1_g : kind == kPhFC ? lp.ln2_g : P.lnf_g;
+                const uint64_t bo = kind == kPhQKV ? lp.ln1_b : kind == kPhFC ? lp.ln2_b : P.lnf_b;
+                load_ln<D>(P.packed + go, P.packed + bo, gr, br, tid);
             }
-            // ---------------- merge the heads' partials, out-projection + residual
-            {
-                stamp(s, 0);
-                const Geo g = geo_of(P, geot, 4 * l + kO);
-                const float bv = bias_prefetch(g, lp.b_o);
-                const int units_eff = P.H * S_eff;
-                // (max, sum) of every unit into stage[2u], stage[2u+1]
-                const int nmz = 2 * units_eff;
+            const Geo g = geo_of(P, geot, mat);
+            const uint64_t boff = kind == kPhQKV ? lp.b_qkv : kind == kPhO ? lp.b_o : kind == kPhFC ? lp.b_fc : lp.b_p;
+            const float bv = (kind != kPhVocab && g.nrows <= NT && tid < g.nrows) ? __ldg(P.packed + boff + g.r0 + tid)
+                                                                                  : 0.0f;
+            // ---- inputs
+            bool ok = true;
+            uint64_t ov[PM];  // out-projection: every split's o words of this thread's coordinates
+            float xv[PD];     // LayerNorm phases: this thread's coordinates of the residual stream
+            if (kind == kPhO) {
+                // (max, sum) of every unit into stage[2u], stage[2u + 1]
+                const int nmz = 2 * P.H * S_eff;
                 uint64_t wmz[2];
                 const bool ok1 = tagged_wait<2>(
-                    wmz, own_words<2>(nmz, tid), tATT,
+                    wmz, own_words<2>(nmz, tid), tag - 1u,
                     [&](int k) {
                         const int w = tid + NT * k;
                         return P.attn_part + (size_t)(w >> 1) * (DH + 2) + (w & 1);
@@ -1067,26 +1160,58 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
                     if (tid + NT * k < nmz) stage[tid + NT * k] = val_of(wmz[k]);
-                // this thread's output coordinates idx = tid + NT*i: every split's o[e]
-                uint64_t ov[PM];
                 uint64_t want = 0;
 #pragma unroll
                 for (int i = 0; i < PD; ++i)
                     if (tid + NT * i < D)
                         for (int sp = 0; sp < S_eff; ++sp) want |= 1ull << (i * kMaxSplits + sp);
                 const bool ok2 = tagged_wait<PM>(
-                    ov, want, tATT,
+                    ov, want, tag - 1u,
                     [&](int k) {
                         const int idx = tid + NT * (k / kMaxSplits), sp = k % kMaxSplits;
                         const int h = idx / DH, e = idx - h * DH;
                         return P.attn_part + (size_t)(h * S_eff + sp) * (DH + 2) + 2 + e;
                     },
                     P);
-                bias_park(g, bv);
-                if (!agree(ok1 && ok2)) { alive = false; break; }
-                stamp(s, 1);
+                ok = ok1 && ok2;
+            } else if (kind == kPhQKV && l == 0) {
+#pragma unroll
+                for (int k = 0; k < PD; ++k) {
+                    const int i = tid + NT * k;
+                    xv[k] = 0.0f;
+                    if (i < D) {
+                        const float pe = __ldg(P.packed + P.wpe_off + (uint64_t)p * D + i);
+                        if constexpr (Q8) {
+                            const uint8_t* row = P.vocab + (uint64_t)tok * row_bytes(D, true);
+                            const float qv = (float)reinterpret_cast<const int8_t*>(row)[i];
+                            const float sv = reinterpret_cast<const float*>(row + D)[i / kGroup];
+                            xv[k] = __fadd_rn(__fmul_rn(qv, sv), pe);
+                        } else {
+                            xv[k] = __fadd_rn(__ldg(P.packed + P.wte_off + (uint64_t)tok * D + i), pe);
+                        }
+                    }
+                }
+            } else if (kind == kPhP) {
+                ok = gather_vec<PV>(P.u, FF, tag - 1u, vin, tid, P);
+            } else {
+                ok = gather_vals<PD>(kind == kPhFC ? P.xb : P.xa, D, tag - 1u, xv, tid, P);
+            }
+            if (has_ln) {
+                // the residual stream, kept for the epilogue's residual add (and the trace)
+#pragma unroll
+                for (int k = 0; k < PD; ++k)
+                    if (tid + NT * k < D) xs[tid + NT * k] = xv[k];
+            }
+            if (g.nrows <= NT && tid < g.nrows) bias_s[tid] = bv;
+            if (!agree(ok)) { alive = false; break; }
+            gstamp(1);
+            cstamp(3);
+            // ---- input transform: LayerNorm, or the merge of the heads' partials
+            if (has_ln) {
+                layernorm_vals<D>(xv, gr, br, vin, red, tid);
+            } else if (kind == kPhO) {
                 // weight of each (head, split): exp(m - M_h) / Z_h, once per CTA
-                if (tid < units_eff) {
+                if (tid < P.H * S_eff) {
                     const int h = tid / S_eff;
                     float M = -INFINITY;
                     for (int sp = 0; sp < S_eff; ++sp) M = fmaxf(M, stage[2 * (h * S_eff + sp)]);
@@ -1112,100 +1237,59 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     }
                     vin[idx] = O;
                 }
-                consumers_sync();
-                quantize_in(D);
-                if (trace_step) {
-                    const bool okq = gather_vec<P3>(P.qkv, 3 * D, tQKV, P.trace + l * trace_layer + 2 * D, tid, P);
-                    if (!agree(okq)) { alive = false; break; }
-                    trace_vec(l * trace_layer + 5 * D, vin, D);
-                }
-                const Epi e{kO, out_tag(tO), lp.b_o, nullptr, nullptr};
-                stamp(s, 3);
-                stamp_chunk = (s == 0);
-                if (!agree(run_phase(KD{}, 4 * l + kO, e))) { alive = false; break; }
-                stamp(s, 2);
             }
-            // ---------------- LN2 + FC + GELU
-            {
-                stamp(s, 0);
-                float gr[PD], br[PD];
-                load_ln<D>(P.packed + lp.ln2_g, P.packed + lp.ln2_b, gr, br, tid);
-                const Geo g = geo_of(P, geot, 4 * l + kFC);
-                const float bv = bias_prefetch(g, lp.b_fc);
-                const bool ok = gather_vec<PD>(P.xb, D, tO, xs, tid, P);
-                bias_park(g, bv);
-                if (!agree(ok)) { alive = false; break; }
-                stamp(s, 1);
-                layernorm_regs<D>(xs, gr, br, vin, red, tid);
-                consumers_sync();
-                quantize_in(D);
-                if (trace_step) {
-                    trace_vec(l * trace_layer + 6 * D, xs, D);
-                    trace_vec(l * trace_layer + 7 * D, vin, D);
-                }
-                const Epi e{kFC, out_tag(tFC), lp.b_fc, nullptr, nullptr};
-                stamp(s, 3);
-                stamp_chunk = (s == 0);
-                if (!agree(run_phase(KD{}, 4 * l + kFC, e))) { alive = false; break; }
-                stamp(s, 2);
-            }
-            // ---------------- MLP projection + residual
-            {
-                stamp(s, 0);
-                const Geo g = geo_of(P, geot, 4 * l + kP);
-                const float bv = bias_prefetch(g, lp.b_p);
-                const bool ok = gather_vec<PF>(P.u, FF, tFC, vin, tid, P);
-                bias_park(g, bv);
-                if (!agree(ok)) { alive = false; break; }
-                stamp(s, 1);
-                quantize_in(FF);
-                if (trace_step) trace_vec(l * trace_layer + 8 * D, vin, FF);
-                const Epi e{kP, out_tag(tP), lp.b_p, nullptr, nullptr};
-                stamp(s, 3);
-                stamp_chunk = (s == 0);
-                if (!agree(run_phase(KF{}, 4 * l + kP, e))) { alive = false; break; }
-                stamp(s, 2);
-            }
-        }
-        if (!alive) break;
-        // ---------------- final LN + tied vocabulary projection + greedy choice
-        {
-            stamp(s, 0);
-            const unsigned tVOC = base + per_step;
-            float gr[PD], br[PD];
-            load_ln<D>(P.packed + P.lnf_g, P.packed + P.lnf_b, gr, br, tid);
-            const bool ok = gather_vec<PD>(P.xa, D, tVOC - 1u, xs, tid, P);
-            if (!agree(ok)) { alive = false; break; }
-            stamp(s, 1);
-            layernorm_regs<D>(xs, gr, br, vin, red, tid);
             consumers_sync();
-            quantize_in(D);
+            if constexpr (Q8) {
+                if (kind == kPhP) quantize_vec<FF>(vin, vq, vs, warp, lane);
+                else quantize_vec<D>(vin, vq, vs, warp, lane);
+                consumers_sync();
+            }
+            // ---- activation trace (step 0, CTA 0): per layer x, LN_1(x), qkv,
+            // attention output, x_mid, LN_2(x_mid), GELU output; then x_final, LN_f(x_final)
             if (trace_step) {
-                trace_vec(L * trace_layer, xs, D);
-                trace_vec(L * trace_layer + D, vin, D);
+                const int tb = l * trace_layer;
+                if (kind == kPhO) {
+                    const bool okq = gather_vec<PV>(P.qkv, 3 * D, tag - 2u, P.trace + tb + 2 * D, tid, P);
+                    if (!agree(okq)) { alive = false; break; }
+                }
+                const int ox = kind == kPhFC ? 6 * D : (kind == kPhQKV || kind == kPhVocab) ? 0 : -1;
+                const int oy = kind == kPhQKV || kind == kPhVocab ? D : kind == kPhO ? 5 * D : kind == kPhFC ? 7 * D : 8 * D;
+                for (int i = tid; i < K; i += NT) {
+                    if (ox >= 0) P.trace[tb + ox + i] = xs[i];
+                    P.trace[tb + oy + i] = vin[i];
+                }
             }
-            best = arg_init();
-            const Epi e{kVocab, 0u, 0ull, nullptr, P.logits ? P.logits + (uint64_t)s * P.logits_stride : nullptr};
-            stamp(s, 3);
-            stamp_chunk = (s == 0);
-            if (!agree(run_phase(KD{}, 4 * L, e))) { alive = false; break; }
-            stamp(s, 2);
-            arg_warp_reduce(best);
-            if (lane == 0) {
-                s_arg[warp * 3 + 0] = best.v;
-                s_arg[warp * 3 + 1] = __uint_as_float(best.i);
-                s_arg[warp * 3 + 2] = (float)best.nf;
-            }
-            consumers_sync();
-            if (tid == 0) {
-                for (int w = 1; w < kConsumerWarps; ++w)
-                    arg_merge(best, s_arg[w * 3 + 0], __float_as_uint(s_arg[w * 3 + 1]), s_arg[w * 3 + 2] != 0.0f);
-                const unsigned tg = out_tag(tVOC);
-                uint64_t* ap = P.arg_part + 2 * (size_t)cta;
-                const unsigned iw = (best.i & 0x7FFFFFFFu) | (best.nf ? 0x80000000u : 0u);
-                st_tagged(ap + 1, tg, __uint_as_float(iw));
-                // release: this CTA's KV rows and choice become visible with it
-                st_tagged_release(ap, tag_pack(tg, best.v));
+            // ---- projection and epilogue
+            if (kind == kPhVocab) best = arg_init();
+            float* kv_row = P.cache + ((uint64_t)p * L + l) * 2 * D;
+            float* lg = (kind == kPhVocab && P.logits) ? P.logits + (uint64_t)s * P.logits_stride : nullptr;
+            int release = 0;
+            cstamp(4);
+            ok = kind == kPhP ? run_gemv(KF{}, kind, mat, out_tag(tag), boff, kv_row, lg, &release)
+                              : run_gemv(KD{}, kind, mat, out_tag(tag), boff, kv_row, lg, &release);
+            if (!agree(ok)) { alive = false; break; }
+            if (warp == 0 && lane < release) mbar_arrive(&empty[(gi + (uint32_t)lane) % kSlots]);
+            gi += (uint32_t)release;
+            gstamp(2);
+            cstamp(6);
+            if (kind == kPhVocab) {
+                arg_warp_reduce(best);
+                if (lane == 0) {
+                    s_arg[warp * 3 + 0] = best.v;
+                    s_arg[warp * 3 + 1] = __uint_as_float(best.i);
+                    s_arg[warp * 3 + 2] = (float)best.nf;
+                }
+                consumers_sync();
+                if (tid == 0) {
+                    for (int w = 1; w < kConsumerWarps; ++w)
+                        arg_merge(best, s_arg[w * 3 + 0], __float_as_uint(s_arg[w * 3 + 1]), s_arg[w * 3 + 2] != 0.0f);
+                    const unsigned tg = out_tag(tag);
+                    uint64_t* ap = P.arg_part + 2 * (size_t)cta;
+                    const unsigned iw = (best.i & 0x7FFFFFFFu) | (best.nf ? 0x80000000u : 0u);
+                    st_tagged(ap + 1, tg, __uint_as_float(iw));
+                    // release: this CTA's KV rows and choice become visible with it
+                    st_tagged_release(ap, tag_pack(tg, best.v));
+                }
             }
         }
     }
@@ -1219,45 +1303,73 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
 // ------------------------------------------------------------ test hooks
 // One projection of the model on a given input vector, with the step
-// kernel's own routines: the activation quantizer and the window GEMV
-// (win_f32 / win_q8), then the epilogue's bias add.  Block: the consumer
-// warps, one window of rows copied into a ring-shaped shared buffer.
+// kernel's own routines: the activation quantizer, then the dot products of
+// one phase share (a spread share computed by the whole block, or a long
+// share streamed one warp per chunk in two rounds), then the epilogue's bias
+// add.  Each block copies its share of rows into a ring-shaped shared buffer.
 template <int K, bool Q8>
-__host__ __device__ constexpr uint32_t project_smem_bytes() {
-    using W = WinGeo<K, Q8>;
-    return (uint32_t)W::CPW * kSlotBytes + align16(K * 4) + align16(K) + align16((K / kGroup) * 4) +
-           (uint32_t)kCoopTaskFloats * 4;
-}
+struct HookGeo {
+    static constexpr int RB = row_bytes(K, Q8);
+    static constexpr int RPC0 = kSlotBytes / RB;
+    static constexpr int RPC = RPC0 > kMaxChunkRows ? kMaxChunkRows : RPC0;  // rows per chunk
+    static constexpr int SPREAD0 = (kSlots / 2) * RPC < kSpreadRows ? (kSlots / 2) * RPC : kSpreadRows;
+    static constexpr int SPREAD1 = Q8 ? kCoopTaskFloats / (K / kGroup) : SPREAD0;
+    static constexpr int ROWS_SPREAD = SPREAD0 < SPREAD1 ? SPREAD0 : SPREAD1;  // the largest spread share
+    static constexpr int CHUNKS_STREAM = 2 * kConsumerWarps;                    // two rounds of chunks
+    static constexpr int SLOTS = CHUNKS_STREAM > kSlots / 2 ? CHUNKS_STREAM : kSlots / 2;
+    static constexpr uint32_t SMEM = (uint32_t)SLOTS * kSlotBytes + align16(K * 4) + align16(K) +
+                                     align16((K / kGroup) * 4) + (uint32_t)kCoopTaskFloats * 4;
+    static_assert(share_spread((ROWS_SPREAD + RPC - 1) / RPC, ROWS_SPREAD, K, Q8), "hook spread share is spread");
+    static_assert(!share_spread(CHUNKS_STREAM, CHUNKS_STREAM * RPC, K, Q8), "hook streamed share streams");
+};
 
 template <int K, bool Q8>
 __global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint8_t* __restrict__ rows, int N,
                                                                       const float* __restrict__ x,
                                                                       const float* __restrict__ bias,
-                                                                      float* __restrict__ y) {
-    using W = WinGeo<K, Q8>;
+                                                                      float* __restrict__ y, int stream) {
+    using H = HookGeo<K, Q8>;
     extern __shared__ __align__(128) uint8_t sm[];
     uint8_t* ring = sm;
-    float* vin = reinterpret_cast<float*>(sm + W::CPW * kSlotBytes);
+    float* vin = reinterpret_cast<float*>(sm + H::SLOTS * kSlotBytes);
     int8_t* vq = reinterpret_cast<int8_t*>(reinterpret_cast<uint8_t*>(vin) + align16(K * 4));
     float* vs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(vq) + align16(K));
     float* scratch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(vs) + align16((K / kGroup) * 4));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int w0 = blockIdx.x * W::WR;
-    const int wn = min(W::WR, N - w0);
-    // rows w0 .. w0+wn-1 into "slots": row r at slot r / RPC, offset (r % RPC) * RB
-    for (int i = tid; i < wn * (W::RB / 16); i += blockDim.x) {
-        const int r = i / (W::RB / 16), q = i - r * (W::RB / 16);
-        const int4 v = reinterpret_cast<const int4*>(rows + (size_t)(w0 + r) * W::RB)[q];
-        reinterpret_cast<int4*>(ring + (size_t)(r / W::RPC) * kSlotBytes + (size_t)(r % W::RPC) * W::RB)[q] = v;
+    const int per_block = stream ? H::CHUNKS_STREAM * H::RPC : H::ROWS_SPREAD;
+    const int w0 = blockIdx.x * per_block;
+    const int wn = min(per_block, N - w0);
+    // rows w0 .. w0+wn-1 into slots: row r at slot r / RPC, offset (r % RPC) * RB
+    for (int i = tid; i < wn * (H::RB / 16); i += blockDim.x) {
+        const int r = i / (H::RB / 16), q = i - r * (H::RB / 16);
+        const int4 v = reinterpret_cast<const int4*>(rows + (size_t)(w0 + r) * H::RB)[q];
+        reinterpret_cast<int4*>(ring + (size_t)(r / H::RPC) * kSlotBytes + (size_t)(r % H::RPC) * H::RB)[q] = v;
     }
     for (int i = tid; i < K; i += blockDim.x) vin[i] = x[i];
     __syncthreads();
     if constexpr (Q8) quantize_vec<K>(vin, vq, vs, warp, lane);
     __syncthreads();
-    float out;
-    if constexpr (Q8) out = win_q8<K>(ring, 0, wn, vq, vs, scratch, tid);
-    else out = win_f32<K>(ring, 0, wn, vin, scratch, tid, lane, warp);
-    if (tid < wn) y[w0 + tid] = bias ? __fadd_rn(out, bias[w0 + tid]) : out;
+    auto out = [&](int j, float v) { y[j] = bias ? __fadd_rn(v, bias[j]) : v; };
+    if (!stream) {
+        float v;
+        if constexpr (Q8) v = coop_q8<K>(ring, 0u, wn, vq, vs, scratch, tid);
+        else v = coop_f32<K>(ring, 0u, wn, vin, scratch, tid);
+        if (tid < wn) out(w0 + tid, v);
+        return;
+    }
+    const int nchunks = (wn + H::RPC - 1) / H::RPC;
+    constexpr int MR = dot_rows<K, Q8>();
+    for (int k = warp; k < nchunks; k += kConsumerWarps) {
+        const uint8_t* w = ring + (size_t)k * kSlotBytes;
+        const int n = min(H::RPC, wn - k * H::RPC);
+        for (int q = 0; q < n; q += MR) {
+            const int m = min(MR, n - q);
+            float v;
+            if constexpr (Q8) v = dot_q8<K>(w + (size_t)q * H::RB, m, vq, vs, scratch + warp * kWarpScratch, lane);
+            else v = dot_f32<K>(w + (size_t)q * H::RB, m, vin, lane);
+            if (lane < m) out(w0 + k * H::RPC + q + lane, v);
+        }
+    }
 }
 
 // The step kernel's greedy-choice routine over n values (one block).
@@ -1283,21 +1395,23 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) argmax_kernel(const float
 }
 
 template <int K, bool Q8>
-static cudaError_t project_t(const uint8_t* rows, int N, const float* x, const float* bias, float* y,
+static cudaError_t project_t(const uint8_t* rows, int N, const float* x, const float* bias, float* y, int stream,
                              cudaStream_t st) {
-    constexpr int rows_per_block = WinGeo<K, Q8>::WR;
-    constexpr uint32_t smem = project_smem_bytes<K, Q8>();
-    cudaError_t e = cudaFuncSetAttribute(project_kernel<K, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    using H = HookGeo<K, Q8>;
+    const int per_block = stream ? H::CHUNKS_STREAM * H::RPC : H::ROWS_SPREAD;
+    cudaError_t e = cudaFuncSetAttribute(project_kernel<K, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)H::SMEM);
     if (e != cudaSuccess) return e;
-    project_kernel<K, Q8><<<(N + rows_per_block - 1) / rows_per_block, kConsumerWarps * 32, smem, st>>>(rows, N, x,
-                                                                                                      bias, y);
+    project_kernel<K, Q8><<<(N + per_block - 1) / per_block, kConsumerWarps * 32, H::SMEM, st>>>(rows, N, x, bias, y,
+                                                                                               stream);
     return cudaGetLastError();
 }
 
 cudaError_t launch_project(const uint8_t* rows, int K, int N, bool q8, const float* x, const float* bias, float* y,
-                           cudaStream_t st) {
-#define GPT2_PROJ(KK)                                                                             \
-    if (K == KK) return q8 ? project_t<KK, true>(rows, N, x, bias, y, st) : project_t<KK, false>(rows, N, x, bias, y, st);
+                           int stream, cudaStream_t st) {
+#define GPT2_PROJ(KK)                                                                                        \
+    if (K == KK)                                                                                             \
+        return q8 ? project_t<KK, true>(rows, N, x, bias, y, stream, st)                                    \
+                  : project_t<KK, false>(rows, N, x, bias, y, stream, st);
     GPT2_PROJ(64) GPT2_PROJ(192) GPT2_PROJ(256) GPT2_PROJ(384) GPT2_PROJ(768) GPT2_PROJ(3072)
 #undef GPT2_PROJ
     return cudaErrorInvalidValue;

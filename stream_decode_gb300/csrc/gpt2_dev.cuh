@@ -19,6 +19,10 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kSlotBytes = 12288;   // one ring slot (one 3072-float row)
 constexpr int kSlots = 16;          // ring depth: 192 KiB of weights in flight per SM
 constexpr float kLnEps = 1e-5f;
+// Least interval between the producer's block-weight chunk issues (ns).
+// 12 KB per 300 ns per SM is about 6 TB/s over 152 SMs: enough to keep the
+// ring full, while spreading the refills that a phase boundary releases.
+constexpr uint32_t kDefaultPaceNs = 300;
 
 // status words written by the device
 enum DevStatus : int {
@@ -118,6 +122,7 @@ struct StepPlan {
     uint64_t wait_limit_ns;     // bound of every spin-wait
     int stall_phase;            // test: CTA 0 skips publishing this phase (-1 = none)
     int prefetch_chunks;        // L2 bulk prefetch distance in chunks (0 = off)
+    uint32_t pace_ns;           // least interval between block-weight chunk issues (0 = unpaced)
 };
 
 // Bytes of one K-major weight row in the device stream.

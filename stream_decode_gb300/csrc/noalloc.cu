@@ -129,6 +129,7 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     P.wait_limit_ns = kWaitNs;
     P.stall_phase = -1;
     P.prefetch_chunks = 0;
+    P.pace_ns = kDefaultPaceNs;
     e = launch_step(P, m->quant == GPT2_INT8_G64, s);
     return e == cudaSuccess ? GPT2_OK : (e == cudaErrorMemoryAllocation ? GPT2_ERR_NOMEM : GPT2_ERR_CUDA);
 }

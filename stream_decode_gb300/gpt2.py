@@ -223,7 +223,7 @@ class Session:
         return STATUS[lib.gpt2_session_set_trace(self.h, _ptr(trace))]
 
     def set_timing(self, stamps) -> str:
-        """Profiling: next run records (phase, CTA, 3) globaltimer stamps into a CUDA int64 tensor."""
+        """Profiling: next run records (phase, CTA, 8) stamps (see gpt2_session_set_timing) into a CUDA int64 tensor."""
         return STATUS[lib.gpt2_session_set_timing(self.h, _ptr(stamps))]
 
     def inject_stall(self, phase: int, wait_limit_ns: int) -> str:
