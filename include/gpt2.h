@@ -87,7 +87,7 @@ size_t gpt2_cache_words_per_position(const gpt2_config* cfg);
  * checkpoint; tokens = 1..max_pos little-endian u32 ids.  Writes the final
  * row's vocab logits to logits_out_host (capacity vocab floats) and
  * *logits_out_len = vocab.  Checks, in order: weights_len, tokens_len, each
- * token. */
+ * token.  Runs the tensor-core prefill (gpt2_session_prefill). */
 gpt2_status gpt2_infer(const gpt2_config* cfg, const void* weights_host, size_t weights_len,
                        const void* tokens_host, size_t tokens_len, float* logits_out_host,
                        size_t* logits_out_len);
@@ -159,6 +159,24 @@ gpt2_status gpt2_session_read_cache(gpt2_session* session, void* cache_host, siz
  * when the call returns. */
 gpt2_status gpt2_session_run(gpt2_session* session, const uint32_t* d_tokens_in, uint32_t n_steps,
                              float* d_logits, size_t logits_stride, uint32_t* d_tokens_out, void* stream);
+
+/* Prefill (README, infer paragraph; the prompt half of a session): the
+ * full-prefix forward pass of n prompt tokens (d_tokens: device u32 ids) on
+ * the tensor cores.  Starts an empty session (position 0, else
+ * GPT2_ERR_POSITION); writes the KV-cache rows of positions 0..n-1, the
+ * vocab logits of the last prompt row to d_logits (device, vocab floats;
+ * NULL: the session's own buffer), and the greedy choice of those logits
+ * (largest, lowest index on ties) as the session's last choice and, if
+ * d_next_token is not NULL, to *d_next_token; leaves the session at
+ * position n, so that gpt2_session_run / gpt2_session_step continue the
+ * prompt.  binary32 models only (GPT2_ERR_CONFIG otherwise); 1 <= n <=
+ * max_pos (GPT2_ERR_TOKENS_LEN).  An out-of-range token or a non-finite
+ * logit is reported by the next gpt2_session_sync.  The first call on a
+ * model makes the TF32 remainders of its block matrices (a one-off copy of
+ * their size) and allocates the session's prefill workspace.
+ * Asynchronous on `stream` (NULL: the session's stream). */
+gpt2_status gpt2_session_prefill(gpt2_session* session, const uint32_t* d_tokens, uint32_t n, float* d_logits,
+                                 uint32_t* d_next_token, void* stream);
 
 /* One step with a host token; outputs as in gpt2_session_run.  Asynchronous. */
 gpt2_status gpt2_session_step(gpt2_session* session, uint32_t token, float* d_logits, uint32_t* d_next_token,

@@ -11,6 +11,7 @@
 #include "../../include/gpt2.h"
 #include "gpt2_dev.cuh"
 #include "model_internal.h"
+#include "prefill.h"
 
 namespace gpt2 {
 cudaError_t launch_step(const StepPlan& P, bool q8, cudaStream_t stream);
@@ -42,6 +43,7 @@ struct gpt2_session {
     uint64_t* timing_next;
     int stall_phase;
     uint64_t wait_limit_ns;
+    PrefillWs pf;  // tensor-core prefill workspace, allocated on first use
 };
 
 namespace {
@@ -273,6 +275,7 @@ void gpt2_model_destroy(gpt2_model* m) {
     cudaFree(m->d_packed);
     cudaFree(m->d_wstream);
     cudaFree(m->d_vocab_q8);
+    cudaFree(m->d_wlo);
     delete m;
 }
 
@@ -338,6 +341,7 @@ void gpt2_session_destroy(gpt2_session* s) {
     if (s->last) cudaStreamSynchronize(s->last);
     cudaFree(s->d_cache);
     cudaFree(s->d_scratch);
+    prefill_free(&s->pf);
     cudaFree(s->d_logits);
     cudaFree(s->d_next);
     if (s->own) cudaStreamDestroy(s->own);
@@ -509,6 +513,26 @@ gpt2_status gpt2_cached_step(const gpt2_config* cfg, const void* weights, size_t
     return GPT2_OK;
 }
 
+gpt2_status gpt2_session_prefill(gpt2_session* s, const uint32_t* d_tokens, uint32_t n, float* d_logits,
+                                 uint32_t* d_next_token, void* stream) {
+    if (!s || !d_tokens) return GPT2_ERR_ARG;
+    gpt2_model* m = s->m;
+    const gpt2_config& c = m->cfg;
+    if (m->quant != GPT2_F32 || !prefill_shape_supported(c)) return GPT2_ERR_CONFIG;
+    if (n == 0 || n > c.max_pos) return GPT2_ERR_TOKENS_LEN;
+    if (s->position != 0) return GPT2_ERR_POSITION;
+    cudaStream_t st = stream ? static_cast<cudaStream_t>(stream) : s->own;
+    cudaError_t e = prefill_make_lo(m, st);
+    if (e == cudaSuccess) e = prefill_alloc(&s->pf, (int)c.max_pos, (int)c.d_model, (int)c.d_ff);
+    if (e == cudaSuccess)
+        e = prefill_enqueue(m, &s->pf, d_tokens, (int)n, s->d_cache, d_logits ? d_logits : s->d_logits, s->d_words,
+                            s->d_last_token, d_next_token, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    s->position = n;
+    s->last = st;
+    return GPT2_OK;
+}
+
 gpt2_status gpt2_infer(const gpt2_config* cfg, const void* weights, size_t weights_len, const void* tokens,
                        size_t tokens_len, float* logits_out, size_t* logits_len) {
     if (!logits_len) return GPT2_ERR_ARG;
@@ -536,7 +560,7 @@ gpt2_status gpt2_infer(const gpt2_config* cfg, const void* weights, size_t weigh
         if (e == cudaSuccess) e = cudaMemcpy(d_ids, ids.data(), sizeof(uint32_t) * n, cudaMemcpyHostToDevice);
         st = cuda_status(e);
     }
-    if (st == GPT2_OK) st = gpt2_session_run(s, d_ids, (uint32_t)n, s->d_logits, 0, nullptr, s->own);
+    if (st == GPT2_OK) st = gpt2_session_prefill(s, d_ids, (uint32_t)n, s->d_logits, nullptr, s->own);
     if (st == GPT2_OK) st = gpt2_session_sync(s);
     if (st == GPT2_OK)
         st = cuda_status(cudaMemcpy(logits_out, s->d_logits, sizeof(float) * cfg->vocab, cudaMemcpyDeviceToHost));

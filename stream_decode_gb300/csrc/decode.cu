@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     constexpr int P3 = (3 * D + NT - 1) / NT;  // qkv words per thread (trace)
     constexpr int PV = PF > P3 ? PF : P3;      // words per thread of any gathered vector
     constexpr int PM = PD * kMaxSplits;        // attention partial words per thread (merge)
-    static_assert(PM <= 64 && PV <= 64, "tagged gathers hold at most 64 words per thread");
+    static_assert(PM + 2 <= 64 && PV <= 64, "tagged gathers hold at most 64 words per thread");
     uint32_t gi = 0;  // chunks consumed (same sequence as the producer)
     using KD = std::integral_constant<int, D>;
     using KF = std::integral_constant<int, FF>;
@@ -808,11 +808,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // agreement barrier (*release = its chunk count); a streamed share's
     // chunks are released by the warp that used them, with a named barrier
     // per round of chunks so warp skew stays below one ring length.
-    auto run_gemv = [&](auto kk, int kind, int mat, unsigned tag, uint64_t boff, float* kv_row, float* lg,
+    auto run_gemv = [&](auto kk, int kind, const Geo& g, unsigned tag, uint64_t boff, float* kv_row, float* lg,
                         int* release) -> bool {
         constexpr int KK = decltype(kk)::value;
         using R = Rows<KK, Q8>;
-        const Geo g = geo_of(P, geot, mat);
         auto epilogue = [&](int j, float y) {
             if (kind == kPhVocab) {
                 if (lg) lg[j] = y;
@@ -1004,8 +1003,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             if (tid < DH) {
                 const int c = tid / DPL, d = tid - c * DPL;
                 float M = -INFINITY;
+#pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stage[(w * LPK + c) * (2 + DPL)]);
                 float Z = 0.0f, O = 0.0f;
+#pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) {
                     const float* st = stage + (w * LPK + c) * (2 + DPL);
                     if (st[0] == -INFINITY) continue;
@@ -1144,36 +1145,36 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                                                                                   : 0.0f;
             // ---- inputs
             bool ok = true;
-            uint64_t ov[PM];  // out-projection: every split's o words of this thread's coordinates
+            uint64_t ov[PM + 2];  // out-projection: o words of every split, then (max, sum) words
             float xv[PD];     // LayerNorm phases: this thread's coordinates of the residual stream
             if (kind == kPhO) {
-                // (max, sum) of every unit into stage[2u], stage[2u + 1]
+                // One wait for every split's o words of this thread's coordinates
+                // (k < PM) and, for threads below 2 * units, one (max, sum) word
+                // (k = PM, PM + 1), which then goes to stage[2u], stage[2u + 1].
                 const int nmz = 2 * P.H * S_eff;
-                uint64_t wmz[2];
-                const bool ok1 = tagged_wait<2>(
-                    wmz, own_words<2>(nmz, tid), tag - 1u,
-                    [&](int k) {
-                        const int w = tid + NT * k;
-                        return P.attn_part + (size_t)(w >> 1) * (DH + 2) + (w & 1);
-                    },
-                    P);
-#pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    if (tid + NT * k < nmz) stage[tid + NT * k] = val_of(wmz[k]);
                 uint64_t want = 0;
 #pragma unroll
                 for (int i = 0; i < PD; ++i)
                     if (tid + NT * i < D)
                         for (int sp = 0; sp < S_eff; ++sp) want |= 1ull << (i * kMaxSplits + sp);
-                const bool ok2 = tagged_wait<PM>(
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (tid + NT * k < nmz) want |= 1ull << (PM + k);
+                ok = tagged_wait<PM + 2>(
                     ov, want, tag - 1u,
                     [&](int k) {
+                        if (k >= PM) {
+                            const int w = tid + NT * (k - PM);
+                            return P.attn_part + (size_t)(w >> 1) * (DH + 2) + (w & 1);
+                        }
                         const int idx = tid + NT * (k / kMaxSplits), sp = k % kMaxSplits;
                         const int h = idx / DH, e = idx - h * DH;
                         return P.attn_part + (size_t)(h * S_eff + sp) * (DH + 2) + 2 + e;
                     },
                     P);
-                ok = ok1 && ok2;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (tid + NT * k < nmz) stage[tid + NT * k] = val_of(ov[PM + k]);
             } else if (kind == kPhQKV && l == 0) {
 #pragma unroll
                 for (int k = 0; k < PD; ++k) {
@@ -1265,8 +1266,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             float* lg = (kind == kPhVocab && P.logits) ? P.logits + (uint64_t)s * P.logits_stride : nullptr;
             int release = 0;
             cstamp(4);
-            ok = kind == kPhP ? run_gemv(KF{}, kind, mat, out_tag(tag), boff, kv_row, lg, &release)
-                              : run_gemv(KD{}, kind, mat, out_tag(tag), boff, kv_row, lg, &release);
+            ok = kind == kPhP ? run_gemv(KF{}, kind, g, out_tag(tag), boff, kv_row, lg, &release)
+                              : run_gemv(KD{}, kind, g, out_tag(tag), boff, kv_row, lg, &release);
             if (!agree(ok)) { alive = false; break; }
             if (warp == 0 && lane < release) mbar_arrive(&empty[(gi + (uint32_t)lane) % kSlots]);
             gi += (uint32_t)release;

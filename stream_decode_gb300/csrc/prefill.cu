@@ -1,0 +1,434 @@
+// prefill.cu -- the full-prefix forward pass of a prompt ("infer", LeanExe
+// GPT-2 README, infer paragraph) on the tensor cores, writing the session's
+// KV cache for every prompt position on the way.
+//
+// Per layer: LN1 -> QKV projection (+ KV-cache rows) -> causal attention ->
+// out-projection + residual -> LN2 -> FC + GELU -> MLP projection +
+// residual; then LN_f and the tied vocabulary projection of the last row
+// only.  The four projections are 3xTF32 tcgen05 GEMMs (tc_gemm.cuh) over
+// 128-row x 64-column tiles, split along K so that about one CTA per SM
+// works; a deterministic reduce kernel sums the splits in split order and
+// applies the projection's epilogue.  Every GEMM input is written with its
+// TF32 remainder (x - hi(x)) next to it; the weights' remainders are made
+// once per model.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "gpt2_dev.cuh"
+#include "model_internal.h"
+#include "prefill.h"
+#include "tc_gemm.cuh"
+
+namespace gpt2 {
+
+namespace {
+
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & ~0x1FFFu); }
+__device__ __forceinline__ float tf32_lo(float x) { return __fsub_rn(x, tf32_hi(x)); }
+
+__device__ __forceinline__ float warp_sum32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float gelu(float x) {
+    const float inner = 0.7978845608f * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + tanhf(inner));
+}
+
+// lo[i] = w[i] - hi(w[i]) over n floats.
+__global__ void split_lo_kernel(const float* __restrict__ w, float* __restrict__ lo, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        lo[i] = tf32_lo(w[i]);
+}
+
+// X[i][:] = wte[tok_i] + wpe[i]; an out-of-range token sets the status and
+// leaves its row unwritten.
+__global__ void embed_kernel(const float* __restrict__ packed, uint64_t wte_off, uint64_t wpe_off,
+                             const uint32_t* __restrict__ tok, int D, uint32_t vocab, float* __restrict__ X,
+                             int* status) {
+    const int i = blockIdx.x;
+    const uint32_t t = tok[i];
+    if (t >= vocab) {
+        if (threadIdx.x == 0) atomicCAS(status, 0, (int)kDevToken);
+        return;
+    }
+    for (int j = threadIdx.x; j < D; j += blockDim.x)
+        X[(size_t)i * D + j] = __fadd_rn(packed[wte_off + (uint64_t)t * D + j], packed[wpe_off + (uint64_t)i * D + j]);
+}
+
+constexpr int kLnRowsPerBlock = 8;
+constexpr int kMaxLanesVals = 32;  // D <= 1024
+
+// Y = LN(X) (mean, then the biased variance of the deviations; eps 1e-5)
+// and its TF32 remainder, one warp per row.
+__global__ void ln_split_kernel(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ b,
+                                int n, int D, float* __restrict__ Y, float* __restrict__ Ylo) {
+    const int row = blockIdx.x * kLnRowsPerBlock + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= n) return;
+    const float* x = X + (size_t)row * D;
+    float v[kMaxLanesVals];
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kMaxLanesVals; ++k) {
+        const int i = lane + 32 * k;
+        v[k] = i < D ? x[i] : 0.0f;
+        s += v[k];
+    }
+    const float mean = warp_sum32(s) / (float)D;
+    float q = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kMaxLanesVals; ++k)
+        if (lane + 32 * k < D) {
+            const float t = v[k] - mean;
+            q = fmaf(t, t, q);
+        }
+    const float den = sqrtf(warp_sum32(q) / (float)D + kLnEps);
+#pragma unroll
+    for (int k = 0; k < kMaxLanesVals; ++k) {
+        const int i = lane + 32 * k;
+        if (i < D) {
+            const float y = (v[k] - mean) / den * g[i] + b[i];
+            Y[(size_t)row * D + i] = y;
+            Ylo[(size_t)row * D + i] = tf32_lo(y);
+        }
+    }
+}
+
+enum ReduceKind : int { kRedQKV = 0, kRedResidual = 1, kRedGelu = 2 };
+
+// y[i][j] = (sum over splits s = 0, 1, ... of part[s][i][j]) + bias[j], then
+// QKV: out[i][j] = y and, for key/value columns, the cache row of
+// position i; residual: X[i][j] += y; GELU: out = gelu(y) and its remainder.
+__global__ void reduce_kernel(const float* __restrict__ part, int splits, int n, int N,
+                              const float* __restrict__ bias, int kind, float* __restrict__ out,
+                              float* __restrict__ out_lo, float* __restrict__ X, float* __restrict__ cache, int L,
+                              int l, int D) {
+    const size_t total = (size_t)n * N;
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int i = (int)(idx / N), j = (int)(idx - (size_t)i * N);
+        float y = 0.0f;
+        for (int s = 0; s < splits; ++s) y += part[((size_t)s * n + i) * N + j];
+        y = __fadd_rn(y, bias[j]);
+        if (kind == kRedQKV) {
+            out[idx] = y;
+            if (j >= D) cache[((size_t)i * L + l) * 2 * D + (j - D)] = y;
+        } else if (kind == kRedResidual) {
+            X[idx] = __fadd_rn(X[idx], y);
+        } else {
+            const float u = gelu(y);
+            out[idx] = u;
+            out_lo[idx] = tf32_lo(u);
+        }
+    }
+}
+
+constexpr int kAttnWarps = 8;
+constexpr int kMaxPrefillKeys = 1024;
+
+// Causal attention of query row i (one warp) and head h over keys 0..i:
+// s_j = (q . k_j) / sqrt(dh); softmax; o = sum_j a_j v_j.  Writes the
+// head's output slice of row i and its remainder.
+__global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float* __restrict__ QKV, int n, int D,
+                                                                    int DH, float* __restrict__ O,
+                                                                    float* __restrict__ Olo) {
+    __shared__ float sc[kAttnWarps][kMaxPrefillKeys];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x, i = blockIdx.y * kAttnWarps + warp;
+    if (i >= n) return;
+    const size_t N3 = 3 * (size_t)D;
+    const float* q = QKV + (size_t)i * N3 + (size_t)h * DH;
+    const float scale = 1.0f / sqrtf((float)DH);
+    float* s = sc[warp];
+    float m = -INFINITY;
+    for (int j = lane; j <= i; j += 32) {
+        const float* k = QKV + (size_t)j * N3 + D + (size_t)h * DH;
+        float dot = 0.0f;
+        for (int e = 0; e < DH; e += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(q + e), c = *reinterpret_cast<const float4*>(k + e);
+            dot = fmaf(a.x, c.x, dot);
+            dot = fmaf(a.y, c.y, dot);
+            dot = fmaf(a.z, c.z, dot);
+            dot = fmaf(a.w, c.w, dot);
+        }
+        const float v = dot * scale;
+        s[j] = v;
+        m = fmaxf(m, v);
+    }
+    m = warp_max32(m);
+    float z = 0.0f;
+    for (int j = lane; j <= i; j += 32) {
+        const float e = expf(s[j] - m);
+        s[j] = e;
+        z += e;
+    }
+    z = warp_sum32(z);
+    __syncwarp();
+    for (int e = lane; e < DH; e += 32) {
+        float acc = 0.0f;
+        for (int j = 0; j <= i; ++j) acc = fmaf(s[j], QKV[(size_t)j * N3 + 2 * D + (size_t)h * DH + e], acc);
+        const float o = acc / z;
+        O[(size_t)i * D + (size_t)h * DH + e] = o;
+        Olo[(size_t)i * D + (size_t)h * DH + e] = tf32_lo(o);
+    }
+}
+
+constexpr int kHeadThreads = 256;
+
+// Greedy choice over the logits (largest value, lowest index on ties; any
+// non-finite value makes the choice 0xFFFFFFFF and sets the status).
+__global__ void __launch_bounds__(256) choice_kernel(const float* __restrict__ v, unsigned n, uint32_t* choice,
+                                                     uint32_t* next, int* status) {
+    __shared__ float s_v[8];
+    __shared__ unsigned s_i[8];
+    __shared__ int s_nf[8];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float bv = -INFINITY;
+    unsigned bi = 0xFFFFFFFFu;
+    int nf = 0;
+    for (unsigned j = tid; j < n; j += 256) {
+        const float x = v[j];
+        if (!isfinite(x)) nf = 1;
+        else if (x > bv || (x == bv && j < bi)) { bv = x; bi = j; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const unsigned oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        nf |= __shfl_xor_sync(0xffffffffu, nf, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) { s_v[warp] = bv; s_i[warp] = bi; s_nf[warp] = nf; }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < 8; ++w) {
+            nf |= s_nf[w];
+            if (s_v[w] > bv || (s_v[w] == bv && s_i[w] < bi)) { bv = s_v[w]; bi = s_i[w]; }
+        }
+        const uint32_t c = nf ? 0xFFFFFFFFu : bi;
+        *choice = c;
+        if (next) *next = c;
+        if (nf) atomicCAS(status, 0, (int)kDevNonfinite);
+    }
+}
+
+// logits[r] = wte[r] . LN_f(X[last]) for r < V; every block recomputes the
+// final LayerNorm of the last row into shared memory (D <= 1024).
+__global__ void __launch_bounds__(kHeadThreads) head_kernel(const float* __restrict__ X, int last,
+                                                            const float* __restrict__ g,
+                                                            const float* __restrict__ b,
+                                                            const float* __restrict__ wte, int D, int V,
+                                                            float* __restrict__ logits) {
+    __shared__ __align__(16) float xs[1024];
+    __shared__ float red[kHeadThreads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float* x = X + (size_t)last * D;
+    float s = 0.0f;
+    for (int i = tid; i < D; i += kHeadThreads) s += x[i];
+    s = warp_sum32(s);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    float t = 0.0f;
+    for (int w = 0; w < kHeadThreads / 32; ++w) t += red[w];
+    const float mean = t / (float)D;
+    __syncthreads();
+    float q = 0.0f;
+    for (int i = tid; i < D; i += kHeadThreads) {
+        const float d = x[i] - mean;
+        q = fmaf(d, d, q);
+    }
+    q = warp_sum32(q);
+    if (lane == 0) red[warp] = q;
+    __syncthreads();
+    float v = 0.0f;
+    for (int w = 0; w < kHeadThreads / 32; ++w) v += red[w];
+    const float den = sqrtf(v / (float)D + kLnEps);
+    for (int i = tid; i < D; i += kHeadThreads) xs[i] = (x[i] - mean) / den * g[i] + b[i];
+    __syncthreads();
+    const int nv = D / 4;
+    const float4* x4 = reinterpret_cast<const float4*>(xs);
+    for (int r = blockIdx.x * (kHeadThreads / 32) + warp; r < V; r += gridDim.x * (kHeadThreads / 32)) {
+        const float4* w4 = reinterpret_cast<const float4*>(wte + (size_t)r * D);
+        float acc = 0.0f;
+        for (int c = lane; c < nv; c += 32) {
+            const float4 a = __ldcs(w4 + c), xx = x4[c];
+            acc = fmaf(a.x, xx.x, acc);
+            acc = fmaf(a.y, xx.y, acc);
+            acc = fmaf(a.z, xx.z, acc);
+            acc = fmaf(a.w, xx.w, acc);
+        }
+        acc = warp_sum32(acc);
+        if (lane == 0) logits[r] = acc;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_ready() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// K-major fp32 matrix [rows][K] (row stride K floats) with a {32, box_rows} box.
+bool kmajor_map(CUtensorMap* map, const float* base, int K, int rows, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 4};
+    cuuint32_t box[2] = {(cuuint32_t)tc::kBlockK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_sms = 0;
+
+// K splits for an (m tiles x n tiles) grid so that about one CTA per SM works.
+int choose_splits(int m_tiles, int n_tiles, int K) {
+    const int nkb = K / tc::kBlockK;
+    const int tiles = m_tiles * n_tiles;
+    int s = (g_sms + tiles / 2) / tiles;
+    if (s < 1) s = 1;
+    if (s > nkb) s = nkb;
+    if (s > kPrefillMaxSplits) s = kPrefillMaxSplits;
+    return s;
+}
+
+}  // namespace
+
+size_t prefill_part_floats(int cap, int D, int FF) {
+    const int n = cap, N = FF > 3 * D ? FF : 3 * D;
+    return (size_t)kPrefillMaxSplits * n * N;
+}
+
+cudaError_t prefill_make_lo(gpt2_model* m, cudaStream_t st) {
+    if (m->d_wlo) return cudaSuccess;
+    const size_t bytes = m->layer_bytes * m->cfg.n_layer;
+    cudaError_t e = cudaMalloc(&m->d_wlo, bytes);
+    if (e != cudaSuccess) return e;
+    split_lo_kernel<<<1024, 256, 0, st>>>(reinterpret_cast<const float*>(m->d_wstream), m->d_wlo, bytes / 4);
+    return cudaGetLastError();
+}
+
+cudaError_t prefill_alloc(PrefillWs* w, int cap, int D, int FF) {
+    if (w->cap >= cap) return cudaSuccess;
+    prefill_free(w);
+    const size_t nd = (size_t)cap * D, nf = (size_t)cap * FF;
+    cudaError_t e = cudaMalloc(&w->X, nd * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&w->A, nd * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&w->Alo, nd * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&w->QKV, 3 * nd * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&w->U, nf * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&w->Ulo, nf * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&w->part, prefill_part_floats(cap, D, FF) * 4);
+    if (e != cudaSuccess) {
+        prefill_free(w);
+        return e;
+    }
+    w->cap = cap;
+    return cudaSuccess;
+}
+
+void prefill_free(PrefillWs* w) {
+    cudaFree(w->X);
+    cudaFree(w->A);
+    cudaFree(w->Alo);
+    cudaFree(w->QKV);
+    cudaFree(w->U);
+    cudaFree(w->Ulo);
+    cudaFree(w->part);
+    *w = PrefillWs{};
+}
+
+bool prefill_shape_supported(const gpt2_config& c) {
+    const int D = (int)c.d_model, FF = (int)c.d_ff, DH = D / (int)c.n_head;
+    return D % tc::kTileN == 0 && FF % tc::kTileN == 0 && D <= 1024 && DH % 4 == 0 && c.max_pos <= kMaxPrefillKeys;
+}
+
+cudaError_t prefill_enqueue(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, int n, float* cache, float* logits,
+                            int* status, uint32_t* d_choice, uint32_t* d_next, cudaStream_t st) {
+    if (!encode_ready()) return cudaErrorNotSupported;
+    if (!g_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_sms <= 0) g_sms = 1;
+    }
+    const gpt2_config& c = m->cfg;
+    const int D = (int)c.d_model, FF = (int)c.d_ff, L = (int)c.n_layer, H = (int)c.n_head, DH = D / H;
+    cudaError_t e = cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc::kTcSmem);
+    if (e != cudaSuccess) return e;
+    const float* P = m->d_packed;
+    const int m_tiles = (n + tc::kTileM - 1) / tc::kTileM;
+
+    // C[n][N] partials of A[n][K] x W[N][K] (W = block matrix `mat` of layer l)
+    auto gemm = [&](const float* A, const float* Alo, int K, int N, int l, int mat, int* splits_out) -> cudaError_t {
+        const uint64_t off = (uint64_t)l * m->layer_bytes + m->mat_off[mat];
+        const float* W = reinterpret_cast<const float*>(m->d_wstream + off);
+        const float* Wlo = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(m->d_wlo) + off);
+        tc::TcMaps maps;
+        if (!kmajor_map(&maps.a_hi, A, K, n, tc::kTileM) || !kmajor_map(&maps.a_lo, Alo, K, n, tc::kTileM) ||
+            !kmajor_map(&maps.b_hi, W, K, N, tc::kTileN) || !kmajor_map(&maps.b_lo, Wlo, K, N, tc::kTileN))
+            return cudaErrorInvalidValue;
+        const int n_tiles = N / tc::kTileN;
+        const int splits = choose_splits(m_tiles, n_tiles, K);
+        *splits_out = splits;
+        tc::tf32x3_gemm_kernel<<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::kTcSmem, st>>>(
+            maps, K, N, n, splits, w->part, status, (int)kDevTimeout);
+        return cudaGetLastError();
+    };
+    auto reduce = [&](int splits, int N, uint64_t bias_off, int kind, float* out, float* out_lo, int l) {
+        const size_t total = (size_t)n * N;
+        const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+        reduce_kernel<<<blocks, 256, 0, st>>>(w->part, splits, n, N, P + bias_off, kind, out, out_lo, w->X, cache, L,
+                                              l, D);
+        return cudaGetLastError();
+    };
+    const int ln_blocks = (n + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
+
+    embed_kernel<<<n, 256, 0, st>>>(P, m->wte_off, m->wpe_off, d_tok, D, c.vocab, w->X, status);
+    e = cudaGetLastError();
+    for (int l = 0; l < L && e == cudaSuccess; ++l) {
+        const LayerParams& lp = m->lp[l];
+        int sp = 1;
+        ln_split_kernel<<<ln_blocks, kLnRowsPerBlock * 32, 0, st>>>(w->X, P + lp.ln1_g, P + lp.ln1_b, n, D, w->A,
+                                                                    w->Alo);
+        if ((e = gemm(w->A, w->Alo, D, 3 * D, l, kQKV, &sp)) != cudaSuccess) break;
+        if ((e = reduce(sp, 3 * D, lp.b_qkv, kRedQKV, w->QKV, nullptr, l)) != cudaSuccess) break;
+        attention_kernel<<<dim3(H, (n + kAttnWarps - 1) / kAttnWarps), kAttnWarps * 32, 0, st>>>(w->QKV, n, D, DH,
+                                                                                                  w->A, w->Alo);
+        if ((e = gemm(w->A, w->Alo, D, D, l, kO, &sp)) != cudaSuccess) break;
+        if ((e = reduce(sp, D, lp.b_o, kRedResidual, nullptr, nullptr, l)) != cudaSuccess) break;
+        ln_split_kernel<<<ln_blocks, kLnRowsPerBlock * 32, 0, st>>>(w->X, P + lp.ln2_g, P + lp.ln2_b, n, D, w->A,
+                                                                    w->Alo);
+        if ((e = gemm(w->A, w->Alo, D, FF, l, kFC, &sp)) != cudaSuccess) break;
+        if ((e = reduce(sp, FF, lp.b_fc, kRedGelu, w->U, w->Ulo, l)) != cudaSuccess) break;
+        if ((e = gemm(w->U, w->Ulo, FF, D, l, kP, &sp)) != cudaSuccess) break;
+        if ((e = reduce(sp, D, lp.b_p, kRedResidual, nullptr, nullptr, l)) != cudaSuccess) break;
+    }
+    if (e != cudaSuccess) return e;
+    head_kernel<<<g_sms, kHeadThreads, 0, st>>>(w->X, n - 1, P + m->lnf_g, P + m->lnf_b, P + m->wte_off, D,
+                                                (int)c.vocab, logits);
+    choice_kernel<<<1, 256, 0, st>>>(logits, c.vocab, d_choice, d_next, status);
+    return cudaGetLastError();
+}
+
+}  // namespace gpt2

@@ -1,0 +1,41 @@
+// prefill.h -- the tensor-core prompt prefill (full-prefix forward pass)
+// shared between prefill.cu and the C ABI in api.cu.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/gpt2.h"
+
+struct gpt2_model;
+
+namespace gpt2 {
+
+constexpr int kPrefillMaxSplits = 16;  // K splits of one projection at most
+
+// Per-session prefill workspace for up to `cap` prompt rows.
+struct PrefillWs {
+    int cap = 0;
+    float* X = nullptr;     // [cap][d] residual stream
+    float* A = nullptr;     // [cap][d] projection input (LN output or attention output)
+    float* Alo = nullptr;   // its TF32 remainder
+    float* QKV = nullptr;   // [cap][3d]
+    float* U = nullptr;     // [cap][d_ff] GELU output
+    float* Ulo = nullptr;   // its TF32 remainder
+    float* part = nullptr;  // split-K partial tiles
+};
+
+bool prefill_shape_supported(const gpt2_config& c);
+// The model's block-matrix TF32 remainders (made once, on stream st).
+cudaError_t prefill_make_lo(gpt2_model* m, cudaStream_t st);
+cudaError_t prefill_alloc(PrefillWs* w, int cap, int D, int FF);
+void prefill_free(PrefillWs* w);
+// Enqueues the prefill of n device token ids; writes cache rows 0..n-1,
+// the logits of row n-1, the greedy choice of those logits into *d_choice
+// (0xFFFFFFFF and status GPT2_ERR_NONFINITE-coded if any logit is not
+// finite) and, if d_next is not null, into *d_next too.
+cudaError_t prefill_enqueue(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, int n, float* cache, float* logits,
+                            int* status, uint32_t* d_choice, uint32_t* d_next, cudaStream_t st);
+
+}  // namespace gpt2

@@ -52,6 +52,7 @@ _SIGS = {
     "gpt2_session_read_cache": ([_vp, _vp, _sz, _szp], _i32),
     "gpt2_session_rewind": ([_vp, _u32], _i32),
     "gpt2_session_run": ([_vp, _vp, _u32, _vp, _sz, _vp, _vp], _i32),
+    "gpt2_session_prefill": ([_vp, _vp, _u32, _vp, _vp, _vp], _i32),
     "gpt2_session_step": ([_vp, _u32, _vp, _vp, _vp], _i32),
     "gpt2_session_step_host": ([_vp, _u32, _vp, _vp], _i32),
     "gpt2_session_sync": ([_vp], _i32),
@@ -203,6 +204,11 @@ class Session:
     def run(self, tokens_in, n_steps: int, logits=None, stride: int = 0, tokens_out=None, stream=None) -> str:
         return STATUS[lib.gpt2_session_run(self.h, _ptr(tokens_in), n_steps, _ptr(logits), stride,
                                            _ptr(tokens_out), _stream(stream))]
+
+    def prefill(self, tokens, n: int, logits=None, next_token=None, stream=None) -> str:
+        """Tensor-core prefill of n device token ids from an empty session (gpt2_session_prefill)."""
+        return STATUS[lib.gpt2_session_prefill(self.h, _ptr(tokens), n, _ptr(logits), _ptr(next_token),
+                                               _stream(stream))]
 
     def step(self, token: int, logits=None, next_token=None, stream=None) -> str:
         return STATUS[lib.gpt2_session_step(self.h, token & 0xFFFFFFFF, _ptr(logits), _ptr(next_token),
