@@ -207,6 +207,39 @@ def kernel_hash():
     return h.hexdigest()
 
 
+PREFILL_GFLOP_128 = 21.82  # GEMMs (2 x 128 x 85M block weights) + attention + the last row's head
+
+
+def prefill_rate(g, torch, shape, w, n: int = 128, reps: int = 10):
+    """The 128-token full-prefix pass (gpt2_session_prefill, tensor cores):
+    median ms over `reps` calls (CUDA events on the launching stream, the
+    session rewound to position 0 between calls) and algorithmic TFLOP/s."""
+    from stream_decode_gb300 import synth
+    model = g.Model(shape, w)
+    sess = g.Session(model)
+    toks = torch.tensor(synth.tokens(shape.vocab, n, seed=11).astype(np.int32), device="cuda")
+    lg = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        assert sess.rewind(0) == "ok" and sess.prefill(toks, n, lg, None, st) == "ok"
+    assert sess.sync() == "ok"
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(reps):
+        assert sess.rewind(0) == "ok"
+        e0.record(st)
+        assert sess.prefill(toks, n, lg, None, st) == "ok"
+        e1.record(st)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert sess.sync() == "ok"
+    sess.close()
+    model.close()
+    ms = float(np.median(times))
+    return {"tokens": n, "ms_per_infer": ms, "TFLOP_per_s": PREFILL_GFLOP_128 * (n / 128) / ms,
+            "arith": "3xTF32 tcgen05 GEMMs, binary32 elsewhere"}
+
+
 def measure_decode(g, torch, shape, w, toks, quant: str, args, rank_sync):
     """Returns (ms per bench step, launches, session) after W warm-ups and K timed steps."""
     q = g.INT8_G64 if quant == "int8" else g.F32
@@ -371,6 +404,7 @@ def main():
             s8.close()
             m8.close()
         extra["long_context_f32"] = long_context(g, torch, w)
+        extra["prefill_f32"] = prefill_rate(g, torch, shape, w)
 
     cpu = None
     if rank == 0:
