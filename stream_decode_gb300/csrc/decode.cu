@@ -334,6 +334,102 @@ __device__ __forceinline__ float coop_f32(const uint8_t* ring, uint32_t c0, int 
     return y;
 }
 
+// Register preload of a spread binary32 share: thread t's float4 columns
+// (t, t + NT, ...) of the share's first ROWS rows are loaded into registers
+// before the phase waits for its inputs, so the smem reads overlap that
+// wait; once the input vector is known the projection is FMAs and the
+// reduction only.  kPreRegs float4 per thread: 8 rows at K = 768, 2 rows
+// x 4 columns at K = 3072 (measured best: more registers spill, as the step
+// kernel is at the 255-register limit).
+constexpr int kPreRegs = 8;
+template <int K>
+struct Pre {
+    static constexpr int NT = kConsumerWarps * 32;
+    static constexpr int NV = K / 4;                 // float4 columns per row
+    static constexpr int NC = (NV + NT - 1) / NT;    // columns per thread
+    static constexpr int ROWS = kPreRegs / NC;       // rows held in registers
+    static_assert(NC * ROWS <= kPreRegs && ROWS >= 1, "preload fits the register block");
+};
+
+template <int K>
+__device__ __forceinline__ uint32_t share_row_off(uint32_t c0, int r) {
+    using R = Rows<K, false>;
+    return ((c0 + (uint32_t)(r / R::RPC)) % kSlots) * (uint32_t)kSlotBytes + (uint32_t)((r % R::RPC) * R::RB);
+}
+
+template <int K>
+__device__ __forceinline__ void preload_share(float4 (&w)[kPreRegs], const uint8_t* ring, uint32_t c0, int nrows,
+                                              int tid) {
+    using Q = Pre<K>;
+#pragma unroll
+    for (int cc = 0; cc < Q::NC; ++cc) {
+        const int col = tid + Q::NT * cc;
+#pragma unroll
+        for (int r = 0; r < Q::ROWS; ++r)
+            if (col < Q::NV && r < nrows)
+                w[cc * Q::ROWS + r] = *reinterpret_cast<const float4*>(ring + share_row_off<K>(c0, r) + 16u * (uint32_t)col);
+    }
+}
+
+// The cooperative projection of a preloaded share, rows r0..r0+NR-1 that
+// are below nrows: rows below Pre<K>::ROWS from registers, the rest from
+// shared memory; warp partials of row r to part[warp][r].
+template <int K, int NR>
+__device__ __forceinline__ void coop_pre_part(const float4 (&wr)[kPreRegs], const uint8_t* ring, uint32_t c0, int r0,
+                                              int nrows, const float* x, float* part, int tid) {
+    using Q = Pre<K>;
+    const int warp = tid >> 5, lane = tid & 31;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    float acc[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int cc = 0; cc < Q::NC; ++cc) {
+        const int col = tid + Q::NT * cc;
+        if (col < Q::NV) {
+            const float4 xv = x4[col];
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                const int r = r0 + i;
+                if (r < nrows) {
+                    float4 wv;
+                    if (r0 == 0 && i < Q::ROWS) wv = wr[cc * Q::ROWS + i];
+                    else wv = *reinterpret_cast<const float4*>(ring + share_row_off<K>(c0, r) + 16u * (uint32_t)col);
+                    acc[i] = fmaf(xv.x, wv.x, acc[i]);
+                    acc[i] = fmaf(xv.y, wv.y, acc[i]);
+                    acc[i] = fmaf(xv.z, wv.z, acc[i]);
+                    acc[i] = fmaf(xv.w, wv.w, acc[i]);
+                }
+            }
+        }
+    }
+    const float t = warp_transpose_sum<NR>(acc, lane);
+    if (lane < NR && r0 + lane < nrows) part[warp * kSpreadRows + r0 + lane] = t;
+}
+
+// Rows 0..nrows-1 (<= kSpreadRows) of a preloaded spread share against x in
+// row groups of 16; thread r < nrows returns row r's total (the warps'
+// partials summed in warp order), others 0.  Contains a barrier over the
+// consumer warps.
+template <int K>
+__device__ __forceinline__ float coop_pre(const float4 (&wr)[kPreRegs], const uint8_t* ring, uint32_t c0, int nrows,
+                                          const float* x, float* part, int tid) {
+    static_assert(Pre<K>::ROWS <= 16, "registers hold rows of the first group only");
+    if (nrows > 8) {
+        coop_pre_part<K, 16>(wr, ring, c0, 0, nrows, x, part, tid);
+        if (nrows > 16) coop_pre_part<K, 16>(wr, ring, c0, 16, nrows, x, part, tid);
+    } else {
+        coop_pre_part<K, 8>(wr, ring, c0, 0, nrows, x, part, tid);
+    }
+    consumers_sync();
+    float y = 0.0f;
+    if (tid < nrows) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) y += part[w * kSpreadRows + tid];
+    }
+    return y;
+}
+
 // Exact int32 sum of the 64 products of one group (two independent dp4a
 // chains; integer addition is exact in any order).
 __device__ __forceinline__ int group_dot(const uint8_t* w, const int8_t* x) {
@@ -809,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // chunks are released by the warp that used them, with a named barrier
     // per round of chunks so warp skew stays below one ring length.
     auto run_gemv = [&](auto kk, int kind, const Geo& g, unsigned tag, uint64_t boff, float* kv_row, float* lg,
-                        int* release) -> bool {
+                        int* release, const float4 (&wr)[kPreRegs]) -> bool {
         constexpr int KK = decltype(kk)::value;
         using R = Rows<KK, Q8>;
         auto epilogue = [&](int j, float y) {
@@ -832,12 +928,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         *release = 0;
         bool ok = true;
         if (share_spread(g.nchunks, g.nrows, KK, Q8)) {
-            if (warp == 0) ok = wait_chunks(gi, g.nchunks);
+            // every warp saw the share's chunks land before the phase's input wait
             cstamp(7);
-            if (!agree(ok)) return false;  // the cooperative body has barriers: all warps or none
             float y;
             if constexpr (Q8) y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
-            else y = coop_f32<KK>(ring, gi, g.nrows, vin, stage, tid);
+            else y = coop_pre<KK>(wr, ring, gi, g.nrows, vin, stage, tid);
             if (tid < g.nrows) epilogue(g.r0 + tid, y);
             cstamp(5);
             *release = g.nchunks;
@@ -1015,10 +1110,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     O = fmaf(st[2 + d], cw, O);
                 }
                 uint64_t* part = P.attn_part + (size_t)u * (DH + 2);
-                st_tagged(part + 2 + tid, tg, O);
-                if (tid == 0) {
-                    st_tagged(part, tg, M);
-                    st_tagged(part + 1, tg, Z);
+                if (S_eff == 1) {
+                    st_tagged(part + 2 + tid, tg, O / Z);  // the head's output, normalised
+                } else {
+                    st_tagged(part + 2 + tid, tg, O);
+                    if (tid == 0) {
+                        st_tagged(part, tg, M);
+                        st_tagged(part + 1, tg, Z);
+                    }
                 }
             }
             consumers_sync();
@@ -1143,15 +1242,28 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             const uint64_t boff = kind == kPhQKV ? lp.b_qkv : kind == kPhO ? lp.b_o : kind == kPhFC ? lp.b_fc : lp.b_p;
             const float bv = (kind != kPhVocab && g.nrows <= NT && tid < g.nrows) ? __ldg(P.packed + boff + g.r0 + tid)
                                                                                   : 0.0f;
-            // ---- inputs
+            // ---- weights of a spread share: every warp checks that the share's
+            // chunks have landed (they were issued phases ago) and, for
+            // binary32, loads its register fragments before waiting for inputs
             bool ok = true;
+            float4 wreg[kPreRegs];
+            const bool spread = share_spread(g.nchunks, g.nrows, kind == kPhP ? FF : D, Q8);
+            if (spread) {
+                ok = wait_chunks(gi, g.nchunks);
+                __syncwarp();
+                if constexpr (!Q8) {
+                    if (kind == kPhP) preload_share<FF>(wreg, ring, gi, g.nrows, tid);
+                    else preload_share<D>(wreg, ring, gi, g.nrows, tid);
+                }
+            }
+            // ---- inputs
             uint64_t ov[PM + 2];  // out-projection: o words of every split, then (max, sum) words
             float xv[PD];     // LayerNorm phases: this thread's coordinates of the residual stream
             if (kind == kPhO) {
                 // One wait for every split's o words of this thread's coordinates
                 // (k < PM) and, for threads below 2 * units, one (max, sum) word
                 // (k = PM, PM + 1), which then goes to stage[2u], stage[2u + 1].
-                const int nmz = 2 * P.H * S_eff;
+                const int nmz = S_eff == 1 ? 0 : 2 * P.H * S_eff;  // one split: outputs already normalised
                 uint64_t want = 0;
 #pragma unroll
                 for (int i = 0; i < PD; ++i)
@@ -1160,7 +1272,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
                     if (tid + NT * k < nmz) want |= 1ull << (PM + k);
-                ok = tagged_wait<PM + 2>(
+                ok = ok & tagged_wait<PM + 2>(
                     ov, want, tag - 1u,
                     [&](int k) {
                         if (k >= PM) {
@@ -1193,9 +1305,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     }
                 }
             } else if (kind == kPhP) {
-                ok = gather_vec<PV>(P.u, FF, tag - 1u, vin, tid, P);
+                ok = ok & gather_vec<PV>(P.u, FF, tag - 1u, vin, tid, P);
             } else {
-                ok = gather_vals<PD>(kind == kPhFC ? P.xb : P.xa, D, tag - 1u, xv, tid, P);
+                ok = ok & gather_vals<PD>(kind == kPhFC ? P.xb : P.xa, D, tag - 1u, xv, tid, P);
             }
             if (has_ln) {
                 // the residual stream, kept for the epilogue's residual add (and the trace)
@@ -1210,6 +1322,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             // ---- input transform: LayerNorm, or the merge of the heads' partials
             if (has_ln) {
                 layernorm_vals<D>(xv, gr, br, vin, red, tid);
+            } else if (kind == kPhO && S_eff == 1) {
+#pragma unroll
+                for (int i = 0; i < PD; ++i)
+                    if (tid + NT * i < D) vin[tid + NT * i] = val_of(ov[i * kMaxSplits]);
             } else if (kind == kPhO) {
                 // weight of each (head, split): exp(m - M_h) / Z_h, once per CTA
                 if (tid < P.H * S_eff) {
@@ -1266,8 +1382,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             float* lg = (kind == kPhVocab && P.logits) ? P.logits + (uint64_t)s * P.logits_stride : nullptr;
             int release = 0;
             cstamp(4);
-            ok = kind == kPhP ? run_gemv(KF{}, kind, g, out_tag(tag), boff, kv_row, lg, &release)
-                              : run_gemv(KD{}, kind, g, out_tag(tag), boff, kv_row, lg, &release);
+            ok = kind == kPhP ? run_gemv(KF{}, kind, g, out_tag(tag), boff, kv_row, lg, &release, wreg)
+                              : run_gemv(KD{}, kind, g, out_tag(tag), boff, kv_row, lg, &release, wreg);
             if (!agree(ok)) { alive = false; break; }
             if (warp == 0 && lane < release) mbar_arrive(&empty[(gi + (uint32_t)lane) % kSlots]);
             gi += (uint32_t)release;

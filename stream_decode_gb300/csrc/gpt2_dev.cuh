@@ -43,7 +43,7 @@ struct LayerParams {
 
 constexpr int kMaxLayers = 16;
 
-constexpr int kMaxSplits = 8;   // key-axis splits per attention head
+constexpr int kMaxSplits = 4;   // key-axis splits per attention head
 constexpr int kMaxGrid = kConsumerWarps * 32;  // CTAs of the step kernel (one per SM on GB300: 152)
 
 // Key-axis splits per head for a grid of G CTAs and H heads.
@@ -52,9 +52,11 @@ __host__ __device__ inline int attn_splits(int G, int H) {
     return s > kMaxSplits ? kMaxSplits : s;
 }
 
-// Splits used at a given number of keys: one per 56 keys (the two passes of
-// 7 warps x 4 keys that a unit loads before waiting for q), at most `cap`.
-constexpr int kKeysPerSplit = 56;
+// Splits used at a given number of keys: one per 128 keys (a unit's seven
+// warps take 56 keys per pass, so a split costs at most three passes), at
+// most `cap`.  Up to 128 keys a head is one unit, whose output is final: the
+// out-projection then gathers it with no merge of partial softmaxes.
+constexpr int kKeysPerSplit = 128;
 __host__ __device__ inline int attn_splits_for(int keys, int cap) {
     const int s = (keys + kKeysPerSplit - 1) / kKeysPerSplit;
     return s < 1 ? 1 : (s > cap ? cap : s);
