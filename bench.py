@@ -349,6 +349,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quant", choices=["f32", "int8"], default="f32")
     ap.add_argument("--no-extra", action="store_true", help="skip the int8 and long-context extras")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="only the 128-token prefill leg (3 warm-up calls, --steps timed calls); prints its JSON")
     ap.add_argument("--decode-steps", type=int, default=112,
                     help="decode positions per bench step (112 = positions 16..127)")
     args = ap.parse_args()
@@ -368,6 +370,10 @@ def main():
     import torch
     ws, rank, local = dist_info()
     torch.cuda.set_device(local)
+    if args.prefill_only:
+        from stream_decode_gb300 import gpt2 as g
+        print(json.dumps(prefill_rate(g, torch, shape, w, reps=max(1, args.steps))), flush=True)
+        return
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
