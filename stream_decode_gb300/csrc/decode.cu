@@ -612,33 +612,89 @@ __device__ __forceinline__ bool gather_vec(const uint64_t* src, int N, unsigned 
     return ok;
 }
 
-// Gathers this thread's words tid + NT*k (k < PN, tid + NT*k < N) of a
-// tagged N-word vector into registers once each carries `tag`.
-template <int PN>
-__device__ __forceinline__ bool gather_vals(const uint64_t* src, int N, unsigned tag, float (&v)[PN], int tid,
-                                            const StepPlan& P) {
+// Pair layout of a vector held in registers: thread tid owns the word
+// pairs q = tid + NT*k (k < PP), i.e. elements 2q and 2q + 1, so that each
+// tagged load moves 16 bytes (two words) and a warp's loads are contiguous.
+template <int N>
+struct Pairs {
+    static constexpr int NT = kConsumerWarps * 32;
+    static constexpr int NP = N / 2;                   // pairs in the vector
+    static constexpr int PP = (NP + NT - 1) / NT;      // pairs per thread (at most)
+};
+
+// Waits until both words of each of this thread's pairs carry `tag` and
+// returns their values in v[2k], v[2k + 1]; addr(q) is the first word of
+// pair q (16-byte aligned).  Returns false when the run is abandoned.
+template <int PP, typename Addr>
+__device__ __forceinline__ bool gather_pairs(float (&v)[2 * PP], int npairs, unsigned tag, Addr addr, int tid,
+                                             const StepPlan& P) {
     constexpr int NT = kConsumerWarps * 32;
-    uint64_t w[PN];
-    const bool ok = tagged_wait<PN>(w, own_words<PN>(N, tid), tag, [&](int k) { return src + tid + NT * k; }, P);
+    uint32_t pending = 0;
 #pragma unroll
-    for (int k = 0; k < PN; ++k) v[k] = (tid + NT * k < N) ? val_of(w[k]) : 0.0f;
-    return ok;
+    for (int k = 0; k < PP; ++k) {
+        v[2 * k] = 0.0f;
+        v[2 * k + 1] = 0.0f;
+        if (tid + NT * k < npairs) pending |= 1u << k;
+    }
+    uint64_t t0 = 0;
+    uint32_t rounds = 0;
+    while (pending) {
+        uint64_t a[PP], b[PP];
+#pragma unroll
+        for (int k = 0; k < PP; ++k)
+            if ((pending >> k) & 1u) ld_tagged_x2(addr(tid + NT * k), a[k], b[k]);
+#pragma unroll
+        for (int k = 0; k < PP; ++k)
+            if (((pending >> k) & 1u) && tag_of(a[k]) == tag && tag_of(b[k]) == tag) {
+                v[2 * k] = val_of(a[k]);
+                v[2 * k + 1] = val_of(b[k]);
+                pending &= ~(1u << k);
+            }
+        if (pending && (++rounds & 7u) == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (waited_long(now - t0) && ld_volatile_int(P.abort_flag)) return false;
+            else if (now - t0 > P.wait_limit_ns) {
+                record_error(P, kDevTimeout);
+                return false;
+            }
+        }
+    }
+    return true;
 }
 
-// LayerNorm of this thread's coordinates v[k] = x[tid + NT*k] into y
-// (shared memory), with the gains/shifts already in registers (loaded before
-// the wait for x, so their latency hides behind it).  One block reduction of
-// (sum x, sum x^2); biased variance E[x^2] - mean^2; eps 1e-5.
-template <int N, int PN>
-__device__ __forceinline__ void layernorm_vals(const float (&v)[PN], const float (&g)[PN], const float (&b)[PN],
-                                               float* y, float* red, int tid) {
+// LayerNorm parameters of this thread's pairs (loaded before the input wait).
+template <int N, int PP>
+__device__ __forceinline__ void load_ln_pairs(const float* g, const float* b, float (&gr)[2 * PP], float (&br)[2 * PP],
+                                              int tid) {
+    constexpr int NT = kConsumerWarps * 32;
+#pragma unroll
+    for (int k = 0; k < PP; ++k) {
+        const int q = tid + NT * k;
+        float2 gv = make_float2(0.0f, 0.0f), bv = make_float2(0.0f, 0.0f);
+        if (q < N / 2) {
+            gv = __ldg(reinterpret_cast<const float2*>(g) + q);
+            bv = __ldg(reinterpret_cast<const float2*>(b) + q);
+        }
+        gr[2 * k] = gv.x;
+        gr[2 * k + 1] = gv.y;
+        br[2 * k] = bv.x;
+        br[2 * k + 1] = bv.y;
+    }
+}
+
+// LayerNorm of the pair-held coordinates into y (shared memory): one block
+// reduction of (sum x, sum x^2); biased variance E[x^2] - mean^2; eps 1e-5.
+template <int N, int PP>
+__device__ __forceinline__ void layernorm_pairs(const float (&v)[2 * PP], const float (&g)[2 * PP],
+                                                const float (&b)[2 * PP], float* y, float* red, int tid) {
     constexpr int NT = kConsumerWarps * 32;
     float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
-    for (int k = 0; k < PN; ++k)
-        if (tid + NT * k < N) {
-            s1 += v[k];
-            s2 = fmaf(v[k], v[k], s2);
+    for (int k = 0; k < PP; ++k)
+        if (tid + NT * k < N / 2) {
+            s1 += v[2 * k] + v[2 * k + 1];
+            s2 = fmaf(v[2 * k], v[2 * k], fmaf(v[2 * k + 1], v[2 * k + 1], s2));
         }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -656,21 +712,13 @@ __device__ __forceinline__ void layernorm_vals(const float (&v)[PN], const float
     }
     constexpr float inv_n = 1.0f / (float)N;
     const float mean = t1 * inv_n;
-    const float var = fmaxf(fmaf(t2, inv_n, -mean * mean), 0.0f);
-    const float rstd = rsqrtf(var + kLnEps);
+    const float rstd = rsqrtf(fmaxf(fmaf(t2, inv_n, -mean * mean), 0.0f) + kLnEps);
 #pragma unroll
-    for (int k = 0; k < PN; ++k)
-        if (tid + NT * k < N) y[tid + NT * k] = fmaf((v[k] - mean) * rstd, g[k], b[k]);
-}
-
-template <int N, int PN>
-__device__ __forceinline__ void load_ln(const float* g, const float* b, float (&gr)[PN], float (&br)[PN], int tid) {
-    constexpr int NT = kConsumerWarps * 32;
-#pragma unroll
-    for (int k = 0; k < PN; ++k) {
-        const int i = tid + NT * k;
-        gr[k] = i < N ? __ldg(g + i) : 0.0f;
-        br[k] = i < N ? __ldg(b + i) : 0.0f;
+    for (int k = 0; k < PP; ++k) {
+        const int q = tid + NT * k;
+        if (q < N / 2)
+            reinterpret_cast<float2*>(y)[q] = make_float2(fmaf((v[2 * k] - mean) * rstd, g[2 * k], b[2 * k]),
+                                                          fmaf((v[2 * k + 1] - mean) * rstd, g[2 * k + 1], b[2 * k + 1]));
     }
 }
 
@@ -843,6 +891,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     constexpr int P3 = (3 * D + NT - 1) / NT;  // qkv words per thread (trace)
     constexpr int PV = PF > P3 ? PF : P3;      // words per thread of any gathered vector
     constexpr int PM = PD * kMaxSplits;        // attention partial words per thread (merge)
+    constexpr int PPD = Pairs<D>::PP;          // word pairs per thread of a D-vector
+    constexpr int PPF = Pairs<FF>::PP;         // word pairs per thread of an FF-vector
+    static_assert(PPF <= 32 && D % 2 == 0 && FF % 2 == 0 && DH % 2 == 0, "pair gathers");
     static_assert(PM + 2 <= 64 && PV <= 64, "tagged gathers hold at most 64 words per thread");
     uint32_t gi = 0;  // chunks consumed (same sequence as the producer)
     using KD = std::integral_constant<int, D>;
@@ -1232,11 +1283,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             // LayerNorm parameters (QKV: ln_1, FC: ln_2, vocabulary: ln_f) and
             // this CTA's bias rows are loaded before the wait for the inputs.
             const bool has_ln = kind == kPhQKV || kind == kPhFC || kind == kPhVocab;
-            float gr[PD], br[PD];
+            float gr[2 * PPD], br[2 * PPD];
             if (has_ln) {
                 const uint64_t go = kind == kPhQKV ? lp.ln1_g : kind == kPhFC ? lp.ln2_g : P.lnf_g;
                 const uint64_t bo = kind == kPhQKV ? lp.ln1_b : kind == kPhFC ? lp.ln2_b : P.lnf_b;
-                load_ln<D>(P.packed + go, P.packed + bo, gr, br, tid);
+                load_ln_pairs<D, PPD>(P.packed + go, P.packed + bo, gr, br, tid);
             }
             const Geo g = geo_of(P, geot, mat);
             const uint64_t boff = kind == kPhQKV ? lp.b_qkv : kind == kPhO ? lp.b_o : kind == kPhFC ? lp.b_fc : lp.b_p;
@@ -1258,12 +1309,26 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             }
             // ---- inputs
             uint64_t ov[PM + 2];  // out-projection: o words of every split, then (max, sum) words
-            float xv[PD];     // LayerNorm phases: this thread's coordinates of the residual stream
-            if (kind == kPhO) {
+            float xv[2 * PPD];  // LayerNorm phases: this thread's pairs of the residual stream
+            if (kind == kPhO && S_eff == 1) {
+                // single-split heads: unit h holds head h's normalised output
+                float ov2[2 * PPD];
+                ok = ok & gather_pairs<PPD>(
+                    ov2, D / 2, tag - 1u,
+                    [&](int q) {
+                        const int idx = 2 * q, h = idx / DH;
+                        return P.attn_part + (size_t)h * (DH + 2) + 2 + (idx - h * DH);
+                    },
+                    tid, P);
+#pragma unroll
+                for (int k = 0; k < PPD; ++k)
+                    if (tid + NT * k < D / 2)
+                        reinterpret_cast<float2*>(vin)[tid + NT * k] = make_float2(ov2[2 * k], ov2[2 * k + 1]);
+            } else if (kind == kPhO) {
                 // One wait for every split's o words of this thread's coordinates
                 // (k < PM) and, for threads below 2 * units, one (max, sum) word
                 // (k = PM, PM + 1), which then goes to stage[2u], stage[2u + 1].
-                const int nmz = S_eff == 1 ? 0 : 2 * P.H * S_eff;  // one split: outputs already normalised
+                const int nmz = 2 * P.H * S_eff;
                 uint64_t want = 0;
 #pragma unroll
                 for (int i = 0; i < PD; ++i)
@@ -1289,8 +1354,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     if (tid + NT * k < nmz) stage[tid + NT * k] = val_of(ov[PM + k]);
             } else if (kind == kPhQKV && l == 0) {
 #pragma unroll
-                for (int k = 0; k < PD; ++k) {
-                    const int i = tid + NT * k;
+                for (int k = 0; k < 2 * PPD; ++k) {
+                    const int i = 2 * (tid + NT * (k >> 1)) + (k & 1);
                     xv[k] = 0.0f;
                     if (i < D) {
                         const float pe = __ldg(P.packed + P.wpe_off + (uint64_t)p * D + i);
@@ -1305,15 +1370,22 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     }
                 }
             } else if (kind == kPhP) {
-                ok = ok & gather_vec<PV>(P.u, FF, tag - 1u, vin, tid, P);
+                float uv[2 * PPF];
+                ok = ok & gather_pairs<PPF>(uv, FF / 2, tag - 1u, [&](int q) { return P.u + 2 * (size_t)q; }, tid, P);
+#pragma unroll
+                for (int k = 0; k < PPF; ++k)
+                    if (tid + NT * k < FF / 2)
+                        reinterpret_cast<float2*>(vin)[tid + NT * k] = make_float2(uv[2 * k], uv[2 * k + 1]);
             } else {
-                ok = ok & gather_vals<PD>(kind == kPhFC ? P.xb : P.xa, D, tag - 1u, xv, tid, P);
+                const uint64_t* src = kind == kPhFC ? P.xb : P.xa;
+                ok = ok & gather_pairs<PPD>(xv, D / 2, tag - 1u, [&](int q) { return src + 2 * (size_t)q; }, tid, P);
             }
             if (has_ln) {
                 // the residual stream, kept for the epilogue's residual add (and the trace)
 #pragma unroll
-                for (int k = 0; k < PD; ++k)
-                    if (tid + NT * k < D) xs[tid + NT * k] = xv[k];
+                for (int k = 0; k < PPD; ++k)
+                    if (tid + NT * k < D / 2)
+                        reinterpret_cast<float2*>(xs)[tid + NT * k] = make_float2(xv[2 * k], xv[2 * k + 1]);
             }
             if (g.nrows <= NT && tid < g.nrows) bias_s[tid] = bv;
             if (!agree(ok)) { alive = false; break; }
@@ -1321,12 +1393,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             cstamp(3);
             // ---- input transform: LayerNorm, or the merge of the heads' partials
             if (has_ln) {
-                layernorm_vals<D>(xv, gr, br, vin, red, tid);
-            } else if (kind == kPhO && S_eff == 1) {
-#pragma unroll
-                for (int i = 0; i < PD; ++i)
-                    if (tid + NT * i < D) vin[tid + NT * i] = val_of(ov[i * kMaxSplits]);
-            } else if (kind == kPhO) {
+                layernorm_pairs<D, PPD>(xv, gr, br, vin, red, tid);
+            } else if (kind == kPhO && S_eff > 1) {
                 // weight of each (head, split): exp(m - M_h) / Z_h, once per CTA
                 if (tid < P.H * S_eff) {
                     const int h = tid / S_eff;

@@ -222,6 +222,11 @@ __device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// Two consecutive tagged words in one 16-byte access (16-byte aligned);
+// each word is single-copy atomic on its own.
+__device__ __forceinline__ void ld_tagged_x2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
 __device__ __forceinline__ uint64_t ld_tagged_acquire(const uint64_t* p) {
     uint64_t v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
