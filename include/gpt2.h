@@ -173,8 +173,10 @@ gpt2_status gpt2_session_run(gpt2_session* session, const uint32_t* d_tokens_in,
  * max_pos (GPT2_ERR_TOKENS_LEN).  An out-of-range token or a non-finite
  * logit is reported by the next gpt2_session_sync.  The first call on a
  * model makes the TF32 remainders of its block matrices (a one-off copy of
- * their size) and allocates the session's prefill workspace.
- * Asynchronous on `stream` (NULL: the session's stream). */
+ * their size) and allocates the session's prefill workspace; the first call
+ * for a given length and buffers records the prefill's launches as a CUDA
+ * graph, which later calls replay.  Asynchronous, ordered on `stream` (a
+ * cudaStream_t; NULL is the default stream). */
 gpt2_status gpt2_session_prefill(gpt2_session* session, const uint32_t* d_tokens, uint32_t n, float* d_logits,
                                  uint32_t* d_next_token, void* stream);
 

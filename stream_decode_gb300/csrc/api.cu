@@ -521,7 +521,7 @@ gpt2_status gpt2_session_prefill(gpt2_session* s, const uint32_t* d_tokens, uint
     if (m->quant != GPT2_F32 || !prefill_shape_supported(c)) return GPT2_ERR_CONFIG;
     if (n == 0 || n > c.max_pos) return GPT2_ERR_TOKENS_LEN;
     if (s->position != 0) return GPT2_ERR_POSITION;
-    cudaStream_t st = stream ? static_cast<cudaStream_t>(stream) : s->own;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = prefill_make_lo(m, st);
     if (e == cudaSuccess) e = prefill_alloc(&s->pf, (int)c.max_pos, (int)c.d_model, (int)c.d_ff);
     if (e == cudaSuccess)

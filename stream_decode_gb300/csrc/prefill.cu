@@ -65,36 +65,49 @@ __global__ void embed_kernel(const float* __restrict__ packed, uint64_t wte_off,
         X[(size_t)i * D + j] = __fadd_rn(packed[wte_off + (uint64_t)t * D + j], packed[wpe_off + (uint64_t)i * D + j]);
 }
 
-constexpr int kLnRowsPerBlock = 8;
-constexpr int kMaxLanesVals = 32;  // D <= 1024
+constexpr int kLnThreads = 128;
 
 // Y = LN(X) (mean, then the biased variance of the deviations; eps 1e-5)
-// and its TF32 remainder, one warp per row.
-__global__ void ln_split_kernel(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ b,
-                                int n, int D, float* __restrict__ Y, float* __restrict__ Ylo) {
-    const int row = blockIdx.x * kLnRowsPerBlock + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (row >= n) return;
+// and its TF32 remainder, one block per row (D <= 1024: 8 values a thread).
+__global__ void __launch_bounds__(kLnThreads) ln_split_kernel(const float* __restrict__ X, const float* __restrict__ g,
+                                                             const float* __restrict__ b, int D,
+                                                             float* __restrict__ Y, float* __restrict__ Ylo) {
+    __shared__ float red[kLnThreads / 32];
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* x = X + (size_t)row * D;
-    float v[kMaxLanesVals];
+    float v[8];
     float s = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kMaxLanesVals; ++k) {
-        const int i = lane + 32 * k;
+    for (int k = 0; k < 8; ++k) {
+        const int i = tid + kLnThreads * k;
         v[k] = i < D ? x[i] : 0.0f;
         s += v[k];
     }
-    const float mean = warp_sum32(s) / (float)D;
+    s = warp_sum32(s);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];
+    const float mean = t / (float)D;
+    __syncthreads();
     float q = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kMaxLanesVals; ++k)
-        if (lane + 32 * k < D) {
-            const float t = v[k] - mean;
-            q = fmaf(t, t, q);
+    for (int k = 0; k < 8; ++k)
+        if (tid + kLnThreads * k < D) {
+            const float d = v[k] - mean;
+            q = fmaf(d, d, q);
         }
-    const float den = sqrtf(warp_sum32(q) / (float)D + kLnEps);
+    q = warp_sum32(q);
+    if (lane == 0) red[warp] = q;
+    __syncthreads();
+    float u = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kMaxLanesVals; ++k) {
-        const int i = lane + 32 * k;
+    for (int w = 0; w < kLnThreads / 32; ++w) u += red[w];
+    const float den = sqrtf(u / (float)D + kLnEps);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = tid + kLnThreads * k;
         if (i < D) {
             const float y = (v[k] - mean) / den * g[i] + b[i];
             Y[(size_t)row * D + i] = y;
@@ -133,52 +146,104 @@ __global__ void reduce_kernel(const float* __restrict__ part, int splits, int n,
 }
 
 constexpr int kAttnWarps = 8;
-constexpr int kMaxPrefillKeys = 1024;
+constexpr int kAttnRows = 32;          // query rows per block
+constexpr int kMaxPrefillKeys = 1024;  // longest prompt (the keys of a block are staged in chunks of kKeyTile)
+constexpr int kKeyTile = 64;
 
-// Causal attention of query row i (one warp) and head h over keys 0..i:
-// s_j = (q . k_j) / sqrt(dh); softmax; o = sum_j a_j v_j.  Writes the
-// head's output slice of row i and its remainder.
+// Causal attention of head h for query rows [r0, r0 + 32) of the prompt:
+// s_j = (q . k_j) / sqrt(dh) over keys j <= i, softmax, o = sum_j a_j v_j
+// (dh <= 64).  The keys and values are staged in shared memory in tiles of
+// 64 (keys padded to dh + 1 floats a row: conflict-free column reads); each
+// warp takes 4 query rows and keeps, per row, the scores of the current
+// tile, an online max / sum and its two output coordinates per lane.
 __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float* __restrict__ QKV, int n, int D,
                                                                     int DH, float* __restrict__ O,
                                                                     float* __restrict__ Olo) {
-    __shared__ float sc[kAttnWarps][kMaxPrefillKeys];
+    __shared__ float ks[kKeyTile][65];
+    __shared__ float vs[kKeyTile][64];
+    __shared__ float qs[kAttnRows][64];
+    __shared__ float ps[kAttnWarps][kKeyTile];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.x, i = blockIdx.y * kAttnWarps + warp;
-    if (i >= n) return;
+    const int h = blockIdx.x, r0 = blockIdx.y * kAttnRows;
     const size_t N3 = 3 * (size_t)D;
-    const float* q = QKV + (size_t)i * N3 + (size_t)h * DH;
     const float scale = 1.0f / sqrtf((float)DH);
-    float* s = sc[warp];
-    float m = -INFINITY;
-    for (int j = lane; j <= i; j += 32) {
-        const float* k = QKV + (size_t)j * N3 + D + (size_t)h * DH;
-        float dot = 0.0f;
-        for (int e = 0; e < DH; e += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(q + e), c = *reinterpret_cast<const float4*>(k + e);
-            dot = fmaf(a.x, c.x, dot);
-            dot = fmaf(a.y, c.y, dot);
-            dot = fmaf(a.z, c.z, dot);
-            dot = fmaf(a.w, c.w, dot);
+    const int rmax = min(r0 + kAttnRows, n);  // rows r0..rmax-1; keys 0..rmax-1
+    for (int i = threadIdx.x; i < kAttnRows * DH; i += blockDim.x) {
+        const int r = i / DH, e = i - r * DH;
+        qs[r][e] = r0 + r < n ? QKV[(size_t)(r0 + r) * N3 + (size_t)h * DH + e] : 0.0f;
+    }
+    constexpr int RPW = kAttnRows / kAttnWarps;  // query rows per warp
+    float m[RPW], z[RPW], o0[RPW], o1[RPW];
+#pragma unroll
+    for (int t = 0; t < RPW; ++t) {
+        m[t] = -INFINITY;
+        z[t] = 0.0f;
+        o0[t] = 0.0f;
+        o1[t] = 0.0f;
+    }
+    for (int j0 = 0; j0 < rmax; j0 += kKeyTile) {
+        const int jn = min(kKeyTile, rmax - j0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < jn * DH; i += blockDim.x) {
+            const int j = i / DH, e = i - j * DH;
+            const size_t base = (size_t)(j0 + j) * N3 + (size_t)h * DH + e;
+            ks[j][e] = QKV[base + D];
+            vs[j][e] = QKV[base + 2 * D];
         }
-        const float v = dot * scale;
-        s[j] = v;
-        m = fmaxf(m, v);
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < RPW; ++t) {
+            const int r = warp * RPW + t, i = r0 + r;
+            if (i >= n) continue;
+            const int kend = min(jn, i - j0 + 1);  // keys of this tile at or before row i
+            if (kend <= 0) continue;
+            // scores of this tile: lane takes keys lane, lane + 32, ...
+            float tmax = -INFINITY;
+            for (int j = lane; j < kend; j += 32) {
+                float dot = 0.0f;
+                for (int e = 0; e < DH; ++e) dot = fmaf(qs[r][e], ks[j][e], dot);
+                const float sc = dot * scale;
+                ps[warp][j] = sc;
+                tmax = fmaxf(tmax, sc);
+            }
+            tmax = warp_max32(tmax);
+            const float mn = fmaxf(m[t], tmax);
+            const float corr = expf(m[t] - mn);  // 0 while m is -inf
+            float tz = 0.0f;
+            for (int j = lane; j < kend; j += 32) {
+                const float e = expf(ps[warp][j] - mn);
+                ps[warp][j] = e;
+                tz += e;
+            }
+            tz = warp_sum32(tz);
+            __syncwarp();
+            float a0 = o0[t] * corr, a1 = o1[t] * corr;
+            for (int j = 0; j < kend; ++j) {
+                const float pj = ps[warp][j];
+                if (lane < DH) a0 = fmaf(pj, vs[j][lane], a0);
+                if (lane + 32 < DH) a1 = fmaf(pj, vs[j][lane + 32], a1);
+            }
+            __syncwarp();
+            o0[t] = a0;
+            o1[t] = a1;
+            z[t] = fmaf(z[t], corr, tz);
+            m[t] = mn;
+        }
     }
-    m = warp_max32(m);
-    float z = 0.0f;
-    for (int j = lane; j <= i; j += 32) {
-        const float e = expf(s[j] - m);
-        s[j] = e;
-        z += e;
-    }
-    z = warp_sum32(z);
-    __syncwarp();
-    for (int e = lane; e < DH; e += 32) {
-        float acc = 0.0f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(s[j], QKV[(size_t)j * N3 + 2 * D + (size_t)h * DH + e], acc);
-        const float o = acc / z;
-        O[(size_t)i * D + (size_t)h * DH + e] = o;
-        Olo[(size_t)i * D + (size_t)h * DH + e] = tf32_lo(o);
+#pragma unroll
+    for (int t = 0; t < RPW; ++t) {
+        const int i = r0 + warp * RPW + t;
+        if (i >= n) continue;
+        if (lane < DH) {
+            const float o = o0[t] / z[t];
+            O[(size_t)i * D + (size_t)h * DH + lane] = o;
+            Olo[(size_t)i * D + (size_t)h * DH + lane] = tf32_lo(o);
+        }
+        if (lane + 32 < DH) {
+            const float o = o1[t] / z[t];
+            O[(size_t)i * D + (size_t)h * DH + lane + 32] = o;
+            Olo[(size_t)i * D + (size_t)h * DH + lane + 32] = tf32_lo(o);
+        }
     }
 }
 
@@ -330,6 +395,13 @@ cudaError_t prefill_make_lo(gpt2_model* m, cudaStream_t st) {
 cudaError_t prefill_alloc(PrefillWs* w, int cap, int D, int FF) {
     if (w->cap >= cap) return cudaSuccess;
     prefill_free(w);
+    cudaError_t es = cudaStreamCreateWithFlags(&w->cs, cudaStreamNonBlocking);
+    if (es == cudaSuccess) es = cudaEventCreateWithFlags(&w->ev_in, cudaEventDisableTiming);
+    if (es == cudaSuccess) es = cudaEventCreateWithFlags(&w->ev_out, cudaEventDisableTiming);
+    if (es != cudaSuccess) {
+        prefill_free(w);
+        return es;
+    }
     const size_t nd = (size_t)cap * D, nf = (size_t)cap * FF;
     cudaError_t e = cudaMalloc(&w->X, nd * 4);
     if (e == cudaSuccess) e = cudaMalloc(&w->A, nd * 4);
@@ -347,6 +419,11 @@ cudaError_t prefill_alloc(PrefillWs* w, int cap, int D, int FF) {
 }
 
 void prefill_free(PrefillWs* w) {
+    if (w->cs) cudaStreamSynchronize(w->cs);
+    if (w->exec) cudaGraphExecDestroy(w->exec);
+    if (w->ev_in) cudaEventDestroy(w->ev_in);
+    if (w->ev_out) cudaEventDestroy(w->ev_out);
+    if (w->cs) cudaStreamDestroy(w->cs);
     cudaFree(w->X);
     cudaFree(w->A);
     cudaFree(w->Alo);
@@ -359,23 +436,18 @@ void prefill_free(PrefillWs* w) {
 
 bool prefill_shape_supported(const gpt2_config& c) {
     const int D = (int)c.d_model, FF = (int)c.d_ff, DH = D / (int)c.n_head;
-    return D % tc::kTileN == 0 && FF % tc::kTileN == 0 && D <= 1024 && DH % 4 == 0 && c.max_pos <= kMaxPrefillKeys;
+    return D % tc::kTileN == 0 && FF % tc::kTileN == 0 && D <= 1024 && DH <= 64 && DH % 4 == 0 &&
+           c.max_pos <= kMaxPrefillKeys;
 }
 
-cudaError_t prefill_enqueue(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, int n, float* cache, float* logits,
-                            int* status, uint32_t* d_choice, uint32_t* d_next, cudaStream_t st) {
-    if (!encode_ready()) return cudaErrorNotSupported;
-    if (!g_sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_sms <= 0) g_sms = 1;
-    }
+namespace {
+
+// Every launch of one prefill, enqueued on stream st.
+cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, int n, float* cache, float* logits,
+                             int* status, uint32_t* d_choice, uint32_t* d_next, cudaStream_t st) {
     const gpt2_config& c = m->cfg;
     const int D = (int)c.d_model, FF = (int)c.d_ff, L = (int)c.n_layer, H = (int)c.n_head, DH = D / H;
-    cudaError_t e = cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc::kTcSmem);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     const float* P = m->d_packed;
     const int m_tiles = (n + tc::kTileM - 1) / tc::kTileM;
 
@@ -402,23 +474,20 @@ cudaError_t prefill_enqueue(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, 
                                               l, D);
         return cudaGetLastError();
     };
-    const int ln_blocks = (n + kLnRowsPerBlock - 1) / kLnRowsPerBlock;
 
     embed_kernel<<<n, 256, 0, st>>>(P, m->wte_off, m->wpe_off, d_tok, D, c.vocab, w->X, status);
     e = cudaGetLastError();
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
         const LayerParams& lp = m->lp[l];
         int sp = 1;
-        ln_split_kernel<<<ln_blocks, kLnRowsPerBlock * 32, 0, st>>>(w->X, P + lp.ln1_g, P + lp.ln1_b, n, D, w->A,
-                                                                    w->Alo);
+        ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + lp.ln1_g, P + lp.ln1_b, D, w->A, w->Alo);
         if ((e = gemm(w->A, w->Alo, D, 3 * D, l, kQKV, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, 3 * D, lp.b_qkv, kRedQKV, w->QKV, nullptr, l)) != cudaSuccess) break;
-        attention_kernel<<<dim3(H, (n + kAttnWarps - 1) / kAttnWarps), kAttnWarps * 32, 0, st>>>(w->QKV, n, D, DH,
-                                                                                                  w->A, w->Alo);
+        attention_kernel<<<dim3(H, (n + kAttnRows - 1) / kAttnRows), kAttnWarps * 32, 0, st>>>(w->QKV, n, D, DH,
+                                                                                                w->A, w->Alo);
         if ((e = gemm(w->A, w->Alo, D, D, l, kO, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, D, lp.b_o, kRedResidual, nullptr, nullptr, l)) != cudaSuccess) break;
-        ln_split_kernel<<<ln_blocks, kLnRowsPerBlock * 32, 0, st>>>(w->X, P + lp.ln2_g, P + lp.ln2_b, n, D, w->A,
-                                                                    w->Alo);
+        ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + lp.ln2_g, P + lp.ln2_b, D, w->A, w->Alo);
         if ((e = gemm(w->A, w->Alo, D, FF, l, kFC, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, FF, lp.b_fc, kRedGelu, w->U, w->Ulo, l)) != cudaSuccess) break;
         if ((e = gemm(w->U, w->Ulo, FF, D, l, kP, &sp)) != cudaSuccess) break;
@@ -429,6 +498,51 @@ cudaError_t prefill_enqueue(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, 
                                                 (int)c.vocab, logits);
     choice_kernel<<<1, 256, 0, st>>>(logits, c.vocab, d_choice, d_next, status);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t prefill_enqueue(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, int n, float* cache, float* logits,
+                            int* status, uint32_t* d_choice, uint32_t* d_next, cudaStream_t st) {
+    if (!encode_ready()) return cudaErrorNotSupported;
+    if (!g_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_sms <= 0) g_sms = 1;
+    }
+    cudaError_t e = cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc::kTcSmem);
+    if (e != cudaSuccess) return e;
+    const void* key[9] = {m, d_tok, reinterpret_cast<const void*>((uintptr_t)n), cache, logits, status, d_choice, d_next,
+                          w->part};
+    bool same = w->exec != nullptr;
+    for (int i = 0; i < 9 && same; ++i) same = key[i] == w->key[i];
+    if (!same) {
+        if (w->exec) {
+            cudaGraphExecDestroy(w->exec);
+            w->exec = nullptr;
+        }
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamBeginCapture(w->cs, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return e;
+        const cudaError_t el = prefill_launches(m, w, d_tok, n, cache, logits, status, d_choice, d_next, w->cs);
+        e = cudaStreamEndCapture(w->cs, &graph);
+        if (el != cudaSuccess) e = el;
+        if (e == cudaSuccess) e = cudaGraphInstantiate(&w->exec, graph, 0);
+        if (graph) cudaGraphDestroy(graph);
+        if (e != cudaSuccess) {
+            w->exec = nullptr;
+            return e;
+        }
+        for (int i = 0; i < 9; ++i) w->key[i] = key[i];
+    }
+    e = cudaEventRecord(w->ev_in, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(w->cs, w->ev_in, 0);
+    if (e == cudaSuccess) e = cudaGraphLaunch(w->exec, w->cs);
+    if (e == cudaSuccess) e = cudaEventRecord(w->ev_out, w->cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, w->ev_out, 0);
+    return e;
 }
 
 }  // namespace gpt2

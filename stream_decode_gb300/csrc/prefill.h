@@ -24,6 +24,13 @@ struct PrefillWs {
     float* U = nullptr;     // [cap][d_ff] GELU output
     float* Ulo = nullptr;   // its TF32 remainder
     float* part = nullptr;  // split-K partial tiles
+    // The prefill's launches, captured once per (model, buffers, length) and
+    // replayed as one CUDA graph on the workspace's stream, ordered after and
+    // before the caller's stream by events.
+    cudaGraphExec_t exec = nullptr;
+    cudaStream_t cs = nullptr;
+    cudaEvent_t ev_in = nullptr, ev_out = nullptr;
+    const void* key[9] = {};
 };
 
 bool prefill_shape_supported(const gpt2_config& c);
