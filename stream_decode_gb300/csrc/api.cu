@@ -19,6 +19,8 @@ int step_max_ctas(int D, int FF, int DH, bool q8, int max_pos);
 bool step_shape_supported(int D, int FF, int DH);
 cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, bool q8, cudaStream_t st);
 cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, cudaStream_t st);
+cudaError_t fold_rows(const uint8_t* rows, int K, int N, const float* g, const float* b, const float* bias, float* c,
+                      float* d, cudaStream_t st);
 cudaError_t launch_project(const uint8_t* rows, int K, int N, bool q8, const float* x, const float* bias, float* y,
                            int stream, cudaStream_t st);
 cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfinite, cudaStream_t st);
@@ -97,6 +99,7 @@ void fill_plan(const gpt2_session* s, StepPlan& P) {
     P.max_pos = (int)c.max_pos;
     P.G = m->G;
     P.packed = m->d_packed;
+    P.fold = m->d_fold;
     P.wstream = m->d_wstream;
     P.layer_bytes = m->layer_bytes;
     for (int i = 0; i < 4; ++i) P.mat_off[i] = m->mat_off[i];
@@ -256,6 +259,20 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
             CK(repack_matrix(m->d_packed + wf[l], base + m->mat_off[kFC], D, FF, q8, 0));
             CK(repack_matrix(m->d_packed + wp[l], base + m->mat_off[kP], FF, D, q8, 0));
         }
+        if (!q8) {
+            const uint64_t fw = fold_layer_words(D, FF);
+            CK(cudaMalloc(&m->d_fold, fw * L * sizeof(float)));
+            for (int l = 0; l < L; ++l) {
+                const uint8_t* base = m->d_wstream + (uint64_t)l * m->layer_bytes;
+                float* f = m->d_fold + (uint64_t)l * fw;
+                const LayerParams& p = m->lp[l];
+                const float* pk = m->d_packed;
+                CK(fold_rows(base + m->mat_off[kQKV], D, 3 * D, pk + p.ln1_g, pk + p.ln1_b, pk + p.b_qkv, f,
+                             f + 3 * D, 0));
+                CK(fold_rows(base + m->mat_off[kFC], D, FF, pk + p.ln2_g, pk + p.ln2_b, pk + p.b_fc, f + 6 * D,
+                             f + 6 * D + FF, 0));
+            }
+        }
         if (q8) {
             CK(cudaMalloc(&m->d_vocab_q8, (uint64_t)cfg->vocab * rbd));
             CK(cudaMemset(m->d_vocab_q8, 0, (uint64_t)cfg->vocab * rbd));
@@ -275,6 +292,7 @@ void gpt2_model_destroy(gpt2_model* m) {
     cudaFree(m->d_packed);
     cudaFree(m->d_wstream);
     cudaFree(m->d_vocab_q8);
+    cudaFree(m->d_fold);
     cudaFree(m->d_wlo);
     delete m;
 }

@@ -42,7 +42,7 @@ namespace gpt2 {
 
 // ----------------------------------------------------------- smem layout
 struct SmemLayout {
-    uint32_t ring, full, empty, xs, vin, vq, vs, red, ored, qh, rsc, stage, bias, geot, misc, plan, total;
+    uint32_t ring, full, empty, xs, vin, vq, vs, red, ored, qh, rsc, stage, fpart, bias, geot, misc, plan, total;
 };
 
 __host__ __device__ constexpr uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -59,6 +59,13 @@ static_assert(kConsumerWarps * 8 * (2 + 8) <= kStageFloats, "attention warp merg
 static_assert(2 * 16 * kMaxSplits <= kStageFloats, "unit (max, sum) pairs fit in stage");
 static_assert(256 + kMaxGrid <= kStageFloats, "greedy choices fit in stage");
 constexpr int kMaxChunkRows = 32;
+// Rows of a spread share (computed by the whole CTA once its chunks landed).
+constexpr int kSpreadRows = 32;
+// Fast phases alternate between two sets of [warps][kSpreadRows] row
+// partials and [warps] (sum x, sum x^2) pairs, so that one phase's partials
+// can be written while slower threads still read the previous phase's.
+constexpr int kFastSet = kConsumerWarps * kSpreadRows + 2 * kConsumerWarps;
+constexpr int kFastPartFloats = 2 * kFastSet;
 
 __host__ __device__ inline SmemLayout smem_layout(int D, int FF, bool q8, int max_pos) {
     SmemLayout s{};
@@ -76,6 +83,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D, int FF, bool q8, int ma
     s.qh = o; o = align16(o + 3 * 64 * 4);  // q_h, k_p, v_p of one attention unit
     s.rsc = o; o = align16(o + (q8 ? kCoopTaskFloats * 4 : 0));  // int8 rescale terms
     s.stage = o; o = align16(o + kStageFloats * 4);  // attention warp merge; (max, sum) pairs; greedy choices
+    s.fpart = o; o = align16(o + kFastPartFloats * 4);  // fast phases: two alternating sets of row partials + LN sums
     s.bias = o; o = align16(o + kConsumerWarps * 32 * 4);
     s.geot = o; o = align16(o + 5 * 32);  // GeoRow table
     s.misc = o; o = align16(o + 64 * 4);
@@ -269,86 +277,17 @@ struct Rows {
     static constexpr int NG = K / kGroup;                                     // int8 groups per row
 };
 
-constexpr int kSpreadRows = 32;
-
 __host__ __device__ constexpr bool share_spread(int nchunks, int nrows, int K, bool q8) {
     return nchunks <= kSlots / 2 && nrows <= kSpreadRows && (!q8 || nrows * (K / kGroup) <= kCoopTaskFloats);
 }
 
-// binary32, cooperative: thread t takes float4 columns t, t + NT, ... of
-// rows 0..nrows-1 (NR >= nrows accumulators); a warp transpose-reduction
-// leaves the warp's partial of row r on lane r, stored to part[warp][r].
-template <int K, int NR>
-__device__ __forceinline__ void coop_f32_part(const uint8_t* ring, uint32_t c0, int nrows, const float* x, float* part,
-                                              int tid) {
-    using R = Rows<K, false>;
-    constexpr int NT = kConsumerWarps * 32;
-    constexpr int NV = K / 4;                  // float4 columns per row
-    constexpr int NC = (NV + NT - 1) / NT;     // columns per thread
-    const int warp = tid >> 5, lane = tid & 31;
-    const float4* x4 = reinterpret_cast<const float4*>(x);
-    float acc[NR];
-#pragma unroll
-    for (int i = 0; i < NR; ++i) acc[i] = 0.0f;
-#pragma unroll
-    for (int cc = 0; cc < NC; ++cc) {
-        const int col = tid + NT * cc;
-        if ((NV % NT) == 0 || col < NV) {
-            const float4 xv = x4[col];
-#pragma unroll
-            for (int i = 0; i < NR; ++i) {
-                if (i < nrows) {
-                    // row i: chunk c0 + i / RPC, byte (i % RPC) * RB of its slot (constants but c0)
-                    const uint32_t off = ((c0 + (uint32_t)(i / R::RPC)) % kSlots) * (uint32_t)kSlotBytes +
-                                         (uint32_t)((i % R::RPC) * R::RB);
-                    const float4 wv = *reinterpret_cast<const float4*>(ring + off + 16u * (uint32_t)col);
-                    acc[i] = fmaf(xv.x, wv.x, acc[i]);
-                    acc[i] = fmaf(xv.y, wv.y, acc[i]);
-                    acc[i] = fmaf(xv.z, wv.z, acc[i]);
-                    acc[i] = fmaf(xv.w, wv.w, acc[i]);
-                }
-            }
-        }
-    }
-    const float t = warp_transpose_sum<NR>(acc, lane);
-    if (lane < NR && lane < nrows) part[warp * kSpreadRows + lane] = t;
-}
-
-// Rows 0..nrows-1 of a spread share against x; thread r < nrows returns
-// row r's total (the warps' partials summed in warp order), others 0.
-// Contains a barrier over the consumer warps: every consumer thread calls it.
-template <int K>
-__device__ __forceinline__ float coop_f32(const uint8_t* ring, uint32_t c0, int nrows, const float* x, float* part,
-                                          int tid) {
-    // a spread share has at most kSlots / 2 chunks of RPC rows
-    constexpr int MAXR = (kSlots / 2) * Rows<K, false>::RPC;
-    if (MAXR > 16 && nrows > 16) coop_f32_part<K, (MAXR > 16 ? 32 : 8)>(ring, c0, nrows, x, part, tid);
-    else if (MAXR > 8 && nrows > 8) coop_f32_part<K, (MAXR > 8 ? 16 : 8)>(ring, c0, nrows, x, part, tid);
-    else coop_f32_part<K, 8>(ring, c0, nrows, x, part, tid);
-    consumers_sync();
-    float y = 0.0f;
-    if (tid < nrows) {
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) y += part[w * kSpreadRows + tid];
-    }
-    return y;
-}
-
-// Register preload of a spread binary32 share: thread t's float4 columns
-// (t, t + NT, ...) of the share's first ROWS rows are loaded into registers
-// before the phase waits for its inputs, so the smem reads overlap that
-// wait; once the input vector is known the projection is FMAs and the
-// reduction only.  kPreRegs float4 per thread: 8 rows at K = 768, 2 rows
-// x 4 columns at K = 3072 (measured best: more registers spill, as the step
-// kernel is at the 255-register limit).
-constexpr int kPreRegs = 8;
+// Column layout of a spread binary32 share: thread t takes the float4
+// columns t, t + NT, ... of every row of the share.
 template <int K>
 struct Pre {
     static constexpr int NT = kConsumerWarps * 32;
     static constexpr int NV = K / 4;                 // float4 columns per row
     static constexpr int NC = (NV + NT - 1) / NT;    // columns per thread
-    static constexpr int ROWS = kPreRegs / NC;       // rows held in registers
-    static_assert(NC * ROWS <= kPreRegs && ROWS >= 1, "preload fits the register block");
 };
 
 template <int K>
@@ -357,29 +296,23 @@ __device__ __forceinline__ uint32_t share_row_off(uint32_t c0, int r) {
     return ((c0 + (uint32_t)(r / R::RPC)) % kSlots) * (uint32_t)kSlotBytes + (uint32_t)((r % R::RPC) * R::RB);
 }
 
-template <int K>
-__device__ __forceinline__ void preload_share(float4 (&w)[kPreRegs], const uint8_t* ring, uint32_t c0, int nrows,
-                                              int tid) {
-    using Q = Pre<K>;
-#pragma unroll
-    for (int cc = 0; cc < Q::NC; ++cc) {
-        const int col = tid + Q::NT * cc;
-#pragma unroll
-        for (int r = 0; r < Q::ROWS; ++r)
-            if (col < Q::NV && r < nrows)
-                w[cc * Q::ROWS + r] = *reinterpret_cast<const float4*>(ring + share_row_off<K>(c0, r) + 16u * (uint32_t)col);
-    }
-}
-
-// The cooperative projection of a preloaded share, rows r0..r0+NR-1 that
-// are below nrows: rows below Pre<K>::ROWS from registers, the rest from
-// shared memory; warp partials of row r to part[warp][r].
-template <int K, int NR>
-__device__ __forceinline__ void coop_pre_part(const float4 (&wr)[kPreRegs], const uint8_t* ring, uint32_t c0, int r0,
-                                              int nrows, const float* x, float* part, int tid) {
+// The cooperative projection of a spread share, rows R0..R0+NR-1 that are
+// below nrows, against x held in registers (this thread's float4 columns,
+// quad layout), weights from shared memory; the warp's partial of row r
+// goes to part[warp][r].  (Variants that keep more values live -- weight
+// rows held in registers across the input wait, or every load of a row
+// group issued before its multiply-adds -- measured slower: the step kernel
+// is at its register limit and the extra live values spill.)
+template <int K, int NR, int R0>
+__device__ __forceinline__ void coop_reg_part(const uint8_t* ring, uint32_t c0, int nrows,
+                                              const float (&x)[4 * Pre<K>::NC], float* part, int tid) {
     using Q = Pre<K>;
     const int warp = tid >> 5, lane = tid & 31;
-    const float4* x4 = reinterpret_cast<const float4*>(x);
+    // whole warps past the row have no columns: their partials are zero
+    if ((Q::NV % Q::NT) != 0 && Q::NC == 1 && (warp * 32) >= Q::NV) {
+        if (lane < NR && R0 + lane < nrows) part[warp * kSpreadRows + R0 + lane] = 0.0f;
+        return;
+    }
     float acc[NR];
 #pragma unroll
     for (int i = 0; i < NR; ++i) acc[i] = 0.0f;
@@ -387,14 +320,12 @@ __device__ __forceinline__ void coop_pre_part(const float4 (&wr)[kPreRegs], cons
     for (int cc = 0; cc < Q::NC; ++cc) {
         const int col = tid + Q::NT * cc;
         if (col < Q::NV) {
-            const float4 xv = x4[col];
+            const float4 xv = make_float4(x[4 * cc], x[4 * cc + 1], x[4 * cc + 2], x[4 * cc + 3]);
 #pragma unroll
             for (int i = 0; i < NR; ++i) {
-                const int r = r0 + i;
+                const int r = R0 + i;
                 if (r < nrows) {
-                    float4 wv;
-                    if (r0 == 0 && i < Q::ROWS) wv = wr[cc * Q::ROWS + i];
-                    else wv = *reinterpret_cast<const float4*>(ring + share_row_off<K>(c0, r) + 16u * (uint32_t)col);
+                    const float4 wv = *reinterpret_cast<const float4*>(ring + share_row_off<K>(c0, r) + 16u * (uint32_t)col);
                     acc[i] = fmaf(xv.x, wv.x, acc[i]);
                     acc[i] = fmaf(xv.y, wv.y, acc[i]);
                     acc[i] = fmaf(xv.z, wv.z, acc[i]);
@@ -404,29 +335,60 @@ __device__ __forceinline__ void coop_pre_part(const float4 (&wr)[kPreRegs], cons
         }
     }
     const float t = warp_transpose_sum<NR>(acc, lane);
-    if (lane < NR && r0 + lane < nrows) part[warp * kSpreadRows + r0 + lane] = t;
+    if (lane < NR && R0 + lane < nrows) part[warp * kSpreadRows + R0 + lane] = t;
 }
 
-// Rows 0..nrows-1 (<= kSpreadRows) of a preloaded spread share against x in
-// row groups of 16; thread r < nrows returns row r's total (the warps'
-// partials summed in warp order), others 0.  Contains a barrier over the
-// consumer warps.
+// Rows 0..nrows-1 (<= kSpreadRows) of a spread share against x (quad
+// layout, registers), in power-of-two row groups: the warps' partials of
+// every row to part; the caller's barrier then lets the row's thread sum
+// them in warp order.
 template <int K>
-__device__ __forceinline__ float coop_pre(const float4 (&wr)[kPreRegs], const uint8_t* ring, uint32_t c0, int nrows,
-                                          const float* x, float* part, int tid) {
-    static_assert(Pre<K>::ROWS <= 16, "registers hold rows of the first group only");
-    if (nrows > 8) {
-        coop_pre_part<K, 16>(wr, ring, c0, 0, nrows, x, part, tid);
-        if (nrows > 16) coop_pre_part<K, 16>(wr, ring, c0, 16, nrows, x, part, tid);
+__device__ __forceinline__ void coop_reg(const uint8_t* ring, uint32_t c0, int nrows, const float (&x)[4 * Pre<K>::NC],
+                                         float* part, int tid) {
+    // a spread share has at most kSlots / 2 chunks of RPC rows
+    constexpr int MAXR = (kSlots / 2) * Rows<K, false>::RPC;
+    if constexpr (MAXR > 8) {
+        if (nrows > 16) {
+            coop_reg_part<K, 16, 0>(ring, c0, nrows, x, part, tid);
+            if (nrows > 24) coop_reg_part<K, 16, 16>(ring, c0, nrows, x, part, tid);
+            else coop_reg_part<K, 8, 16>(ring, c0, nrows, x, part, tid);
+        } else if (nrows > 8) {
+            coop_reg_part<K, 16, 0>(ring, c0, nrows, x, part, tid);
+        } else {
+            coop_reg_part<K, 8, 0>(ring, c0, nrows, x, part, tid);
+        }
     } else {
-        coop_pre_part<K, 8>(wr, ring, c0, 0, nrows, x, part, tid);
+        // long rows (few per share): groups of 4 and 2 waste fewer loads
+        if (nrows > 4) {
+            coop_reg_part<K, 4, 0>(ring, c0, nrows, x, part, tid);
+            if (nrows > 6) coop_reg_part<K, 4, 4>(ring, c0, nrows, x, part, tid);
+            else coop_reg_part<K, 2, 4>(ring, c0, nrows, x, part, tid);
+        } else {
+            coop_reg_part<K, 4, 0>(ring, c0, nrows, x, part, tid);
+        }
     }
-    consumers_sync();
-    float y = 0.0f;
-    if (tid < nrows) {
+}
+
+// This thread's float4 columns of a K-vector in shared memory (quad layout).
+template <int K>
+__device__ __forceinline__ void load_quads(const float* v, float (&x)[4 * Pre<K>::NC], int tid) {
+    using Q = Pre<K>;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) y += part[w * kSpreadRows + tid];
+    for (int cc = 0; cc < Q::NC; ++cc) {
+        const int col = tid + Q::NT * cc;
+        const float4 t = col < Q::NV ? reinterpret_cast<const float4*>(v)[col] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        x[4 * cc] = t.x;
+        x[4 * cc + 1] = t.y;
+        x[4 * cc + 2] = t.z;
+        x[4 * cc + 3] = t.w;
     }
+}
+
+// Row r's total from the warps' partials, summed in warp order.
+__device__ __forceinline__ float sum_warp_parts(const float* part, int r) {
+    float y = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) y += part[w * kSpreadRows + r];
     return y;
 }
 
@@ -648,6 +610,54 @@ __device__ __forceinline__ bool gather_pairs(float (&v)[2 * PP], int npairs, uns
             if (((pending >> k) & 1u) && tag_of(a[k]) == tag && tag_of(b[k]) == tag) {
                 v[2 * k] = val_of(a[k]);
                 v[2 * k + 1] = val_of(b[k]);
+                pending &= ~(1u << k);
+            }
+        if (pending && (++rounds & 7u) == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (waited_long(now - t0) && ld_volatile_int(P.abort_flag)) return false;
+            else if (now - t0 > P.wait_limit_ns) {
+                record_error(P, kDevTimeout);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// Waits until the four words of each of this thread's quads (float4
+// columns c = tid + NT*k, k < NQ, c < nquads) carry `tag` and returns
+// their values in x[4k .. 4k+3]; addr(c) is the first word of quad c (four
+// consecutive words, 16-byte aligned).  Returns false when the run is
+// abandoned.
+template <int NQ, typename Addr>
+__device__ __forceinline__ bool gather_quads(float (&x)[4 * NQ], int nquads, unsigned tag, Addr addr, int tid,
+                                             const StepPlan& P) {
+    constexpr int NT = kConsumerWarps * 32;
+    uint32_t pending = 0;
+#pragma unroll
+    for (int k = 0; k < NQ; ++k) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[4 * k + e] = 0.0f;
+        if (tid + NT * k < nquads) pending |= 1u << k;
+    }
+    uint64_t t0 = 0;
+    uint32_t rounds = 0;
+    while (pending) {
+        uint64_t w[NQ][4];
+#pragma unroll
+        for (int k = 0; k < NQ; ++k)
+            if ((pending >> k) & 1u) {
+                const uint64_t* a = addr(tid + NT * k);
+                ld_tagged_x2(a, w[k][0], w[k][1]);
+                ld_tagged_x2(a + 2, w[k][2], w[k][3]);
+            }
+#pragma unroll
+        for (int k = 0; k < NQ; ++k)
+            if (((pending >> k) & 1u) && tag_of(w[k][0]) == tag && tag_of(w[k][1]) == tag && tag_of(w[k][2]) == tag &&
+                tag_of(w[k][3]) == tag) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[4 * k + e] = val_of(w[k][e]);
                 pending &= ~(1u << k);
             }
         if (pending && (++rounds & 7u) == 0) {
@@ -956,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // chunks are released by the warp that used them, with a named barrier
     // per round of chunks so warp skew stays below one ring length.
     auto run_gemv = [&](auto kk, int kind, const Geo& g, unsigned tag, uint64_t boff, float* kv_row, float* lg,
-                        int* release, const float4 (&wr)[kPreRegs]) -> bool {
+                        int* release) -> bool {
         constexpr int KK = decltype(kk)::value;
         using R = Rows<KK, Q8>;
         auto epilogue = [&](int j, float y) {
@@ -978,16 +988,16 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         };
         *release = 0;
         bool ok = true;
-        if (share_spread(g.nchunks, g.nrows, KK, Q8)) {
-            // every warp saw the share's chunks land before the phase's input wait
-            cstamp(7);
-            float y;
-            if constexpr (Q8) y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
-            else y = coop_pre<KK>(wr, ring, gi, g.nrows, vin, stage, tid);
-            if (tid < g.nrows) epilogue(g.r0 + tid, y);
-            cstamp(5);
-            *release = g.nchunks;
-            return true;
+        if constexpr (Q8) {
+            if (kind != kPhVocab && share_spread(g.nchunks, g.nrows, KK, Q8)) {
+                // every warp saw the share's chunks land before the phase's input wait
+                cstamp(7);
+                const float y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
+                if (tid < g.nrows) epilogue(g.r0 + tid, y);
+                cstamp(5);
+                *release = g.nchunks;
+                return true;
+            }
         }
         constexpr int MR = dot_rows<KK, Q8>();
         static_assert(2 * kConsumerWarps <= kSlots, "a round must stay within one ring length");
@@ -1019,6 +1029,154 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         cstamp(5);
         gi += g.nchunks;
         return ok;
+    };
+
+    // One binary32 fast phase (LN1 + QKV, single-split out-projection,
+    // LN2 + FC, MLP projection) over a spread share: the input is gathered
+    // in the quad layout straight into the registers that the dot products
+    // use; LayerNorm is folded into the projection (row constants c, d) and
+    // its mean and variance are reduced alongside the dot products; one
+    // barrier per phase, after which the share's ring slots are released and
+    // thread r runs row r's epilogue.
+    float* fpart = reinterpret_cast<float*>(smem + lay.fpart);
+    int fast_no = 0;
+    // With from_vin the input is the vector already formed in vin (the
+    // LayerNorm output or merged attention heads of the general path) and
+    // the epilogue adds the plain bias.
+    auto fast_phase = [&](auto kk, int kind, int l, int p, unsigned tok, const Geo& g, unsigned tag,
+                          bool from_vin) -> bool {
+        constexpr int KK = decltype(kk)::value;
+        using Q = Pre<KK>;
+        constexpr bool kLnWidth = KK == D;  // LayerNorm phases project D-vectors
+        const bool has_ln = kLnWidth && !from_vin && (kind == kPhQKV || kind == kPhFC);
+        const LayerParams& lp = P.lp[l];
+        const bool row = tid < g.nrows;
+        const int j = g.r0 + tid;
+        // row constants: the LayerNorm folds, or the bias
+        float cj = 0.0f, dj = 0.0f;
+        if (row) {
+            if (has_ln) {
+                const int N = kind == kPhQKV ? 3 * D : FF;
+                const float* f = P.fold + (uint64_t)l * fold_layer_words(D, FF) + (kind == kPhQKV ? 0 : 6 * D);
+                cj = __ldg(f + j);
+                dj = __ldg(f + N + j);
+            } else {
+                const uint64_t bo = kind == kPhQKV ? lp.b_qkv : kind == kPhO ? lp.b_o : kind == kPhFC ? lp.b_fc : lp.b_p;
+                dj = __ldg(P.packed + bo + j);
+            }
+        }
+        float gq[4 * Q::NC];
+        if constexpr (kLnWidth) {
+            if (has_ln) load_quads<KK>(P.packed + (kind == kPhQKV ? lp.ln1_g : lp.ln2_g), gq, tid);
+        }
+        // the share's chunks were issued phases ago
+        bool ok = wait_chunks(gi, g.nchunks);
+        __syncwarp();
+        cstamp(7);
+        // inputs
+        float x[4 * Q::NC];
+        if (from_vin) {
+            load_quads<KK>(vin, x, tid);
+        } else if (kind == kPhQKV && l == 0) {
+            const float4* te = reinterpret_cast<const float4*>(P.packed + P.wte_off + (uint64_t)tok * D);
+            const float4* pe = reinterpret_cast<const float4*>(P.packed + P.wpe_off + (uint64_t)p * D);
+#pragma unroll
+            for (int cc = 0; cc < Q::NC; ++cc) {
+                const int col = tid + Q::NT * cc;
+                float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
+                if (col < Q::NV) {
+                    a = __ldg(te + col);
+                    b = __ldg(pe + col);
+                }
+                x[4 * cc] = __fadd_rn(a.x, b.x);
+                x[4 * cc + 1] = __fadd_rn(a.y, b.y);
+                x[4 * cc + 2] = __fadd_rn(a.z, b.z);
+                x[4 * cc + 3] = __fadd_rn(a.w, b.w);
+            }
+        } else if (kind == kPhO) {
+            ok = ok & gather_quads<Q::NC>(
+                          x, Q::NV, tag - 1u,
+                          [&](int c) {
+                              const int idx = 4 * c, h = idx / DH;
+                              return P.attn_part + (size_t)h * (DH + 2) + 2 + (idx - h * DH);
+                          },
+                          tid, P);
+        } else {
+            const uint64_t* src = kind == kPhQKV ? P.xa : kind == kPhFC ? P.xb : P.u;
+            ok = ok & gather_quads<Q::NC>(x, Q::NV, tag - 1u, [&](int c) { return src + 4 * (size_t)c; }, tid, P);
+        }
+        gstamp(1);
+        cstamp(3);
+        float* part = fpart + (fast_no & 1) * kFastSet;
+        float2* lns = reinterpret_cast<float2*>(part + kConsumerWarps * kSpreadRows);
+        ++fast_no;
+        float s1 = 0.0f, s2 = 0.0f;
+        if (kLnWidth && has_ln) {
+            // the residual stream for the later residual add, the LayerNorm
+            // sums, then g * x for the folded projection
+#pragma unroll
+            for (int cc = 0; cc < Q::NC; ++cc) {
+                const int col = tid + Q::NT * cc;
+                if (col < Q::NV) {
+                    reinterpret_cast<float4*>(xs)[col] = make_float4(x[4 * cc], x[4 * cc + 1], x[4 * cc + 2], x[4 * cc + 3]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        s1 += x[4 * cc + e];
+                        s2 = fmaf(x[4 * cc + e], x[4 * cc + e], s2);
+                        x[4 * cc + e] *= gq[4 * cc + e];
+                    }
+                }
+            }
+        }
+        cstamp(4);
+        coop_reg<KK>(ring, gi, g.nrows, x, part, tid);
+        if (kLnWidth && has_ln) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+            }
+            if (lane == 0) lns[warp] = make_float2(s1, s2);
+        }
+        cstamp(5);
+        volatile int* slot = s_fail + (agree_no & 1);
+        ++agree_no;
+        if (!ok) *slot = 1;
+        consumers_sync();
+        if (*slot != 0) return false;
+        // every weight read of the share is done
+        if (warp == 0 && lane < g.nchunks) mbar_arrive(&empty[(gi + (uint32_t)lane) % kSlots]);
+        gi += (uint32_t)g.nchunks;
+        if (row) {
+            float y = sum_warp_parts(part, tid);
+            if (kLnWidth && has_ln) {
+                float t1 = 0.0f, t2 = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float2 r = lns[w];
+                    t1 += r.x;
+                    t2 += r.y;
+                }
+                constexpr float inv_n = 1.0f / (float)D;
+                const float mean = t1 * inv_n;
+                const float rstd = rsqrtf(fmaxf(fmaf(t2, inv_n, -mean * mean), 0.0f) + kLnEps);
+                y = fmaf(rstd, fmaf(-mean, cj, y), dj);
+            } else {
+                y = __fadd_rn(y, dj);
+            }
+            const unsigned tg = out_tag(tag);
+            if (kind == kPhQKV) {
+                st_tagged(P.qkv + j, tg, y);
+                if (j >= D) P.cache[((uint64_t)p * L + l) * 2 * D + (j - D)] = y;
+            } else if (kind == kPhFC) {
+                st_tagged(P.u + j, tg, gelu_tanh(y));
+            } else {
+                st_tagged((kind == kPhO ? P.xb : P.xa) + j, tg, __fadd_rn(xs[j], y));
+            }
+        }
+        gstamp(2);
+        cstamp(6);
+        return true;
     };
 
     // Attention of layer l over positions 0..p, split along the key axis.
@@ -1280,6 +1438,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                                                         : kind == kPhO ? (int)kO
                                                         : kind == kPhFC ? (int)kFC : (int)kP);
             const int K = kind == kPhP ? FF : D;
+            const Geo g = geo_of(P, geot, mat);
+            const bool spread = kind != kPhVocab && share_spread(g.nchunks, g.nrows, K, Q8);
+            // binary32 spread shares take the fast phase, on gathered inputs,
+            // except where the general path forms the input vector: the
+            // activation trace, and the merge of split attention heads
+            const bool fast = !Q8 && spread && !trace_step && (kind != kPhO || S_eff == 1);
+            if (!fast) {
             // LayerNorm parameters (QKV: ln_1, FC: ln_2, vocabulary: ln_f) and
             // this CTA's bias rows are loaded before the wait for the inputs.
             const bool has_ln = kind == kPhQKV || kind == kPhFC || kind == kPhVocab;
@@ -1289,23 +1454,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 const uint64_t bo = kind == kPhQKV ? lp.ln1_b : kind == kPhFC ? lp.ln2_b : P.lnf_b;
                 load_ln_pairs<D, PPD>(P.packed + go, P.packed + bo, gr, br, tid);
             }
-            const Geo g = geo_of(P, geot, mat);
             const uint64_t boff = kind == kPhQKV ? lp.b_qkv : kind == kPhO ? lp.b_o : kind == kPhFC ? lp.b_fc : lp.b_p;
             const float bv = (kind != kPhVocab && g.nrows <= NT && tid < g.nrows) ? __ldg(P.packed + boff + g.r0 + tid)
                                                                                   : 0.0f;
-            // ---- weights of a spread share: every warp checks that the share's
-            // chunks have landed (they were issued phases ago) and, for
-            // binary32, loads its register fragments before waiting for inputs
+            // ---- weights of an int8 spread share: every warp checks that the
+            // share's chunks have landed (they were issued phases ago)
             bool ok = true;
-            float4 wreg[kPreRegs];
-            const bool spread = share_spread(g.nchunks, g.nrows, kind == kPhP ? FF : D, Q8);
-            if (spread) {
+            if (Q8 && spread) {
                 ok = wait_chunks(gi, g.nchunks);
                 __syncwarp();
-                if constexpr (!Q8) {
-                    if (kind == kPhP) preload_share<FF>(wreg, ring, gi, g.nrows, tid);
-                    else preload_share<D>(wreg, ring, gi, g.nrows, tid);
-                }
             }
             // ---- inputs
             uint64_t ov[PM + 2];  // out-projection: o words of every split, then (max, sum) words
@@ -1450,8 +1607,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             float* lg = (kind == kPhVocab && P.logits) ? P.logits + (uint64_t)s * P.logits_stride : nullptr;
             int release = 0;
             cstamp(4);
-            ok = kind == kPhP ? run_gemv(KF{}, kind, g, out_tag(tag), boff, kv_row, lg, &release, wreg)
-                              : run_gemv(KD{}, kind, g, out_tag(tag), boff, kv_row, lg, &release, wreg);
+            if (Q8 || !spread) {
+            ok = kind == kPhP ? run_gemv(KF{}, kind, g, out_tag(tag), boff, kv_row, lg, &release)
+                              : run_gemv(KD{}, kind, g, out_tag(tag), boff, kv_row, lg, &release);
             if (!agree(ok)) { alive = false; break; }
             if (warp == 0 && lane < release) mbar_arrive(&empty[(gi + (uint32_t)lane) % kSlots]);
             gi += (uint32_t)release;
@@ -1476,6 +1634,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     st_tagged_release(ap, tag_pack(tg, best.v));
                 }
             }
+            continue;
+            }  // int8 or streamed share
+            }  // general path
+            // ---- binary32 spread share: gathered inputs (fast), or the vector
+            // the general path formed in vin
+            const bool okf = kind == kPhP ? fast_phase(KF{}, kind, l, p, tok, g, tag, !fast)
+                                          : fast_phase(KD{}, kind, l, p, tok, g, tag, !fast);
+            if (!okf) { alive = false; break; }
         }
     }
     // The last step's greedy choice (CTA 0 reports it).
@@ -1537,8 +1703,15 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint
     auto out = [&](int j, float v) { y[j] = bias ? __fadd_rn(v, bias[j]) : v; };
     if (!stream) {
         float v;
-        if constexpr (Q8) v = coop_q8<K>(ring, 0u, wn, vq, vs, scratch, tid);
-        else v = coop_f32<K>(ring, 0u, wn, vin, scratch, tid);
+        if constexpr (Q8) {
+            v = coop_q8<K>(ring, 0u, wn, vq, vs, scratch, tid);
+        } else {
+            float xq[4 * Pre<K>::NC];
+            load_quads<K>(vin, xq, tid);
+            coop_reg<K>(ring, 0u, wn, xq, scratch, tid);
+            __syncthreads();
+            v = tid < wn ? sum_warp_parts(scratch, tid) : 0.0f;
+        }
         if (tid < wn) out(w0 + tid, v);
         return;
     }
@@ -1610,6 +1783,8 @@ cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfin
 // ------------------------------------------------------------ launcher
 template <int D, int FF, int DH, bool Q8>
 static cudaError_t launch_t(const StepPlan& P, cudaStream_t stream) {
+    // binary32 fast phases read the LayerNorm folds of every layer
+    if (!Q8 && P.fold == nullptr) return cudaErrorInvalidValue;
     const SmemLayout lay = smem_layout(D, FF, Q8, P.max_pos);
     auto kern = step_kernel<D, FF, DH, Q8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total);

@@ -93,6 +93,7 @@ struct StepPlan {
     int G;  // CTAs in the grid
     // weights
     const float* packed;        // packed checkpoint on the device
+    const float* fold;          // binary32: per layer the LayerNorm folds c, d of the QKV and FC rows (fold_layer_words)
     const uint8_t* wstream;     // per layer: qkv[3D] rows, o[D], fc[FF], p[D] (K-major rows)
     uint64_t layer_bytes;       // bytes of one layer in wstream
     uint64_t mat_off[4];        // byte offset of each matrix inside a layer
@@ -126,6 +127,15 @@ struct StepPlan {
     int prefetch_chunks;        // L2 bulk prefetch distance in chunks (0 = off)
     uint32_t pace_ns;           // least interval between block-weight chunk issues (0 = unpaced)
 };
+
+// LayerNorm folded into the projection that follows it (binary32 models):
+// with n = (x - mean) * rstd and y = W (g * n + b) + bias,
+//   y_j = rstd * (sum_i W_ji g_i x_i - mean * c_j) + d_j,
+//   c_j = sum_i W_ji g_i,   d_j = bias_j + sum_i W_ji b_i,
+// so the dot products can start on the raw residual stream while its
+// mean and variance are still being reduced.  Per layer: c_qkv[3D],
+// d_qkv[3D], c_fc[FF], d_fc[FF].
+__host__ __device__ constexpr uint64_t fold_layer_words(int D, int FF) { return 2ull * (3ull * D + (uint64_t)FF); }
 
 // Bytes of one K-major weight row in the device stream.
 __host__ __device__ constexpr int row_bytes(int K, bool q8) {

@@ -17,5 +17,6 @@ struct gpt2_model {
     uint64_t mat_off[4];
     uint64_t wte_off, wpe_off, lnf_g, lnf_b;
     gpt2::LayerParams lp[gpt2::kMaxLayers];
+    float* d_fold;  // binary32 models: LayerNorm folds of the QKV and FC rows (fold_layer_words per layer)
     float* d_wlo;  // binary32 models: TF32 remainders of the block matrices (prefill), made on first use
 };

@@ -98,6 +98,7 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     P.max_pos = (int)c.max_pos;
     P.G = m->G;
     P.packed = m->d_packed;
+    P.fold = m->d_fold;
     P.wstream = m->d_wstream;
     P.layer_bytes = m->layer_bytes;
     for (int i = 0; i < 4; ++i) P.mat_off[i] = m->mat_off[i];

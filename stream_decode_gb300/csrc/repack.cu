@@ -64,6 +64,38 @@ __global__ void quantize_out_in_kernel(const float* __restrict__ src, uint8_t* _
     reinterpret_cast<float*>(dst + (size_t)n * rb + K)[g] = s;
 }
 
+// The LayerNorm folds of one K-major binary32 matrix (rows of K floats):
+// c_j = sum_i W_ji g_i and d_j = bias_j + sum_i W_ji b_i, one warp per
+// row, summed in binary64 and rounded once.
+__global__ void fold_kernel(const uint8_t* __restrict__ rows, int K, int N, const float* __restrict__ g,
+                            const float* __restrict__ b, const float* __restrict__ bias, float* __restrict__ c_out,
+                            float* __restrict__ d_out) {
+    const int j = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (j >= N) return;
+    const float* w = reinterpret_cast<const float*>(rows) + (size_t)j * K;
+    double c = 0.0, d = 0.0;
+    for (int i = lane; i < K; i += 32) {
+        c += (double)w[i] * (double)g[i];
+        d += (double)w[i] * (double)b[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+        d += __shfl_xor_sync(0xffffffffu, d, o);
+    }
+    if (lane == 0) {
+        c_out[j] = (float)c;
+        d_out[j] = (float)((double)bias[j] + d);
+    }
+}
+
+cudaError_t fold_rows(const uint8_t* rows, int K, int N, const float* g, const float* b, const float* bias, float* c,
+                      float* d, cudaStream_t st) {
+    const int threads = 256, per_block = threads / 32;
+    fold_kernel<<<(N + per_block - 1) / per_block, threads, 0, st>>>(rows, K, N, g, b, bias, c, d);
+    return cudaGetLastError();
+}
+
 cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, bool q8, cudaStream_t st) {
     const int rb = row_bytes(K, q8);
     if (!q8) {
