@@ -236,6 +236,37 @@ __device__ __forceinline__ void quantize_vec(const float* v, int8_t* q, float* s
     }
 }
 
+// Quantize a K-vector held in the quad layout (thread tid owns float4
+// columns tid + NT*k) per group of 64 into q/s: a group is 16 consecutive
+// columns, i.e. one half-warp, so its largest |v| is four shuffles away.
+// Same rule as quantize_vec; the maximum is exact in any order.  Every
+// consumer thread calls it (the shuffles take all lanes).
+template <int K>
+__device__ __forceinline__ void quantize_quads(const float (&x)[4 * ((K / 4 + kConsumerWarps * 32 - 1) /
+                                                                      (kConsumerWarps * 32))],
+                                               int8_t* q, float* s, int tid) {
+    constexpr int NT = kConsumerWarps * 32, NV = K / 4, NC = (NV + NT - 1) / NT;
+    static_assert(K % kGroup == 0 && NT % 16 == 0, "groups are whole half-warps");
+#pragma unroll
+    for (int cc = 0; cc < NC; ++cc) {
+        const int col = tid + NT * cc;
+        // max of |v| starting from 0; NaN never wins a comparison
+        float m = fmaxf(fmaxf(fmaxf(fabsf(x[4 * cc]), fabsf(x[4 * cc + 1])), fmaxf(fabsf(x[4 * cc + 2]), fabsf(x[4 * cc + 3]))),
+                        0.0f);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (col < NV) {
+            const float sc = __fdiv_rn(m, 127.0f);
+            const uint32_t b0 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc], sc);
+            const uint32_t b1 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc + 1], sc);
+            const uint32_t b2 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc + 2], sc);
+            const uint32_t b3 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc + 3], sc);
+            reinterpret_cast<uint32_t*>(q)[col] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            if ((col & 15) == 0) s[col >> 4] = sc;
+        }
+    }
+}
+
 // Warp transpose-reduction: every lane holds partials v[0..N) of N rows
 // (N a power of two, at most 32).  Plain butterflies fold the lane bits above
 // log2(N), then transpose steps halve the values per lane; lane l ends with
@@ -957,14 +988,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     };
 
     ArgBest best = arg_init();
-    // One projection phase over this CTA's share of rows (input width KK),
-    // with the epilogue of each output row j run by the thread that holds it:
-    // QKV: + bias, tagged store, KV append; O and P: + bias + residual; FC:
-    // + bias, GELU; vocabulary: logits and the running greedy choice.  A
-    // spread share's slots are released by the caller after the phase's
-    // agreement barrier (*release = its chunk count); a streamed share's
-    // chunks are released by the warp that used them, with a named barrier
-    // per round of chunks so warp skew stays below one ring length.
+    // One streamed projection phase over this CTA's share of rows (input
+    // width KK; the vocabulary, or a block matrix whose share is too long to
+    // be spread), one warp per chunk, with the epilogue of each output row j
+    // run by the lane that holds it: QKV: + bias, tagged store, KV append; O
+    // and P: + bias + residual; FC: + bias, GELU; vocabulary: logits and the
+    // running greedy choice.  Chunks are released by the warp that used
+    // them, with a named barrier per round of chunks so warp skew stays below
+    // one ring length (*release stays 0).
     auto run_gemv = [&](auto kk, int kind, const Geo& g, unsigned tag, uint64_t boff, float* kv_row, float* lg,
                         int* release) -> bool {
         constexpr int KK = decltype(kk)::value;
@@ -988,17 +1019,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         };
         *release = 0;
         bool ok = true;
-        if constexpr (Q8) {
-            if (kind != kPhVocab && share_spread(g.nchunks, g.nrows, KK, Q8)) {
-                // every warp saw the share's chunks land before the phase's input wait
-                cstamp(7);
-                const float y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
-                if (tid < g.nrows) epilogue(g.r0 + tid, y);
-                cstamp(5);
-                *release = g.nchunks;
-                return true;
-            }
-        }
         constexpr int MR = dot_rows<KK, Q8>();
         static_assert(2 * kConsumerWarps <= kSlots, "a round must stay within one ring length");
         for (int k0 = 0; k0 < g.nchunks; k0 += kConsumerWarps) {
@@ -1052,10 +1072,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const LayerParams& lp = P.lp[l];
         const bool row = tid < g.nrows;
         const int j = g.r0 + tid;
-        // row constants: the LayerNorm folds, or the bias
+        // row constants: the LayerNorm folds (binary32), or the bias
         float cj = 0.0f, dj = 0.0f;
         if (row) {
-            if (has_ln) {
+            if (!Q8 && has_ln) {
                 const int N = kind == kPhQKV ? 3 * D : FF;
                 const float* f = P.fold + (uint64_t)l * fold_layer_words(D, FF) + (kind == kPhQKV ? 0 : 6 * D);
                 cj = __ldg(f + j);
@@ -1065,9 +1085,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 dj = __ldg(P.packed + bo + j);
             }
         }
-        float gq[4 * Q::NC];
+        float gq[4 * Q::NC], bq[4 * Q::NC];
         if constexpr (kLnWidth) {
-            if (has_ln) load_quads<KK>(P.packed + (kind == kPhQKV ? lp.ln1_g : lp.ln2_g), gq, tid);
+            if (has_ln) {
+                load_quads<KK>(P.packed + (kind == kPhQKV ? lp.ln1_g : lp.ln2_g), gq, tid);
+                if constexpr (Q8) load_quads<KK>(P.packed + (kind == kPhQKV ? lp.ln1_b : lp.ln2_b), bq, tid);
+            }
         }
         // the share's chunks were issued phases ago
         bool ok = wait_chunks(gi, g.nchunks);
@@ -1078,6 +1101,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         if (from_vin) {
             load_quads<KK>(vin, x, tid);
         } else if (kind == kPhQKV && l == 0) {
+            // token + position embedding (int8 models: the tied embedding's
+            // int8 row times its group scale)
             const float4* te = reinterpret_cast<const float4*>(P.packed + P.wte_off + (uint64_t)tok * D);
             const float4* pe = reinterpret_cast<const float4*>(P.packed + P.wpe_off + (uint64_t)p * D);
 #pragma unroll
@@ -1085,7 +1110,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 const int col = tid + Q::NT * cc;
                 float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
                 if (col < Q::NV) {
-                    a = __ldg(te + col);
+                    if constexpr (Q8) {
+                        const uint8_t* row = P.vocab + (uint64_t)tok * row_bytes(D, true);
+                        const char4 qv = reinterpret_cast<const char4*>(row)[col];
+                        const float sv = reinterpret_cast<const float*>(row + D)[(4 * col) / kGroup];
+                        a = make_float4(__fmul_rn((float)qv.x, sv), __fmul_rn((float)qv.y, sv),
+                                        __fmul_rn((float)qv.z, sv), __fmul_rn((float)qv.w, sv));
+                    } else {
+                        a = __ldg(te + col);
+                    }
                     b = __ldg(pe + col);
                 }
                 x[4 * cc] = __fadd_rn(a.x, b.x);
@@ -1112,8 +1145,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         ++fast_no;
         float s1 = 0.0f, s2 = 0.0f;
         if (kLnWidth && has_ln) {
-            // the residual stream for the later residual add, the LayerNorm
-            // sums, then g * x for the folded projection
+            // the residual stream for the later residual add and the
+            // LayerNorm sums; binary32 then takes g * x for the folded
+            // projection
 #pragma unroll
             for (int cc = 0; cc < Q::NC; ++cc) {
                 const int col = tid + Q::NT * cc;
@@ -1123,13 +1157,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     for (int e = 0; e < 4; ++e) {
                         s1 += x[4 * cc + e];
                         s2 = fmaf(x[4 * cc + e], x[4 * cc + e], s2);
-                        x[4 * cc + e] *= gq[4 * cc + e];
+                        if constexpr (!Q8) x[4 * cc + e] *= gq[4 * cc + e];
                     }
                 }
             }
         }
         cstamp(4);
-        coop_reg<KK>(ring, gi, g.nrows, x, part, tid);
+        if constexpr (!Q8) coop_reg<KK>(ring, gi, g.nrows, x, part, tid);
         if (kLnWidth && has_ln) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -1144,26 +1178,47 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         if (!ok) *slot = 1;
         consumers_sync();
         if (*slot != 0) return false;
+        // the mean and inverse deviation of the LayerNorm input
+        auto ln_stats = [&](float& mean, float& rstd) {
+            float t1 = 0.0f, t2 = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float2 r = lns[w];
+                t1 += r.x;
+                t2 += r.y;
+            }
+            constexpr float inv_n = 1.0f / (float)D;
+            mean = t1 * inv_n;
+            rstd = rsqrtf(fmaxf(fmaf(t2, inv_n, -mean * mean), 0.0f) + kLnEps);
+        };
+        float y = 0.0f;
+        if constexpr (Q8) {
+            // int8: LayerNorm in registers, then the quantized input to
+            // shared memory for the (row, group) dot-product tasks
+            if (kLnWidth && has_ln) {
+                float mean, rstd;
+                ln_stats(mean, rstd);
+#pragma unroll
+                for (int e = 0; e < 4 * Q::NC; ++e) x[e] = fmaf((x[e] - mean) * rstd, gq[e], bq[e]);
+            }
+            quantize_quads<KK>(x, vq, vs, tid);
+            consumers_sync();
+            y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
+        } else {
+            if (row) {
+                y = sum_warp_parts(part, tid);
+                if (kLnWidth && has_ln) {
+                    float mean, rstd;
+                    ln_stats(mean, rstd);
+                    y = fmaf(rstd, fmaf(-mean, cj, y), dj);
+                }
+            }
+        }
         // every weight read of the share is done
         if (warp == 0 && lane < g.nchunks) mbar_arrive(&empty[(gi + (uint32_t)lane) % kSlots]);
         gi += (uint32_t)g.nchunks;
         if (row) {
-            float y = sum_warp_parts(part, tid);
-            if (kLnWidth && has_ln) {
-                float t1 = 0.0f, t2 = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float2 r = lns[w];
-                    t1 += r.x;
-                    t2 += r.y;
-                }
-                constexpr float inv_n = 1.0f / (float)D;
-                const float mean = t1 * inv_n;
-                const float rstd = rsqrtf(fmaxf(fmaf(t2, inv_n, -mean * mean), 0.0f) + kLnEps);
-                y = fmaf(rstd, fmaf(-mean, cj, y), dj);
-            } else {
-                y = __fadd_rn(y, dj);
-            }
+            if (Q8 || !(kLnWidth && has_ln)) y = __fadd_rn(y, dj);
             const unsigned tg = out_tag(tag);
             if (kind == kPhQKV) {
                 st_tagged(P.qkv + j, tg, y);
@@ -1440,10 +1495,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             const int K = kind == kPhP ? FF : D;
             const Geo g = geo_of(P, geot, mat);
             const bool spread = kind != kPhVocab && share_spread(g.nchunks, g.nrows, K, Q8);
-            // binary32 spread shares take the fast phase, on gathered inputs,
-            // except where the general path forms the input vector: the
-            // activation trace, and the merge of split attention heads
-            const bool fast = !Q8 && spread && !trace_step && (kind != kPhO || S_eff == 1);
+            // spread shares take the fast phase, on gathered inputs, except
+            // where the general path forms the input vector: the activation
+            // trace, and the merge of split attention heads
+            const bool fast = spread && !trace_step && (kind != kPhO || S_eff == 1);
             if (!fast) {
             // LayerNorm parameters (QKV: ln_1, FC: ln_2, vocabulary: ln_f) and
             // this CTA's bias rows are loaded before the wait for the inputs.
@@ -1457,13 +1512,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             const uint64_t boff = kind == kPhQKV ? lp.b_qkv : kind == kPhO ? lp.b_o : kind == kPhFC ? lp.b_fc : lp.b_p;
             const float bv = (kind != kPhVocab && g.nrows <= NT && tid < g.nrows) ? __ldg(P.packed + boff + g.r0 + tid)
                                                                                   : 0.0f;
-            // ---- weights of an int8 spread share: every warp checks that the
-            // share's chunks have landed (they were issued phases ago)
             bool ok = true;
-            if (Q8 && spread) {
-                ok = wait_chunks(gi, g.nchunks);
-                __syncwarp();
-            }
             // ---- inputs
             uint64_t ov[PM + 2];  // out-projection: o words of every split, then (max, sum) words
             float xv[2 * PPD];  // LayerNorm phases: this thread's pairs of the residual stream
@@ -1582,9 +1631,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             }
             consumers_sync();
             if constexpr (Q8) {
-                if (kind == kPhP) quantize_vec<FF>(vin, vq, vs, warp, lane);
-                else quantize_vec<D>(vin, vq, vs, warp, lane);
-                consumers_sync();
+                // a streamed share's input (a spread share quantizes in its phase)
+                if (!spread) {
+                    if (kind == kPhP) quantize_vec<FF>(vin, vq, vs, warp, lane);
+                    else quantize_vec<D>(vin, vq, vs, warp, lane);
+                    consumers_sync();
+                }
             }
             // ---- activation trace (step 0, CTA 0): per layer x, LN_1(x), qkv,
             // attention output, x_mid, LN_2(x_mid), GELU output; then x_final, LN_f(x_final)
@@ -1607,7 +1659,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             float* lg = (kind == kPhVocab && P.logits) ? P.logits + (uint64_t)s * P.logits_stride : nullptr;
             int release = 0;
             cstamp(4);
-            if (Q8 || !spread) {
+            if (!spread) {
             ok = kind == kPhP ? run_gemv(KF{}, kind, g, out_tag(tag), boff, kv_row, lg, &release)
                               : run_gemv(KD{}, kind, g, out_tag(tag), boff, kv_row, lg, &release);
             if (!agree(ok)) { alive = false; break; }
@@ -1635,10 +1687,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 }
             }
             continue;
-            }  // int8 or streamed share
+            }  // streamed share
             }  // general path
-            // ---- binary32 spread share: gathered inputs (fast), or the vector
-            // the general path formed in vin
+            // ---- spread share: gathered inputs (fast), or the vector the
+            // general path formed in vin
             const bool okf = kind == kPhP ? fast_phase(KF{}, kind, l, p, tok, g, tag, !fast)
                                           : fast_phase(KD{}, kind, l, p, tok, g, tag, !fast);
             if (!okf) { alive = false; break; }
