@@ -228,9 +228,9 @@ __device__ __forceinline__ void quantize_vec(const float* v, int8_t* q, float* s
     for (int k = 0; k < GPW; ++k) {
         const int gi = warp + kConsumerWarps * k;
         if (gi < NG) {
-            const float sc = __fdiv_rn(m[k], 127.0f);
-            q[gi * kGroup + lane] = (int8_t)quantize_one(a[k], sc);
-            q[gi * kGroup + 32 + lane] = (int8_t)quantize_one(b[k], sc);
+            const float sc = __fdiv_rn(m[k], 127.0f), inv = __frcp_rn(sc);
+            q[gi * kGroup + lane] = (int8_t)quantize_fast(a[k], sc, inv);
+            q[gi * kGroup + 32 + lane] = (int8_t)quantize_fast(b[k], sc, inv);
             if (lane == 0) s[gi] = sc;
         }
     }
@@ -256,11 +256,11 @@ __device__ __forceinline__ void quantize_quads(const float (&x)[4 * ((K / 4 + kC
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (col < NV) {
-            const float sc = __fdiv_rn(m, 127.0f);
-            const uint32_t b0 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc], sc);
-            const uint32_t b1 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc + 1], sc);
-            const uint32_t b2 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc + 2], sc);
-            const uint32_t b3 = (uint32_t)(uint8_t)(int8_t)quantize_one(x[4 * cc + 3], sc);
+            const float sc = __fdiv_rn(m, 127.0f), inv = __frcp_rn(sc);
+            const uint32_t b0 = (uint32_t)(uint8_t)(int8_t)quantize_fast(x[4 * cc], sc, inv);
+            const uint32_t b1 = (uint32_t)(uint8_t)(int8_t)quantize_fast(x[4 * cc + 1], sc, inv);
+            const uint32_t b2 = (uint32_t)(uint8_t)(int8_t)quantize_fast(x[4 * cc + 2], sc, inv);
+            const uint32_t b3 = (uint32_t)(uint8_t)(int8_t)quantize_fast(x[4 * cc + 3], sc, inv);
             reinterpret_cast<uint32_t*>(q)[col] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
             if ((col & 15) == 0) s[col >> 4] = sc;
         }
@@ -1176,8 +1176,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         volatile int* slot = s_fail + (agree_no & 1);
         ++agree_no;
         if (!ok) *slot = 1;
-        consumers_sync();
-        if (*slot != 0) return false;
+        // (an int8 phase without LayerNorm agrees at its quantization barrier)
+        if (!Q8 || (kLnWidth && has_ln)) {
+            consumers_sync();
+            if (*slot != 0) return false;
+        }
         // the mean and inverse deviation of the LayerNorm input
         auto ln_stats = [&](float& mean, float& rstd) {
             float t1 = 0.0f, t2 = 0.0f;
@@ -1203,6 +1206,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             }
             quantize_quads<KK>(x, vq, vs, tid);
             consumers_sync();
+            if (!(kLnWidth && has_ln) && *slot != 0) return false;
             y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
         } else {
             if (row) {

@@ -262,4 +262,21 @@ __device__ __forceinline__ int quantize_one(float x, float s) {
     return static_cast<int>(r);
 }
 
+// The same code as quantize_one(x, s), given inv = 1/s rounded to nearest.
+// The product y = x * inv is within 2.5 ulp of the rounded quotient x / s,
+// so their nearest-even integers agree unless a half-integer lies within
+// that distance; for a group's own values |x / s| <= 127, where ulp(y) <=
+// 2^-17.  When y is within 8 * 2^-17 of the half-integer between its
+// neighbouring integers (about one value in 8000), or out of range, or s is
+// 0, the quotient itself decides.
+__device__ __forceinline__ int quantize_fast(float x, float s, float inv) {
+    const float y = __fmul_rn(x, inv);
+    const float d = fabsf(__fsub_rn(__fsub_rn(y, floorf(y)), 0.5f));
+    if (s != 0.0f && fabsf(y) < 128.0f && d > 6.103515625e-05f) {
+        const float r = rintf(y);
+        return static_cast<int>(fminf(fmaxf(r, -127.0f), 127.0f));
+    }
+    return quantize_one(x, s);
+}
+
 }  // namespace gpt2

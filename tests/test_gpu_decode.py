@@ -289,6 +289,42 @@ def test_projections_on_identical_inputs(g, oracle, shape, seed, quant):
     check_projections(g, oracle, shape, w, quant, range(4 * shape.n_layer + 1))
 
 
+def test_int8_activation_codes_near_ties(g, oracle):
+    """The int8 activation quantizer on inputs whose quotients x / s sit
+    at, or a few ulp either side of, the half-integers where nearest-even
+    rounding changes its answer (the quantization rule of the quantized
+    GPT-2 abstract): every code must equal the oracle's, so the int8
+    projection of such a vector is bit-identical to the oracle's."""
+    shape = P.SMALL
+    w = synth.checkpoint(shape, P.SEED_SMALL, "rich")
+    model = g.Model(shape, w, quant=1)
+    om = oracle.model(shape, w, quant=1)
+    rng = np.random.default_rng(2024)
+    for idx in (0, 3):
+        n_in = shape.d_ff if idx % 4 == 3 else shape.d_model
+        x = np.empty(n_in, np.float32)
+        for g0 in range(0, n_in, 64):
+            m = np.float32(rng.uniform(0.25, 4.0))
+            sc = np.float32(m / np.float32(127.0))
+            k = rng.integers(-126, 126, 64).astype(np.float32)
+            v = ((k + np.float32(0.5)) * sc).astype(np.float32)
+            steps = rng.integers(-3, 4, 64)
+            for i in range(64):
+                for _ in range(abs(int(steps[i]))):
+                    v[i] = np.nextafter(v[i], np.float32(np.inf) if steps[i] > 0 else np.float32(-np.inf))
+            v[rng.integers(0, 64)] = m if rng.random() < 0.5 else -m  # the group's largest magnitude
+            x[g0:g0 + 64] = v
+        q, s_ = om.q8_matrix(idx)
+        dx = torch.tensor(x, device="cuda")
+        dy = torch.full((q.shape[0],), float("nan"), device="cuda")
+        assert model.debug_project(idx, dx, dy) == "ok"
+        torch.cuda.synchronize()
+        ref = oracle.linear_q8(x, q, s_, _matrix_bias(shape, w, idx))
+        assert np.array_equal(dy.cpu().numpy().view(np.uint32), ref.view(np.uint32)), f"matrix {idx}"
+    model.close()
+    om.close()
+
+
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
 def test_int8_session(g, oracle, shape, seed):
