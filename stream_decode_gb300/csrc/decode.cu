@@ -424,14 +424,17 @@ __device__ __forceinline__ float sum_warp_parts(const float* part, int r) {
 }
 
 // Exact int32 sum of the 64 products of one group (two independent dp4a
-// chains; integer addition is exact in any order).
-__device__ __forceinline__ int group_dot(const uint8_t* w, const int8_t* x) {
+// chains; integer addition is exact in any order).  The four 16-byte
+// quarters are read starting at quarter rot: lanes whose groups lie 64
+// bytes apart then hit eight distinct bank groups per load instead of two.
+__device__ __forceinline__ int group_dot(const uint8_t* w, const int8_t* x, int rot) {
     const int4* wv = reinterpret_cast<const int4*>(w);
     const int4* xv = reinterpret_cast<const int4*>(x);
     int a0 = 0, a1 = 0;
 #pragma unroll
     for (int v = 0; v < 4; v += 2) {
-        const int4 p = wv[v], q = xv[v], r = wv[v + 1], s = xv[v + 1];
+        const int j0 = (v + rot) & 3, j1 = (v + 1 + rot) & 3;
+        const int4 p = wv[j0], q = xv[j0], r = wv[j1], s = xv[j1];
         a0 = __dp4a(p.x, q.x, a0);
         a1 = __dp4a(r.x, s.x, a1);
         a0 = __dp4a(p.y, q.y, a0);
@@ -445,9 +448,10 @@ __device__ __forceinline__ int group_dot(const uint8_t* w, const int8_t* x) {
 }
 
 // The rescale term of one (row, group): ((float)acc * s_x[g]) * s_w[g],
-// explicitly rounded.
-__device__ __forceinline__ float group_term(const uint8_t* row, int g, int K, const int8_t* xq, const float* xs) {
-    const int acc = group_dot(row + g * kGroup, xq + g * kGroup);
+// explicitly rounded; rot: the caller's lane-dependent quarter rotation.
+__device__ __forceinline__ float group_term(const uint8_t* row, int g, int K, const int8_t* xq, const float* xs,
+                                           int rot) {
+    const int acc = group_dot(row + g * kGroup, xq + g * kGroup, rot);
     return __fmul_rn(__fmul_rn(__int2float_rn(acc), xs[g]), reinterpret_cast<const float*>(row + K)[g]);
 }
 
@@ -482,7 +486,7 @@ __device__ __forceinline__ float coop_q8(const uint8_t* ring, uint32_t c0, int n
         const int i = tk / R::NG, g = tk - i * R::NG;
         const uint8_t* row = ring + (size_t)((c0 + (uint32_t)(i / R::RPC)) % kSlots) * kSlotBytes +
                              (size_t)((i % R::RPC) * R::RB);
-        scr[tk] = group_term(row, g, K, xq, xs);
+        scr[tk] = group_term(row, g, K, xq, xs, (tid >> 1) & 3);
     }
     consumers_sync();
     return tid < nrows ? ordered_sum<R::NG>(scr + tid * R::NG) : 0.0f;
@@ -535,7 +539,7 @@ __device__ __forceinline__ float dot_q8(const uint8_t* w, int m, const int8_t* x
 #pragma unroll 2
     for (int tk = lane; tk < m * R::NG; tk += 32) {
         const int i = tk / R::NG, g = tk - i * R::NG;
-        scr[tk] = group_term(w + (size_t)i * R::RB, g, K, xq, xs);
+        scr[tk] = group_term(w + (size_t)i * R::RB, g, K, xq, xs, (lane >> 1) & 3);
     }
     __syncwarp();
     const float sum = lane < m ? ordered_sum<R::NG>(scr + lane * R::NG) : 0.0f;
