@@ -146,22 +146,25 @@ __global__ void reduce_kernel(const float* __restrict__ part, int splits, int n,
 }
 
 constexpr int kAttnWarps = 8;
-constexpr int kAttnRows = 32;          // query rows per block
+constexpr int kAttnRows = 16;          // query rows per block (two per warp)
 constexpr int kMaxPrefillKeys = 1024;  // longest prompt (the keys of a block are staged in chunks of kKeyTile)
 constexpr int kKeyTile = 64;
 
-// Causal attention of head h for query rows [r0, r0 + 32) of the prompt:
-// s_j = (q . k_j) / sqrt(dh) over keys j <= i, softmax, o = sum_j a_j v_j
-// (dh <= 64).  The keys and values are staged in shared memory in tiles of
-// 64 (keys padded to dh + 1 floats a row: conflict-free column reads); each
-// warp takes 4 query rows and keeps, per row, the scores of the current
-// tile, an online max / sum and its two output coordinates per lane.
+// Causal attention of head h for query rows [r0, r0 + 16) of the prompt:
+// s_j = (q . k_j) / sqrt(dh) over keys j <= i, softmax, o = sum_j a_j v_j.
+// The keys and values are staged in shared memory in tiles of 64 (keys
+// padded to DH + 1 floats a row: conflict-free reads down a column); each
+// warp takes 2 query rows and keeps, per row, the scores of the current
+// tile, an online max / sum and its output coordinates (lane, lane + 32).
+// Dot products and the weighted value sums run in four independent chains.
+template <int DH>
 __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float* __restrict__ QKV, int n, int D,
-                                                                    int DH, float* __restrict__ O,
-                                                                    float* __restrict__ Olo) {
-    __shared__ float ks[kKeyTile][65];
-    __shared__ float vs[kKeyTile][64];
-    __shared__ float qs[kAttnRows][64];
+                                                                    float* __restrict__ O, float* __restrict__ Olo) {
+    static_assert(DH % 4 == 0 && DH <= 64, "head width");
+    constexpr int DPL = (DH + 31) / 32;  // output coordinates per lane
+    __shared__ float ks[kKeyTile][DH + 1];
+    __shared__ __align__(16) float vs[kKeyTile][DH];
+    __shared__ float qs[kAttnRows][DH];
     __shared__ float ps[kAttnWarps][kKeyTile];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x, r0 = blockIdx.y * kAttnRows;
@@ -173,22 +176,27 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float*
         qs[r][e] = r0 + r < n ? QKV[(size_t)(r0 + r) * N3 + (size_t)h * DH + e] : 0.0f;
     }
     constexpr int RPW = kAttnRows / kAttnWarps;  // query rows per warp
-    float m[RPW], z[RPW], o0[RPW], o1[RPW];
+    float m[RPW], z[RPW], o[RPW][DPL];
 #pragma unroll
     for (int t = 0; t < RPW; ++t) {
         m[t] = -INFINITY;
         z[t] = 0.0f;
-        o0[t] = 0.0f;
-        o1[t] = 0.0f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[t][d] = 0.0f;
     }
     for (int j0 = 0; j0 < rmax; j0 += kKeyTile) {
         const int jn = min(kKeyTile, rmax - j0);
         __syncthreads();
-        for (int i = threadIdx.x; i < jn * DH; i += blockDim.x) {
-            const int j = i / DH, e = i - j * DH;
+        for (int i = threadIdx.x; i < jn * (DH / 4); i += blockDim.x) {
+            const int j = i / (DH / 4), e = 4 * (i - j * (DH / 4));
             const size_t base = (size_t)(j0 + j) * N3 + (size_t)h * DH + e;
-            ks[j][e] = QKV[base + D];
-            vs[j][e] = QKV[base + 2 * D];
+            const float4 kv = *reinterpret_cast<const float4*>(QKV + base + D);
+            const float4 vv = *reinterpret_cast<const float4*>(QKV + base + 2 * D);
+            ks[j][e] = kv.x;
+            ks[j][e + 1] = kv.y;
+            ks[j][e + 2] = kv.z;
+            ks[j][e + 3] = kv.w;
+            *reinterpret_cast<float4*>(&vs[j][e]) = vv;
         }
         __syncthreads();
 #pragma unroll
@@ -197,35 +205,66 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float*
             if (i >= n) continue;
             const int kend = min(jn, i - j0 + 1);  // keys of this tile at or before row i
             if (kend <= 0) continue;
-            // scores of this tile: lane takes keys lane, lane + 32, ...
+            // scores of this tile: lane takes keys lane, lane + 32
             float tmax = -INFINITY;
-            for (int j = lane; j < kend; j += 32) {
-                float dot = 0.0f;
-                for (int e = 0; e < DH; ++e) dot = fmaf(qs[r][e], ks[j][e], dot);
-                const float sc = dot * scale;
-                ps[warp][j] = sc;
-                tmax = fmaxf(tmax, sc);
+#pragma unroll
+            for (int jj = 0; jj < kKeyTile; jj += 32) {
+                const int j = jj + lane;
+                if (j < kend) {
+                    float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < DH; e += 4) {
+                        d0 = fmaf(qs[r][e], ks[j][e], d0);
+                        d1 = fmaf(qs[r][e + 1], ks[j][e + 1], d1);
+                        d2 = fmaf(qs[r][e + 2], ks[j][e + 2], d2);
+                        d3 = fmaf(qs[r][e + 3], ks[j][e + 3], d3);
+                    }
+                    const float sc = ((d0 + d1) + (d2 + d3)) * scale;
+                    ps[warp][j] = sc;
+                    tmax = fmaxf(tmax, sc);
+                }
             }
             tmax = warp_max32(tmax);
             const float mn = fmaxf(m[t], tmax);
             const float corr = expf(m[t] - mn);  // 0 while m is -inf
             float tz = 0.0f;
-            for (int j = lane; j < kend; j += 32) {
-                const float e = expf(ps[warp][j] - mn);
-                ps[warp][j] = e;
-                tz += e;
+#pragma unroll
+            for (int jj = 0; jj < kKeyTile; jj += 32) {
+                const int j = jj + lane;
+                if (j < kend) {
+                    const float e = expf(ps[warp][j] - mn);
+                    ps[warp][j] = e;
+                    tz += e;
+                }
             }
             tz = warp_sum32(tz);
             __syncwarp();
-            float a0 = o0[t] * corr, a1 = o1[t] * corr;
-            for (int j = 0; j < kend; ++j) {
+            // weighted values: four chains over keys j = 4u + c
+            float acc[DPL][4];
+#pragma unroll
+            for (int d = 0; d < DPL; ++d)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[d][c] = 0.0f;
+            int j = 0;
+            for (; j + 4 <= kend; j += 4) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float pj = ps[warp][j + c];
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d)
+                        if (lane + 32 * d < DH) acc[d][c] = fmaf(pj, vs[j + c][lane + 32 * d], acc[d][c]);
+                }
+            }
+            for (; j < kend; ++j) {
                 const float pj = ps[warp][j];
-                if (lane < DH) a0 = fmaf(pj, vs[j][lane], a0);
-                if (lane + 32 < DH) a1 = fmaf(pj, vs[j][lane + 32], a1);
+#pragma unroll
+                for (int d = 0; d < DPL; ++d)
+                    if (lane + 32 * d < DH) acc[d][0] = fmaf(pj, vs[j][lane + 32 * d], acc[d][0]);
             }
             __syncwarp();
-            o0[t] = a0;
-            o1[t] = a1;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d)
+                o[t][d] = fmaf(o[t][d], corr, (acc[d][0] + acc[d][1]) + (acc[d][2] + acc[d][3]));
             z[t] = fmaf(z[t], corr, tz);
             m[t] = mn;
         }
@@ -234,15 +273,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float*
     for (int t = 0; t < RPW; ++t) {
         const int i = r0 + warp * RPW + t;
         if (i >= n) continue;
-        if (lane < DH) {
-            const float o = o0[t] / z[t];
-            O[(size_t)i * D + (size_t)h * DH + lane] = o;
-            Olo[(size_t)i * D + (size_t)h * DH + lane] = tf32_lo(o);
-        }
-        if (lane + 32 < DH) {
-            const float o = o1[t] / z[t];
-            O[(size_t)i * D + (size_t)h * DH + lane + 32] = o;
-            Olo[(size_t)i * D + (size_t)h * DH + lane + 32] = tf32_lo(o);
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) {
+            const int e = lane + 32 * d;
+            if (e < DH) {
+                const float v = o[t][d] / z[t];
+                O[(size_t)i * D + (size_t)h * DH + e] = v;
+                Olo[(size_t)i * D + (size_t)h * DH + e] = tf32_lo(v);
+            }
         }
     }
 }
@@ -439,7 +477,7 @@ void prefill_free(PrefillWs* w) {
 
 bool prefill_shape_supported(const gpt2_config& c) {
     const int D = (int)c.d_model, FF = (int)c.d_ff, DH = D / (int)c.n_head;
-    return D % tc::kTileN == 0 && FF % tc::kTileN == 0 && D <= 1024 && DH <= 64 && DH % 4 == 0 &&
+    return D % tc::kTileN == 0 && FF % tc::kTileN == 0 && D <= 1024 && (DH == 16 || DH == 32 || DH == 64) &&
            c.max_pos <= kMaxPrefillKeys;
 }
 
@@ -486,8 +524,10 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
         ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + lp.ln1_g, P + lp.ln1_b, D, w->A, w->Alo);
         if ((e = gemm(w->A, w->Alo, D, 3 * D, l, kQKV, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, 3 * D, lp.b_qkv, kRedQKV, w->QKV, nullptr, l)) != cudaSuccess) break;
-        attention_kernel<<<dim3(H, (n + kAttnRows - 1) / kAttnRows), kAttnWarps * 32, 0, st>>>(w->QKV, n, D, DH,
-                                                                                                w->A, w->Alo);
+        const dim3 agrid(H, (n + kAttnRows - 1) / kAttnRows);
+        if (DH == 64) attention_kernel<64><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
+        else if (DH == 32) attention_kernel<32><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
+        else attention_kernel<16><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
         if ((e = gemm(w->A, w->Alo, D, D, l, kO, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, D, lp.b_o, kRedResidual, nullptr, nullptr, l)) != cudaSuccess) break;
         ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + lp.ln2_g, P + lp.ln2_b, D, w->A, w->Alo);
