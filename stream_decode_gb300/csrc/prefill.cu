@@ -288,21 +288,36 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float*
 constexpr int kHeadThreads = 256;
 
 // Greedy choice over the logits (largest value, lowest index on ties; any
-// non-finite value makes the choice 0xFFFFFFFF and sets the status).
-__global__ void __launch_bounds__(256) choice_kernel(const float* __restrict__ v, unsigned n, uint32_t* choice,
-                                                     uint32_t* next, int* status) {
-    __shared__ float s_v[8];
-    __shared__ unsigned s_i[8];
-    __shared__ int s_nf[8];
+// non-finite value makes the choice 0xFFFFFFFF and sets the status).  One
+// block of 1024 threads; float4 loads when the logits are 16-byte aligned.
+constexpr int kChoiceThreads = 1024;
+__device__ __forceinline__ void choice_take(float x, unsigned j, float& bv, unsigned& bi, int& nf) {
+    if (!isfinite(x)) nf = 1;
+    else if (x > bv || (x == bv && j < bi)) { bv = x; bi = j; }
+}
+__global__ void __launch_bounds__(kChoiceThreads) choice_kernel(const float* __restrict__ v, unsigned n,
+                                                                uint32_t* choice, uint32_t* next, int* status) {
+    __shared__ float s_v[kChoiceThreads / 32];
+    __shared__ unsigned s_i[kChoiceThreads / 32];
+    __shared__ int s_nf[kChoiceThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float bv = -INFINITY;
     unsigned bi = 0xFFFFFFFFu;
     int nf = 0;
-    for (unsigned j = tid; j < n; j += 256) {
-        const float x = v[j];
-        if (!isfinite(x)) nf = 1;
-        else if (x > bv || (x == bv && j < bi)) { bv = x; bi = j; }
+    unsigned done = 0;
+    if ((reinterpret_cast<uintptr_t>(v) & 15u) == 0) {
+        const unsigned n4 = n / 4;
+        const float4* v4 = reinterpret_cast<const float4*>(v);
+        for (unsigned q = tid; q < n4; q += kChoiceThreads) {
+            const float4 x = v4[q];
+            choice_take(x.x, 4 * q, bv, bi, nf);
+            choice_take(x.y, 4 * q + 1, bv, bi, nf);
+            choice_take(x.z, 4 * q + 2, bv, bi, nf);
+            choice_take(x.w, 4 * q + 3, bv, bi, nf);
+        }
+        done = 4 * n4;
     }
+    for (unsigned j = done + tid; j < n; j += kChoiceThreads) choice_take(v[j], j, bv, bi, nf);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -313,7 +328,7 @@ __global__ void __launch_bounds__(256) choice_kernel(const float* __restrict__ v
     if (lane == 0) { s_v[warp] = bv; s_i[warp] = bi; s_nf[warp] = nf; }
     __syncthreads();
     if (tid == 0) {
-        for (int w = 1; w < 8; ++w) {
+        for (int w = 1; w < kChoiceThreads / 32; ++w) {
             nf |= s_nf[w];
             if (s_v[w] > bv || (s_v[w] == bv && s_i[w] < bi)) { bv = s_v[w]; bi = s_i[w]; }
         }
@@ -325,13 +340,19 @@ __global__ void __launch_bounds__(256) choice_kernel(const float* __restrict__ v
 }
 
 // logits[r] = wte[r] . LN_f(X[last]) for r < V; every block recomputes the
-// final LayerNorm of the last row into shared memory (D <= 1024).
+// final LayerNorm of the last row into shared memory (D = 4 * NV <= 1024).
+// A warp takes two rows at a time with all of their float4 loads issued
+// before the first multiply, so enough bytes are in flight to stream the
+// tied embedding at HBM speed.
+template <int NV>
 __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float* __restrict__ X, int last,
                                                             const float* __restrict__ g,
                                                             const float* __restrict__ b,
-                                                            const float* __restrict__ wte, int D, int V,
+                                                            const float* __restrict__ wte, int V,
                                                             float* __restrict__ logits) {
-    __shared__ __align__(16) float xs[1024];
+    constexpr int D = 4 * NV, PL = (NV + 31) / 32;  // float4 per lane per row
+    static_assert(D <= 1024, "row width");
+    __shared__ __align__(16) float xs[D];
     __shared__ float red[kHeadThreads / 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float* x = X + (size_t)last * D;
@@ -357,20 +378,43 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float* __restr
     const float den = sqrtf(v / (float)D + kLnEps);
     for (int i = tid; i < D; i += kHeadThreads) xs[i] = (x[i] - mean) / den * g[i] + b[i];
     __syncthreads();
-    const int nv = D / 4;
     const float4* x4 = reinterpret_cast<const float4*>(xs);
-    for (int r = blockIdx.x * (kHeadThreads / 32) + warp; r < V; r += gridDim.x * (kHeadThreads / 32)) {
-        const float4* w4 = reinterpret_cast<const float4*>(wte + (size_t)r * D);
-        float acc = 0.0f;
-        for (int c = lane; c < nv; c += 32) {
-            const float4 a = __ldcs(w4 + c), xx = x4[c];
-            acc = fmaf(a.x, xx.x, acc);
-            acc = fmaf(a.y, xx.y, acc);
-            acc = fmaf(a.z, xx.z, acc);
-            acc = fmaf(a.w, xx.w, acc);
+    float4 xr[PL];
+#pragma unroll
+    for (int p = 0; p < PL; ++p) {
+        const int c = lane + 32 * p;
+        xr[p] = c < NV ? x4[c] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    const int gw = blockIdx.x * (kHeadThreads / 32) + warp, nw = gridDim.x * (kHeadThreads / 32);
+    for (int r = gw; r < V; r += 2 * nw) {
+        const int r2 = r + nw;
+        const float4* w0 = reinterpret_cast<const float4*>(wte + (size_t)r * D);
+        const float4* w1 = reinterpret_cast<const float4*>(wte + (size_t)(r2 < V ? r2 : r) * D);
+        float4 a0[PL], a1[PL];
+#pragma unroll
+        for (int p = 0; p < PL; ++p) {
+            const int c = lane + 32 * p;
+            a0[p] = c < NV ? __ldcs(w0 + c) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            a1[p] = c < NV ? __ldcs(w1 + c) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
-        acc = warp_sum32(acc);
-        if (lane == 0) logits[r] = acc;
+        float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll
+        for (int p = 0; p < PL; ++p) {
+            acc0 = fmaf(a0[p].x, xr[p].x, acc0);
+            acc0 = fmaf(a0[p].y, xr[p].y, acc0);
+            acc0 = fmaf(a0[p].z, xr[p].z, acc0);
+            acc0 = fmaf(a0[p].w, xr[p].w, acc0);
+            acc1 = fmaf(a1[p].x, xr[p].x, acc1);
+            acc1 = fmaf(a1[p].y, xr[p].y, acc1);
+            acc1 = fmaf(a1[p].z, xr[p].z, acc1);
+            acc1 = fmaf(a1[p].w, xr[p].w, acc1);
+        }
+        acc0 = warp_sum32(acc0);
+        acc1 = warp_sum32(acc1);
+        if (lane == 0) {
+            logits[r] = acc0;
+            if (r2 < V) logits[r2] = acc1;
+        }
     }
 }
 
@@ -477,7 +521,8 @@ void prefill_free(PrefillWs* w) {
 
 bool prefill_shape_supported(const gpt2_config& c) {
     const int D = (int)c.d_model, FF = (int)c.d_ff, DH = D / (int)c.n_head;
-    return D % tc::kTileN == 0 && FF % tc::kTileN == 0 && D <= 1024 && (DH == 16 || DH == 32 || DH == 64) &&
+    return D % tc::kTileN == 0 && FF % tc::kTileN == 0 && (D == 64 || D == 192 || D == 768) &&
+           (DH == 16 || DH == 32 || DH == 64) &&
            c.max_pos <= kMaxPrefillKeys;
 }
 
@@ -537,9 +582,15 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
         if ((e = reduce(sp, D, lp.b_p, kRedResidual, nullptr, nullptr, l)) != cudaSuccess) break;
     }
     if (e != cudaSuccess) return e;
-    head_kernel<<<g_sms, kHeadThreads, 0, st>>>(w->X, n - 1, P + m->lnf_g, P + m->lnf_b, P + m->wte_off, D,
-                                                (int)c.vocab, logits);
-    choice_kernel<<<1, 256, 0, st>>>(logits, c.vocab, d_choice, d_next, status);
+    const float* lg = P + m->lnf_g;
+    const float* lb = P + m->lnf_b;
+    const float* wte = P + m->wte_off;
+    const int hb = 2 * g_sms;  // two blocks per SM
+    if (D == 768) head_kernel<192><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
+    else if (D == 192) head_kernel<48><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
+    else if (D == 64) head_kernel<16><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
+    else return cudaErrorInvalidValue;
+    choice_kernel<<<1, kChoiceThreads, 0, st>>>(logits, c.vocab, d_choice, d_next, status);
     return cudaGetLastError();
 }
 
