@@ -7,10 +7,11 @@
 // residual; then LN_f and the tied vocabulary projection of the last row
 // only.  The four projections are 3xTF32 tcgen05 GEMMs (tc_gemm.cuh) over
 // 128-row x 64-column tiles, split along K over about two thirds of the
-// SMs; a deterministic reduce kernel sums the splits in split order and
-// applies the projection's epilogue.  Every GEMM input is written with its
-// TF32 remainder (x - hi(x)) next to it; the weights' remainders are made
-// once per model.
+// SMs; the splits are summed in split order by the projection's epilogue
+// kernel (QKV + KV-cache rows; GELU), or, for a residual add, by the
+// LayerNorm kernel of the next block input (one row-wise kernel).  Every
+// GEMM input is written with its TF32 remainder (x - hi(x)) next to it; the
+// weights' remainders are made once per model.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -69,20 +70,63 @@ constexpr int kLnThreads = 128;
 
 // Y = LN(X) (mean, then the biased variance of the deviations; eps 1e-5)
 // and its TF32 remainder, one block per row (D <= 1024: 8 values a thread).
-__global__ void __launch_bounds__(kLnThreads) ln_split_kernel(const float* __restrict__ X, const float* __restrict__ g,
+// With part != nullptr the row is first completed as the residual add of a
+// projection: X[i][j] += (sum over splits s = 0, 1, ... of part[s][i][j]) +
+// bias[j], in the split reduce's order, and written back.
+__global__ void __launch_bounds__(kLnThreads) ln_split_kernel(float* __restrict__ X, const float* __restrict__ g,
                                                              const float* __restrict__ b, int D,
-                                                             float* __restrict__ Y, float* __restrict__ Ylo) {
+                                                             float* __restrict__ Y, float* __restrict__ Ylo,
+                                                             const float* __restrict__ part, int splits, int n,
+                                                             const float* __restrict__ bias) {
     __shared__ float red[kLnThreads / 32];
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float* x = X + (size_t)row * D;
+    float* x = X + (size_t)row * D;
     float v[8];
+    if (part) {
+        // split sums in split order; four splits' loads are issued together
+        float y[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = 0.0f;
+        int sp = 0;
+        for (; sp + 4 <= splits; sp += 4) {
+            float a[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int i = tid + kLnThreads * k;
+                    a[u][k] = i < D ? part[((size_t)(sp + u) * n + row) * D + i] : 0.0f;
+                }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) y[k] += a[u][k];
+        }
+        for (; sp < splits; ++sp)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = tid + kLnThreads * k;
+                if (i < D) y[k] += part[((size_t)sp * n + row) * D + i];
+            }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + kLnThreads * k;
+            v[k] = 0.0f;
+            if (i < D) {
+                v[k] = __fadd_rn(x[i], __fadd_rn(y[k], bias[i]));
+                x[i] = v[k];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + kLnThreads * k;
+            v[k] = i < D ? x[i] : 0.0f;
+        }
+    }
     float s = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int i = tid + kLnThreads * k;
-        v[k] = i < D ? x[i] : 0.0f;
-        s += v[k];
-    }
+    for (int k = 0; k < 8; ++k) s += v[k];
     s = warp_sum32(s);
     if (lane == 0) red[warp] = s;
     __syncthreads();
@@ -561,12 +605,20 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
         return cudaGetLastError();
     };
 
+    // LayerNorm of the residual rows into A (+ remainder); with a projection's
+    // partials, the residual add of that projection first (one kernel)
+    auto ln = [&](uint64_t g_off, uint64_t b_off, int splits, uint64_t bias_off) {
+        ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + g_off, P + b_off, D, w->A, w->Alo,
+                                                  splits ? w->part : nullptr, splits, n, P + bias_off);
+        return cudaGetLastError();
+    };
+
     embed_kernel<<<n, 256, 0, st>>>(P, m->wte_off, m->wpe_off, d_tok, D, c.vocab, w->X, status);
     e = cudaGetLastError();
+    if (e == cudaSuccess) e = ln(m->lp[0].ln1_g, m->lp[0].ln1_b, 0, 0);
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
         const LayerParams& lp = m->lp[l];
         int sp = 1;
-        ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + lp.ln1_g, P + lp.ln1_b, D, w->A, w->Alo);
         if ((e = gemm(w->A, w->Alo, D, 3 * D, l, kQKV, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, 3 * D, lp.b_qkv, kRedQKV, w->QKV, nullptr, l)) != cudaSuccess) break;
         const dim3 agrid(H, (n + kAttnRows - 1) / kAttnRows);
@@ -574,12 +626,12 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
         else if (DH == 32) attention_kernel<32><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
         else attention_kernel<16><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
         if ((e = gemm(w->A, w->Alo, D, D, l, kO, &sp)) != cudaSuccess) break;
-        if ((e = reduce(sp, D, lp.b_o, kRedResidual, nullptr, nullptr, l)) != cudaSuccess) break;
-        ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + lp.ln2_g, P + lp.ln2_b, D, w->A, w->Alo);
+        if ((e = ln(lp.ln2_g, lp.ln2_b, sp, lp.b_o)) != cudaSuccess) break;  // residual + LN2
         if ((e = gemm(w->A, w->Alo, D, FF, l, kFC, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, FF, lp.b_fc, kRedGelu, w->U, w->Ulo, l)) != cudaSuccess) break;
         if ((e = gemm(w->U, w->Ulo, FF, D, l, kP, &sp)) != cudaSuccess) break;
-        if ((e = reduce(sp, D, lp.b_p, kRedResidual, nullptr, nullptr, l)) != cudaSuccess) break;
+        if (l + 1 < L) e = ln(m->lp[l + 1].ln1_g, m->lp[l + 1].ln1_b, sp, lp.b_p);  // residual + next LN1
+        else e = reduce(sp, D, lp.b_p, kRedResidual, nullptr, nullptr, l);
     }
     if (e != cudaSuccess) return e;
     const float* lg = P + m->lnf_g;
