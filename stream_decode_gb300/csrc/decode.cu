@@ -75,7 +75,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D, int FF, bool q8, int ma
     s.full = o; o += kSlots * 8;
     s.empty = o; o += kSlots * 8;
     s.xs = o; o = align16(o + D * 4);
-    s.vin = o; o = align16(o + kmax * 4);
+    s.vin = o; o = align16(o + (kmax > kMaxSplits * D ? kmax : kMaxSplits * D) * 4);  // also every split's head outputs
     s.vq = o; o = align16(o + (q8 ? kmax : 0));
     s.vs = o; o = align16(o + (kmax / kGroup) * 4);
     s.red = o; o = align16(o + 64 * 4);
@@ -596,19 +596,6 @@ __device__ __forceinline__ uint64_t own_words(int N, int tid) {
     return m;
 }
 
-// Copies a tagged N-word vector into shared memory once every word carries `tag`.
-template <int MAXC>
-__device__ __forceinline__ bool gather_vec(const uint64_t* src, int N, unsigned tag, float* dst, int tid,
-                                           const StepPlan& P) {
-    constexpr int NT = kConsumerWarps * 32;
-    uint64_t w[MAXC];
-    const bool ok = tagged_wait<MAXC>(w, own_words<MAXC>(N, tid), tag, [&](int k) { return src + tid + NT * k; }, P);
-#pragma unroll
-    for (int k = 0; k < MAXC; ++k)
-        if (tid + NT * k < N) dst[tid + NT * k] = val_of(w[k]);
-    return ok;
-}
-
 // Pair layout of a vector held in registers: thread tid owns the word
 // pairs q = tid + NT*k (k < PP), i.e. elements 2q and 2q + 1, so that each
 // tagged load moves 16 bytes (two words) and a warp's loads are contiguous.
@@ -931,15 +918,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
     // ================================================= consumer warps
     constexpr int NT = kConsumerWarps * 32;
-    constexpr int PD = (D + NT - 1) / NT;      // D-vector words per thread
-    constexpr int PF = (FF + NT - 1) / NT;     // FF-vector words per thread
-    constexpr int P3 = (3 * D + NT - 1) / NT;  // qkv words per thread (trace)
-    constexpr int PV = PF > P3 ? PF : P3;      // words per thread of any gathered vector
-    constexpr int PM = PD * kMaxSplits;        // attention partial words per thread (merge)
     constexpr int PPD = Pairs<D>::PP;          // word pairs per thread of a D-vector
+    constexpr int PPS = Pairs<kMaxSplits * D>::PP;  // ... of every key split's head outputs
+    constexpr int PPQ = Pairs<3 * D>::PP;      // ... of the qkv vector (trace)
     constexpr int PPF = Pairs<FF>::PP;         // word pairs per thread of an FF-vector
-    static_assert(PPF <= 32 && D % 2 == 0 && FF % 2 == 0 && DH % 2 == 0, "pair gathers");
-    static_assert(PM + 2 <= 64 && PV <= 64, "tagged gathers hold at most 64 words per thread");
+    static_assert(PPF <= 32 && PPS <= 32 && D % 2 == 0 && FF % 2 == 0 && DH % 2 == 0, "pair gathers");
     uint32_t gi = 0;  // chunks consumed (same sequence as the producer)
     using KD = std::integral_constant<int, D>;
     using KF = std::integral_constant<int, FF>;
@@ -1522,7 +1505,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                                                                                   : 0.0f;
             bool ok = true;
             // ---- inputs
-            uint64_t ov[PM + 2];  // out-projection: o words of every split, then (max, sum) words
             float xv[2 * PPD];  // LayerNorm phases: this thread's pairs of the residual stream
             if (kind == kPhO && S_eff == 1) {
                 // single-split heads: unit h holds head h's normalised output
@@ -1539,33 +1521,29 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     if (tid + NT * k < D / 2)
                         reinterpret_cast<float2*>(vin)[tid + NT * k] = make_float2(ov2[2 * k], ov2[2 * k + 1]);
             } else if (kind == kPhO) {
-                // One wait for every split's o words of this thread's coordinates
-                // (k < PM) and, for threads below 2 * units, one (max, sum) word
-                // (k = PM, PM + 1), which then goes to stage[2u], stage[2u + 1].
-                const int nmz = 2 * P.H * S_eff;
-                uint64_t want = 0;
+                // Every split's unnormalised outputs, as one vector of
+                // S_eff * D words (word sp * D + idx, head h = idx / DH),
+                // gathered in pairs into vin; the (max, sum) pair of each of
+                // the H * S_eff units into stage[2u], stage[2u + 1].
+                float uv[2 * PPS];
+                ok = ok & gather_pairs<PPS>(
+                              uv, (S_eff * D) / 2, tag - 1u,
+                              [&](int q) {
+                                  const int v = 2 * q, sp = v / D, idx = v - sp * D, h = idx / DH;
+                                  return P.attn_part + (size_t)(h * S_eff + sp) * (DH + 2) + 2 + (idx - h * DH);
+                              },
+                              tid, P);
 #pragma unroll
-                for (int i = 0; i < PD; ++i)
-                    if (tid + NT * i < D)
-                        for (int sp = 0; sp < S_eff; ++sp) want |= 1ull << (i * kMaxSplits + sp);
-#pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    if (tid + NT * k < nmz) want |= 1ull << (PM + k);
-                ok = ok & tagged_wait<PM + 2>(
-                    ov, want, tag - 1u,
-                    [&](int k) {
-                        if (k >= PM) {
-                            const int w = tid + NT * (k - PM);
-                            return P.attn_part + (size_t)(w >> 1) * (DH + 2) + (w & 1);
-                        }
-                        const int idx = tid + NT * (k / kMaxSplits), sp = k % kMaxSplits;
-                        const int h = idx / DH, e = idx - h * DH;
-                        return P.attn_part + (size_t)(h * S_eff + sp) * (DH + 2) + 2 + e;
-                    },
-                    P);
-#pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    if (tid + NT * k < nmz) stage[tid + NT * k] = val_of(ov[PM + k]);
+                for (int k = 0; k < PPS; ++k)
+                    if (tid + NT * k < (S_eff * D) / 2)
+                        reinterpret_cast<float2*>(vin)[tid + NT * k] = make_float2(uv[2 * k], uv[2 * k + 1]);
+                float mz[2];
+                ok = ok & gather_pairs<1>(mz, P.H * S_eff, tag - 1u,
+                                          [&](int q) { return P.attn_part + (size_t)q * (DH + 2); }, tid, P);
+                if (tid < P.H * S_eff) {
+                    stage[2 * tid] = mz[0];
+                    stage[2 * tid + 1] = mz[1];
+                }
             } else if (kind == kPhQKV && l == 0) {
 #pragma unroll
                 for (int k = 0; k < 2 * PPD; ++k) {
@@ -1623,17 +1601,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     ored[tid] = (ms == -INFINITY) ? 0.0f : expf(ms - M) / Z;
                 }
                 consumers_sync();
-#pragma unroll
-                for (int i = 0; i < PD; ++i) {
-                    const int idx = tid + NT * i;
-                    if (idx >= D) continue;
+                // (each element's split words are read and its merged value
+                // written by the same thread)
+                for (int idx = tid; idx < D; idx += NT) {
                     const int h = idx / DH;
                     float O = 0.0f;
-#pragma unroll
-                    for (int sp = 0; sp < kMaxSplits; ++sp) {
-                        if (sp >= S_eff) break;
-                        O = fmaf(ored[h * S_eff + sp], val_of(ov[i * kMaxSplits + sp]), O);
-                    }
+                    for (int sp = 0; sp < S_eff; ++sp) O = fmaf(ored[h * S_eff + sp], vin[sp * D + idx], O);
                     vin[idx] = O;
                 }
             }
@@ -1651,7 +1624,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             if (trace_step) {
                 const int tb = l * trace_layer;
                 if (kind == kPhO) {
-                    const bool okq = gather_vec<PV>(P.qkv, 3 * D, tag - 2u, P.trace + tb + 2 * D, tid, P);
+                    float qv[2 * PPQ];
+                    const bool okq = gather_pairs<PPQ>(qv, (3 * D) / 2, tag - 2u,
+                                                       [&](int q) { return P.qkv + 2 * (size_t)q; }, tid, P);
+#pragma unroll
+                    for (int k = 0; k < PPQ; ++k)
+                        if (tid + NT * k < (3 * D) / 2) {
+                            P.trace[tb + 2 * D + 2 * (tid + NT * k)] = qv[2 * k];
+                            P.trace[tb + 2 * D + 2 * (tid + NT * k) + 1] = qv[2 * k + 1];
+                        }
                     if (!agree(okq)) { alive = false; break; }
                 }
                 const int ox = kind == kPhFC ? 6 * D : (kind == kPhQKV || kind == kPhVocab) ? 0 : -1;
