@@ -118,6 +118,19 @@ def dist_info():
     return ws, rank, local
 
 
+def combine_replicas(ms_local: float, ws: int):
+    """Whole-job figures of N independent replicas: the slowest rank's ms per
+    launch (max over ranks, gloo) and the tokens of all ranks over that time."""
+    ms = ms_local
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_local], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, ws * DECODE / (ms * 1e-3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -383,12 +396,7 @@ def main():
     from stream_decode_gb300 import gpt2 as g
 
     ms, launches, model, sess, first, clocks = measure_decode(g, torch, shape, w, toks, args.quant, args, rank_sync)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * DECODE / (ms * 1e-3)
+    ms, value = combine_replicas(ms, ws)
 
     peak, peak_kind = _peaks()
     launch_bytes = sum(step_bytes(shape, args.quant, p) for p in range(PROMPT, PROMPT + DECODE))
