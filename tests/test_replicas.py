@@ -34,7 +34,7 @@ def _rank(rank, ws, port, ms_by_rank, out):
 def test_two_rank_replicas_take_the_slowest_rank():
     ws, port = 2, _free_port()
     ms_by_rank = [17.5, 19.25]
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank, args=(ws, port, ms_by_rank, out), nprocs=ws, join=True)
         res = dict(out)
