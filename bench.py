@@ -53,9 +53,9 @@ def step_bytes(shape, quant: str, p: int) -> int:
     0..p-1, this position's KV write and the logits write."""
     d, F, L, V = shape.d_model, shape.d_ff, shape.n_layer, shape.vocab
     params = L * (2 * d + 3 * d + d + 2 * d + F + d) + 2 * d + d  # LN, biases, final LN, one wpe row
-    if quant == "f32":
+    if quant in ("f32", "f16"):
         mats = L * (d * 3 * d + d * d + d * F + F * d) + V * d
-        weights = 4 * (mats + params)
+        weights = (4 if quant == "f32" else 2) * mats + 4 * params
     else:
         rb = lambda K: K + (K // 64) * 4
         mats = L * (3 * d * rb(d) + d * rb(d) + F * rb(d) + d * rb(F)) + V * rb(d)
@@ -158,7 +158,7 @@ def reference_arm(args, shape, w, toks):
     ws, rank, _ = dist_info()
     if rank != 0:
         return
-    quant = 1 if args.quant == "int8" else 0
+    quant = {"f32": 0, "int8": 1, "f16": 2}[args.quant]
     per_step = 2
     from oracle import Oracle
     om = Oracle().model(shape, w, quant=quant)
@@ -182,7 +182,7 @@ def reference_arm(args, shape, w, toks):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if quant == 0 else "int8", "data": "synthetic",
+            "dtype": args.quant, "data": "synthetic",
             "config": workload_config(args),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -193,7 +193,7 @@ def workload_config(args):
     return {"workload": f"gpt2-124m {args.quant} cachedStep greedy decode, 16-token prompt then {DECODE} steps "
                         f"(positions 16..{15 + DECODE}), one persistent launch per {DECODE} steps",
             "tokens_per_step": DECODE, "positions": f"16..{15 + DECODE}", "model_shape": "12x768, 12 heads, ffn 3072, "
-            "vocab 50257", "l2": "inputs larger than L2 (weights 495 MB f32 / 132 MB int8 per token)",
+            "vocab 50257", "l2": "inputs larger than L2 (weights 495 MB f32 / 249 MB f16 / 132 MB int8 per token)",
             "parallelism": f"replicas x{args.gpus}"}
 
 
@@ -255,7 +255,7 @@ def prefill_rate(g, torch, shape, w, n: int = 128, reps: int = 10):
 
 def measure_decode(g, torch, shape, w, toks, quant: str, args, rank_sync):
     """Returns (ms per bench step, launches, session) after W warm-ups and K timed steps."""
-    q = g.INT8_G64 if quant == "int8" else g.F32
+    q = {"f32": g.F32, "int8": g.INT8_G64, "f16": g.F16}[quant]
     model = g.Model(shape, w, quant=q)
     sess = g.Session(model)
     V = shape.vocab
@@ -360,8 +360,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--quant", choices=["f32", "int8"], default="f32")
-    ap.add_argument("--no-extra", action="store_true", help="skip the int8 and long-context extras")
+    ap.add_argument("--quant", choices=["f32", "int8", "f16"], default="f32")
+    ap.add_argument("--no-extra", action="store_true", help="skip the int8, binary16, long-context and prefill extras")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the 128-token prefill leg (3 warm-up calls, --steps timed calls); prints its JSON")
     ap.add_argument("--decode-steps", type=int, default=112,
@@ -417,13 +417,21 @@ def main():
                                     "frac_of_peak": b8 / (ms8 * 1e-3) / 1e9 / peak}
             s8.close()
             m8.close()
+            ms16, _, m16, s16, _, _ = measure_decode(g, torch, shape, w, toks, "f16", args, lambda: None)
+            b16 = sum(step_bytes(shape, "f16", p) for p in range(PROMPT, PROMPT + DECODE))
+            extra["f16_decode"] = {"tokens_per_s": DECODE / (ms16 * 1e-3), "ms_per_step": ms16,
+                                   "GB_per_s": b16 / (ms16 * 1e-3) / 1e9,
+                                   "frac_of_peak": b16 / (ms16 * 1e-3) / 1e9 / peak,
+                                   "weights": "block matrices and tied embedding in binary16, rest binary32"}
+            s16.close()
+            m16.close()
         extra["long_context_f32"] = long_context(g, torch, w)
         extra["prefill_f32"] = prefill_rate(g, torch, shape, w)
 
     cpu = None
     if rank == 0:
         n_dec = 16
-        rate, dt = oracle_decode_rate(shape, w, toks, 1 if args.quant == "int8" else 0, n_dec)
+        rate, dt = oracle_decode_rate(shape, w, toks, {"f32": 0, "int8": 1, "f16": 2}[args.quant], n_dec)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n_dec} greedy decode steps at positions 16..31 after an untimed 16-token prompt "
                          f"({dt:.1f} s of single-threaded C on {cpu_cores()} available host cores)"}

@@ -58,8 +58,11 @@ typedef enum gpt2_status {
 } gpt2_status;
 
 typedef enum gpt2_quant {
-    GPT2_F32 = 0,     /* binary32 weights and arithmetic */
-    GPT2_INT8_G64 = 1 /* int8 weights and projection inputs, scales per 64 inputs, int32 sums */
+    GPT2_F32 = 0,      /* binary32 weights and arithmetic */
+    GPT2_INT8_G64 = 1, /* int8 weights and projection inputs, scales per 64 inputs, int32 sums */
+    GPT2_F16 = 2       /* the 48 block matrices and the tied embedding stored as binary16 (rounded to
+                          nearest-even at load), widened to binary32 before every multiply-add;
+                          everything else binary32 (the gpt2.s page's half-precision weight option) */
 } gpt2_quant;
 
 /* In a device token array: use the previous step's greedy choice. */
@@ -110,7 +113,8 @@ gpt2_status gpt2_cached_step(const gpt2_config* cfg, const void* weights_host, s
 
 /* Uploads the packed checkpoint and builds the device weight streams
  * (K-major copies of the block matrices; for GPT2_INT8_G64 the int8 copies
- * of the 48 block matrices and the tied wte with their group scales).
+ * of the 48 block matrices and the tied wte with their group scales; for
+ * GPT2_F16 binary16 copies of both).
  * grid_ctas: CTAs of the persistent step kernel, 0 = one per SM.
  * Synchronous.  Checks weights_len, the shape and the quantization. */
 gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights_host, size_t weights_len, int quant,
@@ -257,7 +261,8 @@ gpt2_status gpt2_cached_step_noalloc(const gpt2_model* model, float* d_cache, ui
  * matrix (rows spread over warps for block matrices, one warp per ring chunk
  * for the vocabulary): for int8 models the per-64 activation quantizer, the
  * dp4a group sums and the fixed-order rescale; for binary32 models the float4
- * dot products.  Enqueued on `stream`. */
+ * dot products; for binary16 models the same on widened binary16 weights.
+ * Enqueued on `stream`. */
 gpt2_status gpt2_debug_project(gpt2_model* model, int index, const float* d_x, float* d_y, void* stream);
 
 /* Test hook: the step kernel's greedy-choice routine over d_values[n]:

@@ -191,12 +191,45 @@ class Oracle:
         return OracleModel(self, shape, weights, quant)
 
 
+def round_f16(shape, weights) -> np.ndarray:
+    """The half-precision weight option (gpt2.s page, half-precision weight
+    paragraph, read as: the weight matrices are stored in binary16 and widened
+    to binary32 for the arithmetic): a copy of the packed checkpoint whose
+    tied embedding and 48 block matrices are rounded to the nearest binary16
+    value (ties to even, numpy's IEEE conversion); wpe, the LayerNorm
+    parameters and the biases keep their binary32 values.  The model computed
+    on this checkpoint in binary32 is the binary16-weight model."""
+    d, f, V = shape.d_model, shape.d_ff, shape.vocab
+    w = np.array(weights, dtype=np.float32, copy=True)
+
+    def rnd(o, n):
+        w[o:o + n] = w[o:o + n].astype(np.float16).astype(np.float32)
+
+    rnd(0, V * d)  # wte
+    o = V * d + shape.n_pos * d
+    for _ in range(shape.n_layer):
+        o += 2 * d  # ln_1
+        rnd(o, d * 3 * d)
+        o += d * 3 * d + 3 * d
+        rnd(o, d * d)
+        o += d * d + d + 2 * d  # w_o, b_o, ln_2
+        rnd(o, d * f)
+        o += d * f + f
+        rnd(o, f * d)
+        o += f * d + d
+    assert o + 2 * d == w.size
+    return w
+
+
 class OracleModel:
-    """A parsed (and for quant=1, int8-quantized) oracle model."""
+    """A parsed oracle model: quant=0 binary32, quant=1 int8-quantized,
+    quant=2 binary16 weights (binary32 arithmetic on round_f16's checkpoint)."""
 
     def __init__(self, o: Oracle, shape, weights, quant: int):
         self.o, self.shape, self.quant = o, shape, quant
         w = np.ascontiguousarray(weights)
+        if quant == 2:
+            w, quant = round_f16(shape, w), 0
         st = C.c_int()
         self._cfg = _cfg(shape)
         self.h = o.lib.ref_model_create(C.byref(self._cfg), w.ctypes.data, w.nbytes, quant, C.byref(st))

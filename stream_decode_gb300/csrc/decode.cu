@@ -103,7 +103,7 @@ struct Geo {
     int nchunks;
 };
 
-__device__ __forceinline__ Geo phase_geo(const StepPlan& P, int ph, int cta, bool q8) {
+__device__ __forceinline__ Geo phase_geo(const StepPlan& P, int ph, int cta, int wf) {
     int N, K;
     const uint8_t* mat;
     if (ph == 4 * P.L) {
@@ -115,7 +115,7 @@ __device__ __forceinline__ Geo phase_geo(const StepPlan& P, int ph, int cta, boo
         mat = P.wstream + (uint64_t)l * P.layer_bytes + P.mat_off[m];
     }
     Geo g;
-    g.rb = row_bytes(K, q8);
+    g.rb = row_bytes(K, wf);
     g.r0 = (int)(((long long)cta * N) / P.G);
     int r1 = (int)(((long long)(cta + 1) * N) / P.G);
     g.nrows = r1 - g.r0;
@@ -300,16 +300,17 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[N], int lane) {
 // each weight byte is read from shared memory once and every thread works.
 // Longer shares (the vocabulary) stream: one warp per chunk, chunks
 // released as they are used.
-template <int K, bool Q8>
+template <int K, int WF>
 struct Rows {
-    static constexpr int RB = row_bytes(K, Q8);                               // bytes per row
+    static constexpr int RB = row_bytes(K, WF);                               // bytes per row
     static constexpr int RPC0 = kSlotBytes / RB;
     static constexpr int RPC = RPC0 > kMaxChunkRows ? kMaxChunkRows : RPC0;  // rows per chunk
     static constexpr int NG = K / kGroup;                                     // int8 groups per row
 };
 
 __host__ __device__ constexpr bool share_spread(int nchunks, int nrows, int K, bool q8) {
-    return nchunks <= kSlots / 2 && nrows <= kSpreadRows && (!q8 || nrows * (K / kGroup) <= kCoopTaskFloats);
+    return nchunks <= kSlots / 2 && nrows <= kSpreadRows && (!q8 || nrows * (K / kGroup) <= kCoopTaskFloats) &&
+           (q8 || K / 4 <= kConsumerWarps * 32 || nrows <= 8);  // rows longer than the CTA: groups of 4 + 4
 }
 
 // Column layout of a spread binary32 share: thread t takes the float4
@@ -321,9 +322,9 @@ struct Pre {
     static constexpr int NC = (NV + NT - 1) / NT;    // columns per thread
 };
 
-template <int K>
+template <int K, int WF = kWF32>
 __device__ __forceinline__ uint32_t share_row_off(uint32_t c0, int r) {
-    using R = Rows<K, false>;
+    using R = Rows<K, WF>;
     return ((c0 + (uint32_t)(r / R::RPC)) % kSlots) * (uint32_t)kSlotBytes + (uint32_t)((r % R::RPC) * R::RB);
 }
 
@@ -334,7 +335,20 @@ __device__ __forceinline__ uint32_t share_row_off(uint32_t c0, int r) {
 // rows held in registers across the input wait, or every load of a row
 // group issued before its multiply-adds -- measured slower: the step kernel
 // is at its register limit and the extra live values spill.)
-template <int K, int NR, int R0>
+// Four consecutive weights of a binary32 or binary16 row, as binary32.
+template <int WF>
+__device__ __forceinline__ float4 weight4(const uint8_t* row, int col) {
+    if constexpr (WF == kWF16) {
+        const uint2 h = *reinterpret_cast<const uint2*>(row + 8u * (uint32_t)col);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return *reinterpret_cast<const float4*>(row + 16u * (uint32_t)col);
+    }
+}
+
+template <int K, int NR, int R0, int WF = kWF32>
 __device__ __forceinline__ void coop_reg_part(const uint8_t* ring, uint32_t c0, int nrows,
                                               const float (&x)[4 * Pre<K>::NC], float* part, int tid) {
     using Q = Pre<K>;
@@ -356,7 +370,7 @@ __device__ __forceinline__ void coop_reg_part(const uint8_t* ring, uint32_t c0, 
             for (int i = 0; i < NR; ++i) {
                 const int r = R0 + i;
                 if (r < nrows) {
-                    const float4 wv = *reinterpret_cast<const float4*>(ring + share_row_off<K>(c0, r) + 16u * (uint32_t)col);
+                    const float4 wv = weight4<WF>(ring + share_row_off<K, WF>(c0, r), col);
                     acc[i] = fmaf(xv.x, wv.x, acc[i]);
                     acc[i] = fmaf(xv.y, wv.y, acc[i]);
                     acc[i] = fmaf(xv.z, wv.z, acc[i]);
@@ -373,29 +387,28 @@ __device__ __forceinline__ void coop_reg_part(const uint8_t* ring, uint32_t c0, 
 // layout, registers), in power-of-two row groups: the warps' partials of
 // every row to part; the caller's barrier then lets the row's thread sum
 // them in warp order.
-template <int K>
+template <int K, int WF = kWF32>
 __device__ __forceinline__ void coop_reg(const uint8_t* ring, uint32_t c0, int nrows, const float (&x)[4 * Pre<K>::NC],
                                          float* part, int tid) {
-    // a spread share has at most kSlots / 2 chunks of RPC rows
-    constexpr int MAXR = (kSlots / 2) * Rows<K, false>::RPC;
-    if constexpr (MAXR > 8) {
+    if constexpr (Pre<K>::NC == 1) {
+        // rows of at most the CTA's width: groups of 16, the tail in 8
         if (nrows > 16) {
-            coop_reg_part<K, 16, 0>(ring, c0, nrows, x, part, tid);
-            if (nrows > 24) coop_reg_part<K, 16, 16>(ring, c0, nrows, x, part, tid);
-            else coop_reg_part<K, 8, 16>(ring, c0, nrows, x, part, tid);
+            coop_reg_part<K, 16, 0, WF>(ring, c0, nrows, x, part, tid);
+            if (nrows > 24) coop_reg_part<K, 16, 16, WF>(ring, c0, nrows, x, part, tid);
+            else coop_reg_part<K, 8, 16, WF>(ring, c0, nrows, x, part, tid);
         } else if (nrows > 8) {
-            coop_reg_part<K, 16, 0>(ring, c0, nrows, x, part, tid);
+            coop_reg_part<K, 16, 0, WF>(ring, c0, nrows, x, part, tid);
         } else {
-            coop_reg_part<K, 8, 0>(ring, c0, nrows, x, part, tid);
+            coop_reg_part<K, 8, 0, WF>(ring, c0, nrows, x, part, tid);
         }
     } else {
-        // long rows (few per share): groups of 4 and 2 waste fewer loads
+        // long rows (at most 8 per spread share): groups of 4 and 2 waste fewer loads
         if (nrows > 4) {
-            coop_reg_part<K, 4, 0>(ring, c0, nrows, x, part, tid);
-            if (nrows > 6) coop_reg_part<K, 4, 4>(ring, c0, nrows, x, part, tid);
-            else coop_reg_part<K, 2, 4>(ring, c0, nrows, x, part, tid);
+            coop_reg_part<K, 4, 0, WF>(ring, c0, nrows, x, part, tid);
+            if (nrows > 6) coop_reg_part<K, 4, 4, WF>(ring, c0, nrows, x, part, tid);
+            else coop_reg_part<K, 2, 4, WF>(ring, c0, nrows, x, part, tid);
         } else {
-            coop_reg_part<K, 4, 0>(ring, c0, nrows, x, part, tid);
+            coop_reg_part<K, 4, 0, WF>(ring, c0, nrows, x, part, tid);
         }
     }
 }
@@ -499,15 +512,14 @@ __host__ __device__ constexpr int dot_rows() {
     return !Q8 ? 4 : ((kWarpScratch / (K / kGroup)) < 32 ? (kWarpScratch / (K / kGroup)) : 32);
 }
 
-// binary32, streaming: m <= 4 consecutive rows at w against x[0..K); lane
+// binary32 or binary16 weights, streaming: m <= 4 consecutive rows at w against x[0..K); lane
 // i < m returns row i's total.  Lanes stride float4 columns; one butterfly
 // transpose per call.
-template <int K>
+template <int K, int WF = kWF32>
 __device__ __forceinline__ float dot_f32(const uint8_t* w, int m, const float* x, int lane) {
-    using R = Rows<K, false>;
-    constexpr int NV = K / 4, T = (NV + 31) / 32, S4 = R::RB / 16;
+    using R = Rows<K, WF>;
+    constexpr int NV = K / 4, T = (NV + 31) / 32;
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    const float4* w4 = reinterpret_cast<const float4*>(w);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 2
     for (int t = 0; t < T; ++t) {
@@ -517,7 +529,7 @@ __device__ __forceinline__ float dot_f32(const uint8_t* w, int m, const float* x
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 if (i < m) {
-                    const float4 wv = w4[i * S4 + idx];
+                    const float4 wv = weight4<WF>(w + (size_t)i * R::RB, idx);
                     acc[i] = fmaf(xv.x, wv.x, acc[i]);
                     acc[i] = fmaf(xv.y, wv.y, acc[i]);
                     acc[i] = fmaf(xv.z, wv.z, acc[i]);
@@ -769,8 +781,9 @@ constexpr int kStamps = 8;
 // merge, quantizer, dot products, epilogue, attention) exists once in the
 // binary: a layer executes far more code than an SM's instruction cache
 // holds when each phase carries inlined copies of its own.
-template <int D, int FF, int DH, bool Q8>
+template <int D, int FF, int DH, int WQ>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepPlan plan) {
+    constexpr bool Q8 = WQ == kWQ8;
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout lay = smem_layout(D, FF, Q8, plan.max_pos);
     // Every field of the plan is read from a shared-memory copy: kernel
@@ -818,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         s_fail[0] = 0;
         s_fail[1] = 0;
         for (int m = 0; m < 5; ++m) {
-            const Geo g0 = phase_geo(P, m == kVocab ? 4 * L : m, cta, Q8);
+            const Geo g0 = phase_geo(P, m == kVocab ? 4 * L : m, cta, WQ);
             geot[m] = GeoRow{g0.r0, g0.nrows, g0.rb, g0.rpc, g0.nchunks, 0, 0, 0};
         }
         fence_mbar_init();
@@ -986,7 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     auto run_gemv = [&](auto kk, int kind, const Geo& g, unsigned tag, uint64_t boff, float* kv_row, float* lg,
                         int* release) -> bool {
         constexpr int KK = decltype(kk)::value;
-        using R = Rows<KK, Q8>;
+        using R = Rows<KK, WQ>;
         auto epilogue = [&](int j, float y) {
             if (kind == kPhVocab) {
                 if (lg) lg[j] = y;
@@ -1024,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                         if constexpr (Q8)
                             y = dot_q8<KK>(w + (size_t)q * R::RB, m, vq, vs, rsc + warp * kWarpScratch, lane);
                         else
-                            y = dot_f32<KK>(w + (size_t)q * R::RB, m, vin, lane);
+                            y = dot_f32<KK, WQ>(w + (size_t)q * R::RB, m, vin, lane);
                         if (lane < m) epilogue(g.r0 + k * R::RPC + q + lane, y);
                     }
                     __syncwarp();
@@ -1089,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             load_quads<KK>(vin, x, tid);
         } else if (kind == kPhQKV && l == 0) {
             // token + position embedding (int8 models: the tied embedding's
-            // int8 row times its group scale)
+            // int8 row times its group scale; binary16 models: its binary16 row)
             const float4* te = reinterpret_cast<const float4*>(P.packed + P.wte_off + (uint64_t)tok * D);
             const float4* pe = reinterpret_cast<const float4*>(P.packed + P.wpe_off + (uint64_t)p * D);
 #pragma unroll
@@ -1098,11 +1111,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
                 if (col < Q::NV) {
                     if constexpr (Q8) {
-                        const uint8_t* row = P.vocab + (uint64_t)tok * row_bytes(D, true);
+                        const uint8_t* row = P.vocab + (uint64_t)tok * row_bytes(D, kWQ8);
                         const char4 qv = reinterpret_cast<const char4*>(row)[col];
                         const float sv = reinterpret_cast<const float*>(row + D)[(4 * col) / kGroup];
                         a = make_float4(__fmul_rn((float)qv.x, sv), __fmul_rn((float)qv.y, sv),
                                         __fmul_rn((float)qv.z, sv), __fmul_rn((float)qv.w, sv));
+                    } else if constexpr (WQ == kWF16) {
+                        a = weight4<kWF16>(P.vocab + (uint64_t)tok * row_bytes(D, kWF16), col);
                     } else {
                         a = __ldg(te + col);
                     }
@@ -1150,7 +1165,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             }
         }
         cstamp(4);
-        if constexpr (!Q8) coop_reg<KK>(ring, gi, g.nrows, x, part, tid);
+        if constexpr (!Q8) coop_reg<KK, WQ>(ring, gi, g.nrows, x, part, tid);
         if (kLnWidth && has_ln) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -1552,10 +1567,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     if (i < D) {
                         const float pe = __ldg(P.packed + P.wpe_off + (uint64_t)p * D + i);
                         if constexpr (Q8) {
-                            const uint8_t* row = P.vocab + (uint64_t)tok * row_bytes(D, true);
+                            const uint8_t* row = P.vocab + (uint64_t)tok * row_bytes(D, kWQ8);
                             const float qv = (float)reinterpret_cast<const int8_t*>(row)[i];
                             const float sv = reinterpret_cast<const float*>(row + D)[i / kGroup];
                             xv[k] = __fadd_rn(__fmul_rn(qv, sv), pe);
+                        } else if constexpr (WQ == kWF16) {
+                            const __half* row = reinterpret_cast<const __half*>(P.vocab) + (uint64_t)tok * D;
+                            xv[k] = __fadd_rn(__half2float(row[i]), pe);
                         } else {
                             xv[k] = __fadd_rn(__ldg(P.packed + P.wte_off + (uint64_t)tok * D + i), pe);
                         }
@@ -1699,12 +1717,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 // one phase share (a spread share computed by the whole block, or a long
 // share streamed one warp per chunk in two rounds), then the epilogue's bias
 // add.  Each block copies its share of rows into a ring-shaped shared buffer.
-template <int K, bool Q8>
+template <int K, int WQ>
 struct HookGeo {
-    static constexpr int RB = row_bytes(K, Q8);
+    static constexpr bool Q8 = WQ == kWQ8;
+    static constexpr int RB = row_bytes(K, WQ);
     static constexpr int RPC0 = kSlotBytes / RB;
     static constexpr int RPC = RPC0 > kMaxChunkRows ? kMaxChunkRows : RPC0;  // rows per chunk
-    static constexpr int SPREAD0 = (kSlots / 2) * RPC < kSpreadRows ? (kSlots / 2) * RPC : kSpreadRows;
+    static constexpr int SPREADR = (kSlots / 2) * RPC < kSpreadRows ? (kSlots / 2) * RPC : kSpreadRows;
+    // rows longer than the CTA are spread at most 8 to a share
+    static constexpr int SPREAD0 = (!Q8 && K / 4 > kConsumerWarps * 32 && SPREADR > 8) ? 8 : SPREADR;
     static constexpr int SPREAD1 = Q8 ? kCoopTaskFloats / (K / kGroup) : SPREAD0;
     static constexpr int ROWS_SPREAD = SPREAD0 < SPREAD1 ? SPREAD0 : SPREAD1;  // the largest spread share
     static constexpr int CHUNKS_STREAM = 2 * kConsumerWarps;                    // two rounds of chunks
@@ -1715,12 +1736,13 @@ struct HookGeo {
     static_assert(!share_spread(CHUNKS_STREAM, CHUNKS_STREAM * RPC, K, Q8), "hook streamed share streams");
 };
 
-template <int K, bool Q8>
+template <int K, int WQ>
 __global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint8_t* __restrict__ rows, int N,
                                                                       const float* __restrict__ x,
                                                                       const float* __restrict__ bias,
                                                                       float* __restrict__ y, int stream) {
-    using H = HookGeo<K, Q8>;
+    using H = HookGeo<K, WQ>;
+    constexpr bool Q8 = H::Q8;
     extern __shared__ __align__(128) uint8_t sm[];
     uint8_t* ring = sm;
     float* vin = reinterpret_cast<float*>(sm + H::SLOTS * kSlotBytes);
@@ -1749,7 +1771,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint
         } else {
             float xq[4 * Pre<K>::NC];
             load_quads<K>(vin, xq, tid);
-            coop_reg<K>(ring, 0u, wn, xq, scratch, tid);
+            coop_reg<K, WQ>(ring, 0u, wn, xq, scratch, tid);
             __syncthreads();
             v = tid < wn ? sum_warp_parts(scratch, tid) : 0.0f;
         }
@@ -1765,7 +1787,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint
             const int m = min(MR, n - q);
             float v;
             if constexpr (Q8) v = dot_q8<K>(w + (size_t)q * H::RB, m, vq, vs, scratch + warp * kWarpScratch, lane);
-            else v = dot_f32<K>(w + (size_t)q * H::RB, m, vin, lane);
+            else v = dot_f32<K, WQ>(w + (size_t)q * H::RB, m, vin, lane);
             if (lane < m) out(w0 + k * H::RPC + q + lane, v);
         }
     }
@@ -1793,24 +1815,25 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) argmax_kernel(const float
     }
 }
 
-template <int K, bool Q8>
+template <int K, int WQ>
 static cudaError_t project_t(const uint8_t* rows, int N, const float* x, const float* bias, float* y, int stream,
                              cudaStream_t st) {
-    using H = HookGeo<K, Q8>;
+    using H = HookGeo<K, WQ>;
     const int per_block = stream ? H::CHUNKS_STREAM * H::RPC : H::ROWS_SPREAD;
-    cudaError_t e = cudaFuncSetAttribute(project_kernel<K, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)H::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(project_kernel<K, WQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)H::SMEM);
     if (e != cudaSuccess) return e;
-    project_kernel<K, Q8><<<(N + per_block - 1) / per_block, kConsumerWarps * 32, H::SMEM, st>>>(rows, N, x, bias, y,
+    project_kernel<K, WQ><<<(N + per_block - 1) / per_block, kConsumerWarps * 32, H::SMEM, st>>>(rows, N, x, bias, y,
                                                                                                stream);
     return cudaGetLastError();
 }
 
-cudaError_t launch_project(const uint8_t* rows, int K, int N, bool q8, const float* x, const float* bias, float* y,
+cudaError_t launch_project(const uint8_t* rows, int K, int N, int wq, const float* x, const float* bias, float* y,
                            int stream, cudaStream_t st) {
 #define GPT2_PROJ(KK)                                                                                        \
     if (K == KK)                                                                                             \
-        return q8 ? project_t<KK, true>(rows, N, x, bias, y, stream, st)                                    \
-                  : project_t<KK, false>(rows, N, x, bias, y, stream, st);
+        return wq == kWQ8    ? project_t<KK, kWQ8>(rows, N, x, bias, y, stream, st)                          \
+               : wq == kWF16 ? project_t<KK, kWF16>(rows, N, x, bias, y, stream, st)                         \
+                             : project_t<KK, kWF32>(rows, N, x, bias, y, stream, st);
     GPT2_PROJ(64) GPT2_PROJ(192) GPT2_PROJ(256) GPT2_PROJ(384) GPT2_PROJ(768) GPT2_PROJ(3072)
 #undef GPT2_PROJ
     return cudaErrorInvalidValue;
@@ -1822,12 +1845,13 @@ cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfin
 }
 
 // ------------------------------------------------------------ launcher
-template <int D, int FF, int DH, bool Q8>
+template <int D, int FF, int DH, int WQ>
 static cudaError_t launch_t(const StepPlan& P, cudaStream_t stream) {
-    // binary32 fast phases read the LayerNorm folds of every layer
+    constexpr bool Q8 = WQ == kWQ8;
+    // binary32 and binary16 fast phases read the LayerNorm folds of every layer
     if (!Q8 && P.fold == nullptr) return cudaErrorInvalidValue;
     const SmemLayout lay = smem_layout(D, FF, Q8, P.max_pos);
-    auto kern = step_kernel<D, FF, DH, Q8>;
+    auto kern = step_kernel<D, FF, DH, WQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1843,10 +1867,10 @@ static cudaError_t launch_t(const StepPlan& P, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
-template <int D, int FF, int DH, bool Q8>
+template <int D, int FF, int DH, int WQ>
 static int max_ctas_t(int max_pos) {
-    const SmemLayout lay = smem_layout(D, FF, Q8, max_pos);
-    auto kern = step_kernel<D, FF, DH, Q8>;
+    const SmemLayout lay = smem_layout(D, FF, WQ == kWQ8, max_pos);
+    auto kern = step_kernel<D, FF, DH, WQ>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total) != cudaSuccess)
         return 0;
     int per_sm = 0;
@@ -1862,23 +1886,22 @@ bool step_shape_supported(int D, int FF, int DH) {
            (D == 64 && FF == 256 && DH == 16);
 }
 
-uint32_t step_smem_bytes(int D, int FF, bool q8, int max_pos) { return smem_layout(D, FF, q8, max_pos).total; }
+#define GPT2_DISPATCH_WQ(FN, d, ff, dh, ...)                     \
+    return wq == kWQ8 ? FN<d, ff, dh, kWQ8>(__VA_ARGS__)         \
+           : wq == kWF16 ? FN<d, ff, dh, kWF16>(__VA_ARGS__)     \
+                         : FN<d, ff, dh, kWF32>(__VA_ARGS__);
+#define GPT2_DISPATCH(FN, ...)                                                       \
+    if (D == 768 && FF == 3072 && DH == 64) GPT2_DISPATCH_WQ(FN, 768, 3072, 64, __VA_ARGS__) \
+    if (D == 192 && FF == 384 && DH == 64) GPT2_DISPATCH_WQ(FN, 192, 384, 64, __VA_ARGS__)   \
+    if (D == 64 && FF == 256 && DH == 16) GPT2_DISPATCH_WQ(FN, 64, 256, 16, __VA_ARGS__)
 
-#define GPT2_DISPATCH(FN, ...)                                                                  \
-    if (D == 768 && FF == 3072 && DH == 64)                                                      \
-        return q8 ? FN<768, 3072, 64, true>(__VA_ARGS__) : FN<768, 3072, 64, false>(__VA_ARGS__); \
-    if (D == 192 && FF == 384 && DH == 64)                                                       \
-        return q8 ? FN<192, 384, 64, true>(__VA_ARGS__) : FN<192, 384, 64, false>(__VA_ARGS__);   \
-    if (D == 64 && FF == 256 && DH == 16)                                                        \
-        return q8 ? FN<64, 256, 16, true>(__VA_ARGS__) : FN<64, 256, 16, false>(__VA_ARGS__);
-
-cudaError_t launch_step(const StepPlan& P, bool q8, cudaStream_t stream) {
+cudaError_t launch_step(const StepPlan& P, int wq, cudaStream_t stream) {
     const int D = P.D, FF = P.FF, DH = P.D / P.H;
     GPT2_DISPATCH(launch_t, P, stream)
     return cudaErrorInvalidValue;
 }
 
-int step_max_ctas(int D, int FF, int DH, bool q8, int max_pos) {
+int step_max_ctas(int D, int FF, int DH, int wq, int max_pos) {
     GPT2_DISPATCH(max_ctas_t, max_pos)
     return 0;
 }

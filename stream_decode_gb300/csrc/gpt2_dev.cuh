@@ -4,6 +4,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace gpt2 {
@@ -137,9 +138,14 @@ struct StepPlan {
 // d_qkv[3D], c_fc[FF], d_fc[FF].
 __host__ __device__ constexpr uint64_t fold_layer_words(int D, int FF) { return 2ull * (3ull * D + (uint64_t)FF); }
 
+// Weight formats of the device streams: binary32; int8 group-64 codes with
+// their binary32 group scales; binary16 (weights rounded to nearest-even
+// half precision, widened to binary32 before every multiply-add).
+enum WeightFormat : int { kWF32 = 0, kWQ8 = 1, kWF16 = 2 };
+
 // Bytes of one K-major weight row in the device stream.
-__host__ __device__ constexpr int row_bytes(int K, bool q8) {
-    return q8 ? K + ((K / kGroup) * 4 + 15) / 16 * 16 : K * 4;
+__host__ __device__ constexpr int row_bytes(int K, int wf) {
+    return wf == kWQ8 ? K + ((K / kGroup) * 4 + 15) / 16 * 16 : (wf == kWF16 ? K * 2 : K * 4);
 }
 
 // --------------------------------------------------------------- PTX helpers

@@ -12,7 +12,7 @@ struct gpt2_model {
     int G;
     float* d_packed;
     uint8_t* d_wstream;
-    uint8_t* d_vocab_q8;
+    uint8_t* d_vocab;  // int8 and binary16 models: the tied embedding's rows in the model's weight format
     uint64_t layer_bytes;
     uint64_t mat_off[4];
     uint64_t wte_off, wpe_off, lnf_g, lnf_b;

@@ -3,7 +3,9 @@
 // The packed checkpoint stores block matrices [in][out] (gpt2.s page,
 // weight-layout paragraph).  The step kernel wants each output's weights
 // contiguous (K-major rows) so that a CTA's share of outputs is one byte
-// range.  binary32 models get a transposed copy; int8 models get, per output
+// range.  binary32 models get a transposed copy, binary16 models a
+// transposed copy rounded to nearest-even half precision (and a binary16
+// copy of the tied embedding); int8 models get, per output
 // row, K int8 codes followed by the K/64 group scales (padded to 16 bytes),
 // quantized with the rule of the quantized GPT-2 abstract: scale =
 // maxabs/127 over 64 consecutive inputs of the row, nearest-even, saturate.
@@ -26,6 +28,27 @@ __global__ void transpose_kernel(const float* __restrict__ src, uint8_t* __restr
         const int n = n0 + dy, k = k0 + threadIdx.x;
         if (n < N && k < K) reinterpret_cast<float*>(dst + (size_t)n * rb)[k] = tile[threadIdx.x][dy];
     }
+}
+
+// The same into rows of K binary16 values (nearest-even).
+__global__ void transpose_f16_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int K, int N, int rb) {
+    __shared__ float tile[32][33];
+    const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+        const int k = k0 + dy, n = n0 + threadIdx.x;
+        tile[dy][threadIdx.x] = (k < K && n < N) ? src[(size_t)k * N + n] : 0.0f;
+    }
+    __syncthreads();
+    for (int dy = threadIdx.y; dy < 32; dy += blockDim.y) {
+        const int n = n0 + dy, k = k0 + threadIdx.x;
+        if (n < N && k < K) reinterpret_cast<__half*>(dst + (size_t)n * rb)[k] = __float2half_rn(tile[threadIdx.x][dy]);
+    }
+}
+
+// Rows already K-major (the tied wte [N][K]) to binary16 rows.
+__global__ void to_f16_kernel(const float* __restrict__ src, __half* __restrict__ dst, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = __float2half_rn(src[i]);
 }
 
 // One thread per (output n, group g): weights W[64g .. 64g+63][n] of a [K][N] matrix.
@@ -64,19 +87,22 @@ __global__ void quantize_out_in_kernel(const float* __restrict__ src, uint8_t* _
     reinterpret_cast<float*>(dst + (size_t)n * rb + K)[g] = s;
 }
 
-// The LayerNorm folds of one K-major binary32 matrix (rows of K floats):
+// The LayerNorm folds of one K-major matrix (rows of K binary32 or binary16
+// values, the latter the model's weights as stored):
 // c_j = sum_i W_ji g_i and d_j = bias_j + sum_i W_ji b_i, one warp per
 // row, summed in binary64 and rounded once.
+template <typename T>
 __global__ void fold_kernel(const uint8_t* __restrict__ rows, int K, int N, const float* __restrict__ g,
                             const float* __restrict__ b, const float* __restrict__ bias, float* __restrict__ c_out,
                             float* __restrict__ d_out) {
     const int j = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
     if (j >= N) return;
-    const float* w = reinterpret_cast<const float*>(rows) + (size_t)j * K;
+    const T* w = reinterpret_cast<const T*>(rows) + (size_t)j * K;
     double c = 0.0, d = 0.0;
     for (int i = lane; i < K; i += 32) {
-        c += (double)w[i] * (double)g[i];
-        d += (double)w[i] * (double)b[i];
+        const double wi = (double)(float)w[i];
+        c += wi * (double)g[i];
+        d += wi * (double)b[i];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -89,18 +115,29 @@ __global__ void fold_kernel(const uint8_t* __restrict__ rows, int K, int N, cons
     }
 }
 
-cudaError_t fold_rows(const uint8_t* rows, int K, int N, const float* g, const float* b, const float* bias, float* c,
-                      float* d, cudaStream_t st) {
+cudaError_t fold_rows(const uint8_t* rows, int K, int N, int wf, const float* g, const float* b, const float* bias,
+                      float* c, float* d, cudaStream_t st) {
     const int threads = 256, per_block = threads / 32;
-    fold_kernel<<<(N + per_block - 1) / per_block, threads, 0, st>>>(rows, K, N, g, b, bias, c, d);
+    if (wf == kWF16)
+        fold_kernel<__half><<<(N + per_block - 1) / per_block, threads, 0, st>>>(rows, K, N, g, b, bias, c, d);
+    else
+        fold_kernel<float><<<(N + per_block - 1) / per_block, threads, 0, st>>>(rows, K, N, g, b, bias, c, d);
     return cudaGetLastError();
 }
 
-cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, bool q8, cudaStream_t st) {
-    const int rb = row_bytes(K, q8);
-    if (!q8) {
+cudaError_t rows_to_f16(const float* src, uint8_t* dst, size_t n, cudaStream_t st) {
+    to_f16_kernel<<<1024, 256, 0, st>>>(src, reinterpret_cast<__half*>(dst), n);
+    return cudaGetLastError();
+}
+
+cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, int wf, cudaStream_t st) {
+    const int rb = row_bytes(K, wf);
+    if (wf == kWF32) {
         dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
         transpose_kernel<<<grid, block, 0, st>>>(src_in_out, dst, K, N, rb);
+    } else if (wf == kWF16) {
+        dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
+        transpose_f16_kernel<<<grid, block, 0, st>>>(src_in_out, dst, K, N, rb);
     } else {
         dim3 grid((N + 127) / 128, K / kGroup), block(128);
         quantize_in_out_kernel<<<grid, block, 0, st>>>(src_in_out, dst, K, N, rb);

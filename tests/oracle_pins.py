@@ -345,7 +345,71 @@ def check_validation(o, shape=synth.GPT2_TINY, seed=synth.SEED_TINY):
     assert o.infer(shape, w, np.zeros(shape.max_pos, "<u4").tobytes())[0] == "ok"
 
 
+# ------------------------------------------------------------- binary16 weights
+def _binary16_representable(x: np.ndarray) -> np.ndarray:
+    """True where x is a binary16 value: at most 11 significant bits with an
+    exponent in range, or a multiple of 2^-24 below 2^-14 (subnormals);
+    decided with frexp and integer tests, not with a float16 conversion."""
+    x = x.astype(np.float64)
+    m, e = np.frexp(x)  # x = m * 2^e, 0.5 <= |m| < 1
+    normal = (np.abs(x) >= 2.0 ** -14) & (np.abs(x) <= 65504.0)
+    sig = m * 2.0 ** 11
+    ok_normal = normal & (sig == np.round(sig))
+    sub = x * 2.0 ** 24
+    ok_sub = (np.abs(x) < 2.0 ** -14) & (sub == np.round(sub))
+    return ok_normal | ok_sub
+
+
+def check_round_f16(o, shape=synth.GPT2_TINY, seed=synth.SEED_TINY):
+    """The binary16-weight checkpoint: hand-worked round-to-nearest-even
+    cases, which tensors are rounded (layout by name), representability and
+    the half-ulp error bound (2^-11 relative for normal values)."""
+    from oracle import round_f16
+    w = synth.checkpoint(shape, seed, "rich")
+    lay = synth.layout(shape)
+    o_te = lay["wte"][0]
+    # planted values and their hand-rounded binary16 images
+    cases = [
+        (1.0 + 2.0 ** -11, 1.0),                  # tie, 1 is even
+        (1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -9),  # tie, 1 + 2 ulp is even
+        (1.0 + 2.0 ** -11 + 2.0 ** -20, 1.0 + 2.0 ** -10),  # above the tie
+        (-(1.0 + 2.0 ** -11), -1.0),
+        (2.0 ** -25, 0.0),                        # tie with 0 below the least subnormal
+        (3 * 2.0 ** -25, 2.0 ** -23),             # subnormal tie to even
+        (0.1, 1638.0 / 16384.0),                  # 0.1 -> 0x2E66
+        (65504.0, 65504.0),                       # largest finite
+    ]
+    for i, (v, _) in enumerate(cases):
+        w[o_te + i] = v
+    r = round_f16(shape, w)
+    for i, (v, want) in enumerate(cases):
+        assert r[o_te + i] == np.float32(want), (v, r[o_te + i], want)
+    for name, v in lay.items():
+        if name == "_words":
+            continue
+        off, n = v
+        a, b = w[off:off + n], r[off:off + n]
+        if name == "wte" or name.split(".")[-1].startswith("w_"):
+            assert _binary16_representable(b).all(), name
+            big = np.abs(a) >= 2.0 ** -14
+            rel = np.abs(b[big].astype(np.float64) - a[big]) / np.abs(a[big].astype(np.float64))
+            assert rel.max() <= 2.0 ** -11, name
+            assert (np.abs(b[~big].astype(np.float64) - a[~big]) <= 2.0 ** -25).all(), name
+            assert not np.array_equal(a, b), name  # random weights do move
+        else:
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), name
+    # the quant=2 model is the binary32 model on the rounded checkpoint and stays near it
+    w = synth.checkpoint(shape, seed, "rich")  # without the planted values
+    r = round_f16(shape, w)
+    toks = list(synth.tokens(shape.vocab, 4))
+    lh, _, _ = o.model(shape, w, quant=2).session(toks, 4)
+    lr, _, _ = o.model(shape, r, quant=0).session(toks, 4)
+    lf, _, _ = o.model(shape, w, quant=0).session(toks, 4)
+    assert np.array_equal(lh.view(np.uint32), lr.view(np.uint32))
+    assert 0 < np.abs(lh - lf).max() < 0.05
+
+
 FAST_CHECKS = [check_sizes, check_forward_vs_torch, check_cached_equals_infer, check_cache_prefix_kept,
                check_zero_blocks, check_layernorm, check_gelu, check_attention, check_linear_f32,
                check_argmax, check_quantizer, check_q8_group_dots, check_linear_q8_exact,
-               check_linear_q8_bound, check_q8_model, check_validation]
+               check_linear_q8_bound, check_q8_model, check_round_f16, check_validation]

@@ -72,7 +72,25 @@ def test_124m_int8_decode_128_positions(g, oracle, w124m, ref_f32):
           f"greedy agreement {greedy_agreement(ref, ch):.3f}")
 
 
-@pytest.mark.parametrize("quant", [0, 1], ids=["f32", "int8"])
+def test_124m_f16_decode_128_positions(g, oracle, w124m):
+    """Binary16 weight storage at full size: against the oracle's
+    binary16-weight model, to the binary32 bar."""
+    s = synth.GPT2_124M
+    om = oracle.model(s, w124m, quant=2)
+    seq, ref, ref_ch, ref_cache = oracle_greedy(om, synth.tokens(s.vocab, 16), 128)
+    om.close()
+    model = g.Model(s, w124m, quant=g.F16)
+    sess = g.Session(model)
+    logits, ch = run(sess, list(seq), 128)
+    err = np.abs(logits - ref).max(axis=1)
+    assert err.max() <= LOGIT_TOL, err.max()
+    assert greedy_agreement(ref, ch) >= AGREE_MIN
+    assert disagreements_are_near_ties(ref, ch, LOGIT_TOL)
+    cache = sess.read_cache()
+    assert np.abs(cache - ref_cache).max() <= LOGIT_TOL
+
+
+@pytest.mark.parametrize("quant", [0, 1, 2], ids=["f32", "int8", "f16"])
 def test_124m_projections_on_identical_inputs(g, oracle, w124m, quant):
     from test_gpu_decode import check_projections
     L = 12

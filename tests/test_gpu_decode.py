@@ -19,6 +19,7 @@ from gpu_util import (AGREE_MIN, GREEDY, LOGIT_TOL, dev_tokens, disagreements_ar
 from stream_decode_gb300 import synth  # noqa: E402
 
 import oracle_pins as P  # noqa: E402
+from oracle import round_f16  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -246,21 +247,24 @@ def _matrix_bias(shape, w, idx):
 def check_projections(g, oracle, shape, w, quant, indices, seed=31):
     """Every projection of the model on a seeded input vector: int8 models
     bit for bit against the oracle's int8 projection (codes, int32 group
-    sums, fixed-order rescale, bias); binary32 models within 1e-5."""
+    sums, fixed-order rescale, bias); binary32 models within 1e-5, and
+    binary16-weight models within 1e-5 of the binary32 projection with the
+    oracle's rounded weights."""
     model = g.Model(shape, w, quant=quant)
-    om = oracle.model(shape, w, quant=quant)
+    q8 = quant == 1
+    om = oracle.model(shape, w, quant=quant) if q8 else None
     p = None
     for idx in indices:
         n_in = shape.d_ff if (idx % 4 == 3 and idx != 4 * shape.n_layer) else shape.d_model
         x = (2.0 * synth.normals(seed + idx, 0, n_in)).astype(np.float32)
         x[::97] *= 3.0
         dx = torch.tensor(x, device="cuda")
-        q, s = (om.q8_matrix(idx) if quant else (None, None))
-        n_out = q.shape[0] if quant else None
-        if not quant:
+        q, s = (om.q8_matrix(idx) if q8 else (None, None))
+        n_out = q.shape[0] if q8 else None
+        if not q8:
             if p is None:
                 import torch_gpt2
-                p = torch_gpt2.parse(shape, w)
+                p = torch_gpt2.parse(shape, round_f16(shape, w) if quant == 2 else w)
             if idx == 4 * shape.n_layer:
                 wm = p["wte"].numpy().T
             else:
@@ -271,19 +275,20 @@ def check_projections(g, oracle, shape, w, quant, indices, seed=31):
         torch.cuda.synchronize()
         y = dy.cpu().numpy()
         b = _matrix_bias(shape, w, idx)
-        if quant:
+        if q8:
             ref = oracle.linear_q8(x, q, s, b)
             assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), f"matrix {idx}"
         else:
             ref = oracle.linear_f32(x, wm.astype(np.float32), b)
             assert np.abs(y - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max()), f"matrix {idx}"
     model.close()
-    om.close()
+    if om is not None:
+        om.close()
 
 
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
-@pytest.mark.parametrize("quant", [0, 1], ids=["f32", "int8"])
+@pytest.mark.parametrize("quant", [0, 1, 2], ids=["f32", "int8", "f16"])
 def test_projections_on_identical_inputs(g, oracle, shape, seed, quant):
     w = synth.checkpoint(shape, seed, "rich")
     check_projections(g, oracle, shape, w, quant, range(4 * shape.n_layer + 1))
@@ -350,3 +355,12 @@ def test_f32_traced_stages_close_to_oracle(g, oracle):
                                                                                     shape.n_layer * per + d]
         assert np.abs(nxt - otr[l]).max() < 1e-4, l
     assert np.abs(logits - ol).max() <= LOGIT_TOL
+
+
+# ------------------------------------------------------------------ binary16 weights
+@pytest.mark.parametrize("shape,seed,grid", [(synth.GPT2_TINY, synth.SEED_TINY, 0), (synth.GPT2_TINY, synth.SEED_TINY, 7),
+                                             (P.SMALL, P.SEED_SMALL, 0)], ids=["tiny", "tiny-grid7", "small"])
+def test_f16_session(g, oracle, shape, seed, grid):
+    """Binary16 weight storage: the oracle's binary16-weight model (binary32
+    arithmetic on the rounded checkpoint) is matched to the binary32 bar."""
+    _check_f32_session(_session_case(g, oracle, shape, seed, "rich", 2, grid))
