@@ -354,6 +354,59 @@ def long_context(g, torch, w, reps=20):
     return out
 
 
+BLOCK_PARAMS_124M = 12 * (768 * 2304 + 768 * 768 + 768 * 3072 + 3072 * 768)  # block-matrix weights
+
+
+def batched_decode(g, torch, shape, w, B: int, reps: int = 5):
+    """B independent sessions (gpt2_batch_run): a 16-token teacher-forced
+    prompt each, then 112 greedy steps at positions 16..127 per timed run
+    (the batch rewound to 16 before each run, logits written every step).
+    Returns tokens/s over all sessions and the algorithmic bytes and flops:
+    the binary32 weights once per step for all B rows, each session's KV
+    rows and logits; 2 flops per weight per session plus attention."""
+    from stream_decode_gb300 import synth
+    model = g.Model(shape, w)
+    bt = g.Batch(model, B)
+    V = shape.vocab
+    prompt = synth.tokens(V, PROMPT * B, seed=77).reshape(PROMPT, B).astype(np.int32)
+    d_prompt = torch.tensor(prompt, device="cuda")
+    pout = torch.zeros((PROMPT, B), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    assert bt.run(d_prompt, PROMPT, None, 0, pout, stream) == "ok"
+    assert bt.sync() == "ok"
+    dec = torch.full((DECODE, B), -1, dtype=torch.int32, device="cuda")
+    dec[0] = pout[PROMPT - 1]
+    dout = torch.zeros((DECODE, B), dtype=torch.int32, device="cuda")
+    logits = torch.empty((B, V), dtype=torch.float32, device="cuda")
+
+    def one():
+        assert bt.rewind(PROMPT, stream) == "ok"
+        assert bt.run(dec, DECODE, logits, 0, dout, stream) == "ok"
+
+    for _ in range(3):
+        one()
+    assert bt.sync() == "ok"
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert bt.sync() == "ok"
+    ms = e0.elapsed_time(e1) / reps
+    bt.close()
+    model.close()
+    d, L = shape.d_model, shape.n_layer
+    weights = step_bytes(shape, "f32", 0) - KV_ROW_BYTES - 4 * V
+    by = DECODE * weights + B * sum(KV_ROW_BYTES * (p + 1) + 4 * V for p in range(PROMPT, PROMPT + DECODE))
+    fl = sum(B * (2 * (BLOCK_PARAMS_124M + V * d) + L * 4 * d * (p + 1)) for p in range(PROMPT, PROMPT + DECODE))
+    return {"sessions": B, "tokens_per_s": B * DECODE / (ms * 1e-3), "ms_per_112_steps": ms,
+            "us_per_step": 1e3 * ms / DECODE, "GB_per_s": by / (ms * 1e-3) / 1e9,
+            "TFLOP_per_s": fl / (ms * 1e-3) / 1e12,
+            "arith": "3xTF32 tcgen05 projections (vocabulary included), binary32 elsewhere"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,6 +479,7 @@ def main():
             s16.close()
             m16.close()
         extra["long_context_f32"] = long_context(g, torch, w)
+        extra["batched_f32"] = [batched_decode(g, torch, shape, w, B) for B in (16, 64, 256)]
         extra["prefill_f32"] = prefill_rate(g, torch, shape, w)
 
     cpu = None

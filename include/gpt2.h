@@ -70,6 +70,10 @@ typedef enum gpt2_quant {
 
 typedef struct gpt2_model gpt2_model;
 typedef struct gpt2_session gpt2_session;
+typedef struct gpt2_batch gpt2_batch;
+
+/* Most sessions one gpt2_batch steps together. */
+#define GPT2_BATCH_MAX 256u
 
 /* Packed checkpoint size in 32-bit words (LeanExe GPT-2 README, packed
  * checkpoint paragraph: wte, all stored position rows, the blocks, the final
@@ -197,6 +201,63 @@ gpt2_status gpt2_session_step_host(gpt2_session* session, uint32_t token, float*
 /* Waits for the session's queued work and returns (and clears) the first
  * device-side failure recorded since the last sync. */
 gpt2_status gpt2_session_sync(gpt2_session* session);
+
+/* ---------------------------------------------------------------------
+ * Batched independent sessions: B decode sessions of one binary32 model
+ * stepped together.  Every step is one cachedStep (README, cachedStep
+ * paragraph) per session, each at its own position on its own KV cache;
+ * the sessions share only the weights, whose bytes one step reads once for
+ * all B rows (tensor-core projections).
+ * ------------------------------------------------------------------- */
+
+/* Creates a batch of n_sessions (1..GPT2_BATCH_MAX) empty sessions (position
+ * 0, no previous choice) with device KV caches of max_pos positions each.
+ * binary32 models of a shape the tensor-core path supports only
+ * (GPT2_ERR_CONFIG otherwise; the same shapes as gpt2_session_prefill).  The
+ * first batch of a model makes the TF32 remainders of its block matrices
+ * and of the tied embedding (one-off copies of their size, owned by the
+ * model).  The batch refers to the model, which must outlive it. */
+gpt2_status gpt2_batch_create(gpt2_model* model, uint32_t n_sessions, gpt2_batch** out);
+void gpt2_batch_destroy(gpt2_batch* batch);
+uint32_t gpt2_batch_size(const gpt2_batch* batch);
+/* Position of session `index` (0 for a bad batch or index). */
+uint32_t gpt2_batch_position(const gpt2_batch* batch, uint32_t index);
+
+/* Session `index`: copies a host cache of len bytes (a whole number of
+ * positions, fewer than max_pos; boundary layout) into its cache, sets its
+ * position to that number and forgets its previous choice.  Synchronous. */
+gpt2_status gpt2_batch_load_cache(gpt2_batch* batch, uint32_t index, const void* cache_host, size_t len);
+
+/* Session `index`: copies its cache (position positions) to cache_host
+ * (capacity bytes).  Synchronous; waits for queued steps. */
+gpt2_status gpt2_batch_read_cache(gpt2_batch* batch, uint32_t index, void* cache_host, size_t capacity,
+                                  size_t* len);
+
+/* Enqueues n_steps steps of every session on `stream` (a cudaStream_t; NULL
+ * is the default stream).  d_tokens_in: device array [n_steps][B] of token
+ * ids; GPT2_TOKEN_GREEDY takes that session's previous greedy choice.
+ * d_logits (may be NULL): device output, session b of step s at d_logits +
+ * s*logits_stride + b*vocab floats (logits_stride 0 = every step overwrites
+ * one [B][vocab] block; else at least B*vocab).  d_tokens_out (may be NULL):
+ * device array [n_steps][B] of greedy choices (largest, lowest index on
+ * ties; 0xFFFFFFFF if a logit of that row was not finite).  Host-side
+ * checks: n_steps >= 1, every position + n_steps <= max_pos.  The positions
+ * advance when the call returns.  An out-of-range token, a greedy token
+ * without a previous choice and non-finite logits are reported by the next
+ * gpt2_batch_sync; after such a failure the caches and positions are
+ * unspecified until reloaded.  The first call for a set of buffers records
+ * one step's launches as a CUDA graph, replayed once per step. */
+gpt2_status gpt2_batch_run(gpt2_batch* batch, const uint32_t* d_tokens_in, uint32_t n_steps, float* d_logits,
+                           size_t logits_stride, uint32_t* d_tokens_out, void* stream);
+
+/* Every session back to `position` (each must be at or past it, else
+ * GPT2_ERR_POSITION and nothing changes), with no previous choice; its
+ * cache rows below `position` are kept.  Asynchronous, ordered on `stream`. */
+gpt2_status gpt2_batch_rewind(gpt2_batch* batch, uint32_t position, void* stream);
+
+/* Waits for the batch's queued steps and returns (and clears) the first
+ * device-side failure recorded since the last sync. */
+gpt2_status gpt2_batch_sync(gpt2_batch* batch);
 
 /* Debug: enqueue the next run with an activation trace.  d_trace receives,
  * for step 0 of that run only, per layer: x_in[d], LN1(x)[d], qkv[3d],

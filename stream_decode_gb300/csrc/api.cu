@@ -299,6 +299,7 @@ void gpt2_model_destroy(gpt2_model* m) {
     cudaFree(m->d_vocab);
     cudaFree(m->d_fold);
     cudaFree(m->d_wlo);
+    cudaFree(m->d_wte_lo);
     delete m;
 }
 

@@ -19,4 +19,5 @@ struct gpt2_model {
     gpt2::LayerParams lp[gpt2::kMaxLayers];
     float* d_fold;  // binary32 models: LayerNorm folds of the QKV and FC rows (fold_layer_words per layer)
     float* d_wlo;  // binary32 models: TF32 remainders of the block matrices (prefill), made on first use
+    float* d_wte_lo;  // binary32 models: TF32 remainders of the tied embedding (batched decode), made on first use
 };

@@ -21,173 +21,12 @@
 #include "gpt2_dev.cuh"
 #include "model_internal.h"
 #include "prefill.h"
+#include "rows.cuh"
 #include "tc_gemm.cuh"
 
 namespace gpt2 {
 
 namespace {
-
-__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & ~0x1FFFu); }
-__device__ __forceinline__ float tf32_lo(float x) { return __fsub_rn(x, tf32_hi(x)); }
-
-__device__ __forceinline__ float warp_sum32(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-__device__ __forceinline__ float warp_max32(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ float gelu(float x) {
-    const float inner = 0.7978845608f * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.0f + tanhf(inner));
-}
-
-// lo[i] = w[i] - hi(w[i]) over n floats.
-__global__ void split_lo_kernel(const float* __restrict__ w, float* __restrict__ lo, size_t n) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        lo[i] = tf32_lo(w[i]);
-}
-
-// X[i][:] = wte[tok_i] + wpe[i]; an out-of-range token sets the status and
-// leaves its row unwritten.
-__global__ void embed_kernel(const float* __restrict__ packed, uint64_t wte_off, uint64_t wpe_off,
-                             const uint32_t* __restrict__ tok, int D, uint32_t vocab, float* __restrict__ X,
-                             int* status) {
-    const int i = blockIdx.x;
-    const uint32_t t = tok[i];
-    if (t >= vocab) {
-        if (threadIdx.x == 0) atomicCAS(status, 0, (int)kDevToken);
-        return;
-    }
-    for (int j = threadIdx.x; j < D; j += blockDim.x)
-        X[(size_t)i * D + j] = __fadd_rn(packed[wte_off + (uint64_t)t * D + j], packed[wpe_off + (uint64_t)i * D + j]);
-}
-
-constexpr int kLnThreads = 128;
-
-// Y = LN(X) (mean, then the biased variance of the deviations; eps 1e-5)
-// and its TF32 remainder, one block per row (D <= 1024: 8 values a thread).
-// With part != nullptr the row is first completed as the residual add of a
-// projection: X[i][j] += (sum over splits s = 0, 1, ... of part[s][i][j]) +
-// bias[j], in the split reduce's order, and written back.
-__global__ void __launch_bounds__(kLnThreads) ln_split_kernel(float* __restrict__ X, const float* __restrict__ g,
-                                                             const float* __restrict__ b, int D,
-                                                             float* __restrict__ Y, float* __restrict__ Ylo,
-                                                             const float* __restrict__ part, int splits, int n,
-                                                             const float* __restrict__ bias) {
-    __shared__ float red[kLnThreads / 32];
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float* x = X + (size_t)row * D;
-    float v[8];
-    if (part) {
-        // split sums in split order; four splits' loads are issued together
-        float y[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) y[k] = 0.0f;
-        int sp = 0;
-        for (; sp + 4 <= splits; sp += 4) {
-            float a[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int i = tid + kLnThreads * k;
-                    a[u][k] = i < D ? part[((size_t)(sp + u) * n + row) * D + i] : 0.0f;
-                }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) y[k] += a[u][k];
-        }
-        for (; sp < splits; ++sp)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int i = tid + kLnThreads * k;
-                if (i < D) y[k] += part[((size_t)sp * n + row) * D + i];
-            }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + kLnThreads * k;
-            v[k] = 0.0f;
-            if (i < D) {
-                v[k] = __fadd_rn(x[i], __fadd_rn(y[k], bias[i]));
-                x[i] = v[k];
-            }
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = tid + kLnThreads * k;
-            v[k] = i < D ? x[i] : 0.0f;
-        }
-    }
-    float s = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) s += v[k];
-    s = warp_sum32(s);
-    if (lane == 0) red[warp] = s;
-    __syncthreads();
-    float t = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];
-    const float mean = t / (float)D;
-    __syncthreads();
-    float q = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (tid + kLnThreads * k < D) {
-            const float d = v[k] - mean;
-            q = fmaf(d, d, q);
-        }
-    q = warp_sum32(q);
-    if (lane == 0) red[warp] = q;
-    __syncthreads();
-    float u = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kLnThreads / 32; ++w) u += red[w];
-    const float den = sqrtf(u / (float)D + kLnEps);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int i = tid + kLnThreads * k;
-        if (i < D) {
-            const float y = (v[k] - mean) / den * g[i] + b[i];
-            Y[(size_t)row * D + i] = y;
-            Ylo[(size_t)row * D + i] = tf32_lo(y);
-        }
-    }
-}
-
-enum ReduceKind : int { kRedQKV = 0, kRedResidual = 1, kRedGelu = 2 };
-
-// y[i][j] = (sum over splits s = 0, 1, ... of part[s][i][j]) + bias[j], then
-// QKV: out[i][j] = y and, for key/value columns, the cache row of
-// position i; residual: X[i][j] += y; GELU: out = gelu(y) and its remainder.
-__global__ void reduce_kernel(const float* __restrict__ part, int splits, int n, int N,
-                              const float* __restrict__ bias, int kind, float* __restrict__ out,
-                              float* __restrict__ out_lo, float* __restrict__ X, float* __restrict__ cache, int L,
-                              int l, int D) {
-    const size_t total = (size_t)n * N;
-    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (size_t)gridDim.x * blockDim.x) {
-        const int i = (int)(idx / N), j = (int)(idx - (size_t)i * N);
-        float y = 0.0f;
-        for (int s = 0; s < splits; ++s) y += part[((size_t)s * n + i) * N + j];
-        y = __fadd_rn(y, bias[j]);
-        if (kind == kRedQKV) {
-            out[idx] = y;
-            if (j >= D) cache[((size_t)i * L + l) * 2 * D + (j - D)] = y;
-        } else if (kind == kRedResidual) {
-            X[idx] = __fadd_rn(X[idx], y);
-        } else {
-            const float u = gelu(y);
-            out[idx] = u;
-            out_lo[idx] = tf32_lo(u);
-        }
-    }
-}
 
 constexpr int kAttnWarps = 8;
 constexpr int kAttnRows = 16;          // query rows per block (two per warp)
@@ -335,10 +174,6 @@ constexpr int kHeadThreads = 256;
 // non-finite value makes the choice 0xFFFFFFFF and sets the status).  One
 // block of 1024 threads; float4 loads when the logits are 16-byte aligned.
 constexpr int kChoiceThreads = 1024;
-__device__ __forceinline__ void choice_take(float x, unsigned j, float& bv, unsigned& bi, int& nf) {
-    if (!isfinite(x)) nf = 1;
-    else if (x > bv || (x == bv && j < bi)) { bv = x; bi = j; }
-}
 __global__ void __launch_bounds__(kChoiceThreads) choice_kernel(const float* __restrict__ v, unsigned n,
                                                                 uint32_t* choice, uint32_t* next, int* status) {
     __shared__ float s_v[kChoiceThreads / 32];
@@ -462,9 +297,13 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float* __restr
     }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------- host side
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+int g_sms = 0;
 
 bool encode_ready() {
     std::call_once(g_encode_once, [] {
@@ -489,8 +328,6 @@ bool kmajor_map(CUtensorMap* map, const float* base, int K, int rows, int box_ro
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_sms = 0;
-
 // K splits for an (m tiles x n tiles) grid.
 int choose_splits(int m_tiles, int n_tiles, int K) {
     const int nkb = K / tc::kBlockK;
@@ -507,6 +344,42 @@ int choose_splits(int m_tiles, int n_tiles, int K) {
 
 }  // namespace
 
+bool tc_ready() {
+    if (!encode_ready()) return false;
+    if (!g_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_sms <= 0) g_sms = 1;
+    }
+    return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)tc::kTcSmem) == cudaSuccess;
+}
+
+int tc_sm_count() { return g_sms; }
+
+cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W, const float* Wlo, int w_rows, int K,
+                    int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st) {
+    if (K % tc::kBlockK || N % tc::kTileN || w_rows > N || m_rows <= 0) return cudaErrorInvalidValue;
+    tc::TcMaps maps;
+    if (!kmajor_map(&maps.a_hi, A, K, m_rows, tc::kTileM) || !kmajor_map(&maps.a_lo, Alo, K, m_rows, tc::kTileM) ||
+        !kmajor_map(&maps.b_hi, W, K, w_rows, tc::kTileN) || !kmajor_map(&maps.b_lo, Wlo, K, w_rows, tc::kTileN))
+        return cudaErrorInvalidValue;
+    const int m_tiles = (m_rows + tc::kTileM - 1) / tc::kTileM, n_tiles = N / tc::kTileN;
+    int splits = choose_splits(m_tiles, n_tiles, K);
+    if (splits > max_splits) splits = max_splits < 1 ? 1 : max_splits;
+    *splits_out = splits;
+    tc::tf32x3_gemm_kernel<<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::kTcSmem, st>>>(
+        maps, K, N, m_rows, splits, part, status, (int)kDevTimeout);
+    return cudaGetLastError();
+}
+
+cudaError_t split_lo(const float* w, float* lo, size_t n, cudaStream_t st) {
+    split_lo_kernel<<<1024, 256, 0, st>>>(w, lo, n);
+    return cudaGetLastError();
+}
+
+
 size_t prefill_part_floats(int cap, int D, int FF) {
     const int n = cap, N = FF > 3 * D ? FF : 3 * D;
     return (size_t)kPrefillMaxSplits * n * N;
@@ -517,8 +390,7 @@ cudaError_t prefill_make_lo(gpt2_model* m, cudaStream_t st) {
     const size_t bytes = m->layer_bytes * m->cfg.n_layer;
     cudaError_t e = cudaMalloc(&m->d_wlo, bytes);
     if (e != cudaSuccess) return e;
-    split_lo_kernel<<<1024, 256, 0, st>>>(reinterpret_cast<const float*>(m->d_wstream), m->d_wlo, bytes / 4);
-    return cudaGetLastError();
+    return split_lo(reinterpret_cast<const float*>(m->d_wstream), m->d_wlo, bytes / 4, st);
 }
 
 cudaError_t prefill_alloc(PrefillWs* w, int cap, int D, int FF) {
@@ -579,29 +451,19 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
     const int D = (int)c.d_model, FF = (int)c.d_ff, L = (int)c.n_layer, H = (int)c.n_head, DH = D / H;
     cudaError_t e = cudaSuccess;
     const float* P = m->d_packed;
-    const int m_tiles = (n + tc::kTileM - 1) / tc::kTileM;
 
     // C[n][N] partials of A[n][K] x W[N][K] (W = block matrix `mat` of layer l)
     auto gemm = [&](const float* A, const float* Alo, int K, int N, int l, int mat, int* splits_out) -> cudaError_t {
         const uint64_t off = (uint64_t)l * m->layer_bytes + m->mat_off[mat];
         const float* W = reinterpret_cast<const float*>(m->d_wstream + off);
         const float* Wlo = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(m->d_wlo) + off);
-        tc::TcMaps maps;
-        if (!kmajor_map(&maps.a_hi, A, K, n, tc::kTileM) || !kmajor_map(&maps.a_lo, Alo, K, n, tc::kTileM) ||
-            !kmajor_map(&maps.b_hi, W, K, N, tc::kTileN) || !kmajor_map(&maps.b_lo, Wlo, K, N, tc::kTileN))
-            return cudaErrorInvalidValue;
-        const int n_tiles = N / tc::kTileN;
-        const int splits = choose_splits(m_tiles, n_tiles, K);
-        *splits_out = splits;
-        tc::tf32x3_gemm_kernel<<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::kTcSmem, st>>>(
-            maps, K, N, n, splits, w->part, status, (int)kDevTimeout);
-        return cudaGetLastError();
+        return tc_gemm(A, Alo, n, W, Wlo, N, K, N, kPrefillMaxSplits, splits_out, w->part, status, st);
     };
     auto reduce = [&](int splits, int N, uint64_t bias_off, int kind, float* out, float* out_lo, int l) {
         const size_t total = (size_t)n * N;
         const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
         reduce_kernel<<<blocks, 256, 0, st>>>(w->part, splits, n, N, P + bias_off, kind, out, out_lo, w->X, cache, L,
-                                              l, D);
+                                              l, D, nullptr, 0);
         return cudaGetLastError();
     };
 
@@ -637,7 +499,7 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
     const float* lg = P + m->lnf_g;
     const float* lb = P + m->lnf_b;
     const float* wte = P + m->wte_off;
-    const int hb = 2 * g_sms;  // two blocks per SM
+    const int hb = 2 * tc_sm_count();  // two blocks per SM
     if (D == 768) head_kernel<192><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
     else if (D == 192) head_kernel<48><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
     else if (D == 64) head_kernel<16><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
@@ -650,16 +512,8 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
 
 cudaError_t prefill_enqueue(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, int n, float* cache, float* logits,
                             int* status, uint32_t* d_choice, uint32_t* d_next, cudaStream_t st) {
-    if (!encode_ready()) return cudaErrorNotSupported;
-    if (!g_sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_sms <= 0) g_sms = 1;
-    }
-    cudaError_t e = cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc::kTcSmem);
-    if (e != cudaSuccess) return e;
+    if (!tc_ready()) return cudaErrorNotSupported;
+    cudaError_t e = cudaSuccess;
     const void* key[9] = {m, d_tok, reinterpret_cast<const void*>((uintptr_t)n), cache, logits, status, d_choice, d_next,
                           w->part};
     bool same = w->exec != nullptr;

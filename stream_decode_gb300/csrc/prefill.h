@@ -34,6 +34,22 @@ struct PrefillWs {
 };
 
 bool prefill_shape_supported(const gpt2_config& c);
+
+// The 3xTF32 tensor-core GEMM shared by the prefill and the batched decode
+// step.  tc_ready() looks up the tensor-map encoder and the SM count once
+// and sets the kernel's shared-memory size; false if either is missing.
+bool tc_ready();
+int tc_sm_count();
+// part[split][m][n] for m < m_rows, n < N: the split's K range of
+// A[m][:] . W[n][:] with both operands K-major binary32 ([rows][K]) and
+// their TF32 remainders Alo, Wlo beside them.  W has w_rows <= N rows; the
+// columns n >= w_rows read zeros.  K a multiple of 32, N of 64; base
+// addresses 16-byte aligned.  *splits_out = the number of K splits chosen
+// (at most max_splits); part holds splits x m_rows x N floats.
+cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W, const float* Wlo, int w_rows, int K,
+                    int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st);
+// lo[i] = w[i] - (w[i] with its low 13 mantissa bits cleared), i < n.
+cudaError_t split_lo(const float* w, float* lo, size_t n, cudaStream_t st);
 // The model's block-matrix TF32 remainders (made once, on stream st).
 cudaError_t prefill_make_lo(gpt2_model* m, cudaStream_t st);
 cudaError_t prefill_alloc(PrefillWs* w, int cap, int D, int FF);

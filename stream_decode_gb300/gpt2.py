@@ -62,6 +62,15 @@ _SIGS = {
     "gpt2_debug_project": ([_vp, _i32, _vp, _vp, _vp], _i32),
     "gpt2_debug_argmax": ([_vp, _u32, _vp, _vp, _vp], _i32),
     "gpt2_cached_step_noalloc": ([_vp, _vp, _u32, _u32, _vp, _vp, _vp], _i32),
+    "gpt2_batch_create": ([_vp, _u32, C.POINTER(_vp)], _i32),
+    "gpt2_batch_destroy": ([_vp], None),
+    "gpt2_batch_size": ([_vp], _u32),
+    "gpt2_batch_position": ([_vp, _u32], _u32),
+    "gpt2_batch_load_cache": ([_vp, _u32, _vp, _sz], _i32),
+    "gpt2_batch_read_cache": ([_vp, _u32, _vp, _sz, _szp], _i32),
+    "gpt2_batch_run": ([_vp, _vp, _u32, _vp, _sz, _vp, _vp], _i32),
+    "gpt2_batch_sync": ([_vp], _i32),
+    "gpt2_batch_rewind": ([_vp, _u32, _vp], _i32),
     "gpt2_status_name": ([_i32], C.c_char_p),
     "gpt2_last_cuda_error": ([C.POINTER(C.c_char_p)], _i32),
 }
@@ -238,6 +247,53 @@ class Session:
     def close(self):
         if getattr(self, "h", None):
             lib.gpt2_session_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        self.close()
+
+
+class Batch:
+    """B independent decode sessions of one binary32 model stepped together
+    (gpt2_batch_*)."""
+
+    def __init__(self, model: Model, n_sessions: int):
+        self.model = model
+        h = C.c_void_p()
+        _check("gpt2_batch_create", lib.gpt2_batch_create(model.h, n_sessions, C.byref(h)))
+        self.h = h
+        self.size = int(lib.gpt2_batch_size(h))
+
+    def position(self, index: int) -> int:
+        return int(lib.gpt2_batch_position(self.h, index))
+
+    def load_cache(self, index: int, cache: np.ndarray) -> str:
+        c = np.ascontiguousarray(cache, np.float32)
+        return STATUS[lib.gpt2_batch_load_cache(self.h, index, c.ctypes.data if c.size else None, c.nbytes)]
+
+    def read_cache(self, index: int) -> np.ndarray:
+        n = self.position(index) * cache_words_per_position(self.model.shape)
+        out = np.empty(n, np.float32)
+        got = C.c_size_t()
+        _check("gpt2_batch_read_cache", lib.gpt2_batch_read_cache(self.h, index, out.ctypes.data if n else None,
+                                                                  out.nbytes, C.byref(got)))
+        return out[:got.value // 4]
+
+    def run(self, tokens_in, n_steps: int, logits=None, stride: int = 0, tokens_out=None, stream=None) -> str:
+        """tokens_in: CUDA int32/uint32 tensor [n_steps][B]; logits: CUDA
+        float tensor (step s, session b at s * stride + b * vocab)."""
+        return STATUS[lib.gpt2_batch_run(self.h, _ptr(tokens_in), n_steps, _ptr(logits), stride, _ptr(tokens_out),
+                                         _stream(stream))]
+
+    def rewind(self, position: int, stream=None) -> str:
+        return STATUS[lib.gpt2_batch_rewind(self.h, position, _stream(stream))]
+
+    def sync(self) -> str:
+        return STATUS[lib.gpt2_batch_sync(self.h)]
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib.gpt2_batch_destroy(self.h)
             self.h = None
 
     def __del__(self):
