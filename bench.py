@@ -417,6 +417,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the int8, binary16, long-context and prefill extras")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the 128-token prefill leg (3 warm-up calls, --steps timed calls); prints its JSON")
+    ap.add_argument("--batch-only", type=int, default=0, metavar="B",
+                    help="only the batched leg with B sessions (3 warm-up runs, --steps timed runs); prints its JSON")
     ap.add_argument("--decode-steps", type=int, default=112,
                     help="decode positions per bench step (112 = positions 16..127)")
     args = ap.parse_args()
@@ -439,6 +441,10 @@ def main():
     if args.prefill_only:
         from stream_decode_gb300 import gpt2 as g
         print(json.dumps(prefill_rate(g, torch, shape, w, reps=max(1, args.steps))), flush=True)
+        return
+    if args.batch_only:
+        from stream_decode_gb300 import gpt2 as g
+        print(json.dumps(batched_decode(g, torch, shape, w, args.batch_only, reps=max(1, args.steps))), flush=True)
         return
     if ws > 1:
         import torch.distributed as dist
