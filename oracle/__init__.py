@@ -68,9 +68,11 @@ class Oracle:
         L.ref_group_scale.restype = C.c_float
         L.ref_quantize.argtypes = [_f32p, C.c_int, C.c_float, _i8p]
         L.ref_quantize_groups.argtypes = [_f32p, C.c_int, _i8p, _f32p]
+        L.ref_quantize_row.argtypes = [_f32p, C.c_int, _i8p, _f32p]
         L.ref_q8_group_dots.argtypes = [_i8p, _i8p, C.c_int, _i32p]
         L.ref_linear_f32.argtypes = [_f32p, _f32p, C.c_void_p, C.c_int, C.c_int, _f32p]
         L.ref_linear_q8.argtypes = [_f32p, _i8p, _f32p, C.c_void_p, C.c_int, C.c_int, _f32p]
+        L.ref_linear_q8_rowx.argtypes = [_f32p, _i8p, _f32p, C.c_void_p, C.c_int, C.c_int, _f32p]
         L.ref_attention_head.argtypes = [_f32p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_size_t,
                                          _f32p, C.c_void_p]
         L.ref_model_create.argtypes = [C.POINTER(_Cfg), C.c_void_p, C.c_size_t, C.c_int, C.POINTER(C.c_int)]
@@ -127,6 +129,15 @@ class Oracle:
         self.lib.ref_quantize_groups(x, x.size, q, s)
         return q, s
 
+    def quantize_row(self, x):
+        """One scale for the whole vector (the rejected per-activation-row
+        design of the quantized GPT-2 abstract): (codes, scale per group slot)."""
+        x = np.ascontiguousarray(x, np.float32)
+        q = np.empty(x.size, np.int8)
+        s = np.empty(x.size // 64, np.float32)
+        self.lib.ref_quantize_row(x, x.size, q, s)
+        return q, s
+
     def q8_group_dots(self, xq, wq):
         xq = np.ascontiguousarray(xq, np.int8)
         wq = np.ascontiguousarray(wq, np.int8)
@@ -143,14 +154,15 @@ class Oracle:
         self.lib.ref_linear_f32(x, w, None if bb is None else bb.ctypes.data, n_in, n_out, y)
         return y
 
-    def linear_q8(self, x, wq_out_in, ws, b=None):
+    def linear_q8(self, x, wq_out_in, ws, b=None, per_row_x=False):
         x = np.ascontiguousarray(x, np.float32)
         wq = np.ascontiguousarray(wq_out_in, np.int8)
         ws = np.ascontiguousarray(ws, np.float32)
         n_out, n_in = wq.shape
         y = np.empty(n_out, np.float32)
         bb = None if b is None else np.ascontiguousarray(b, np.float32)
-        self.lib.ref_linear_q8(x, wq, ws, None if bb is None else bb.ctypes.data, n_in, n_out, y)
+        f = self.lib.ref_linear_q8_rowx if per_row_x else self.lib.ref_linear_q8
+        f(x, wq, ws, None if bb is None else bb.ctypes.data, n_in, n_out, y)
         return y
 
     def attention_head(self, q, keys, values):
@@ -222,8 +234,10 @@ def round_f16(shape, weights) -> np.ndarray:
 
 
 class OracleModel:
-    """A parsed oracle model: quant=0 binary32, quant=1 int8-quantized,
-    quant=2 binary16 weights (binary32 arithmetic on round_f16's checkpoint)."""
+    """A parsed oracle model: quant=0 binary32, quant=1 int8 group-64,
+    quant=2 binary16 weights (binary32 arithmetic on round_f16's checkpoint),
+    quant=3 int8 with one weight scale per output row, quant=4 int8 with
+    per-row weight scales and one scale per projection input."""
 
     def __init__(self, o: Oracle, shape, weights, quant: int):
         self.o, self.shape, self.quant = o, shape, quant

@@ -43,6 +43,14 @@
  *     ((float)acc_g * s_x[g]) * s_w[j][g]) + b_j.
  *  R8 max_pos is a configuration field (128 for the pages' entry points,
  *     1024 for the long-context configuration).
+ *  R15 per-row weight scales (quant 3): one scale per output row, maxabs over
+ *     the row's inputs / 127, codes as in R7; the rescale keeps R7's order
+ *     with the row's scale in every group's place: y_j = (sum over g
+ *     ascending of ((float)acc_g * s_x[g]) * s_w[j]) + b_j.  Activations keep
+ *     their group-64 scales.
+ *  R16 per-activation-row scales (quant 4, the abstract's rejected first
+ *     design): as R15, and every projection input quantized with one scale
+ *     for the whole vector (maxabs / 127), s_x[g] = that scale for all g.
  */
 #include <math.h>
 #include <stddef.h>
@@ -102,7 +110,8 @@ typedef struct {
 
 typedef struct {
     ref_config cfg;
-    int quant; /* 0 = binary32, 1 = int8 group-64 */
+    int quant; /* 0 = binary32, 1 = int8 group-64, 3 = int8 per-row weight scales (R15),
+                  4 = int8 per-row weight and activation scales (R16) */
     float *words;
     const float *wte, *wpe, *lnf_g, *lnf_b;
     ref_block *blocks;
@@ -210,6 +219,14 @@ void ref_quantize_groups(const float *x, int n, int8_t *q, float *s) {
     }
 }
 
+/* Quantize a whole vector with one scale [R16]: maxabs over all n / 127;
+ * the scale is written to each of the n/64 group slots. */
+void ref_quantize_row(const float *x, int n, int8_t *q, float *s) {
+    float sr = ref_group_scale(x, n);
+    ref_quantize(x, n, sr, q);
+    for (int g = 0; g < n / REF_GROUP; g++) s[g] = sr;
+}
+
 /* int32 accumulators of one row against a quantized input, per group [P2]. */
 void ref_q8_group_dots(const int8_t *xq, const int8_t *wq, int n, int32_t *acc) {
     for (int g = 0; g < n / REF_GROUP; g++) {
@@ -237,15 +254,18 @@ void ref_linear_f32(const float *x, const float *w, const float *b, int n_in, in
         for (int j = 0; j < n_out; j++) y[j] = y[j] + b[j];
 }
 
-/* int8 projection [P2; R7]: quantize x per group, int32 group sums, then the
- * fixed rescale order. */
-void ref_linear_q8(const float *x, const int8_t *wq, const float *ws, const float *b, int n_in, int n_out,
-                   float *y) {
+/* int8 projection [P2; R7]: quantize x per group (per_row_x: one scale for
+ * all of x [R16]), int32 group sums, then the fixed rescale order. */
+static void linear_q8(const float *x, const int8_t *wq, const float *ws, const float *b, int n_in, int n_out,
+                      float *y, int per_row_x) {
     int ng = n_in / REF_GROUP;
     int8_t *xq = (int8_t *)malloc((size_t)n_in);
     float *xs = (float *)malloc(sizeof(float) * (size_t)ng);
     int32_t *acc = (int32_t *)malloc(sizeof(int32_t) * (size_t)ng);
-    ref_quantize_groups(x, n_in, xq, xs);
+    if (per_row_x)
+        ref_quantize_row(x, n_in, xq, xs);
+    else
+        ref_quantize_groups(x, n_in, xq, xs);
     for (int j = 0; j < n_out; j++) {
         ref_q8_group_dots(xq, wq + (size_t)j * n_in, n_in, acc);
         float sum = 0.0f;
@@ -255,6 +275,17 @@ void ref_linear_q8(const float *x, const int8_t *wq, const float *ws, const floa
     free(xq);
     free(xs);
     free(acc);
+}
+
+void ref_linear_q8(const float *x, const int8_t *wq, const float *ws, const float *b, int n_in, int n_out,
+                   float *y) {
+    linear_q8(x, wq, ws, b, n_in, n_out, y, 0);
+}
+
+/* The same with the input quantized with one scale [R16]. */
+void ref_linear_q8_rowx(const float *x, const int8_t *wq, const float *ws, const float *b, int n_in, int n_out,
+                        float *y) {
+    linear_q8(x, wq, ws, b, n_in, n_out, y, 1);
 }
 
 /* One attention head over n_src cached rows [P1 model paragraph; R4].
@@ -309,6 +340,25 @@ static void q8_from_in_out(const float *w, int n_in, int n_out, ref_q8_matrix *m
         }
 }
 
+/* Per-row weight scales [R15]: row j (output j) = w[.][j] of an [in][out]
+ * matrix, or w[j][.] of an [out][in] one; one scale for the whole row,
+ * written to each of its group slots. */
+static void q8_rows(const float *w, int n_in, int n_out, int in_out, ref_q8_matrix *m) {
+    int ng = n_in / REF_GROUP;
+    m->n_in = n_in;
+    m->n_out = n_out;
+    m->q = (int8_t *)malloc((size_t)n_in * n_out);
+    m->s = (float *)malloc(sizeof(float) * (size_t)ng * n_out);
+    float *row = (float *)malloc(sizeof(float) * (size_t)n_in);
+    for (int j = 0; j < n_out; j++) {
+        for (int i = 0; i < n_in; i++) row[i] = in_out ? w[(size_t)i * n_out + j] : w[(size_t)j * n_in + i];
+        float s = ref_group_scale(row, n_in);
+        ref_quantize(row, n_in, s, m->q + (size_t)j * n_in);
+        for (int g = 0; g < ng; g++) m->s[(size_t)j * ng + g] = s;
+    }
+    free(row);
+}
+
 static void q8_from_out_in(const float *w, int n_in, int n_out, ref_q8_matrix *m) {
     /* w is [out][in] (the tied wte). */
     int ng = n_in / REF_GROUP;
@@ -341,11 +391,11 @@ void ref_model_free(ref_model *m) {
 }
 
 /* Parse the packed checkpoint [P1 packed checkpoint paragraph; R1] and, for
- * quant == 1, build the int8 copies [P2; R7].  Returns NULL with *status set
+ * quant 1, 3 or 4, build the int8 copies [P2; R7; R15].  Returns NULL with *status set
  * on a bad configuration or weight length. */
 ref_model *ref_model_create(const ref_config *c, const void *weights, size_t weights_len, int quant, int *status) {
     *status = REF_OK;
-    if (!config_ok(c) || (quant != 0 && quant != 1)) {
+    if (!config_ok(c) || (quant != 0 && quant != 1 && quant != 3 && quant != 4)) {
         *status = REF_ERR_CONFIG;
         return NULL;
     }
@@ -406,6 +456,17 @@ ref_model *ref_model_create(const ref_config *c, const void *weights, size_t wei
             q8_from_in_out(b->w_p, (int)f, (int)d, &m->q8[4 * l + 3]);
         }
         q8_from_out_in(m->wte, (int)d, (int)c->vocab, &m->q8[4 * c->n_layer]);
+    } else if (quant == 3 || quant == 4) {
+        int nm = 4 * (int)c->n_layer + 1;
+        m->q8 = (ref_q8_matrix *)calloc((size_t)nm, sizeof(ref_q8_matrix));
+        for (uint32_t l = 0; l < c->n_layer; l++) {
+            const ref_block *b = &m->blocks[l];
+            q8_rows(b->w_qkv, (int)d, (int)(3 * d), 1, &m->q8[4 * l + 0]);
+            q8_rows(b->w_o, (int)d, (int)d, 1, &m->q8[4 * l + 1]);
+            q8_rows(b->w_fc, (int)d, (int)f, 1, &m->q8[4 * l + 2]);
+            q8_rows(b->w_p, (int)f, (int)d, 1, &m->q8[4 * l + 3]);
+        }
+        q8_rows(m->wte, (int)d, (int)c->vocab, 0, &m->q8[4 * c->n_layer]);
     }
     return m;
 }
@@ -422,9 +483,9 @@ int ref_model_get_q8(const ref_model *m, int index, int8_t *q, float *s) {
 
 static void project(const ref_model *m, int qindex, const float *x, const float *w, const float *b, int n_in,
                     int n_out, float *y) {
-    if (m->quant == 1) {
+    if (m->q8) {
         const ref_q8_matrix *q = &m->q8[qindex];
-        ref_linear_q8(x, q->q, q->s, b, n_in, n_out, y);
+        linear_q8(x, q->q, q->s, b, n_in, n_out, y, m->quant == 4);
     } else {
         ref_linear_f32(x, w, b, n_in, n_out, y);
     }
@@ -448,7 +509,7 @@ static void forward_token(const ref_model *m, float *cache, uint32_t token, uint
     float *u = (float *)malloc(sizeof(float) * f);
 
     /* Embedding: token row plus position row [P1 model paragraph; R7 for int8]. */
-    if (m->quant == 1) {
+    if (m->q8) {
         const ref_q8_matrix *e = &m->q8[4 * L];
         int ng = d / REF_GROUP;
         for (int i = 0; i < d; i++) {
@@ -491,9 +552,9 @@ static void forward_token(const ref_model *m, float *cache, uint32_t token, uint
     if (logits) {
         /* final normalization and tied vocabulary projection (no bias) */
         ref_layernorm(x, m->lnf_g, m->lnf_b, d, a);
-        if (m->quant == 1) {
+        if (m->q8) {
             const ref_q8_matrix *e = &m->q8[4 * L];
-            ref_linear_q8(a, e->q, e->s, NULL, d, (int)c->vocab, logits);
+            linear_q8(a, e->q, e->s, NULL, d, (int)c->vocab, logits, m->quant == 4);
         } else {
             for (uint32_t j = 0; j < c->vocab; j++) {
                 const float *w = m->wte + (size_t)j * d;

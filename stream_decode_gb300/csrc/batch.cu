@@ -10,9 +10,10 @@
 // embedding of each session's token at its position, a decode attention
 // kernel (one block per (head, session) over that session's keys), the tied
 // vocabulary projection as one more GEMM (N = vocab, padded to 64 with
-// zero rows), and a row-wise greedy choice that also advances the
-// positions.  A step is one CUDA graph (captured once per set of output
-// buffers) replayed once per step.
+// zero rows), and the greedy choice (chunks of each row in parallel, then
+// one thread per session, which also advances the positions).  A step is
+// one CUDA graph (captured once per set of output buffers) replayed once
+// per step.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -157,35 +158,46 @@ __global__ void __launch_bounds__(kBAttnThreads) batch_attention_kernel(const fl
     }
 }
 
-constexpr int kBChoiceThreads = 512;
+constexpr int kBChoiceThreads = 256;
+constexpr int kChoiceChunk = 4096;  // logits of one row per block of the logits kernel
 
-// Row b (one block): logits[n] = sum over the vocabulary GEMM's splits of
-// part[s][b][n], n < V (part rows are ldp floats apart, B rows a split);
-// copied to out + step * stride + b * V when out is given; greedy choice
-// (largest, lowest index on ties; any non-finite value: 0xFFFFFFFF and the
-// status) into tokens_out[step * B + b] when given and into last[b]; then
-// pos[b] advances.  The last block to finish advances *step.
-__global__ void __launch_bounds__(kBChoiceThreads) batch_choice_kernel(
+// Block (c, b): logits n of row b in chunk c ([c * 4096, (c + 1) * 4096) and
+// n < V) = the sum over the vocabulary GEMM's splits of part[s][b][n] (part
+// rows are ldp floats apart, a multiple of 64; B rows a split), copied to
+// out + step * stride + b * V when out is given; the chunk's greedy
+// candidate (largest, lowest index on ties, any non-finite value flagged)
+// goes to cand_v / cand_i / cand_nf[b * C + c].
+__global__ void __launch_bounds__(kBChoiceThreads) batch_logits_kernel(
     const float* __restrict__ part, int splits, int ldp, int V, float* __restrict__ out, size_t stride,
-    uint32_t* __restrict__ tokens_out, uint32_t* __restrict__ last, int* __restrict__ pos, int* step,
-    unsigned* done, int* status) {
+    const int* __restrict__ step, float* __restrict__ cand_v, unsigned* __restrict__ cand_i,
+    int* __restrict__ cand_nf) {
     __shared__ float s_v[kBChoiceThreads / 32];
     __shared__ unsigned s_i[kBChoiceThreads / 32];
     __shared__ int s_nf[kBChoiceThreads / 32];
-    __shared__ int s_step;
-    const int b = blockIdx.x, B = gridDim.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) s_step = *step;
-    __syncthreads();
-    const int st = s_step;
-    float* o = out ? out + (size_t)st * stride + (size_t)b * V : nullptr;
+    const int c = blockIdx.x, C = gridDim.x, b = blockIdx.y, B = gridDim.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* o = out ? out + (size_t)(*step) * stride + (size_t)b * V : nullptr;
     float bv = -INFINITY;
     unsigned bi = 0xFFFFFFFFu;
     int nf = 0;
-    for (int n = tid; n < V; n += kBChoiceThreads) {
-        float x = part[(size_t)b * ldp + n];
-        for (int s = 1; s < splits; ++s) x += part[((size_t)s * B + b) * ldp + n];
-        if (o) o[n] = x;
-        choice_take(x, (unsigned)n, bv, bi, nf);
+    const int n_end = min(V, (c + 1) * kChoiceChunk);
+    for (int n = c * kChoiceChunk + 4 * tid; n < n_end; n += 4 * kBChoiceThreads) {
+        // 16-byte loads: rows start on 64-float boundaries and n is a multiple of 4
+        float4 x = *reinterpret_cast<const float4*>(part + (size_t)b * ldp + n);
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 y = *reinterpret_cast<const float4*>(part + ((size_t)sp * B + b) * ldp + n);
+            x.x += y.x;
+            x.y += y.y;
+            x.z += y.z;
+            x.w += y.w;
+        }
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (n + k < n_end) {
+                if (o) o[n + k] = xv[k];
+                choice_take(xv[k], (unsigned)(n + k), bv, bi, nf);
+            }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -211,17 +223,43 @@ __global__ void __launch_bounds__(kBChoiceThreads) batch_choice_kernel(
                 bi = s_i[w];
             }
         }
-        const uint32_t c = nf ? 0xFFFFFFFFu : bi;
-        if (tokens_out) tokens_out[(size_t)st * B + b] = c;
-        last[b] = c;
-        pos[b] += 1;
-        if (nf) atomicCAS(status, 0, (int)kDevNonfinite);
-        __threadfence();
-        if (atomicAdd(done, 1u) == (unsigned)B - 1) {
-            *done = 0;
-            *step = st + 1;
+        cand_v[(size_t)b * C + c] = bv;
+        cand_i[(size_t)b * C + c] = bi;
+        cand_nf[(size_t)b * C + c] = nf;
+    }
+}
+
+// One block of B threads: thread b combines row b's C chunk candidates
+// (same rule), writes the choice (0xFFFFFFFF and the status if any logit
+// was not finite) to tokens_out[step * B + b] when given and to last[b],
+// and advances pos[b]; then the step counter advances.
+__global__ void batch_pick_kernel(const float* __restrict__ cand_v, const unsigned* __restrict__ cand_i,
+                                  const int* __restrict__ cand_nf, int C, uint32_t* __restrict__ tokens_out,
+                                  uint32_t* __restrict__ last, int* __restrict__ pos, int* step, int* status) {
+    __shared__ int s_step;
+    const int b = threadIdx.x, B = blockDim.x;
+    if (b == 0) s_step = *step;
+    __syncthreads();
+    const int st = s_step;
+    float bv = -INFINITY;
+    unsigned bi = 0xFFFFFFFFu;
+    int nf = 0;
+    for (int c = 0; c < C; ++c) {
+        const float v = cand_v[(size_t)b * C + c];
+        const unsigned i = cand_i[(size_t)b * C + c];
+        nf |= cand_nf[(size_t)b * C + c];
+        if (v > bv || (v == bv && i < bi)) {
+            bv = v;
+            bi = i;
         }
     }
+    const uint32_t ch = nf ? 0xFFFFFFFFu : bi;
+    if (tokens_out) tokens_out[(size_t)st * B + b] = ch;
+    last[b] = ch;
+    pos[b] += 1;
+    if (nf) atomicCAS(status, 0, (int)kDevNonfinite);
+    __syncthreads();
+    if (b == 0) *step = st + 1;
 }
 
 // Every session back to position p with no previous choice.
@@ -251,9 +289,10 @@ struct gpt2_batch {
     float* Ulo = nullptr;
     float* part = nullptr;  // split-K partials of the block projections
     float* vpart = nullptr; // [B][v_pad] vocabulary products
+    float* cand = nullptr;  // [3][B][chunks] greedy candidates of the logits chunks (value, index, non-finite)
     int* d_pos = nullptr;   // [B] positions
     uint32_t* d_last = nullptr;  // [B] previous greedy choices
-    int* d_words = nullptr;      // [0] status, [1] step counter, [2] finished-rows counter
+    int* d_words = nullptr;      // [0] status, [1] step counter
     std::vector<uint32_t> pos;   // host copy of the positions
     cudaStream_t cs = nullptr, last = nullptr;
     cudaEvent_t ev_in = nullptr, ev_out = nullptr;
@@ -330,9 +369,14 @@ cudaError_t batch_launches(gpt2_batch* bt, const uint32_t* d_tokens_in, float* d
     e = tc_gemm(bt->A, bt->Alo, B, P + m->wte_off, m->d_wte_lo, (int)c.vocab, D, bt->v_pad, 1, &vs, bt->vpart,
                 status, st);
     if (e != cudaSuccess) return e;
-    batch_choice_kernel<<<B, kBChoiceThreads, 0, st>>>(bt->vpart, vs, bt->v_pad, (int)c.vocab, d_logits, stride,
-                                                       d_tokens_out, bt->d_last, bt->d_pos, bt->d_words + 1,
-                                                       reinterpret_cast<unsigned*>(bt->d_words + 2), status);
+    const int C = (bt->v_pad + kChoiceChunk - 1) / kChoiceChunk;
+    float* cv = bt->cand;
+    unsigned* ci = reinterpret_cast<unsigned*>(bt->cand + (size_t)B * C);
+    int* cnf = reinterpret_cast<int*>(bt->cand + 2 * (size_t)B * C);
+    batch_logits_kernel<<<dim3(C, B), kBChoiceThreads, 0, st>>>(bt->vpart, vs, bt->v_pad, (int)c.vocab, d_logits,
+                                                                stride, bt->d_words + 1, cv, ci, cnf);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    batch_pick_kernel<<<1, B, 0, st>>>(cv, ci, cnf, C, d_tokens_out, bt->d_last, bt->d_pos, bt->d_words + 1, status);
     return cudaGetLastError();
 }
 
@@ -382,6 +426,8 @@ gpt2_status gpt2_batch_create(gpt2_model* m, uint32_t n_sessions, gpt2_batch** o
     if (e == cudaSuccess) e = cudaMalloc(&bt->Ulo, sizeof(float) * B * FF);
     if (e == cudaSuccess) e = cudaMalloc(&bt->part, sizeof(float) * kBatchMaxSplits * B * N);
     if (e == cudaSuccess) e = cudaMalloc(&bt->vpart, sizeof(float) * B * bt->v_pad);
+    if (e == cudaSuccess)
+        e = cudaMalloc(&bt->cand, sizeof(float) * 3 * B * ((bt->v_pad + kChoiceChunk - 1) / kChoiceChunk));
     if (e == cudaSuccess) e = cudaMalloc(&bt->d_pos, sizeof(int) * B);
     if (e == cudaSuccess) e = cudaMemset(bt->d_pos, 0, sizeof(int) * B);
     if (e == cudaSuccess) e = cudaMalloc(&bt->d_last, sizeof(uint32_t) * B);
@@ -414,6 +460,7 @@ void gpt2_batch_destroy(gpt2_batch* bt) {
     cudaFree(bt->Ulo);
     cudaFree(bt->part);
     cudaFree(bt->vpart);
+    cudaFree(bt->cand);
     cudaFree(bt->d_pos);
     cudaFree(bt->d_last);
     cudaFree(bt->d_words);
@@ -491,7 +538,7 @@ gpt2_status gpt2_batch_run(gpt2_batch* bt, const uint32_t* d_tokens_in, uint32_t
     }
     e = cudaEventRecord(bt->ev_in, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(bt->cs, bt->ev_in, 0);
-    if (e == cudaSuccess) e = cudaMemsetAsync(bt->d_words + 1, 0, sizeof(int) * 2, bt->cs);  // step, finished rows
+    if (e == cudaSuccess) e = cudaMemsetAsync(bt->d_words + 1, 0, sizeof(int), bt->cs);  // step counter
     for (uint32_t s = 0; s < n_steps && e == cudaSuccess; ++s) e = cudaGraphLaunch(bt->exec, bt->cs);
     if (e == cudaSuccess) e = cudaEventRecord(bt->ev_out, bt->cs);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, bt->ev_out, 0);

@@ -409,7 +409,66 @@ def check_round_f16(o, shape=synth.GPT2_TINY, seed=synth.SEED_TINY):
     assert 0 < np.abs(lh - lf).max() < 0.05
 
 
+# ------------------------------------------------------------- per-row int8 scales
+def check_q8_row_scales(o, shape=SMALL, seed=SEED_SMALL):
+    """Per-row weight scales (quant 3) and per-activation-row scales (quant
+    4, the quantized GPT-2 abstract's rejected first design): every matrix
+    row has one scale, 127 times it is the row's largest magnitude, the
+    largest code is 127 and every code is within half a step of its weight
+    (checked in float64 against the checkpoint); the per-row activation
+    quantizer on a hand-worked vector; and the ablation changes the model's
+    logits."""
+    w = synth.checkpoint(shape, seed, "rich")
+    p = torch_gpt2.parse(shape, w)
+    L = shape.n_layer
+    m3 = o.model(shape, w, quant=3)
+    m1 = o.model(shape, w, quant=1)
+    differ = False
+    for idx in range(4 * L + 1):
+        if idx == 4 * L:
+            W = p["wte"].numpy()  # [out][in]
+        else:
+            W = p["blocks"][idx // 4][["w_qkv", "w_o", "w_fc", "w_p"][idx % 4]].numpy().T  # [out][in]
+        q, sc = m3.q8_matrix(idx)
+        s = sc[:, :1].astype(np.float64)
+        assert (sc == sc[:, :1]).all(), idx  # one scale per row
+        mx = np.abs(W).max(axis=1, keepdims=True)
+        assert (np.abs(127.0 * s - mx) <= 1e-6 * mx).all(), idx
+        assert (np.abs(q).max(axis=1) == 127).all(), idx
+        assert (np.abs(q * s - W) <= 0.5 * s * (1 + 1e-6)).all(), idx
+        differ |= not np.array_equal(m1.q8_matrix(idx)[1], sc)
+    assert differ  # group scales are not per-row scales on this shape
+    # hand-worked per-row activation codes: the largest magnitude sits in the
+    # second group; one scale 2/127 for the whole vector
+    x = np.zeros(128, np.float32)
+    x[64], x[0], x[1], x[2], x[65] = -2.0, 1.0, -1.0, 0.001, 0.5
+    qx, sx = o.quantize_row(x)
+    assert np.array_equal(sx, np.full(2, np.float32(2.0) / np.float32(127.0), np.float32))
+    want = np.zeros(128, np.int8)
+    # 1/(2/127) = 63.5 -> 64 (even); 0.001 -> 0.0635 -> 0; 0.5 -> 31.75 -> 32
+    want[64], want[0], want[1], want[2], want[65] = -127, 64, -64, 0, 32
+    assert np.array_equal(qx, want)
+    # the ablation changes the logits; both stay near the binary32 model
+    toks = list(synth.tokens(shape.vocab, 4))
+    lf, _, _ = o.model(shape, w, quant=0).session(toks, 4)
+    l3, _, _ = m3.session(toks, 4)
+    m4 = o.model(shape, w, quant=4)
+    l4, _, _ = m4.session(toks, 4)
+    assert not np.array_equal(l3, l4)
+    # already the first block's output differs (the block projections take
+    # one activation scale, not only the vocabulary projection)
+    row = o.cache_words_per_position(shape)
+    t3 = m3.cached_step(np.zeros(row, np.float32), int(toks[1]), 1, trace=True)[3]
+    t4 = m4.cached_step(np.zeros(row, np.float32), int(toks[1]), 1, trace=True)[3]
+    assert not np.array_equal(t3[0], t4[0])
+    m4.close()
+    assert np.abs(l3 - lf).max() < 0.2 and np.abs(l4 - lf).max() < 0.5
+    m1.close()
+    m3.close()
+
+
 FAST_CHECKS = [check_sizes, check_forward_vs_torch, check_cached_equals_infer, check_cache_prefix_kept,
                check_zero_blocks, check_layernorm, check_gelu, check_attention, check_linear_f32,
                check_argmax, check_quantizer, check_q8_group_dots, check_linear_q8_exact,
-               check_linear_q8_bound, check_q8_model, check_round_f16, check_validation]
+               check_linear_q8_bound, check_q8_model, check_round_f16, check_q8_row_scales,
+               check_validation]

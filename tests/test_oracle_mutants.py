@@ -43,6 +43,16 @@ MUTANTS = [
      "for (size_t i = (size_t)position * row; i < ((size_t)position + 1) * row; i++) store_le_f32"),
     ("position_bound_off_by_one", "if (position >= c->max_pos) return REF_ERR_POSITION;",
      "if (position > c->max_pos) return REF_ERR_POSITION;"),
+    ("row_scale_from_first_group", "float s = ref_group_scale(row, n_in);",
+     "float s = ref_group_scale(row, REF_GROUP);"),
+    ("row_scale_in_slot0_only", "for (int g = 0; g < ng; g++) m->s[(size_t)j * ng + g] = s;",
+     "m->s[(size_t)j * ng] = s;"),
+    ("row_gather_transposed", "row[i] = in_out ? w[(size_t)i * n_out + j] : w[(size_t)j * n_in + i];",
+     "row[i] = in_out ? w[(size_t)j * n_in + i] : w[(size_t)j * n_in + i];"),
+    ("activation_row_scale_first_group", "float sr = ref_group_scale(x, n);",
+     "float sr = ref_group_scale(x, REF_GROUP);"),
+    ("ablation_ignored", "linear_q8(x, q->q, q->s, b, n_in, n_out, y, m->quant == 4);",
+     "linear_q8(x, q->q, q->s, b, n_in, n_out, y, 0);"),
     ("token_bound_off_by_one", "if (token >= c->vocab) return REF_ERR_TOKEN;",
      "if (token > c->vocab) return REF_ERR_TOKEN;"),
 ]
