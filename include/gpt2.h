@@ -60,9 +60,12 @@ typedef enum gpt2_status {
 typedef enum gpt2_quant {
     GPT2_F32 = 0,      /* binary32 weights and arithmetic */
     GPT2_INT8_G64 = 1, /* int8 weights and projection inputs, scales per 64 inputs, int32 sums */
-    GPT2_F16 = 2       /* the 48 block matrices and the tied embedding stored as binary16 (rounded to
+    GPT2_F16 = 2,      /* the 48 block matrices and the tied embedding stored as binary16 (rounded to
                           nearest-even at load), widened to binary32 before every multiply-add;
                           everything else binary32 (the gpt2.s page's half-precision weight option) */
+    GPT2_INT8_ROW = 3  /* as GPT2_INT8_G64, but one weight scale per output row (maxabs over the whole
+                          row / 127); the rescale keeps the grouped order with the row's scale in every
+                          group's place; projection inputs keep their group-64 scales */
 } gpt2_quant;
 
 /* In a device token array: use the previous step's greedy choice. */

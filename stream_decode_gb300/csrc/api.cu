@@ -17,9 +17,10 @@ namespace gpt2 {
 cudaError_t launch_step(const StepPlan& P, int wq, cudaStream_t stream);
 int step_max_ctas(int D, int FF, int DH, int wq, int max_pos);
 bool step_shape_supported(int D, int FF, int DH);
-cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, int wf, cudaStream_t st);
+cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, int wf, bool per_row,
+                          cudaStream_t st);
 cudaError_t rows_to_f16(const float* src, uint8_t* dst, size_t n, cudaStream_t st);
-cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, cudaStream_t st);
+cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, bool per_row, cudaStream_t st);
 cudaError_t fold_rows(const uint8_t* rows, int K, int N, int wf, const float* g, const float* b, const float* bias,
                       float* c, float* d, cudaStream_t st);
 cudaError_t launch_project(const uint8_t* rows, int K, int N, int wq, const float* x, const float* bias, float* y,
@@ -104,7 +105,7 @@ void fill_plan(const gpt2_session* s, StepPlan& P) {
     P.wstream = m->d_wstream;
     P.layer_bytes = m->layer_bytes;
     for (int i = 0; i < 4; ++i) P.mat_off[i] = m->mat_off[i];
-    P.vocab = m->quant != GPT2_F32 ? m->d_vocab : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
+    P.vocab = m->wfmt != kWF32 ? m->d_vocab : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
     P.wte_off = m->wte_off;
     P.wpe_off = m->wpe_off;
     P.lnf_g = m->lnf_g;
@@ -156,7 +157,7 @@ gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t t
     if (pf) P.prefetch_chunks = atoi(pf);
     const char* pace = getenv("GPT2_PACE_NS");
     if (pace) P.pace_ns = (uint32_t)atoi(pace);
-    cudaError_t e = launch_step(P, s->m->quant, stream);
+    cudaError_t e = launch_step(P, s->m->wfmt, stream);
     if (e != cudaSuccess) return cuda_status(e);
     s->trace_next = nullptr;
     s->timing_next = nullptr;
@@ -203,11 +204,15 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
                               int grid_ctas, gpt2_model** out) {
     if (!out) return GPT2_ERR_ARG;
     *out = nullptr;
-    if (!config_ok(cfg) || (quant != GPT2_F32 && quant != GPT2_INT8_G64 && quant != GPT2_F16)) return GPT2_ERR_CONFIG;
+    if (!config_ok(cfg) || (quant != GPT2_F32 && quant != GPT2_INT8_G64 && quant != GPT2_F16 &&
+                            quant != GPT2_INT8_ROW))
+        return GPT2_ERR_CONFIG;
     if (!weights || weights_len != words_of(cfg) * 4) return GPT2_ERR_WEIGHTS_LEN;
     const int D = (int)cfg->d_model, FF = (int)cfg->d_ff, L = (int)cfg->n_layer;
-    const bool q8 = quant == GPT2_INT8_G64;
-    const int wfmt = quant;  // the weight format of the device streams (kWF32, kWQ8, kWF16)
+    // the weight format of the device streams: per-row int8 scales use the
+    // grouped layout with the row's scale in every group slot
+    const int wfmt = quant == GPT2_INT8_ROW ? kWQ8 : quant;
+    const bool q8 = wfmt == kWQ8, per_row = quant == GPT2_INT8_ROW;
     const int maxc = step_max_ctas(D, FF, D / (int)cfg->n_head, wfmt, (int)cfg->max_pos);
     if (maxc <= 0) return GPT2_ERR_CUDA;
     if (grid_ctas < 0 || grid_ctas > maxc) return GPT2_ERR_CONFIG;
@@ -217,6 +222,7 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
     if (!m) return GPT2_ERR_NOMEM;
     m->cfg = *cfg;
     m->quant = quant;
+    m->wfmt = wfmt;
     m->G = grid_ctas ? grid_ctas : maxc;
     {
         // word offsets of the packed checkpoint (README packed checkpoint
@@ -256,10 +262,10 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
         CK(cudaMemset(m->d_wstream, 0, m->layer_bytes * L));
         for (int l = 0; l < L; ++l) {
             uint8_t* base = m->d_wstream + (uint64_t)l * m->layer_bytes;
-            CK(repack_matrix(m->d_packed + wq[l], base + m->mat_off[kQKV], D, 3 * D, wfmt, 0));
-            CK(repack_matrix(m->d_packed + wo[l], base + m->mat_off[kO], D, D, wfmt, 0));
-            CK(repack_matrix(m->d_packed + wf[l], base + m->mat_off[kFC], D, FF, wfmt, 0));
-            CK(repack_matrix(m->d_packed + wp[l], base + m->mat_off[kP], FF, D, wfmt, 0));
+            CK(repack_matrix(m->d_packed + wq[l], base + m->mat_off[kQKV], D, 3 * D, wfmt, per_row, 0));
+            CK(repack_matrix(m->d_packed + wo[l], base + m->mat_off[kO], D, D, wfmt, per_row, 0));
+            CK(repack_matrix(m->d_packed + wf[l], base + m->mat_off[kFC], D, FF, wfmt, per_row, 0));
+            CK(repack_matrix(m->d_packed + wp[l], base + m->mat_off[kP], FF, D, wfmt, per_row, 0));
         }
         if (!q8) {
             const uint64_t fw = fold_layer_words(D, FF);
@@ -278,7 +284,7 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
         if (q8) {
             CK(cudaMalloc(&m->d_vocab, (uint64_t)cfg->vocab * rbd));
             CK(cudaMemset(m->d_vocab, 0, (uint64_t)cfg->vocab * rbd));
-            CK(quantize_rows(m->d_packed + m->wte_off, m->d_vocab, D, (int)cfg->vocab, 0));
+            CK(quantize_rows(m->d_packed + m->wte_off, m->d_vocab, D, (int)cfg->vocab, per_row, 0));
         } else if (wfmt == kWF16) {
             CK(cudaMalloc(&m->d_vocab, (uint64_t)cfg->vocab * rbd));
             CK(rows_to_f16(m->d_packed + m->wte_off, m->d_vocab, (size_t)cfg->vocab * D, 0));
@@ -305,7 +311,7 @@ void gpt2_model_destroy(gpt2_model* m) {
 
 gpt2_status gpt2_model_read_q8(gpt2_model* m, int index, int8_t* q_host, float* s_host) {
     if (!m || !q_host || !s_host) return GPT2_ERR_ARG;
-    if (m->quant != GPT2_INT8_G64) return GPT2_ERR_CONFIG;
+    if (m->wfmt != kWQ8) return GPT2_ERR_CONFIG;
     const int D = (int)m->cfg.d_model, FF = (int)m->cfg.d_ff, L = (int)m->cfg.n_layer;
     if (index < 0 || index > 4 * L) return GPT2_ERR_ARG;
     int K, N;
@@ -479,14 +485,13 @@ gpt2_status gpt2_debug_project(gpt2_model* m, int index, const float* d_x, float
     if (!m || !d_x || !d_y) return GPT2_ERR_ARG;
     const int D = (int)m->cfg.d_model, FF = (int)m->cfg.d_ff, L = (int)m->cfg.n_layer;
     if (index < 0 || index > 4 * L) return GPT2_ERR_ARG;
-    const bool q8 = m->quant == GPT2_INT8_G64;
     int K, N;
     const uint8_t* rows;
     const float* bias = nullptr;
     if (index == 4 * L) {
         K = D;
         N = (int)m->cfg.vocab;
-        rows = m->quant != GPT2_F32 ? m->d_vocab : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
+        rows = m->wfmt != kWF32 ? m->d_vocab : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
     } else {
         const int l = index / 4, k = index % 4;
         K = (k == kP) ? FF : D;
@@ -497,7 +502,7 @@ gpt2_status gpt2_debug_project(gpt2_model* m, int index, const float* d_x, float
         bias = m->d_packed + b;
     }
     // the path the step kernel takes for this matrix at one CTA per SM: streaming for the vocabulary
-    return cuda_status(launch_project(rows, K, N, m->quant, d_x, bias, d_y, index == 4 * L ? 1 : 0, (cudaStream_t)stream));
+    return cuda_status(launch_project(rows, K, N, m->wfmt, d_x, bias, d_y, index == 4 * L ? 1 : 0, (cudaStream_t)stream));
 }
 
 gpt2_status gpt2_debug_argmax(const float* d_values, uint32_t n, uint32_t* d_index, int* d_nonfinite,

@@ -8,7 +8,8 @@
 
 struct gpt2_model {
     gpt2_config cfg;
-    int quant;
+    int quant;  // gpt2_quant of the model
+    int wfmt;   // weight format of the device streams (kWF32, kWQ8, kWF16)
     int G;
     float* d_packed;
     uint8_t* d_wstream;

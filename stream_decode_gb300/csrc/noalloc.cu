@@ -102,7 +102,7 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     P.wstream = m->d_wstream;
     P.layer_bytes = m->layer_bytes;
     for (int i = 0; i < 4; ++i) P.mat_off[i] = m->mat_off[i];
-    P.vocab = m->quant != GPT2_F32 ? m->d_vocab : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
+    P.vocab = m->wfmt != kWF32 ? m->d_vocab : reinterpret_cast<const uint8_t*>(m->d_packed + m->wte_off);
     P.wte_off = m->wte_off;
     P.wpe_off = m->wpe_off;
     P.lnf_g = m->lnf_g;
@@ -131,6 +131,6 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     P.stall_phase = -1;
     P.prefetch_chunks = 0;
     P.pace_ns = kDefaultPaceNs;
-    e = launch_step(P, m->quant, s);
+    e = launch_step(P, m->wfmt, s);
     return e == cudaSuccess ? GPT2_OK : (e == cudaErrorMemoryAllocation ? GPT2_ERR_NOMEM : GPT2_ERR_CUDA);
 }

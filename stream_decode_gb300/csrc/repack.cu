@@ -8,7 +8,9 @@
 // copy of the tied embedding); int8 models get, per output
 // row, K int8 codes followed by the K/64 group scales (padded to 16 bytes),
 // quantized with the rule of the quantized GPT-2 abstract: scale =
-// maxabs/127 over 64 consecutive inputs of the row, nearest-even, saturate.
+// maxabs/127 over 64 consecutive inputs of the row, nearest-even, saturate
+// (or, with per-row weight scales, one scale over the whole row, repeated
+// in every group slot).
 #include <cuda_runtime.h>
 
 #include "gpt2_dev.cuh"
@@ -87,6 +89,41 @@ __global__ void quantize_out_in_kernel(const float* __restrict__ src, uint8_t* _
     reinterpret_cast<float*>(dst + (size_t)n * rb + K)[g] = s;
 }
 
+// Per-row weight scales, one thread per output n of a [K][N] matrix: one
+// scale for the row's K weights (maxabs / 127), written to each of the K/64
+// group slots, so the grouped kernels read it unchanged.
+__global__ void quantize_in_out_row_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int K, int N,
+                                           int rb) {
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    float m = 0.0f;
+    for (int k = 0; k < K; ++k) {
+        const float a = fabsf(src[(size_t)k * N + n]);
+        if (a > m) m = a;
+    }
+    const float s = __fdiv_rn(m, 127.0f);
+    int8_t* q = reinterpret_cast<int8_t*>(dst + (size_t)n * rb);
+    for (int k = 0; k < K; ++k) q[k] = (int8_t)quantize_one(src[(size_t)k * N + n], s);
+    for (int g = 0; g < K / kGroup; ++g) reinterpret_cast<float*>(dst + (size_t)n * rb + K)[g] = s;
+}
+
+// The same for the rows of an [N][K] matrix (the tied wte), one thread per row.
+__global__ void quantize_out_in_row_kernel(const float* __restrict__ src, uint8_t* __restrict__ dst, int K, int N,
+                                           int rb) {
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    const float* row = src + (size_t)n * K;
+    float m = 0.0f;
+    for (int k = 0; k < K; ++k) {
+        const float a = fabsf(row[k]);
+        if (a > m) m = a;
+    }
+    const float s = __fdiv_rn(m, 127.0f);
+    int8_t* q = reinterpret_cast<int8_t*>(dst + (size_t)n * rb);
+    for (int k = 0; k < K; ++k) q[k] = (int8_t)quantize_one(row[k], s);
+    for (int g = 0; g < K / kGroup; ++g) reinterpret_cast<float*>(dst + (size_t)n * rb + K)[g] = s;
+}
+
 // The LayerNorm folds of one K-major matrix (rows of K binary32 or binary16
 // values, the latter the model's weights as stored):
 // c_j = sum_i W_ji g_i and d_j = bias_j + sum_i W_ji b_i, one warp per
@@ -130,8 +167,13 @@ cudaError_t rows_to_f16(const float* src, uint8_t* dst, size_t n, cudaStream_t s
     return cudaGetLastError();
 }
 
-cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, int wf, cudaStream_t st) {
+cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, int wf, bool per_row,
+                          cudaStream_t st) {
     const int rb = row_bytes(K, wf);
+    if (wf == kWQ8 && per_row) {
+        quantize_in_out_row_kernel<<<(N + 127) / 128, 128, 0, st>>>(src_in_out, dst, K, N, rb);
+        return cudaGetLastError();
+    }
     if (wf == kWF32) {
         dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
         transpose_kernel<<<grid, block, 0, st>>>(src_in_out, dst, K, N, rb);
@@ -145,8 +187,12 @@ cudaError_t repack_matrix(const float* src_in_out, uint8_t* dst, int K, int N, i
     return cudaGetLastError();
 }
 
-cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, cudaStream_t st) {
-    const int rb = row_bytes(K, true);
+cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, bool per_row, cudaStream_t st) {
+    const int rb = row_bytes(K, kWQ8);
+    if (per_row) {
+        quantize_out_in_row_kernel<<<(N + 127) / 128, 128, 0, st>>>(src_out_in, dst, K, N, rb);
+        return cudaGetLastError();
+    }
     const long long n = (long long)N * (K / kGroup);
     quantize_out_in_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src_out_in, dst, K, N, rb);
     return cudaGetLastError();

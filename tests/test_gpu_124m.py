@@ -55,16 +55,17 @@ def test_124m_f32_decode_128_positions(g, w124m, ref_f32):
         assert top2[1] - top2[0] <= LOGIT_TOL, f"greedy run left the oracle's path at step {d[0]}"
 
 
-def test_124m_int8_decode_128_positions(g, oracle, w124m, ref_f32):
+@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+def test_124m_int8_decode_128_positions(g, oracle, w124m, ref_f32, quant):
     s = synth.GPT2_124M
-    om = oracle.model(s, w124m, quant=1)
+    om = oracle.model(s, w124m, quant=quant)
     seq, ref, ref_ch, _ = oracle_greedy(om, synth.tokens(s.vocab, 16), 128)
     om.close()
     of = oracle.model(s, w124m)
     ref_f32_same, _, _ = of.session(list(seq), 128)
     of.close()
     tol = int8_tolerance(ref, ref_f32_same)
-    logits, ch = run(g.Session(g.Model(s, w124m, quant=1)), list(seq), 128)
+    logits, ch = run(g.Session(g.Model(s, w124m, quant=quant)), list(seq), 128)
     err = np.abs(logits - ref).max(axis=1)
     assert err.max() <= tol, (err.max(), tol)
     assert disagreements_are_near_ties(ref, ch, tol)
@@ -90,7 +91,7 @@ def test_124m_f16_decode_128_positions(g, oracle, w124m):
     assert np.abs(cache - ref_cache).max() <= LOGIT_TOL
 
 
-@pytest.mark.parametrize("quant", [0, 1, 2], ids=["f32", "int8", "f16"])
+@pytest.mark.parametrize("quant", [0, 1, 2, 3], ids=["f32", "int8", "f16", "int8_row"])
 def test_124m_projections_on_identical_inputs(g, oracle, w124m, quant):
     from test_gpu_decode import check_projections
     L = 12

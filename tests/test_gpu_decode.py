@@ -215,10 +215,11 @@ def test_run_to_run_determinism(g):
 # ------------------------------------------------------------------ int8
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
-def test_int8_weight_codes_bit_exact(g, oracle, shape, seed):
+@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+def test_int8_weight_codes_bit_exact(g, oracle, shape, seed, quant):
     w = synth.checkpoint(shape, seed, "rich")
-    model = g.Model(shape, w, quant=g.INT8_G64)
-    om = oracle.model(shape, w, quant=1)
+    model = g.Model(shape, w, quant=quant)
+    om = oracle.model(shape, w, quant=quant)
     for idx in range(4 * shape.n_layer + 1):
         q, s = model.read_q8(idx)
         oq, os_ = om.q8_matrix(idx)
@@ -251,7 +252,7 @@ def check_projections(g, oracle, shape, w, quant, indices, seed=31):
     binary16-weight models within 1e-5 of the binary32 projection with the
     oracle's rounded weights."""
     model = g.Model(shape, w, quant=quant)
-    q8 = quant == 1
+    q8 = quant in (1, 3)
     om = oracle.model(shape, w, quant=quant) if q8 else None
     p = None
     for idx in indices:
@@ -288,7 +289,7 @@ def check_projections(g, oracle, shape, w, quant, indices, seed=31):
 
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
-@pytest.mark.parametrize("quant", [0, 1, 2], ids=["f32", "int8", "f16"])
+@pytest.mark.parametrize("quant", [0, 1, 2, 3], ids=["f32", "int8", "f16", "int8_row"])
 def test_projections_on_identical_inputs(g, oracle, shape, seed, quant):
     w = synth.checkpoint(shape, seed, "rich")
     check_projections(g, oracle, shape, w, quant, range(4 * shape.n_layer + 1))
@@ -332,8 +333,10 @@ def test_int8_activation_codes_near_ties(g, oracle):
 
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
-def test_int8_session(g, oracle, shape, seed):
-    logits, ch, ref, ref_ch, cache, ref_cache, greedy_ch, seq = _session_case(g, oracle, shape, seed, "rich", 1, 0)
+@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+def test_int8_session(g, oracle, shape, seed, quant):
+    logits, ch, ref, ref_ch, cache, ref_cache, greedy_ch, seq = _session_case(g, oracle, shape, seed, "rich", quant,
+                                                                               0)
     w = synth.checkpoint(shape, seed, "rich")
     ref_f32, _, _ = oracle.model(shape, w).session(list(seq), shape.max_pos)
     tol = int8_tolerance(ref, ref_f32)
