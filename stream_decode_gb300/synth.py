@@ -139,8 +139,13 @@ def checkpoint(s: Shape, seed: int, variant: str = "plain", block: int = 1 << 23
     LayerNorm gains 1 + N(0, 0.1), so a dropped bias or gain shows up.
     ``zero_blocks``: as plain, but every block matrix and bias is zero, so
     each block is the identity map on the residual stream.
+    ``outlier_channels``: as plain, but in every LayerNorm 4 fixed channels
+    (0, d/4 + 1, d/2 + 2, 3d/4 + 3) have gain 20, so every normalised
+    projection input carries a few coordinates about 20 times larger than
+    the rest (the shape of the large-magnitude activation channels of
+    trained GPT-2 models; used by the int8 scale-granularity ablation).
     """
-    if variant not in ("plain", "rich", "zero_blocks"):
+    if variant not in ("plain", "rich", "zero_blocks", "outlier_channels"):
         raise ValueError(variant)
     lay = layout(s)
     n = lay["_words"]
@@ -158,6 +163,9 @@ def checkpoint(s: Shape, seed: int, variant: str = "plain", block: int = 1 << 23
                 out[o:o + cnt] = (1.0 + 0.1 * normals(seed ^ 0xA5A5, o, cnt)).astype(np.float32)
             else:
                 out[o:o + cnt] = 1.0
+                if variant == "outlier_channels":
+                    for c in (0, cnt // 4 + 1, cnt // 2 + 2, 3 * cnt // 4 + 3):
+                        out[o + c] = 20.0
         elif base.endswith("_b") and base.startswith("ln") or base.startswith("b_"):
             if variant != "rich":
                 out[o:o + cnt] = 0.0
