@@ -72,9 +72,10 @@ def test_noalloc_matches_session_step_124m(g, w124m):
     _compare(g, synth.GPT2_124M, w124m, g.F32, n_calls=3)
 
 
-def test_noalloc_matches_session_step_int8(g):
+@pytest.mark.parametrize("fmt", ["INT8_G64", "F16", "INT8_ROW"])
+def test_noalloc_matches_session_step_other_formats(g, fmt):
     shape = synth.GPT2_TINY
-    _compare(g, shape, synth.checkpoint(shape, synth.SEED_TINY, "rich"), g.INT8_G64)
+    _compare(g, shape, synth.checkpoint(shape, synth.SEED_TINY, "rich"), getattr(g, fmt))
 
 
 def test_noalloc_rejects_bad_arguments(g):
