@@ -201,6 +201,17 @@ gpt2_status gpt2_session_step(gpt2_session* session, uint32_t token, float* d_lo
 gpt2_status gpt2_session_step_host(gpt2_session* session, uint32_t token, float* logits_host,
                                    uint32_t* next_token_host);
 
+/* A run with host buffers end to end: n_steps token ids from host memory
+ * (GPT2_TOKEN_GREEDY as in gpt2_session_run; every other id checked < vocab
+ * on the host, else GPT2_ERR_TOKEN and nothing runs), one persistent launch,
+ * then every step's logits (n_steps*vocab floats, row s at s*vocab) to
+ * logits_host and the greedy choices (n_steps ids) to tokens_out_host; either
+ * may be NULL.  Pinned host memory makes the copies asynchronous; the call
+ * waits for them and returns any device status.  The device buffers are
+ * session-owned and grow to the largest n_steps seen. */
+gpt2_status gpt2_session_run_host(gpt2_session* session, const uint32_t* tokens_host, uint32_t n_steps,
+                                  float* logits_host, uint32_t* tokens_out_host);
+
 /* Waits for the session's queued work and returns (and clears) the first
  * device-side failure recorded since the last sync. */
 gpt2_status gpt2_session_sync(gpt2_session* session);

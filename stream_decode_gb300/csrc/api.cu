@@ -48,6 +48,11 @@ struct gpt2_session {
     int stall_phase;
     uint64_t wait_limit_ns;
     PrefillWs pf;  // tensor-core prefill workspace, allocated on first use
+    // gpt2_session_run_host buffers (grown on demand): tokens in, logits, choices
+    uint32_t* d_run_in = nullptr;
+    float* d_run_logits = nullptr;
+    uint32_t* d_run_out = nullptr;
+    uint32_t run_cap = 0;
 };
 
 namespace {
@@ -374,6 +379,9 @@ void gpt2_session_destroy(gpt2_session* s) {
     prefill_free(&s->pf);
     cudaFree(s->d_logits);
     cudaFree(s->d_next);
+    cudaFree(s->d_run_in);
+    cudaFree(s->d_run_logits);
+    cudaFree(s->d_run_out);
     if (s->own) cudaStreamDestroy(s->own);
     delete s;
 }
@@ -458,6 +466,43 @@ gpt2_status gpt2_session_step_host(gpt2_session* s, uint32_t token, float* logit
                             s->own);
     if (e == cudaSuccess && next_host)
         e = cudaMemcpyAsync(next_host, s->d_next, sizeof(uint32_t), cudaMemcpyDeviceToHost, s->own);
+    if (e != cudaSuccess) return cuda_status(e);
+    return gpt2_session_sync(s);
+}
+
+gpt2_status gpt2_session_run_host(gpt2_session* s, const uint32_t* tokens_host, uint32_t n_steps, float* logits_host,
+                                  uint32_t* tokens_out_host) {
+    if (!s || !tokens_host) return GPT2_ERR_ARG;
+    const gpt2_config& c = s->m->cfg;
+    if (n_steps == 0) return GPT2_ERR_TOKENS_LEN;
+    if ((uint64_t)s->position + n_steps > c.max_pos) return GPT2_ERR_POSITION;
+    for (uint32_t i = 0; i < n_steps; ++i)
+        if (tokens_host[i] != GPT2_TOKEN_GREEDY && tokens_host[i] >= c.vocab) return GPT2_ERR_TOKEN;
+    cudaError_t e = cudaStreamSynchronize(s->last);
+    if (e == cudaSuccess && n_steps > s->run_cap) {
+        cudaFree(s->d_run_in);
+        cudaFree(s->d_run_logits);
+        cudaFree(s->d_run_out);
+        s->d_run_in = s->d_run_out = nullptr;
+        s->d_run_logits = nullptr;
+        s->run_cap = 0;
+        e = cudaMalloc(&s->d_run_in, sizeof(uint32_t) * n_steps);
+        if (e == cudaSuccess) e = cudaMalloc(&s->d_run_out, sizeof(uint32_t) * n_steps);
+        if (e == cudaSuccess) e = cudaMalloc(&s->d_run_logits, sizeof(float) * c.vocab * n_steps);
+        if (e == cudaSuccess) s->run_cap = n_steps;
+    }
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(s->d_run_in, tokens_host, sizeof(uint32_t) * n_steps, cudaMemcpyHostToDevice, s->own);
+    if (e != cudaSuccess) return cuda_status(e);
+    gpt2_status st = enqueue_run(s, s->d_run_in, 0, n_steps, logits_host ? s->d_run_logits : nullptr, c.vocab,
+                                 s->d_run_out, s->own);
+    if (st != GPT2_OK) return st;
+    if (logits_host)
+        e = cudaMemcpyAsync(logits_host, s->d_run_logits, sizeof(float) * c.vocab * n_steps, cudaMemcpyDeviceToHost,
+                            s->own);
+    if (e == cudaSuccess && tokens_out_host)
+        e = cudaMemcpyAsync(tokens_out_host, s->d_run_out, sizeof(uint32_t) * n_steps, cudaMemcpyDeviceToHost,
+                            s->own);
     if (e != cudaSuccess) return cuda_status(e);
     return gpt2_session_sync(s);
 }

@@ -55,6 +55,7 @@ _SIGS = {
     "gpt2_session_prefill": ([_vp, _vp, _u32, _vp, _vp, _vp], _i32),
     "gpt2_session_step": ([_vp, _u32, _vp, _vp, _vp], _i32),
     "gpt2_session_step_host": ([_vp, _u32, _vp, _vp], _i32),
+    "gpt2_session_run_host": ([_vp, _vp, _u32, _vp, _vp], _i32),
     "gpt2_session_sync": ([_vp], _i32),
     "gpt2_session_set_trace": ([_vp, _vp], _i32),
     "gpt2_session_inject_stall": ([_vp, _u32, C.c_uint64], _i32),
@@ -230,6 +231,17 @@ class Session:
         npt = None if next_host is None else (next_host.data_ptr() if hasattr(next_host, "data_ptr")
                                               else next_host.ctypes.data)
         return STATUS[lib.gpt2_session_step_host(self.h, token & 0xFFFFFFFF, lp, npt)]
+
+    def run_host(self, tokens_host, n_steps: int, logits_host=None, tokens_out_host=None) -> str:
+        """Host buffers (numpy arrays or pinned CPU torch tensors): tokens_host
+        uint32/int32[n_steps]; logits_host float32[n_steps][vocab]; tokens_out_host
+        uint32/int32[n_steps]."""
+        def hp(t):
+            if t is None:
+                return None
+            return t.data_ptr() if hasattr(t, "data_ptr") else t.ctypes.data
+        return STATUS[lib.gpt2_session_run_host(self.h, hp(tokens_host), n_steps, hp(logits_host),
+                                                hp(tokens_out_host))]
 
     def sync(self) -> str:
         return STATUS[lib.gpt2_session_sync(self.h)]

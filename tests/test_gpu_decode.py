@@ -166,6 +166,31 @@ def test_step_apis_agree(g, oracle):
     assert b.step(shape.vocab, d_logits, d_next) == "token"
 
 
+def test_run_host_matches_device_run(g):
+    """gpt2_session_run_host (host token ids in, every step's logits and
+    choices back in host memory) gives the device run's bits, with greedy
+    feedback, and checks its host tokens before any launch."""
+    shape = synth.GPT2_TINY
+    w = synth.checkpoint(shape, synth.SEED_TINY, "rich")
+    model = g.Model(shape, w)
+    toks = [int(t) for t in synth.tokens(shape.vocab, 4, seed=9)] + [GREEDY] * 8
+    a, b = g.Session(model), g.Session(model)
+    la, ca = run(a, toks, 12)
+    hl = np.full((12, shape.vocab), np.nan, np.float32)
+    ho = np.zeros(12, np.uint32)
+    assert b.run_host(np.array(toks, np.int64).astype(np.uint32), 12, hl, ho) == "ok"
+    assert np.array_equal(hl.view(np.uint32), la.view(np.uint32)), "same kernel, same bits"
+    assert np.array_equal(ho.astype(np.int64), np.asarray(ca, np.int64) & 0xFFFFFFFF)
+    assert b.position == 12
+    c = g.Session(model)
+    assert c.run_host(np.array([1, shape.vocab], np.uint32), 2) == "token" and c.position == 0
+    assert c.run_host(np.zeros(shape.max_pos + 1, np.uint32), shape.max_pos + 1) == "position"
+    assert c.run_host(np.array([3], np.uint32), 1) == "ok" and c.position == 1  # outputs optional
+    for sess in (a, b, c):
+        sess.close()
+    model.close()
+
+
 def test_greedy_token_without_history_is_an_error(g):
     shape = synth.GPT2_TINY
     sess = g.Session(g.Model(shape, synth.checkpoint(shape, synth.SEED_TINY)))
