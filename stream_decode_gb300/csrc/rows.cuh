@@ -69,22 +69,22 @@ __global__ void __launch_bounds__(kLnThreads) ln_split_kernel(float* __restrict_
     float* x = X + (size_t)row * D;
     float v[8];
     if (part) {
-        // split sums in split order; four splits' loads are issued together
+        // split sums in split order; eight splits' loads are issued together
         float y[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) y[k] = 0.0f;
         int sp = 0;
-        for (; sp + 4 <= splits; sp += 4) {
-            float a[4][8];
+        for (; sp + 8 <= splits; sp += 8) {
+            float a[8][8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const int i = tid + kLnThreads * k;
                     a[u][k] = i < D ? part[((size_t)(sp + u) * n + row) * D + i] : 0.0f;
                 }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) y[k] += a[u][k];
         }
