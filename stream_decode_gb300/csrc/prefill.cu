@@ -362,7 +362,8 @@ cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W
                     int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st) {
     if (K % tc::kBlockK || N % tc::kTileN || w_rows > N || m_rows <= 0) return cudaErrorInvalidValue;
     tc::TcMaps maps;
-    if (!kmajor_map(&maps.a_hi, A, K, m_rows, tc::kTileM) || !kmajor_map(&maps.a_lo, Alo, K, m_rows, tc::kTileM) ||
+    const int a_rows = m_rows <= tc::kTileM / 2 ? tc::kTileM / 2 : tc::kTileM;  // A rows loaded per tile
+    if (!kmajor_map(&maps.a_hi, A, K, m_rows, a_rows) || !kmajor_map(&maps.a_lo, Alo, K, m_rows, a_rows) ||
         !kmajor_map(&maps.b_hi, W, K, w_rows, tc::kTileN) || !kmajor_map(&maps.b_lo, Wlo, K, w_rows, tc::kTileN))
         return cudaErrorInvalidValue;
     const int m_tiles = (m_rows + tc::kTileM - 1) / tc::kTileM, n_tiles = N / tc::kTileN;
@@ -370,7 +371,7 @@ cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W
     if (splits > max_splits) splits = max_splits < 1 ? 1 : max_splits;
     *splits_out = splits;
     tc::tf32x3_gemm_kernel<<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::kTcSmem, st>>>(
-        maps, K, N, m_rows, splits, part, status, (int)kDevTimeout);
+        maps, K, N, m_rows, splits, part, status, (int)kDevTimeout, a_rows);
     return cudaGetLastError();
 }
 

@@ -111,11 +111,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 // One CTA: tile (blockIdx.x = n tile, blockIdx.y = split, blockIdx.z = m
 // tile) over K blocks [kb0, kb1) of the split; writes part[split][row][col]
-// for rows < m_rows (TMA fills rows past m_rows with zeros).  err: set to
+// for rows < m_rows (TMA fills rows past m_rows with zeros).  a_rows: rows
+// of each A tile loaded, 128, or 64 when m_rows <= 64: accumulator row r
+// depends only on A row r, so the unloaded upper half of the A tiles only
+// feeds accumulator rows that are never stored.  err: set to
 // err_code (if still 0) when any wait expires.
 __global__ void __launch_bounds__(kTcThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ TcMaps maps, int K, int N, int m_rows, int splits, float* part,
-                       int* err, int err_code) {
+                       int* err, int err_code, int a_rows) {
     extern __shared__ uint8_t tc_smem_raw[];
     // 1024-byte aligned stage area (swizzle atoms), barriers after it
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             uint8_t* st = base + s * kStageBytes;
-            tc_arrive_expect(&full[s], kStageBytes);
+            tc_arrive_expect(&full[s], 2u * (uint32_t)a_rows * kBlockK * 4u + 2u * kBBytes);
             tma_load_2d(st, &maps.a_hi, kb * kBlockK, m0, &full[s]);
             tma_load_2d(st + kABytes, &maps.a_lo, kb * kBlockK, m0, &full[s]);
             tma_load_2d(st + 2 * kABytes, &maps.b_hi, kb * kBlockK, n0, &full[s]);
