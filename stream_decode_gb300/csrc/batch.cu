@@ -52,7 +52,8 @@ __global__ void batch_embed_kernel(const float* __restrict__ packed, uint64_t wt
 
 constexpr int kBAttnThreads = 128;
 constexpr int kLanesPerKey = 8;
-constexpr int kKeySlots = kBAttnThreads / kLanesPerKey;  // keys in flight per pass
+constexpr int kKeySlots = kBAttnThreads / kLanesPerKey;  // keys per pass
+constexpr int kPassGroup = 4;                            // passes whose loads are issued together
 
 template <int N>
 __device__ __forceinline__ void load_n(const float* p, float (&r)[N]) {
@@ -106,32 +107,40 @@ __global__ void __launch_bounds__(kBAttnThreads) batch_attention_kernel(const fl
     for (int d = 0; d < DPL; ++d) o[d] = 0.0f;
     // Every lane of the block makes the same number of passes (the shuffles
     // below name the whole warp); a slot whose key of this pass lies past p
-    // takes part in the shuffles and skips the update.
-    for (int j0 = 0; j0 <= p; j0 += kKeySlots) {
-        const int j = j0 + slot;
-        const bool have = j <= p;
-        float k[DPL], v[DPL];
-        if (have) {
-            load_n<DPL>(kb + (size_t)j * row, k);
-            load_n<DPL>(kb + (size_t)j * row + D, v);
-        } else {
+    // takes part in the shuffles and skips the update.  The keys and values
+    // of kPassGroup passes are loaded before the first of them is used, so
+    // their cache round trips overlap.
+    for (int jg = 0; jg <= p; jg += kPassGroup * kKeySlots) {
+        float k[kPassGroup][DPL], v[kPassGroup][DPL];
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) k[d] = v[d] = 0.0f;
+        for (int g = 0; g < kPassGroup; ++g) {
+            const int j = jg + g * kKeySlots + slot;
+            if (j <= p) {
+                load_n<DPL>(kb + (size_t)j * row, k[g]);
+                load_n<DPL>(kb + (size_t)j * row + D, v[g]);
+            } else {
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) k[g][d] = v[g][d] = 0.0f;
+            }
         }
-        float s = 0.0f;
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) s = fmaf(q[d], k[d], s);
+        for (int g = 0; g < kPassGroup; ++g) {
+            const bool have = jg + g * kKeySlots + slot <= p;
+            float s = 0.0f;
 #pragma unroll
-        for (int off = 1; off < kLanesPerKey; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (have) {
-            s *= scale;
-            const float mn = fmaxf(m, s);
-            const float corr = expf(m - mn);  // 0 while m is -inf
-            const float e = expf(s - mn);
-            z = fmaf(z, corr, e);
+            for (int d = 0; d < DPL; ++d) s = fmaf(q[d], k[g][d], s);
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) o[d] = fmaf(o[d], corr, e * v[d]);
-            m = mn;
+            for (int off = 1; off < kLanesPerKey; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (have) {
+                s *= scale;
+                const float mn = fmaxf(m, s);
+                const float corr = expf(m - mn);  // 0 while m is -inf
+                const float e = expf(s - mn);
+                z = fmaf(z, corr, e);
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) o[d] = fmaf(o[d], corr, e * v[g][d]);
+                m = mn;
+            }
         }
     }
     if (e8 == 0) {
