@@ -144,3 +144,10 @@ def test_batch_validation(g):
     bt.close()
     mq.close()
     model.close()
+
+
+def test_124m_long_context_batch(g, oracle, w124m):
+    """The long-context configuration (max_pos 1024): three sessions at
+    cached lengths 600, 900 and 1020 (seeded synthetic caches), two steps
+    each, so the decode attention runs up to 64 passes of 16 keys."""
+    _check_batch(g, oracle, synth.GPT2_124M_LONG, w124m, 3, 2, [600, 900, 1020])
