@@ -29,7 +29,7 @@ namespace gpt2 {
 namespace {
 
 constexpr int kAttnWarps = 8;
-constexpr int kAttnRows = 16;          // query rows per block (two per warp)
+constexpr int kAttnRows = 8;           // query rows per block (one per warp)
 constexpr int kMaxPrefillKeys = 1024;  // longest prompt (the keys of a block are staged in chunks of kKeyTile)
 constexpr int kKeyTile = 64;
 
