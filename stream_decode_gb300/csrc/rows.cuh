@@ -52,10 +52,11 @@ __global__ void embed_kernel(const float* __restrict__ packed, uint64_t wte_off,
         X[(size_t)i * D + j] = __fadd_rn(packed[wte_off + (uint64_t)t * D + j], packed[wpe_off + (uint64_t)i * D + j]);
 }
 
-constexpr int kLnThreads = 128;
+constexpr int kLnThreads = 256;
 
 // Y = LN(X) (mean, then the biased variance of the deviations; eps 1e-5)
-// and its TF32 remainder, one block per row (D <= 1024: 8 values a thread).
+// and its TF32 remainder, one block of 256 threads per row (up to 8 values a
+// thread: D <= 2048).
 // With part != nullptr the row is first completed as the residual add of a
 // projection: X[i][j] += (sum over splits s = 0, 1, ... of part[s][i][j]) +
 // bias[j], in the split reduce's order, and written back.
