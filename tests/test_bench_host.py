@@ -63,3 +63,20 @@ def test_traffic_record_lookup():
         assert e["dram_bytes_per_launch_112_steps"] == e["dram_bytes_read"] + e["dram_bytes_write"]
         assert bench.traffic_from_profiles(e["kernel_sha256"], q) == e["dram_bytes_per_launch_112_steps"]
         assert bench.traffic_from_profiles("0" * 64, q) is None
+
+
+def test_byte_components_match_the_printed_sizes():
+    """The parts of the bench's byte count against the sizes the gpt2.s page
+    prints for the same tensors (MB = 10^6 bytes, matched to the printed digits)."""
+    with open(os.path.join(bench.ROOT, "tests", "golden", "page_identities.json")) as f:
+        g = json.load(f)
+    d, F, L, V = S.d_model, S.d_ff, S.n_layer, S.vocab
+    blocks = 4 * L * (d * 3 * d + d * d + d * F + F * d)
+    assert round(blocks / 1e6) == g["block_matrices_mb"]["value"]
+    padded = (V + 63) // 64 * 64  # the vocabulary padded to whole 64-row tiles
+    assert padded == g["wte_padded_rows"]["value"]
+    assert int(4 * padded * d / 1e6) == g["wte_tiled_mb"]["value"]
+    assert int(S.n_pos * KV_ROW / 1e6) == g["kv_cache_mb_1024"]["value"]
+    # the f32 step reads exactly these blocks plus the unpadded wte and the small tensors
+    small = bench.step_bytes(S, "f32", 0) - blocks - 4 * V * d - KV_ROW - 4 * V
+    assert small == 4 * (L * (9 * d + F) + 2 * d + d)  # LN, biases, final LN, one wpe row
