@@ -134,6 +134,16 @@ void gpt2_model_destroy(gpt2_model* model);
  * binary32 model. */
 gpt2_status gpt2_model_read_q8(gpt2_model* model, int index, int8_t* q_host, float* s_host);
 
+/* Which kernel runs this model's decode steps: 1 the cluster step kernel
+ * (binary32 and binary16 models: thread-block clusters that complete each
+ * projection's split-K partials in distributed shared memory), 0 the
+ * per-phase step kernel (int8 models, or any model created while the
+ * environment variable GPT2_STEP_KERNEL was "legacy").  For the cluster
+ * kernel *clusters and *cluster_size receive its grid (clusters x CTAs per
+ * cluster); for the other they receive 0 and its CTA count.  Either pointer
+ * may be NULL.  Returns -1 for a NULL model. */
+int gpt2_model_step_kernel(const gpt2_model* model, uint32_t* clusters, uint32_t* cluster_size);
+
 /* A session owns a device KV cache of max_pos positions and the step
  * kernel's scratch; it starts empty at position 0.  Synchronous. */
 gpt2_status gpt2_session_create(gpt2_model* model, gpt2_session** out);
@@ -287,7 +297,22 @@ gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
  * complete, when its projection started (after LayerNorm / head merge /
  * quantization), when thread 0's projection work ended and when its outputs
  * were stored; [7] clock64 when the phase's first weight chunk was known to
- * have landed.  Attention phases fill [0..6] only.  Pass NULL to stop. */
+ * have landed.  Attention phases fill [0..6] only.
+ * Models on the cluster step kernel (gpt2_model_step_kernel == 1) use
+ * another layout: d_stamps holds 8 + grid_ctas * (16*n_layer + 4) u64.
+ * Words 0..5 receive, when a bounded wait of the run gives up, the wait's
+ * kind (1 ring chunk, 2 distributed-shared-memory gather, 3 tagged words,
+ * 4 greedy partials), the CTA, the step, the layer and two words about what
+ * was awaited (for kind 4: (partial index << 32 | tag), and the word last
+ * seen); all 0 when none gave up.  Then per CTA (CTA-major), for step 0,
+ * per layer 16 words: the globaltimer (ns) when the block input was formed,
+ * QKV partials done, q/k/v gathered, attention done, head outputs gathered,
+ * out-projection partials stored, attention residual formed, FC partials
+ * done, GELU outputs gathered, MLP partials stored (a CTA of a cluster
+ * without a head leaves the second to sixth at 0); then for the QKV,
+ * out-projection, FC and MLP shares of warp 0, (clock64 cycles waiting for
+ * weight chunks << 32 | cycles in all); 2 words unused.  Then final input
+ * formed, gathered, LN_f done, vocabulary rows done.  Pass NULL to stop. */
 gpt2_status gpt2_session_set_timing(gpt2_session* session, uint64_t* d_stamps);
 
 /* Debug/test: make the next run's CTA 0 skip publishing one phase so that
@@ -313,13 +338,19 @@ gpt2_status gpt2_session_inject_stall(gpt2_session* session, uint32_t phase, uin
  *   d_logits      device output of vocab floats, or NULL;
  *   d_next_token  device output of the greedy choice, or NULL; it reads
  *                 0xFFFFFFFF after the step if a logit was not finite or the
- *                 step gave up on a device-side wait.
- * The step kernel's scratch is a file-scope static device array of 256 KiB
- * (GPT-2 124M on 152 CTAs uses about 70 KB).  Every GPU that loads the
- * library holds it until the process exits.  A model whose scratch would
- * not fit is rejected with GPT2_ERR_SCRATCH before any device work.  The
- * first call on each device looks the array's device address up (once, with
- * that device current); make that first call before any stream capture.
+ *                 step gave up on a device-side wait.  It is the call's only
+ *                 failure signal (the host reads no status back): pass it
+ *                 whenever a failed step must be detected; with NULL a
+ *                 failed step leaves d_logits partly written, unnoticed.
+ * The step kernel's scratch is a file-scope static device array of 512 KiB
+ * (GPT-2 124M uses about 360 KB on the cluster step kernel, 70 KB on the
+ * per-phase kernel).  Every GPU that loads the library's device code holds
+ * it until the process exits.  A model whose scratch would not fit is
+ * rejected with GPT2_ERR_SCRATCH before any device work.  gpt2_model_create
+ * loads the array's module and looks its device address up on the device
+ * that is current (CUDA may load modules lazily, so this is where the array
+ * comes into being); a call on a device where no model was created does that
+ * set-up itself, so make such a first call before any stream capture.
  * No call allocates: no cudaMalloc, no cudaFree, no allocating library
  * routine.  All calls share the one array, and it keeps the previous call's
  * contents.  Each call clears, on `stream`, what must start at zero (phase

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgpt2gb.so")
-SOURCES = ["api.cu", "decode.cu", "repack.cu", "noalloc.cu", "prefill.cu", "batch.cu"]
+SOURCES = ["api.cu", "decode.cu", "cstep.cu", "repack.cu", "noalloc.cu", "prefill.cu", "batch.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

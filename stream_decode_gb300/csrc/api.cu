@@ -26,6 +26,12 @@ cudaError_t fold_rows(const uint8_t* rows, int K, int N, int wf, const float* g,
 cudaError_t launch_project(const uint8_t* rows, int K, int N, int wq, const float* x, const float* bias, float* y,
                            int stream, cudaStream_t st);
 cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfinite, cudaStream_t st);
+bool cstep_supported(int D, int FF, int DH, int wf);
+cudaError_t cgeo_make(int L, int D, int H, int FF, int wf, int want_ctas, CGeo* out);
+cudaError_t cstream_build(const uint8_t* wstream, uint64_t layer_bytes, const uint64_t mat_off[4], int L, int D,
+                          int H, int FF, int wf, const CGeo& g, uint8_t* dst, cudaStream_t st);
+cudaError_t launch_cstep(const CPlan& P, int wf, cudaStream_t stream);
+bool noalloc_prepare();
 }  // namespace gpt2
 
 using namespace gpt2;
@@ -33,8 +39,10 @@ using namespace gpt2;
 struct gpt2_session {
     gpt2_model* m;
     float* d_cache;
-    unsigned char* d_scratch;  // ScratchLayout: status words, last token, tagged exchange buffers
+    unsigned char* d_scratch;  // ScratchLayout or CScratch: status words, last token, tagged exchange buffers
     ScratchLayout lay;
+    CScratch clay;
+    size_t xoff, xtotal;       // the tagged exchange words: [xoff, xtotal) of d_scratch
     int* d_words;  // [0] status, [1] abort
     uint32_t* d_last_token;
     float* d_logits;       // session-owned logits for gpt2_session_step_host
@@ -132,7 +140,25 @@ void fill_plan(const gpt2_session* s, StepPlan& P) {
     P.pace_ns = kDefaultPaceNs;
 }
 
-unsigned phases_per_step(const gpt2_model* m) { return 5u * m->cfg.n_layer + 1u; }
+unsigned phases_per_step(const gpt2_model* m) {
+    return m->ckern ? 2u * m->cfg.n_layer + 1u : 5u * m->cfg.n_layer + 1u;
+}
+
+// The cluster kernel's plan: the shared StepPlan fields, its geometry and
+// its exchange buffers.
+void fill_cplan(const gpt2_model* m, unsigned char* scratch, const CScratch& k, float* cache, CPlan& C) {
+    C.g = m->cg;
+    C.cstream = m->d_cstream;
+    C.partO = reinterpret_cast<uint64_t*>(scratch + k.partO);
+    C.partP = reinterpret_cast<uint64_t*>(scratch + k.partP);
+    StepPlan& P = C.s;
+    P.xa = P.xb = P.qkv = P.u = P.attn_part = nullptr;
+    P.arg_part = reinterpret_cast<uint64_t*>(scratch + k.arg);
+    P.status = reinterpret_cast<int*>(scratch + k.words);
+    P.abort_flag = reinterpret_cast<int*>(scratch + k.words) + 1;
+    P.last_token = reinterpret_cast<uint32_t*>(scratch + k.last_token);
+    P.cache = cache;
+}
 
 // Enqueue one run; the caller has validated sizes.
 gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t token0, uint32_t n_steps,
@@ -142,7 +168,7 @@ gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t t
     const unsigned need = n_steps * phases_per_step(s->m);
     if (s->epoch > (1u << 30)) {
         // tags restart: clear every exchanged word so no stale tag can match
-        cudaError_t e = cudaMemsetAsync(s->d_scratch + s->lay.xa, 0, s->lay.total - s->lay.xa, stream);
+        cudaError_t e = cudaMemsetAsync(s->d_scratch + s->xoff, 0, s->xtotal - s->xoff, stream);
         if (e != cudaSuccess) return cuda_status(e);
         s->epoch = 0;
     }
@@ -162,7 +188,16 @@ gpt2_status enqueue_run(gpt2_session* s, const uint32_t* d_tokens_in, uint32_t t
     if (pf) P.prefetch_chunks = atoi(pf);
     const char* pace = getenv("GPT2_PACE_NS");
     if (pace) P.pace_ns = (uint32_t)atoi(pace);
-    cudaError_t e = launch_step(P, s->m->wfmt, stream);
+    cudaError_t e;
+    if (s->m->ckern) {
+        CPlan C;
+        memset(&C, 0, sizeof(C));
+        C.s = P;
+        fill_cplan(s->m, s->d_scratch, s->clay, s->d_cache, C);
+        e = launch_cstep(C, s->m->wfmt, stream);
+    } else {
+        e = launch_step(P, s->m->wfmt, stream);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     s->trace_next = nullptr;
     s->timing_next = nullptr;
@@ -294,7 +329,22 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
             CK(cudaMalloc(&m->d_vocab, (uint64_t)cfg->vocab * rbd));
             CK(rows_to_f16(m->d_packed + m->wte_off, m->d_vocab, (size_t)cfg->vocab * D, 0));
         }
+        // decode steps: the cluster step kernel where it supports the shape
+        // and weight format (GPT2_STEP_KERNEL=legacy keeps step_kernel)
+        const char* sk = getenv("GPT2_STEP_KERNEL");
+        const bool legacy = sk && strcmp(sk, "legacy") == 0;
+        if (!legacy && cstep_supported(D, FF, D / (int)cfg->n_head, wfmt)) {
+            CK(cgeo_make(L, D, (int)cfg->n_head, FF, wfmt, grid_ctas, &m->cg));
+            CK(cudaMalloc(&m->d_cstream, m->cg.layer_bytes * L));
+            CK(cstream_build(m->d_wstream, m->layer_bytes, m->mat_off, L, D, (int)cfg->n_head, FF, wfmt, m->cg,
+                             m->d_cstream, 0));
+            m->ckern = 1;
+            m->G = m->cg.G;
+        }
         CK(cudaDeviceSynchronize());
+        // the no-allocation entry point's scratch array, set up here so that
+        // its calls do none
+        if (!noalloc_prepare()) CK(cudaErrorInitializationError);
     }
     *out = m;
     return GPT2_OK;
@@ -311,7 +361,15 @@ void gpt2_model_destroy(gpt2_model* m) {
     cudaFree(m->d_fold);
     cudaFree(m->d_wlo);
     cudaFree(m->d_wte_lo);
+    cudaFree(m->d_cstream);
     delete m;
+}
+
+int gpt2_model_step_kernel(const gpt2_model* m, uint32_t* clusters, uint32_t* cluster_size) {
+    if (!m) return -1;
+    if (clusters) *clusters = m->ckern ? (uint32_t)m->cg.NC : 0u;
+    if (cluster_size) *cluster_size = m->ckern ? (uint32_t)m->cg.CS : (uint32_t)m->G;
+    return m->ckern;
 }
 
 gpt2_status gpt2_model_read_q8(gpt2_model* m, int index, int8_t* q_host, float* s_host) {
@@ -352,12 +410,22 @@ gpt2_status gpt2_session_create(gpt2_model* m, gpt2_session** out) {
     {
         const gpt2_config& c = m->cfg;
         s->lay = scratch_layout((int)c.d_model, (int)c.n_head, (int)c.d_ff, m->G);
+        size_t words_off = s->lay.words, last_off = s->lay.last_token;
+        s->xoff = s->lay.xa;
+        s->xtotal = s->lay.total;
+        if (m->ckern) {
+            s->clay = cscratch_layout((int)c.d_model, (int)c.n_head, m->cg.NC, m->cg.G);
+            words_off = s->clay.words;
+            last_off = s->clay.last_token;
+            s->xoff = s->clay.partO;
+            s->xtotal = s->clay.total;
+        }
         CK(cudaMalloc(&s->d_cache, sizeof(float) * row_words(&c) * c.max_pos));
         CK(cudaMemset(s->d_cache, 0, sizeof(float) * row_words(&c) * c.max_pos));
-        CK(cudaMalloc(&s->d_scratch, s->lay.total));
-        CK(cudaMemset(s->d_scratch, 0, s->lay.total));
-        s->d_words = reinterpret_cast<int*>(s->d_scratch + s->lay.words);
-        s->d_last_token = reinterpret_cast<uint32_t*>(s->d_scratch + s->lay.last_token);
+        CK(cudaMalloc(&s->d_scratch, s->xtotal));
+        CK(cudaMemset(s->d_scratch, 0, s->xtotal));
+        s->d_words = reinterpret_cast<int*>(s->d_scratch + words_off);
+        s->d_last_token = reinterpret_cast<uint32_t*>(s->d_scratch + last_off);
         CK(cudaMemset(s->d_last_token, 0xFF, sizeof(uint32_t) * 2));
         CK(cudaMalloc(&s->d_logits, sizeof(float) * c.vocab));
         CK(cudaMalloc(&s->d_next, sizeof(uint32_t)));
@@ -399,7 +467,7 @@ gpt2_status gpt2_session_sync(gpt2_session* s) {
     if (words[0] == 0 && words[1] == 0) return GPT2_OK;
     // A failed run leaves exchanged words mid-sequence: clear them and restart the tags.
     e = cudaMemset(s->d_words, 0, sizeof(int) * 4);
-    if (e == cudaSuccess) e = cudaMemset(s->d_scratch + s->lay.xa, 0, s->lay.total - s->lay.xa);
+    if (e == cudaSuccess) e = cudaMemset(s->d_scratch + s->xoff, 0, s->xtotal - s->xoff);
     if (e != cudaSuccess) return cuda_status(e);
     s->epoch = 0;
     return words[0] ? (gpt2_status)words[0] : GPT2_ERR_TIMEOUT;

@@ -1,0 +1,1453 @@
+// cstep.cu -- the cluster step kernel: one cooperative launch of NC thread-
+// block clusters of CS CTAs runs a run of cached GPT-2 steps (LeanExe GPT-2
+// README, cachedStep paragraph; model paragraph for the block order).
+//
+// Work split (cstep.cuh has the geometry): rank r of each cluster owns the
+// column slice [r*SW, (r+1)*SW) of the model width.  Every projection is
+// split along its INPUT dimension by slice inside a cluster, and the slices'
+// partial dot products are completed by one all-gather over distributed
+// shared memory (st.async with mbarrier transaction counts).  The heads and
+// FC rows are split across clusters; the out-projection and the MLP
+// projection are split-K partials per head / per cluster, summed by their
+// consumers in a fixed order.  Hence per layer:
+//   A  [clusters with a head]  slice of x formed from the MLP partials ->
+//      LN1-folded QKV partials over the slice -> all-gather (q, k, v) ->
+//      attention over this CTA's keys -> all-gather (max, sum, weighted
+//      values) -> merged head output -> this CTA's SW rows of the head's
+//      out-projection partial -> tagged words.
+//   B  [every cluster]  slice of x formed from the heads' partials ->
+//      LN2-folded FC partials over the slice -> all-gather -> GELU of the
+//      cluster's FC rows -> this CTA's SW rows of the MLP partial over those
+//      FC rows -> tagged words.
+// The vocabulary rows are split across all CTAs; the greedy choice is
+// reduced at the start of the next step (one release/acquire per step, which
+// also orders the KV-cache stores before the next step's attention).
+//
+// LayerNorm is folded into the projection that follows it,
+//   y_j = rstd * (sum_i W_ji g_i (x_i - s) - (mean - s) c_j) + d_j,
+// with c_j = sum_i W_ji g_i and d_j = bias_j + sum_i W_ji b_i made at load
+// time.  The shift s is a mean every CTA already holds (the embedding's exact
+// mean, then the previous LayerNorm's mean), so the dot products never
+// carry the residual's common offset; the variance comes from each slice's
+// two-pass sums of squares around its own mean, merged pairwise (Chan et
+// al.'s update), so no E[x^2] - mean^2 cancellation occurs.
+//
+// One producer warp per CTA streams the CTA's parts of every weight matrix,
+// in step order, through a shared-memory ring (cp.async.bulk, mbarriers).
+// Every wait is bounded by a wall-clock limit; a CTA that gives up records
+// GPT2_ERR_TIMEOUT, raises the grid's abort word and leaves its loops, and
+// all CTAs of a cluster meet at a final cluster barrier so that no CTA exits
+// while a peer may still write into its shared memory.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "cstep.cuh"
+
+namespace gpt2 {
+
+namespace {
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// 16 bytes into a peer's shared memory, completing on the peer's mbarrier.
+__device__ __forceinline__ void st_async4(uint32_t raddr, float4 v, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     raddr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Named barrier over the consumer warps only.
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory"); }
+
+// ---------------------------------------------------------------- math
+__device__ __forceinline__ float cgelu(float x) {
+    const float inner = 0.7978845608f * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + tanhf(inner));
+}
+
+template <int N>
+__device__ __forceinline__ float transpose_sum(float (&v)[N], int lane) {
+#pragma unroll
+    for (int o = 16; o >= N; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+#pragma unroll
+    for (int o = N / 2; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+template <int WF>
+__device__ __forceinline__ float4 w4(const uint8_t* row, int col) {
+    if constexpr (WF == kWF16) {
+        const uint2 h = *reinterpret_cast<const uint2*>(row + 8u * (uint32_t)col);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    } else {
+        return *reinterpret_cast<const float4*>(row + 16u * (uint32_t)col);
+    }
+}
+
+__device__ __forceinline__ float4 lds4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+
+// Four consecutive weights at shared address a, as binary32.
+template <int WF>
+__device__ __forceinline__ float4 ldsw(uint32_t a) {
+    if constexpr (WF == kWF16) {
+        uint32_t lo, hi;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(a));
+        const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+        const float2 q = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        return make_float4(p.x, p.y, q.x, q.y);
+    } else {
+        return lds4(a);
+    }
+}
+
+__device__ __forceinline__ float dot4(float a, float4 w, float4 x) {
+    a = fmaf(x.x, w.x, a);
+    a = fmaf(x.y, w.y, a);
+    a = fmaf(x.z, w.z, a);
+    return fmaf(x.w, w.w, a);
+}
+
+// Bytes of one 4-weight unit of the cluster stream.
+template <int WF>
+__host__ __device__ constexpr uint32_t unit_bytes() { return WF == kWF16 ? 8u : 16u; }
+
+// One ring chunk of R <= 32 rows of the cluster stream, stored interleaved
+// by 4-weight units (unit c of row i at (c * R + i) * unit bytes), against x
+// (W4 float4s at shared address x): lane i < R returns row i's dot product.
+// A lane walks its own row, so no reduction across lanes is needed; the
+// lanes of a warp read consecutive units (no bank conflicts) and the input
+// unit is a broadcast.
+template <int WF>
+__device__ __forceinline__ float chunk_rows(uint32_t w, int R, int W4, uint32_t x, int lane) {
+    constexpr uint32_t UB = unit_bytes<WF>();
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    if (lane < R) {
+        const uint32_t step = (uint32_t)R * UB;
+        uint32_t wa = w + (uint32_t)lane * UB;
+        int c = 0;
+        for (; c + 4 <= W4; c += 4, wa += 4 * step) {
+            const float4 w0 = ldsw<WF>(wa), w1 = ldsw<WF>(wa + step), w2 = ldsw<WF>(wa + 2 * step),
+                         w3 = ldsw<WF>(wa + 3 * step);
+            const uint32_t xa = x + 16u * (uint32_t)c;
+            a0 = dot4(a0, w0, lds4(xa));
+            a1 = dot4(a1, w1, lds4(xa + 16));
+            a2 = dot4(a2, w2, lds4(xa + 32));
+            a3 = dot4(a3, w3, lds4(xa + 48));
+        }
+        for (; c < W4; ++c, wa += step) a0 = dot4(a0, ldsw<WF>(wa), lds4(x + 16u * (uint32_t)c));
+    }
+    return (a0 + a1) + (a2 + a3);
+}
+
+// NR consecutive K-major rows (pitch pb bytes, W4 float4 columns each) in
+// shared memory against x (W4 float4s): lanes stride the columns, then one
+// transpose-reduction; lane i < n returns row i's total.  For the long
+// vocabulary rows.
+template <int NR, int W4, int WF>
+__device__ __forceinline__ float long_rows(uint32_t w, uint32_t pb, int n, uint32_t x, int lane) {
+    constexpr uint32_t UB = unit_bytes<WF>();
+    float acc[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int t = 0; t < (W4 + 31) / 32; ++t) {
+        const int cc = lane + 32 * t;
+        if ((W4 % 32) == 0 || cc < W4) {
+            const float4 xv = lds4(x + 16u * (uint32_t)cc);
+#pragma unroll
+            for (int i = 0; i < NR; ++i)
+                if (i < n) acc[i] = dot4(acc[i], ldsw<WF>(w + (uint32_t)i * pb + UB * (uint32_t)cc), xv);
+        }
+    }
+    return transpose_sum<NR>(acc, lane);
+}
+
+__device__ __forceinline__ void crecord_error(const StepPlan& P, int code) {
+    atomicCAS(P.status, 0, code);
+    atomicExch(P.abort_flag, 1);
+}
+
+// Greedy choice order: larger value first, then lower index.
+struct Best {
+    float v;
+    unsigned i;
+    int nf;
+};
+__device__ __forceinline__ bool better(float v, unsigned i, float bv, unsigned bi) {
+    return v > bv || (v == bv && i < bi);
+}
+__device__ __forceinline__ void best_update(Best& b, float v, unsigned j) {
+    if (!isfinite(v)) b.nf = 1;
+    else if (better(v, j, b.v, b.i)) { b.v = v; b.i = j; }
+}
+__device__ __forceinline__ void best_merge(Best& b, float v, unsigned i, int nf) {
+    b.nf |= nf;
+    if (better(v, i, b.v, b.i)) { b.v = v; b.i = i; }
+}
+__device__ __forceinline__ void best_warp(Best& b) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, b.v, o);
+        const unsigned oi = __shfl_xor_sync(0xffffffffu, b.i, o);
+        const int onf = __shfl_xor_sync(0xffffffffu, b.nf, o);
+        best_merge(b, ov, oi, onf);
+    }
+}
+
+// Cold path of a bounded wait that gave up: records the timeout and, when
+// the run is profiled, which wait, CTA, step and layer (first one only).
+__device__ __noinline__ void cwait_gave_up(const StepPlan& P, int kind, int cta, int step, int layer, uint64_t what,
+                                          uint64_t seen) {
+    if (P.timing && atomicCAS(reinterpret_cast<unsigned long long*>(P.timing), 0ull, (unsigned long long)kind) == 0ull) {
+        P.timing[1] = (uint64_t)cta;
+        P.timing[2] = (uint64_t)step;
+        P.timing[3] = (uint64_t)layer;
+        P.timing[4] = what;
+        P.timing[5] = seen;
+    }
+    crecord_error(P, kDevTimeout);
+}
+
+// Activation trace (step 0 of a traced run): copies, and a LayerNorm output
+// (x - mean) * rstd * g + b of a slice; out of line, off the hot path.
+__device__ __noinline__ void ctrace_copy(float* dst, const float* src, int n, int tid) {
+    for (int i = tid; i < n; i += kCWarps * 32) dst[i] = src[i];
+}
+__device__ __noinline__ void ctrace_ln(float* dst, const float* xs, float mean, float rstd, const float* g,
+                                       const float* b, int n, int tid) {
+    for (int i = tid; i < n; i += kCWarps * 32) dst[i] = fmaf((xs[i] - mean) * rstd, __ldg(g + i), __ldg(b + i));
+}
+
+// A contiguous run of weight rows that one CTA streams: n rows of pb bytes,
+// rpc rows per ring chunk.
+struct Share {
+    const uint8_t* base;
+    uint32_t pb;
+    int n, rpc, nch;
+};
+__device__ __forceinline__ Share make_share(const uint8_t* base, uint32_t pb, int n) {
+    Share s;
+    s.base = base;
+    s.pb = pb;
+    s.n = n;
+    s.rpc = (int)(kCSlotBytes / pb);
+    if (s.rpc > 32) s.rpc = 32;  // a chunk's rows are one warp's lanes
+    if (s.rpc > n) s.rpc = n > 0 ? n : 1;
+    s.nch = n > 0 ? (n + s.rpc - 1) / s.rpc : 0;
+    return s;
+}
+
+// Stops checking the grid's abort word until a wait has lasted this long (a
+// word polled by every thread of every CTA would be a hot L2 line).
+constexpr uint64_t kCAbortCheckNs = 20000;
+
+}  // namespace
+
+// Phases with tagged outputs per step: per layer A (out-projection partials)
+// and B (MLP partials); then the greedy partials.
+__host__ __device__ inline int cphases_per_step(int L) { return 2 * L + 1; }
+
+template <int D, int FF, int DH, int WF>
+__global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_constant__ CPlan plan) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const CSmem lay = csmem_layout(D, DH, plan.g.CS, plan.g.SW, plan.g.nfc_max, plan.g.slots);
+    {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&plan);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(smem + lay.plan);
+        static_assert(sizeof(CPlan) % 4 == 0, "plan copies as words");
+        for (int i = threadIdx.x; i < (int)(sizeof(CPlan) / 4); i += blockDim.x) dst[i] = src[i];
+    }
+    __syncthreads();
+    const CPlan& CP = *reinterpret_cast<const CPlan*>(smem + lay.plan);
+    const StepPlan& P = CP.s;
+    const CGeo& GG = CP.g;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = blockIdx.x;
+    const int CS = GG.CS, SW = GG.SW, NSL = GG.slots;
+    const int r = (int)cluster_rank();
+    const int c = cta / CS;
+    const int L = P.L, H = P.H;
+    const int nh = cg_heads(GG, H, c);
+    const int f0 = GG.fc0[c], nfc = GG.fc0[c + 1] - GG.fc0[c];
+    const int nfc4 = (nfc + 3) & ~3;
+    const int col0 = r * SW;
+    constexpr int NT = kCWarps * 32;
+    const uint64_t head_bytes = cg_head_bytes(GG, DH);
+    const uint32_t wb = (uint32_t)GG.wb;
+
+    uint8_t* ring = smem + lay.ring;
+    const uint32_t ring_s = smem_addr(ring);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + lay.empty);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);  // mA[2], mT[2], mB[2], mX
+    float* gA = reinterpret_cast<float*>(smem + lay.gA);
+    float* gT = reinterpret_cast<float*>(smem + lay.gT);
+    float* gB = reinterpret_cast<float*>(smem + lay.gB);
+    float* gX = reinterpret_cast<float*>(smem + lay.gX);
+    float* pa = reinterpret_cast<float*>(smem + lay.pa);
+    float* qkv = reinterpret_cast<float*>(smem + lay.qkv);
+    float* oh = reinterpret_cast<float*>(smem + lay.oh);
+    float* uu = reinterpret_cast<float*>(smem + lay.uu);
+    float* xs = reinterpret_cast<float*>(smem + lay.xs);
+    float* xin = reinterpret_cast<float*>(smem + lay.xin);
+    float* xf = reinterpret_cast<float*>(smem + lay.xf);
+    float* stage = reinterpret_cast<float*>(smem + lay.stage);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + lay.misc);
+    volatile int* s_fail = s_abort + 1;  // two slots, alternating per agreement point
+    unsigned* s_tok = reinterpret_cast<unsigned*>(smem + lay.misc) + 4;
+    volatile int* s_nf = s_abort + 5;
+    float* s_red = reinterpret_cast<float*>(smem + lay.misc) + 8;   // [warps] block reductions
+    float* s_arg = reinterpret_cast<float*>(smem + lay.misc) + 24;  // [warps][3]
+    float* s_stA = reinterpret_cast<float*>(smem + lay.misc) + 48;  // stage A slice (mean, M2)
+
+    if (tid == 0) {
+        for (int i = 0; i < NSL; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
+        // Every gather barrier is armed for its first use before any peer can
+        // write into this CTA (the cluster barrier below), and re-armed for
+        // its next use as soon as a use completes (gather_wait), which is
+        // always before a peer can send that next use's data: a barrier is
+        // never armed after data for its phase has arrived.
+        {
+            const int nfc4_ = ((plan.g.fc0[blockIdx.x / plan.g.CS + 1] - plan.g.fc0[blockIdx.x / plan.g.CS]) + 3) & ~3;
+            for (int i = 0; i < 2; ++i) {
+                mbar_arrive_expect_tx(&bars[0 + i], (uint32_t)(plan.g.CS * (3 * DH + 4) * 4));
+                mbar_arrive_expect_tx(&bars[2 + i], (uint32_t)(plan.g.CS * (DH + 4) * 4));
+                mbar_arrive_expect_tx(&bars[4 + i], (uint32_t)(plan.g.CS * (nfc4_ + 4) * 4));
+            }
+            mbar_arrive_expect_tx(&bars[6], (uint32_t)(D * 4));
+        }
+        *s_abort = ld_volatile_int(P.abort_flag);
+        s_fail[0] = 0;
+        s_fail[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // every CTA's barriers are initialised before any peer writes into them
+    cluster_barrier();
+
+    // The share sequence of a step, identical on both sides of the ring:
+    // per layer, per head slot k: QKV part, out-projection part; then the
+    // FC part and the MLP part; then the vocabulary rows.
+    auto part_base = [&](int l) -> const uint8_t* {
+        return CP.cstream + (uint64_t)l * GG.layer_bytes + GG.seg[c] + (uint64_t)r * GG.cta_bytes[c];
+    };
+    auto share_qkv = [&](int l, int k) { return make_share(part_base(l) + k * head_bytes, (uint32_t)SW * wb, 3 * DH); };
+    auto share_wo = [&](int l, int k) {
+        return make_share(part_base(l) + k * head_bytes + (uint64_t)3 * DH * SW * wb, (uint32_t)DH * wb, SW);
+    };
+    auto share_fc = [&](int l) { return make_share(part_base(l) + nh * head_bytes, (uint32_t)SW * wb, nfc); };
+    auto share_wp = [&](int l) {
+        return make_share(part_base(l) + nh * head_bytes + (uint64_t)nfc * SW * wb, (uint32_t)nfc * wb, SW);
+    };
+    const int V = P.V;
+    const int v0 = (int)(((long long)cta * V) / GG.G), v1 = (int)(((long long)(cta + 1) * V) / GG.G);
+    const uint32_t rbv = (uint32_t)row_bytes(D, WF);
+    // vocabulary rows per chunk: a power of two (its transpose-reduction), at most 32
+    constexpr int kVocabFit = kCSlotBytes / row_bytes(D, WF);
+    constexpr int kVocabRows = kVocabFit >= 32 ? 32 : kVocabFit >= 16 ? 16 : kVocabFit >= 8 ? 8 : kVocabFit >= 4 ? 4
+                                                                                              : kVocabFit >= 2 ? 2 : 1;
+    auto share_vocab = [&]() {
+        Share sh = make_share(P.vocab + (uint64_t)v0 * rbv, rbv, v1 - v0);
+        sh.rpc = kVocabRows < sh.n ? kVocabRows : (sh.n > 0 ? sh.n : 1);
+        sh.nch = sh.n > 0 ? (sh.n + sh.rpc - 1) / sh.rpc : 0;
+        return sh;
+    };
+
+    // ================================================= producer warp
+    if (warp == kCWarps) {
+        if (lane == 0 && !*s_abort) {
+            const uint64_t pol = policy_evict_first();
+            uint32_t gi = 0;
+            bool stop = false;
+            // Pacing: the block-matrix chunks are issued at least pace_ns per
+            // 12 KB apart (scaled by the chunk's bytes).  Without it, the
+            // slots a stage releases are refilled by every CTA at the same
+            // moment, and that burst queues in front of the latency-bound
+            // loads of the exchanges.  The vocabulary streams unpaced.
+            uint64_t next_issue = 0;
+            auto issue = [&](const Share& sh, bool paced) {
+                for (int k = 0; k < sh.nch && !stop; ++k) {
+                    const int slot = (int)(gi % (uint32_t)NSL);
+                    const uint32_t fill = gi / (uint32_t)NSL;
+                    if (fill > 0) {
+                        uint64_t t0 = 0;
+                        uint32_t spins = 0;
+                        while (!mbar_try_wait(&empty[slot], (fill - 1) & 1)) {
+                            if (*s_abort) { stop = true; break; }
+                            if ((++spins & 255) == 0) {
+                                const uint64_t now = globaltimer_ns();
+                                if (t0 == 0) t0 = now;
+                                else if (now - t0 > 2 * P.wait_limit_ns) {
+                                    crecord_error(P, kDevTimeout);
+                                    stop = true;
+                                    break;
+                                }
+                            }
+                        }
+                        if (stop) break;
+                    }
+                    const int r0 = k * sh.rpc;
+                    const int n = min(sh.rpc, sh.n - r0);
+                    const uint32_t bytes = (uint32_t)n * sh.pb;
+                    if (paced && P.pace_ns != 0) {
+                        uint64_t now = globaltimer_ns();
+                        while (now < next_issue && !*s_abort) {
+                            __nanosleep(32);
+                            now = globaltimer_ns();
+                        }
+                        next_issue = (now > next_issue ? now : next_issue) +
+                                     (uint64_t)P.pace_ns * bytes / (uint64_t)kCSlotBytes;
+                    }
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    bulk_load(ring + (size_t)slot * kCSlotBytes, sh.base + (uint64_t)r0 * sh.pb, bytes, &full[slot], pol);
+                    ++gi;
+                }
+            };
+            for (int s = 0; s < P.n_steps && !stop; ++s) {
+                for (int l = 0; l < L && !stop; ++l) {
+                    for (int k = 0; k < nh; ++k) {
+                        issue(share_qkv(l, k), true);
+                        issue(share_wo(l, k), true);
+                    }
+                    issue(share_fc(l), true);
+                    issue(share_wp(l), true);
+                }
+                issue(share_vocab(), false);
+            }
+            // every issued copy lands before this thread leaves
+            const uint32_t nslot = gi < (uint32_t)NSL ? gi : (uint32_t)NSL;
+            for (uint32_t i = 0; i < nslot; ++i) {
+                const uint32_t last = gi - 1 - i;
+                const int slot = (int)(last % (uint32_t)NSL);
+                uint64_t t0 = 0;
+                uint32_t spins = 0;
+                while (!mbar_try_wait(&full[slot], (last / (uint32_t)NSL) & 1)) {
+                    if ((++spins & 255) == 0) {
+                        const uint64_t now = globaltimer_ns();
+                        if (t0 == 0) t0 = now;
+                        else if (now - t0 > 2 * P.wait_limit_ns) { crecord_error(P, kDevTimeout); break; }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        cluster_barrier();
+        return;
+    }
+
+    // ================================================= consumer warps
+    uint32_t gi = 0;  // chunks consumed
+    // Profiling (step 0) and the location of a wait that gave up.
+    uint64_t* stamps = P.timing ? P.timing + 8 + (size_t)cta * cstamps_per_cta(L) : nullptr;
+    int cur_step = 0, cur_layer = 0;
+    auto stamp = [&](int k) {
+        if (stamps && cur_step == 0 && tid == 0) stamps[k] = globaltimer_ns();
+    };
+    const unsigned per_step = (unsigned)cphases_per_step(L);
+    const bool tracing = P.trace != nullptr;
+    const int trace_layer = 8 * D + FF;
+    const unsigned stall_tag = P.stall_phase >= 0 ? P.epoch + (unsigned)P.stall_phase : 0u;
+    auto out_tag = [&](unsigned t) -> unsigned { return (cta == 0 && t == stall_tag) ? t - 1u : t; };
+    int agree_no = 0;
+    auto agree = [&](bool ok) -> bool {
+        volatile int* slot = s_fail + (agree_no & 1);
+        ++agree_no;
+        if (!ok) *slot = 1;
+        csync();
+        return *slot == 0;
+    };
+    auto note_give_up = [&](int kind, bool abort, uint64_t what) {
+        if (stamps) {
+            stamps[16 * L + 4] = (uint64_t)kind | (abort ? 0x100ull : 0ull) | ((uint64_t)threadIdx.x << 16);
+            stamps[16 * L + 5] = (uint64_t)cur_step;
+            stamps[16 * L + 6] = (uint64_t)cur_layer;
+            stamps[16 * L + 7] = what;
+        }
+    };
+    auto timed_out = [&](uint64_t& t0, int kind, uint64_t what = 0, uint64_t seen = 0) -> bool {
+        const uint64_t now = globaltimer_ns();
+        if (t0 == 0) { t0 = now; return false; }
+        if (now - t0 > kCAbortCheckNs && ld_volatile_int(P.abort_flag)) {
+            note_give_up(kind, true, what);
+            return true;
+        }
+        if (now - t0 > P.wait_limit_ns) {
+            note_give_up(kind, false, what);
+            cwait_gave_up(P, kind, cta, cur_step, cur_layer, what, seen);
+            return true;
+        }
+        return false;
+    };
+    // Warp-uniform bounded wait for ring chunk cc.
+    auto wait_chunk = [&](uint32_t cc) -> bool {
+        const int slot = (int)(cc % (uint32_t)NSL);
+        const uint32_t par = (cc / (uint32_t)NSL) & 1;
+        uint64_t t0 = 0;
+        uint32_t spins = 0;
+        while (!__all_sync(0xffffffffu, mbar_try_wait(&full[slot], par))) {
+            if ((++spins & 63) == 0) {
+                int give_up = lane == 0 ? (int)timed_out(t0, 1, cc) : 0;
+                if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+            }
+        }
+        return true;
+    };
+    // Bounded wait for one phase of a local mbarrier that peers complete.
+    auto wait_bar = [&](uint64_t* bar, uint32_t par) -> bool {
+        uint64_t t0 = 0;
+        uint32_t spins = 0;
+        while (!mbar_try_wait(bar, par)) {
+            if ((++spins & 63) == 0 && timed_out(t0, 2, ((uint64_t)(bar - bars) << 8) | par)) return false;
+        }
+        return true;
+    };
+    // n floats (n % 4 == 0) at src into this CTA's row `dst` of a gather
+    // buffer in every CTA of the cluster (same offset), completing on each
+    // peer's mbarrier bar.
+    auto bcast = [&](const float* src, const float* dst, int n, uint64_t* bar) {
+        const int nv = n >> 2;
+        const uint32_t la = smem_addr(dst), lb = smem_addr(bar);
+        for (int k = tid; k < nv * CS; k += NT) {
+            const int dr = k / nv, v = k - dr * nv;
+            st_async4(mapa(la + 16u * (uint32_t)v, (uint32_t)dr), reinterpret_cast<const float4*>(src)[v],
+                      mapa(lb, (uint32_t)dr));
+        }
+    };
+    // Waits (bounded) for a gather of `bytes` on this CTA's mbarrier (armed
+    // in advance), agrees on the outcome, and re-arms the barrier for its
+    // next use.  Contains an agreement barrier.
+    auto gather_wait = [&](uint64_t* bar, uint32_t bytes, uint32_t par) -> bool {
+        const bool ok = agree(wait_bar(bar, par));
+        if (ok && tid == 0) mbar_arrive_expect_tx(bar, bytes);
+        return ok;
+    };
+    // Rows of a share against x4 (W4 float4 columns); row i's dot product to
+    // out[i].  Chunk k is taken by warp k % 8.
+    uint64_t prof_wait = 0, prof_total = 0;  // warp 0, last share: clock64 cycles waiting for chunks, in all
+    // The chunks are taken in rounds of one per warp with a barrier between
+    // rounds.  The ring's barriers are waited on by phase parity, which is
+    // only unambiguous if the previous fill of a chunk's slot has landed;
+    // the rounds keep every warp within one round of the others, so the
+    // previous fill of any slot this round uses (kCWarps <= slots) was
+    // consumed in an earlier round.
+    auto run_share = [&](const Share& sh, const float* x, int W4, float* out) -> bool {
+        bool ok = true;
+        const uint32_t x_s = smem_addr(x);
+        const long long t_in = clock64();
+        long long t_wait = 0;
+        for (int k0 = 0; k0 < sh.nch; k0 += kCWarps) {
+            const int k = k0 + warp;
+            if (ok && k < sh.nch) {
+                const uint32_t cc = gi + (uint32_t)k;
+                const long long tw = clock64();
+                ok = wait_chunk(cc);
+                t_wait += clock64() - tw;
+                if (ok) {
+                    const uint32_t w = ring_s + (cc % (uint32_t)NSL) * (uint32_t)kCSlotBytes;
+                    const int n = min(sh.rpc, sh.n - k * sh.rpc);
+                    const float v = chunk_rows<WF>(w, n, W4, x_s, lane);
+                    if (lane < n) out[k * sh.rpc + lane] = v;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[cc % (uint32_t)NSL]);
+                }
+            }
+            if (k0 + kCWarps < sh.nch) csync();
+        }
+        gi += (uint32_t)sh.nch;
+        prof_wait = (uint64_t)t_wait;
+        prof_total = (uint64_t)(clock64() - t_in);
+        return ok;
+    };
+    // Deterministic block sum over the consumer threads (same value in all).
+    auto block_sum = [&](float v) -> float {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) s_red[warp] = v;
+        csync();
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kCWarps; ++w) t += s_red[w];
+        csync();
+        return t;
+    };
+    // Waits until every one of nw partial vectors (base + k * D, k < nw) has
+    // this slice's last word tagged `tag`: one lane of warp 0 per vector
+    // polls that sentinel, so a waiting CTA keeps nw loads in flight rather
+    // than one per word.  Called by every consumer thread; ends with an
+    // agreement barrier.
+    auto wait_sentinels = [&](const uint64_t* base, int nw, unsigned tag) -> bool {
+        bool ok = true;
+        if (warp == 0) {
+            const uint64_t* sp = base + (size_t)lane * D + col0 + (SW - 1);
+            bool done = lane >= nw;
+            uint64_t t0 = 0;
+            uint32_t spins = 0;
+            while (true) {
+                if (!done) done = tag_of(ld_tagged(sp)) == tag;
+                if (__all_sync(0xffffffffu, done)) break;
+                if ((++spins & 15) == 0) {
+                    const unsigned pend = __ballot_sync(0xffffffffu, !done);
+                    const int give = lane == 0 ? (int)timed_out(t0, 3, (uint64_t)pend) : 0;
+                    if (__shfl_sync(0xffffffffu, give, 0)) { ok = false; break; }
+                }
+            }
+        }
+        return agree(ok);
+    };
+    // The ordered sum of the nw tagged words base[k * D + col] (k < nw) of
+    // this thread's column, once their sentinels carry `tag` (words still in
+    // flight from the same stores are re-read).
+    auto gather_sum = [&](const uint64_t* base, int nw, int col, unsigned tag, float& sum) -> bool {
+        constexpr int B = 8;
+        sum = 0.0f;
+        uint64_t t0 = 0;
+        for (int k0 = 0; k0 < nw; k0 += B) {
+            uint64_t w[B];
+            uint32_t pending = 0;
+#pragma unroll
+            for (int i = 0; i < B; ++i)
+                if (k0 + i < nw) pending |= 1u << i;
+            while (pending) {
+#pragma unroll
+                for (int i = 0; i < B; ++i)
+                    if ((pending >> i) & 1u) w[i] = ld_tagged(base + (size_t)(k0 + i) * D + col);
+#pragma unroll
+                for (int i = 0; i < B; ++i)
+                    if (((pending >> i) & 1u) && tag_of(w[i]) == tag) pending &= ~(1u << i);
+                if (pending && timed_out(t0, 3)) return false;
+            }
+#pragma unroll
+            for (int i = 0; i < B; ++i)
+                if (k0 + i < nw) sum += val_of(w[i]);
+        }
+        return true;
+    };
+    // This slice's (mean, M2) of x - s (two passes over SW values), by warp 0, into dst[0..1].
+    auto slice_stats = [&](float s, float* dst) {
+        if (warp != 0) return;
+        float a = 0.0f;
+        for (int e = lane; e < SW; e += 32) a += xs[e] - s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        const float mean = a / (float)SW;
+        float q = 0.0f;
+        for (int e = lane; e < SW; e += 32) {
+            const float d = (xs[e] - s) - mean;
+            q = fmaf(d, d, q);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+        if (lane == 0) {
+            dst[0] = mean;
+            dst[1] = q;
+        }
+    };
+    // Merged (mean, M2) of CS slices whose stats sit at base + r' * stride.
+    auto merge_stats = [&](const float* base, int stride, float& mean, float& rstd) {
+        float n = 0.0f, mu = 0.0f, m2 = 0.0f;
+        for (int k = 0; k < CS; ++k) {
+            const float nb = (float)SW, mb = base[k * stride], qb = base[k * stride + 1];
+            const float nn = n + nb, dl = mb - mu;
+            mu = mu + dl * (nb / nn);
+            m2 = m2 + qb + dl * dl * (n * nb / nn);
+            n = nn;
+        }
+        mean = mu;
+        rstd = 1.0f / sqrtf(m2 / (float)D + kLnEps);
+    };
+
+    // Greedy partials of the previous step (tag), reduced in every CTA; the
+    // acquire pairs with each CTA's release, so the KV rows of that step are
+    // visible to this step's attention.
+    auto reduce_choice = [&](unsigned tag) -> bool {
+        bool ok = true;
+        if (tid < GG.G) {
+            const uint64_t* ap = P.arg_part + 2 * (size_t)tid;
+            uint64_t t0 = 0;
+            uint64_t w0 = ld_tagged_acquire(ap);
+            while (tag_of(w0) != tag) {
+                if (timed_out(t0, 4, ((uint64_t)tid << 32) | tag, w0)) { ok = false; break; }
+                w0 = ld_tagged_acquire(ap);
+            }
+            if (ok) {
+                const uint64_t w1 = ld_tagged(ap + 1);
+                if (tag_of(w1) != tag) {
+                    crecord_error(P, kDevTimeout);
+                    ok = false;
+                }
+                stage[tid] = val_of(w0);
+                stage[384 + tid] = val_of(w1);
+            }
+        }
+        if (!agree(ok)) return false;
+        if (warp == 0) {
+            Best b{-INFINITY, 0xFFFFFFFFu, 0};
+            for (int k = lane; k < GG.G; k += 32) {
+                const unsigned iw = __float_as_uint(stage[384 + k]);
+                best_merge(b, stage[k], iw & 0x7FFFFFFFu, (int)(iw >> 31));
+            }
+            best_warp(b);
+            if (lane == 0) {
+                *s_tok = b.nf ? 0xFFFFFFFFu : b.i;
+                *s_nf = b.nf;
+            }
+        }
+        csync();
+        return true;
+    };
+    auto publish_choice = [&](int s_done, unsigned choice, int nf) {
+        if (tid == 0 && cta == 0) {
+            if (P.tokens_out) P.tokens_out[s_done] = choice;
+            *P.last_token = choice;
+            if (nf) atomicCAS(P.status, 0, (int)kDevNonfinite);
+        }
+    };
+
+    // Attention of head h (layer l, position p) over this CTA's keys
+    // [k0, k1) of 0..p: (max, sum, unnormalised weighted values) into
+    // pa[0], pa[1], pa[4 .. 4 + DH).  LPK lanes per key, DPL dims per lane;
+    // the current position's key and value come from qkv (this step's).
+    constexpr int LPK = DH >= 32 ? 8 : 4;
+    constexpr int KPW = 32 / LPK;
+    constexpr int DPL = DH / LPK;
+    constexpr int F4 = DPL / 4;
+    constexpr int KPP = kCWarps * KPW;
+    static_assert(DPL % 4 == 0, "a lane holds whole float4s of a head row");
+    const int ks = lane / LPK, dc = lane % LPK;
+    float4 ka[F4], va[F4];
+    auto fetch = [&](const float* kv0, int j, int k1, int p, float4 (&kk)[F4], float4 (&vv)[F4]) {
+        if (j < k1 && j < p) {
+            const float4* row = reinterpret_cast<const float4*>(kv0 + (uint64_t)j * L * 2 * D);
+#pragma unroll
+            for (int f = 0; f < F4; ++f) {
+                kk[f] = __ldcg(row + f);
+                vv[f] = __ldcg(row + D / 4 + f);
+            }
+        }
+    };
+    auto attention = [&](int l, int h, int p) {
+        const int n = p + 1;
+        const int k0 = (int)(((long long)r * n) / CS), k1 = (int)(((long long)(r + 1) * n) / CS);
+        const float* kv0 = P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL;
+        const float den = sqrtf((float)DH);
+        const float4* q4 = reinterpret_cast<const float4*>(qkv + dc * DPL);
+        float m = -INFINITY, z = 0.0f;
+        float acc[DPL];
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[d] = 0.0f;
+        int j = k0 + warp * KPW + ks;
+        for (int jb = k0 + warp * KPW; jb < k1; jb += KPP, j += KPP) {
+            float4 kb[F4], vb[F4];
+            fetch(kv0, j + KPP, k1, p, kb, vb);  // next pass
+            if (j == p) {
+#pragma unroll
+                for (int f = 0; f < F4; ++f) {
+                    ka[f] = reinterpret_cast<const float4*>(qkv + DH + dc * DPL)[f];
+                    va[f] = reinterpret_cast<const float4*>(qkv + 2 * DH + dc * DPL)[f];
+                }
+            }
+            float dot = 0.0f;
+#pragma unroll
+            for (int f = 0; f < F4; ++f) {
+                const float4 qf = q4[f];
+                dot += qf.x * ka[f].x + qf.y * ka[f].y + qf.z * ka[f].z + qf.w * ka[f].w;
+            }
+#pragma unroll
+            for (int o = 1; o < LPK; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            if (j < k1) {
+                const float sc = dot / den;
+                const float mn = fmaxf(m, sc);
+                const float corr = expf(m - mn);
+                const float e = expf(sc - mn);
+                z = fmaf(z, corr, e);
+#pragma unroll
+                for (int f = 0; f < F4; ++f) {
+                    acc[4 * f + 0] = fmaf(acc[4 * f + 0], corr, e * va[f].x);
+                    acc[4 * f + 1] = fmaf(acc[4 * f + 1], corr, e * va[f].y);
+                    acc[4 * f + 2] = fmaf(acc[4 * f + 2], corr, e * va[f].z);
+                    acc[4 * f + 3] = fmaf(acc[4 * f + 3], corr, e * va[f].w);
+                }
+                m = mn;
+            }
+#pragma unroll
+            for (int f = 0; f < F4; ++f) {
+                ka[f] = kb[f];
+                va[f] = vb[f];
+            }
+        }
+        // merge the key slots of the warp (lanes with the same dc)
+#pragma unroll
+        for (int o = LPK; o < 32; o <<= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, m, o);
+            const float oz = __shfl_xor_sync(0xffffffffu, z, o);
+            const float mn = fmaxf(m, om);
+            const float c1 = (m == -INFINITY) ? 0.0f : expf(m - mn);
+            const float c2 = (om == -INFINITY) ? 0.0f : expf(om - mn);
+            z = z * c1 + oz * c2;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) {
+                const float oa = __shfl_xor_sync(0xffffffffu, acc[d], o);
+                acc[d] = acc[d] * c1 + oa * c2;
+            }
+            m = mn;
+        }
+        if (ks == 0) {
+            float* st = stage + (warp * LPK + dc) * (2 + DPL);
+            st[0] = m;
+            st[1] = z;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) st[2 + d] = acc[d];
+        }
+        csync();
+        if (tid < DH) {
+            const int cq = tid / DPL, d = tid - cq * DPL;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, stage[(w * LPK + cq) * (2 + DPL)]);
+            float Z = 0.0f, O = 0.0f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kCWarps; ++w) {
+                    const float* st = stage + (w * LPK + cq) * (2 + DPL);
+                    if (st[0] == -INFINITY) continue;
+                    const float cw = expf(st[0] - M);
+                    Z = fmaf(st[1], cw, Z);
+                    O = fmaf(st[2 + d], cw, O);
+                }
+            }
+            pa[4 + tid] = O;
+            if (tid == 0) {
+                pa[0] = M;
+                pa[1] = Z;
+                pa[2] = 0.0f;
+                pa[3] = 0.0f;
+            }
+        }
+    };
+
+    const float* fold = P.fold;
+    const uint64_t fold_words = fold_layer_words(D, FF);
+    unsigned prev_choice = *P.last_token;
+    bool alive = !*s_abort;
+    uint32_t useA = 0, useT = 0, useB = 0;  // uses of the double-buffered gathers
+    float* s_st = s_stA;                      // this slice's (mean, M2) of the LayerNorm input
+    int s = 0;
+    for (; s < P.n_steps && alive; ++s) {
+        const int p = P.p0 + s;
+        const unsigned base = P.epoch + (unsigned)s * per_step;
+        const bool tr = tracing && s == 0;
+        cur_step = s;
+        cur_layer = 0;
+        if (s > 0) {
+            if (!reduce_choice(base)) { alive = false; break; }
+            prev_choice = *s_tok;
+            const int nf = *s_nf;
+            publish_choice(s - 1, prev_choice, nf);
+            if (nf) { alive = false; break; }
+        }
+        unsigned tok = P.tokens_in ? P.tokens_in[s] : P.token0;
+        if (tok == 0xFFFFFFFFu) tok = prev_choice;
+        if (tok >= (unsigned)V) {
+            if (tid == 0 && cta == 0) crecord_error(P, kDevToken);
+            alive = false;
+            break;
+        }
+        // ---- embedding (every CTA forms the whole vector for its exact mean)
+        float esum = 0.0f;
+        for (int i = tid; i < D; i += NT) {
+            float te;
+            if constexpr (WF == kWF16) te = __half2float(reinterpret_cast<const __half*>(P.vocab)[(uint64_t)tok * D + i]);
+            else te = __ldg(P.packed + P.wte_off + (uint64_t)tok * D + i);
+            const float x = __fadd_rn(te, __ldg(P.packed + P.wpe_off + (uint64_t)p * D + i));
+            xf[i] = x;
+            esum += x;
+        }
+        const float mu_emb = block_sum(esum) / (float)D;  // (block_sum ends with a barrier: xf complete)
+        for (int e = tid; e < SW; e += NT) xs[e] = xf[col0 + e];
+        float shift = mu_emb;  // the last LayerNorm mean every CTA of this cluster holds
+        csync();
+
+        for (int l = 0; l < L && alive; ++l) {
+            cur_layer = l;
+            const LayerParams& lp = P.lp[l];
+            const unsigned tagA = base + 2u * (unsigned)l + 1u, tagB = tagA + 1u;
+            const float* fl = fold + (uint64_t)l * fold_words;
+            const float g1 = tid < SW ? __ldg(P.packed + lp.ln1_g + col0 + tid) : 0.0f;
+            const float g2 = tid < SW ? __ldg(P.packed + lp.ln2_g + col0 + tid) : 0.0f;
+            float ln_shift = shift;  // shift of the LayerNorm being folded
+            // Micro-phases of the layer, one runtime loop so that each routine
+            // (gather, dot products, all-gather, store) has one copy in the
+            // binary: per head slot k of this cluster QKV (0), attention (1),
+            // out-projection (2); then FC (3) and MLP projection (4).
+            const int nmp = 3 * nh + 2;
+            for (int mp = 0; mp < nmp; ++mp) {
+                const int kind = mp < 3 * nh ? mp % 3 : 3 + (mp - 3 * nh);
+                const int k = mp < 3 * nh ? mp / 3 : 0;
+                const int h = c + k * GG.NC;
+                // ---- the residual slice a LayerNorm of this micro-phase reads
+                if ((kind == 0 && k == 0) || kind == 3) {
+                    // q = 0: the previous layer's MLP partials (block input);
+                    // q = 1: this layer's out-projection partials (attention residual)
+                    const int q0 = (l > 0 && (kind == 0 || nh == 0)) ? 0 : 1, q1 = kind == 3 ? 1 : 0;
+                    for (int q = q0; q <= q1 && alive; ++q) {
+                        const uint64_t* src = q == 0 ? CP.partP + (size_t)((l - 1) & 1) * GG.NC * D : CP.partO;
+                        const int nw = q == 0 ? GG.NC : H;
+                        const unsigned tg = q == 0 ? tagA - 1u : tagA;
+                        const float bv = tid < SW ? __ldg(P.packed + (q == 0 ? P.lp[l - 1].b_p : lp.b_o) + col0 + tid) : 0.0f;
+                        if (!wait_sentinels(src, nw, tg)) { alive = false; break; }
+                        bool ok = true;
+                        if (tid < SW) {
+                            float y;
+                            ok = gather_sum(src + col0, nw, tid, tg, y);
+                            xs[tid] = __fadd_rn(xs[tid], __fadd_rn(y, bv));
+                        }
+                        if (!agree(ok)) { alive = false; break; }
+                        stamp(16 * l + (q == 0 ? 0 : 6));
+                        if (tr && c == 0) ctrace_copy(P.trace + (size_t)l * trace_layer + (q == 0 ? 0 : 6 * D) + col0, xs, SW, tid);
+                    }
+                    if (!alive) break;
+                    if (l == 0 && kind == 0) {
+                        stamp(0);
+                        if (tr && c == 0) ctrace_copy(P.trace + col0, xs, SW, tid);
+                    }
+                    ln_shift = shift;
+                    if (tid < SW) xin[tid] = (kind == 0 ? g1 : g2) * (xs[tid] - ln_shift);
+                    csync();
+                    slice_stats(ln_shift, s_st);
+                }
+                // ---- dot products of this micro-phase's share (attention has none)
+                if (kind != 1) {
+                    Share sh;
+                    const float* xv;
+                    int W4;
+                    if (kind == 0) { sh = share_qkv(l, k); xv = xin; W4 = SW / 4; }
+                    else if (kind == 2) { sh = share_wo(l, k); xv = oh; W4 = DH / 4; }
+                    else if (kind == 3) { sh = share_fc(l); xv = xin; W4 = SW / 4; }
+                    else { sh = share_wp(l); xv = uu; W4 = nfc4 / 4; }
+                    const bool ok = run_share(sh, xv, W4, pa);
+                    if (tid == 0 && (kind == 0 || kind == 3)) {
+                        const int n0 = kind == 0 ? 3 * DH : nfc4;
+                        pa[n0] = s_st[0];
+                        pa[n0 + 1] = s_st[1];
+                        pa[n0 + 2] = 0.0f;
+                        pa[n0 + 3] = 0.0f;
+                    }
+                    if (stamps && cur_step == 0 && tid == 0) {
+                        const int sl = 16 * l + 10 + (kind == 0 ? 0 : kind == 2 ? 1 : kind == 3 ? 2 : 3) * 1;
+                        stamps[sl] = (prof_wait << 32) | (prof_total & 0xFFFFFFFFull);
+                    }
+                    if (!agree(ok)) { alive = false; break; }
+                    stamp(16 * l + (kind == 0 ? 1 : kind == 2 ? 5 : kind == 3 ? 7 : 9));
+                } else {
+                    attention(l, h, p);
+                    csync();
+                    stamp(16 * l + 3);
+                }
+                // ---- the cluster all-gather (QKV partials, attention partials, FC partials)
+                if (kind == 0 || kind == 1 || kind == 3) {
+                    uint32_t u;
+                    int rowl, nsend;
+                    float* gbuf;
+                    uint64_t* bar;
+                    if (kind == 0) {
+                        u = useA++;
+                        rowl = 3 * DH + 4;
+                        nsend = rowl;
+                        gbuf = gA + (size_t)(u & 1) * CS * rowl;
+                        bar = &bars[0 + (u & 1)];
+                    } else if (kind == 1) {
+                        u = useT++;
+                        rowl = DH + 4;
+                        nsend = rowl;
+                        gbuf = gT + (size_t)(u & 1) * CS * rowl;
+                        bar = &bars[2 + (u & 1)];
+                    } else {
+                        u = useB++;
+                        rowl = GG.nfc_max + 4;
+                        nsend = nfc4 + 4;
+                        gbuf = gB + (size_t)(u & 1) * CS * rowl;
+                        bar = &bars[4 + (u & 1)];
+                    }
+                    bcast(pa, gbuf + (size_t)r * rowl, nsend, bar);
+                    // loaded while the gather completes: the first keys of this
+                    // CTA's attention share, and this thread's fold constants
+                    float cj = 0.0f, dj = 0.0f;
+                    int J = 0;
+                    if (kind == 0) {
+                        const int n = p + 1;
+                        const int kk0 = (int)(((long long)r * n) / CS), kk1 = (int)(((long long)(r + 1) * n) / CS);
+                        fetch(P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL, kk0 + warp * KPW + ks, kk1, p, ka, va);
+                        if (tid < 3 * DH) {
+                            J = (tid / DH) * D + h * DH + (tid % DH);
+                            cj = __ldg(fl + J);
+                            dj = __ldg(fl + 3 * D + J);
+                        }
+                    } else if (kind == 3 && tid < nfc) {
+                        J = f0 + tid;
+                        cj = __ldg(fl + 6 * D + J);
+                        dj = __ldg(fl + 6 * D + FF + J);
+                    }
+                    if (!gather_wait(bar, (uint32_t)(CS * nsend * 4), (u >> 1) & 1)) { alive = false; break; }
+                    stamp(16 * l + (kind == 0 ? 2 : kind == 1 ? 4 : 8));
+                    // ---- epilogues of the gathered values
+                    if (kind == 0) {
+                        float mean, rstd;
+                        merge_stats(gbuf + 3 * DH, rowl, mean, rstd);
+                        if (tid < 3 * DH) {
+                            float a = 0.0f;
+                            for (int q = 0; q < CS; ++q) a += gbuf[(size_t)q * rowl + tid];
+                            const float y = fmaf(rstd, fmaf(-mean, cj, a), dj);
+                            qkv[tid] = y;
+                            if (tid >= DH && (tid % CS) == r) {
+                                const int off = tid < 2 * DH ? h * DH + (tid - DH) : D + h * DH + (tid - 2 * DH);
+                                P.cache[((uint64_t)p * L + l) * 2 * D + off] = y;
+                            }
+                            if (tr && r == 0) P.trace[(size_t)l * trace_layer + 2 * D + J] = y;
+                        }
+                        if (tr && c == 0 && k == 0)
+                            ctrace_ln(P.trace + (size_t)l * trace_layer + D + col0, xs, ln_shift + mean, rstd,
+                                      P.packed + lp.ln1_g + col0, P.packed + lp.ln1_b + col0, SW, tid);
+                        if (k == nh - 1) shift = ln_shift + mean;
+                    } else if (kind == 1) {
+                        if (tid < DH) {
+                            float M = -INFINITY;
+                            for (int q = 0; q < CS; ++q) M = fmaxf(M, gbuf[(size_t)q * rowl]);
+                            float Z = 0.0f, O = 0.0f;
+                            for (int q = 0; q < CS; ++q) {
+                                const float* row = gbuf + (size_t)q * rowl;
+                                if (row[0] == -INFINITY) continue;
+                                const float cw = expf(row[0] - M);
+                                Z = fmaf(row[1], cw, Z);
+                                O = fmaf(row[4 + tid], cw, O);
+                            }
+                            const float o = O / Z;
+                            oh[tid] = o;
+                            if (tr && r == 0) P.trace[(size_t)l * trace_layer + 5 * D + h * DH + tid] = o;
+                        }
+                    } else {
+                        float mean, rstd;
+                        merge_stats(gbuf + nfc4, rowl, mean, rstd);
+                        for (int j = tid; j < nfc; j += NT) {
+                            float a = 0.0f;
+                            for (int q = 0; q < CS; ++q) a += gbuf[(size_t)q * rowl + j];
+                            float cc = cj, dd = dj;
+                            if (j != tid) {
+                                cc = __ldg(fl + 6 * D + f0 + j);
+                                dd = __ldg(fl + 6 * D + FF + f0 + j);
+                            }
+                            const float uv = cgelu(fmaf(rstd, fmaf(-mean, cc, a), dd));
+                            uu[j] = uv;
+                            if (tr && r == 0) P.trace[(size_t)l * trace_layer + 8 * D + f0 + j] = uv;
+                        }
+                        if (tr && c == 0)
+                            ctrace_ln(P.trace + (size_t)l * trace_layer + 7 * D + col0, xs, ln_shift + mean, rstd,
+                                      P.packed + lp.ln2_g + col0, P.packed + lp.ln2_b + col0, SW, tid);
+                        shift = ln_shift + mean;
+                    }
+                    csync();
+                } else {
+                    // ---- out-projection (2) or MLP (4) partials of this CTA's output rows
+                    uint64_t* dst = kind == 2 ? CP.partO + (size_t)h * D + col0
+                                              : CP.partP + ((size_t)(l & 1) * GG.NC + c) * D + col0;
+                    const unsigned tg = out_tag(kind == 2 ? tagA : tagB);
+                    for (int e = tid; e < SW; e += NT) st_tagged(dst + e, tg, pa[e]);
+                }
+            }
+        }
+        if (!alive) break;
+        // ================= final LayerNorm and the vocabulary rows
+        {
+            const unsigned tin = base + 2u * (unsigned)L;  // last layer's B
+            const uint64_t* src = CP.partP + (size_t)((L - 1) & 1) * GG.NC * D;
+            const float bp = tid < SW ? __ldg(P.packed + P.lp[L - 1].b_p + col0 + tid) : 0.0f;
+            if (!wait_sentinels(src, GG.NC, tin)) { alive = false; break; }
+            bool ok = true;
+            if (tid < SW) {
+                float y;
+                ok = gather_sum(src + col0, GG.NC, tid, tin, y);
+                xs[tid] = __fadd_rn(xs[tid], __fadd_rn(y, bp));
+            }
+            if (!agree(ok)) { alive = false; break; }
+        }
+        stamp(16 * L + 0);
+        bcast(xs, gX + col0, SW, &bars[6]);
+        {
+            if (!gather_wait(&bars[6], (uint32_t)(D * 4), (uint32_t)s & 1)) { alive = false; break; }
+        }
+        stamp(16 * L + 1);
+        // LN_f over the whole vector: mean, then squares around it (the oracle's two passes)
+        float sx = 0.0f;
+        for (int i = tid; i < D; i += NT) sx += gX[i];
+        const float mean = block_sum(sx) / (float)D;
+        float sq = 0.0f;
+        for (int i = tid; i < D; i += NT) {
+            const float d = gX[i] - mean;
+            sq = fmaf(d, d, sq);
+        }
+        const float var = block_sum(sq) / (float)D;
+        const float den = sqrtf(var + kLnEps);
+        for (int i = tid; i < D; i += NT) {
+            const float y = __fadd_rn(__fmul_rn(__fdiv_rn(__fsub_rn(gX[i], mean), den), __ldg(P.packed + P.lnf_g + i)),
+                                      __ldg(P.packed + P.lnf_b + i));
+            xf[i] = y;
+        }
+        if (tr && cta == 0) {
+            ctrace_copy(P.trace + (size_t)L * trace_layer, gX, D, tid);
+            ctrace_copy(P.trace + (size_t)L * trace_layer + D, xf, D, tid);
+        }
+        csync();
+        stamp(16 * L + 2);
+        // vocabulary rows of this CTA: logits and the running greedy choice
+        {
+            const Share sh = share_vocab();
+            float* lg = P.logits ? P.logits + (uint64_t)s * P.logits_stride : nullptr;
+            Best best{-INFINITY, 0xFFFFFFFFu, 0};
+            bool ok = true;
+            const uint32_t xf_s = smem_addr(xf);
+            // rounds of one chunk per warp, as in run_share
+            for (int k0 = 0; k0 < sh.nch; k0 += kCWarps) {
+                const int kc = k0 + warp;
+                if (ok && kc < sh.nch) {
+                    const uint32_t cc = gi + (uint32_t)kc;
+                    ok = wait_chunk(cc);
+                    if (ok) {
+                        const uint32_t w = ring_s + (cc % (uint32_t)NSL) * (uint32_t)kCSlotBytes;
+                        const int n = min(sh.rpc, sh.n - kc * sh.rpc);
+                        const float v = long_rows<kVocabRows, D / 4, WF>(w, sh.pb, n, xf_s, lane);
+                        if (lane < n) {
+                            const int j = v0 + kc * sh.rpc + lane;
+                            if (lg) lg[j] = v;
+                            best_update(best, v, (unsigned)j);
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[cc % (uint32_t)NSL]);
+                    }
+                }
+                if (k0 + kCWarps < sh.nch) csync();
+            }
+            gi += (uint32_t)sh.nch;
+            best_warp(best);
+            if (lane == 0) {
+                s_arg[warp * 3 + 0] = best.v;
+                s_arg[warp * 3 + 1] = __uint_as_float(best.i);
+                s_arg[warp * 3 + 2] = (float)best.nf;
+            }
+            if (!agree(ok)) { alive = false; break; }
+            if (tid == 0) {
+                Best b = {s_arg[0], __float_as_uint(s_arg[1]), s_arg[2] != 0.0f};
+                for (int w = 1; w < kCWarps; ++w)
+                    best_merge(b, s_arg[w * 3 + 0], __float_as_uint(s_arg[w * 3 + 1]), s_arg[w * 3 + 2] != 0.0f);
+                if (stamps && s == 0) stamps[16 * L + 3] = globaltimer_ns();
+                const unsigned tg = out_tag(base + per_step);
+                uint64_t* ap = P.arg_part + 2 * (size_t)cta;
+                const unsigned iw = (b.i & 0x7FFFFFFFu) | (b.nf ? 0x80000000u : 0u);
+                st_tagged(ap + 1, tg, __uint_as_float(iw));
+                // release: this CTA's KV rows and choice become visible with it
+                st_tagged_release(ap, tag_pack(tg, b.v));
+            }
+        }
+    }
+    // The last step's greedy choice (CTA 0 reports it).
+    if (alive && s == P.n_steps && cta == 0) {
+        if (reduce_choice(P.epoch + (unsigned)P.n_steps * per_step)) publish_choice(s - 1, *s_tok, *s_nf);
+    }
+    if (tid == 0) *s_abort = 1;  // the producer stops issuing
+    cluster_barrier();
+}
+
+// ------------------------------------------------------------ weight layout
+// Byte offset of weight e of row i in a share of n rows of W weights (wb
+// bytes each): rows are grouped into ring chunks of rpc rows (rpc =
+// min(32, slot bytes / row bytes)), and inside a chunk of R rows the rows
+// are interleaved by 4-weight units: unit c of row i' at (c * R + i') units.
+__host__ __device__ inline uint64_t cunit_off(int i, int e, int n, int W, int wb) {
+    const uint32_t pb = (uint32_t)W * (uint32_t)wb;
+    int rpc = (int)(kCSlotBytes / pb);
+    if (rpc > 32) rpc = 32;
+    if (rpc > n) rpc = n;
+    const int k = i / rpc, i2 = i - k * rpc;
+    const int R = (n - k * rpc) < rpc ? (n - k * rpc) : rpc;
+    const int cu = e >> 2, sub = e & 3;
+    return (uint64_t)k * rpc * pb + ((uint64_t)cu * R + i2) * 4u * wb + (uint64_t)sub * wb;
+}
+
+// Copies one layer of the K-major device stream (rows [out][in], row pitch
+// rbd for width-D inputs and rbf for width-FF inputs, wb bytes per weight)
+// into the cluster layout: block (c*CS + r) writes CTA (c, r)'s part.
+__global__ void clayout_kernel(const uint8_t* __restrict__ src, const CGeo g, int D, int H, int FF, int DH,
+                               uint64_t mat_qkv, uint64_t mat_o, uint64_t mat_fc, uint64_t mat_p, uint32_t rbd,
+                               uint32_t rbf, uint8_t* __restrict__ dst) {
+    const int cta = blockIdx.x, c = cta / g.CS, r = cta % g.CS;
+    const int wb = g.wb, SW = g.SW, col0 = r * SW;
+    const int nh = cg_heads(g, H, c);
+    const int f0 = g.fc0[c], nfc = g.fc0[c + 1] - f0;
+    uint8_t* out = dst + g.seg[c] + (uint64_t)r * g.cta_bytes[c];
+    auto copy = [&](uint8_t* d, const uint8_t* s_) {
+        if (wb == 4) *reinterpret_cast<uint32_t*>(d) = *reinterpret_cast<const uint32_t*>(s_);
+        else *reinterpret_cast<uint16_t*>(d) = *reinterpret_cast<const uint16_t*>(s_);
+    };
+    uint64_t o = 0;
+    for (int k = 0; k < nh; ++k) {
+        const int h = c + k * g.NC;
+        for (int t = threadIdx.x; t < 3 * DH * SW; t += blockDim.x) {
+            const int i = t / SW, e = t - i * SW;
+            const int J = (i / DH) * D + h * DH + (i % DH);
+            copy(out + o + cunit_off(i, e, 3 * DH, SW, wb),
+                 src + mat_qkv + (uint64_t)J * rbd + (uint64_t)(col0 + e) * wb);
+        }
+        o += (uint64_t)3 * DH * SW * wb;
+        for (int t = threadIdx.x; t < SW * DH; t += blockDim.x) {
+            const int i = t / DH, e = t - i * DH;
+            copy(out + o + cunit_off(i, e, SW, DH, wb),
+                 src + mat_o + (uint64_t)(col0 + i) * rbd + (uint64_t)(h * DH + e) * wb);
+        }
+        o += (uint64_t)SW * DH * wb;
+    }
+    for (int t = threadIdx.x; t < nfc * SW; t += blockDim.x) {
+        const int i = t / SW, e = t - i * SW;
+        copy(out + o + cunit_off(i, e, nfc, SW, wb), src + mat_fc + (uint64_t)(f0 + i) * rbd + (uint64_t)(col0 + e) * wb);
+    }
+    o += (uint64_t)nfc * SW * wb;
+    for (int t = threadIdx.x; t < SW * nfc; t += blockDim.x) {
+        const int i = t / nfc, e = t - i * nfc;
+        copy(out + o + cunit_off(i, e, SW, nfc, wb), src + mat_p + (uint64_t)(col0 + i) * rbf + (uint64_t)(f0 + e) * wb);
+    }
+}
+
+// ------------------------------------------------------------ host side
+namespace {
+
+template <int D, int FF, int DH, int WF>
+cudaError_t set_attrs(uint32_t smem) {
+    auto kern = cstep_kernel<D, FF, DH, WF>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+template <int D, int FF, int DH, int WF>
+cudaError_t launch_t(const CPlan& P, cudaStream_t stream) {
+    const CSmem lay = csmem_layout(D, DH, P.g.CS, P.g.SW, P.g.nfc_max, P.g.slots);
+    cudaError_t e = set_attrs<D, FF, DH, WF>(lay.total);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.g.G);
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = lay.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P.g.CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, cstep_kernel<D, FF, DH, WF>, P);
+}
+
+template <int D, int FF, int DH, int WF>
+int max_clusters_t(int CS, uint32_t smem) {
+    if (set_attrs<D, FF, DH, WF>(smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CS);
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)cstep_kernel<D, FF, DH, WF>, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+#define CSTEP_DISPATCH_WF(FN, d, ff, dh, ...)                 \
+    return wf == kWF16 ? FN<d, ff, dh, kWF16>(__VA_ARGS__) : FN<d, ff, dh, kWF32>(__VA_ARGS__);
+#define CSTEP_DISPATCH(FN, ...)                                                                \
+    if (D == 768 && FF == 3072 && DH == 64) { CSTEP_DISPATCH_WF(FN, 768, 3072, 64, __VA_ARGS__) } \
+    if (D == 192 && FF == 384 && DH == 64) { CSTEP_DISPATCH_WF(FN, 192, 384, 64, __VA_ARGS__) }   \
+    if (D == 64 && FF == 256 && DH == 16) { CSTEP_DISPATCH_WF(FN, 64, 256, 16, __VA_ARGS__) }
+
+int max_clusters(int D, int FF, int DH, int wf, int CS, uint32_t smem) {
+    CSTEP_DISPATCH(max_clusters_t, CS, smem)
+    return 0;
+}
+
+// Cluster size per model width: a slice of 128 floats (one warp of float4
+// columns) where the width allows.
+int preferred_cs(int D) {
+    if (D % 128 == 0 && D / 128 <= 8) return D / 128;
+    if (D % 32 == 0 && D / 32 <= 8) return D / 32;
+    return 1;
+}
+
+}  // namespace
+
+bool cstep_supported(int D, int FF, int DH, int wf) {
+    if (wf != kWF32 && wf != kWF16) return false;
+    return (D == 768 && FF == 3072 && DH == 64) || (D == 192 && FF == 384 && DH == 64) ||
+           (D == 64 && FF == 256 && DH == 16);
+}
+
+// Chooses the cluster geometry: clusters of CS CTAs (CS = D / 128 at GPT-2
+// 124M, i.e. 6), as many clusters as are co-resident (at most want_ctas / CS
+// when want_ctas > 0), the FC rows split so that every CTA streams about the
+// same bytes per layer (head clusters also stream QKV and out-projection
+// parts), in multiples of 8 rows.
+cudaError_t cgeo_make(int L, int D, int H, int FF, int wf, int want_ctas, CGeo* out) {
+    (void)L;
+    const int DH = D / H;
+    CGeo g;
+    memset(&g, 0, sizeof(g));
+    int CS = preferred_cs(D);
+    const char* env_cs = getenv("GPT2_CLUSTER_SIZE");
+    if (env_cs) CS = atoi(env_cs);
+    if (CS < 1 || CS > 16 || D % CS != 0 || (D / CS) % 8 != 0) return cudaErrorInvalidValue;
+    g.CS = CS;
+    g.SW = D / CS;
+    g.wb = wf == kWF16 ? 2 : 4;
+    if (g.SW > kCWarps * 32 || FF % 8 != 0 || DH % 8 != 0) return cudaErrorInvalidValue;
+    // clusters co-resident at one CTA per SM (the kernel's ring takes what
+    // shared memory the rest leaves)
+    int maxc = max_clusters(D, FF, DH, wf, CS, (uint32_t)kCMaxSmem);
+    if (maxc <= 0) return cudaErrorInvalidConfiguration;
+    int NC = maxc < kCMaxClusters ? maxc : kCMaxClusters;
+    if (want_ctas > 0) {
+        const int w = (want_ctas + CS - 1) / CS;
+        if (w < NC) NC = w;
+    }
+    while (NC > 1 && FF / NC < 8) --NC;
+    while (NC > 1 && NC * CS > kCWarps * 32) --NC;  // one greedy partial per consumer thread
+    g.NC = NC;
+    g.G = NC * CS;
+    g.HPC = (H + NC - 1) / NC;
+    // FC rows: head clusters carry 4 * DH * SW weights of attention per head
+    // and CTA; an FC row costs 2 * SW weights per CTA (FC and MLP parts), so
+    // equal bytes per CTA means nfc_c = base - 2 * DH * heads(c).  frac
+    // (GPT2_FC_BALANCE, default 1) scales that correction; 0 gives equal rows.
+    double frac = 1.0;
+    const char* env_bal = getenv("GPT2_FC_BALANCE");
+    if (env_bal) frac = atof(env_bal);
+    std::vector<int> nrow(NC);
+    {
+        double corr = 0.0;
+        for (int c = 0; c < NC; ++c) corr += frac * 2.0 * DH * cg_heads(g, H, c);
+        const double base = ((double)FF + corr) / NC;
+        int tot = 0;
+        for (int c = 0; c < NC; ++c) {
+            const double w = base - frac * 2.0 * DH * cg_heads(g, H, c);
+            int n = (int)(w / 8.0 + 0.5) * 8;
+            if (n < 8) n = 8;
+            nrow[c] = n;
+            tot += n;
+        }
+        // bring the total to FF in steps of 8 rows, largest clusters first
+        for (int it = 0; tot != FF && it < 100000; ++it) {
+            int best = -1;
+            for (int c = 0; c < NC; ++c) {
+                if (tot > FF && nrow[c] > 8 && (best < 0 || nrow[c] > nrow[best])) best = c;
+                if (tot < FF && (best < 0 || nrow[c] < nrow[best])) best = c;
+            }
+            if (best < 0) return cudaErrorInvalidValue;
+            nrow[best] += tot > FF ? -8 : 8;
+            tot += tot > FF ? -8 : 8;
+        }
+        if (tot != FF) return cudaErrorInvalidValue;
+    }
+    {
+        int o = 0;
+        g.nfc_max = 0;
+        for (int c = 0; c < NC; ++c) {
+            g.fc0[c] = o;
+            o += nrow[c];
+            if (nrow[c] > g.nfc_max) g.nfc_max = nrow[c];
+        }
+        g.fc0[NC] = o;
+    }
+    // stream layout
+    uint64_t off = 0;
+    for (int c = 0; c < NC; ++c) {
+        const int nh = cg_heads(g, H, c), nfc = g.fc0[c + 1] - g.fc0[c];
+        g.cta_bytes[c] = (uint64_t)nh * cg_head_bytes(g, DH) + (uint64_t)2 * nfc * g.SW * g.wb;
+        g.seg[c] = off;
+        off += (uint64_t)CS * g.cta_bytes[c];
+    }
+    g.seg[NC] = off;
+    g.layer_bytes = off;
+    // ring: as many slots as fit
+    // at least one round of chunks (one per consumer warp) must fit the ring
+    int slots = kCMaxSlots;
+    while (slots > kCWarps && csmem_layout(D, DH, CS, g.SW, g.nfc_max, slots).total > (uint32_t)kCMaxSmem) --slots;
+    if (csmem_layout(D, DH, CS, g.SW, g.nfc_max, slots).total > (uint32_t)kCMaxSmem) return cudaErrorInvalidValue;
+    g.slots = slots;
+    *out = g;
+    return cudaSuccess;
+}
+
+cudaError_t cstream_build(const uint8_t* wstream, uint64_t layer_bytes, const uint64_t mat_off[4], int L, int D,
+                          int H, int FF, int wf, const CGeo& g, uint8_t* dst, cudaStream_t st) {
+    const uint32_t rbd = (uint32_t)row_bytes(D, wf), rbf = (uint32_t)row_bytes(FF, wf);
+    for (int l = 0; l < L; ++l) {
+        const uint8_t* src = wstream + (uint64_t)l * layer_bytes;
+        clayout_kernel<<<g.G, 256, 0, st>>>(src, g, D, H, FF, D / H, mat_off[kQKV], mat_off[kO], mat_off[kFC],
+                                            mat_off[kP], rbd, rbf, dst + (uint64_t)l * g.layer_bytes);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_cstep(const CPlan& P, int wf, cudaStream_t stream) {
+    const int D = P.s.D, FF = P.s.FF, DH = P.s.D / P.s.H;
+    CSTEP_DISPATCH(launch_t, P, stream)
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gpt2

@@ -6,24 +6,37 @@
 //   LN2 + FC + GELU, MLP-proj + residual] -> LN_f + tied vocab projection ->
 //   greedy argmax.
 //
-// Work split: every projection is split by OUTPUT rows across the G CTAs.
-// The device keeps every block matrix K-major ([out][in], one contiguous row
-// per output), so CTA c's share of a matrix is one contiguous byte range.
-// Each CTA has one producer warp that streams its shares of all matrices, in
-// step order, through a ring of shared-memory slots with cp.async.bulk and
-// mbarriers; it never waits on activations, so weight streaming runs ahead
-// of the grid-wide dependencies (bounded only by the ring depth and an
-// optional L2 bulk prefetch further ahead).  Eight consumer warps take the
-// chunks round-robin and compute complete dot products from shared memory,
-// so no cross-CTA reduction is needed.  Phases are ordered by per-CTA epoch
-// flags (release/acquire at gpu scope); every spin-wait is bounded by a
-// wall-clock limit after which the kernel records GPT2_ERR_TIMEOUT, sets a
-// global abort word, drains its own bulk copies and returns.
+// This is the step kernel for int8 models (and for every format when
+// GPT2_STEP_KERNEL=legacy); binary32 and binary16 models step on the cluster
+// kernel in cstep.cu.
+//
+// Work split: every projection is split by OUTPUT rows across the G CTAs
+// (one per SM).  The device keeps every block matrix K-major ([out][in], one
+// contiguous row per output), so CTA c's share of a matrix is one contiguous
+// byte range.  Each CTA has 7 consumer warps and 1 producer warp; the
+// producer streams this CTA's shares of all matrices, in step order, through
+// a ring of shared-memory slots with cp.async.bulk and mbarriers and never
+// waits on activations, so weight streaming runs ahead of the grid-wide
+// dependencies (bounded by the ring depth).  Small shares are computed
+// cooperatively by the whole CTA from registers; the vocabulary streams one
+// warp per chunk.  Complete dot products need no cross-CTA reduction.
+//
+// Exchange between phases: every value a phase publishes is one 64-bit
+// tagged word (phase tag << 32 | float bits), stored relaxed at gpu scope
+// and polled by its consumers until the tag matches; a 64-bit word is
+// single-copy atomic, so no flag or fence is needed per phase.  The only
+// release/acquire is one per step, on the greedy partials, which orders the
+// plain KV-cache stores before the next step's attention.  Every spin-wait
+// is bounded by a wall-clock limit after which the kernel records
+// GPT2_ERR_TIMEOUT, sets a global abort word, drains its own bulk copies and
+// returns.
 //
 // Attention is split along the key axis ("flash-decoding" split-KV, lean /
-// llm-web page, GPU-path paragraph): CTA c owns (head, key range) units and
-// writes an unnormalised partial (max, sum, o[64]); the out-projection phase
-// merges the partials of every head before its GEMV.
+// llm-web page, GPU-path paragraph): a unit is (head, key split), one split
+// per 128 keys.  Up to 128 keys a head is a single unit whose output is
+// normalised, and the out-projection gathers it like any vector; with
+// several splits each unit stores (max, sum, unnormalised o) and the
+// out-projection merges them by the log-sum-exp rule before its GEMV.
 //
 // int8 (quantized GPT-2 abstract): projection inputs are quantized per group
 // of 64 coordinates right after they are formed (in shared memory); the

@@ -4,6 +4,7 @@
 #include <cstdint>
 
 #include "../../include/gpt2.h"
+#include "cstep.cuh"
 #include "gpt2_dev.cuh"
 
 struct gpt2_model {
@@ -21,4 +22,7 @@ struct gpt2_model {
     float* d_fold;  // binary32 models: LayerNorm folds of the QKV and FC rows (fold_layer_words per layer)
     float* d_wlo;  // binary32 models: TF32 remainders of the block matrices (prefill), made on first use
     float* d_wte_lo;  // binary32 models: TF32 remainders of the tied embedding (batched decode), made on first use
+    int ckern;        // 1: decode steps run on the cluster step kernel (cstep.cu), 0: on step_kernel (decode.cu)
+    gpt2::CGeo cg;    // its geometry
+    uint8_t* d_cstream;  // its weight stream
 };

@@ -17,7 +17,10 @@
 // the device array, so a kernel given it would fault or, where the GPU can
 // reach host memory, silently use the wrong memory.  The device address is
 // fetched once per device with cudaGetSymbolAddress, with that device
-// current, on the first call made on it.
+// current: gpt2_model_create does it (noalloc_prepare), which also makes
+// CUDA load this module and its array there even under lazy module loading,
+// so stepping itself does no set-up; a call on a device where no model was
+// created does the set-up on its first call.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -29,14 +32,16 @@
 
 namespace gpt2 {
 cudaError_t launch_step(const StepPlan& P, int wq, cudaStream_t stream);
+cudaError_t launch_cstep(const CPlan& P, int wf, cudaStream_t stream);
 }
 
 using namespace gpt2;
 
 namespace {
 
-// Largest scratch one call may use (GPT-2 124M on 152 CTAs needs about 70 KB).
-constexpr size_t kScratchMax = 256 * 1024;
+// Largest scratch one call may use (GPT-2 124M needs about 360 KB on the
+// cluster step kernel, 70 KB on the per-phase kernel).
+constexpr size_t kScratchMax = 512 * 1024;
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -64,6 +69,14 @@ gpt2_status scratch_base(unsigned char** out) {
 
 }  // namespace
 
+namespace gpt2 {
+// Set-up of the scratch array on the current device (called by gpt2_model_create).
+bool noalloc_prepare() {
+    unsigned char* base = nullptr;
+    return scratch_base(&base) == GPT2_OK;
+}
+}  // namespace gpt2
+
 extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_cache, uint32_t position,
                                                 uint32_t token, float* d_logits, uint32_t* d_next_token,
                                                 void* stream) {
@@ -72,7 +85,9 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     if (token >= c.vocab) return GPT2_ERR_TOKEN;
     if (position >= c.max_pos) return GPT2_ERR_POSITION;
     const ScratchLayout k = scratch_layout((int)c.d_model, (int)c.n_head, (int)c.d_ff, m->G);
-    if (k.total > kScratchMax) return GPT2_ERR_SCRATCH;
+    const CScratch ck = cscratch_layout((int)c.d_model, (int)c.n_head, m->cg.NC, m->cg.G);
+    const size_t need = m->ckern ? ck.total : k.total;
+    if (need > kScratchMax) return GPT2_ERR_SCRATCH;
     unsigned char* base = nullptr;
     gpt2_status st = scratch_base(&base);
     if (st != GPT2_OK) return st;
@@ -82,8 +97,8 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     // phases from the same start, so the status words and every tagged
     // exchange word must start at zero (no stale tag may match); the greedy
     // history starts empty.
-    cudaError_t e = cudaMemsetAsync(base, 0, k.total, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(base + k.last_token, 0xFF, 8, s);
+    cudaError_t e = cudaMemsetAsync(base, 0, need, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + (m->ckern ? ck.last_token : k.last_token), 0xFF, 8, s);
     if (e == cudaSuccess && d_next_token) e = cudaMemsetAsync(d_next_token, 0xFF, 4, s);
     if (e != cudaSuccess) return GPT2_ERR_CUDA;
 
@@ -131,6 +146,23 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     P.stall_phase = -1;
     P.prefetch_chunks = 0;
     P.pace_ns = kDefaultPaceNs;
-    e = launch_step(P, m->wfmt, s);
+    if (m->ckern) {
+        // the cluster step kernel: the same plan, its geometry and exchange words
+        CPlan C;
+        memset(&C, 0, sizeof(C));
+        C.s = P;
+        C.g = m->cg;
+        C.cstream = m->d_cstream;
+        C.partO = reinterpret_cast<uint64_t*>(base + ck.partO);
+        C.partP = reinterpret_cast<uint64_t*>(base + ck.partP);
+        C.s.xa = C.s.xb = C.s.qkv = C.s.u = C.s.attn_part = nullptr;
+        C.s.arg_part = reinterpret_cast<uint64_t*>(base + ck.arg);
+        C.s.status = reinterpret_cast<int*>(base + ck.words);
+        C.s.abort_flag = reinterpret_cast<int*>(base + ck.words) + 1;
+        C.s.last_token = reinterpret_cast<uint32_t*>(base + ck.last_token);
+        e = launch_cstep(C, m->wfmt, s);
+    } else {
+        e = launch_step(P, m->wfmt, s);
+    }
     return e == cudaSuccess ? GPT2_OK : (e == cudaErrorMemoryAllocation ? GPT2_ERR_NOMEM : GPT2_ERR_CUDA);
 }

@@ -45,6 +45,7 @@ _SIGS = {
     "gpt2_model_create": ([_cfgp, _vp, _sz, _i32, _i32, C.POINTER(_vp)], _i32),
     "gpt2_model_destroy": ([_vp], None),
     "gpt2_model_read_q8": ([_vp, _i32, _vp, _vp], _i32),
+    "gpt2_model_step_kernel": ([_vp, C.POINTER(_u32), C.POINTER(_u32)], _i32),
     "gpt2_session_create": ([_vp, C.POINTER(_vp)], _i32),
     "gpt2_session_destroy": ([_vp], None),
     "gpt2_session_position": ([_vp], _u32),
@@ -161,6 +162,15 @@ class Model:
         sc = np.empty((n_out, n_in // 64), np.float32)
         _check("gpt2_model_read_q8", lib.gpt2_model_read_q8(self.h, index, q.ctypes.data, sc.ctypes.data))
         return q, sc
+
+    @property
+    def step_kernel(self):
+        """(kind, clusters, cluster_size): kind "cluster" or "phase"
+        (gpt2_model_step_kernel); for "phase" clusters is 0 and cluster_size
+        the CTA count."""
+        nc, cs = C.c_uint32(), C.c_uint32()
+        k = lib.gpt2_model_step_kernel(self.h, C.byref(nc), C.byref(cs))
+        return ("cluster" if k == 1 else "phase"), nc.value, cs.value
 
     def debug_project(self, index: int, x, y, stream=None) -> str:
         """Test hook: projection `index` of x (CUDA tensor) into y (CUDA tensor)."""

@@ -142,6 +142,22 @@ def test_byte_level_validation_matches_oracle(g, oracle):
     P.check_validation(g)  # the pins' validation table, run against the GPU library
 
 
+@pytest.mark.parametrize("shape,quant,kind", [(synth.GPT2_TINY, 0, "cluster"), (synth.GPT2_TINY, 2, "cluster"),
+                                              (P.SMALL, 0, "cluster"), (synth.GPT2_TINY, 1, "phase"),
+                                              (synth.GPT2_TINY, 3, "phase")],
+                         ids=["tiny-f32", "tiny-f16", "small-f32", "tiny-int8", "tiny-int8row"])
+def test_step_kernel_in_use(g, shape, quant, kind):
+    """binary32 and binary16 models step on the cluster kernel (the session
+    tests above therefore test it); int8 models on the per-phase kernel."""
+    model = g.Model(shape, synth.checkpoint(shape, synth.SEED_TINY if shape is synth.GPT2_TINY else P.SEED_SMALL),
+                    quant=quant)
+    k, nc, cs = model.step_kernel
+    assert k == kind
+    if kind == "cluster":
+        assert nc >= 1 and cs >= 1 and shape.d_model % cs == 0
+    model.close()
+
+
 def test_step_apis_agree(g, oracle):
     shape = synth.GPT2_TINY
     w = synth.checkpoint(shape, synth.SEED_TINY, "rich")

@@ -65,3 +65,30 @@ def test_cache_shape_and_scale():
     c = synth.cache(S, 5, seed=1)
     assert c.dtype == np.float32 and c.size == 5 * S.n_layer * 2 * S.d_model
     assert abs(c.std() - 0.5) < 0.05
+
+
+def test_offset_residual_variant_is_rich_plus_the_stated_offsets():
+    lay = synth.layout(S)
+    rich = synth.checkpoint(S, synth.SEED_TINY, "rich")
+    off = synth.checkpoint(S, synth.SEED_TINY, "offset_residual")
+    d = S.d_model
+    diff = (off.astype(np.float64) - rich.astype(np.float64))
+    o, n = lay["wte"]
+    wd = diff[o:o + n].reshape(S.vocab, d)
+    big = [5, d // 3 + 7, 2 * d // 3 + 11]
+    assert np.allclose(wd[:, big], 100.0, atol=1e-3)
+    rest = np.delete(wd, big, axis=1)
+    assert (rest == 0.0).all()
+    o, n = lay["wpe"]
+    assert np.allclose(diff[o:o + n], 3.0, atol=1e-5)
+    for l in range(S.n_layer):
+        o, n = lay[f"h{l}.b_o"]
+        assert np.allclose(diff[o:o + n], 0.25, atol=1e-6)
+    o, n = lay["h0.b_p"]
+    bp = diff[o:o + n]
+    assert abs(bp[d // 2] - 100.0) < 1e-3 and (np.delete(bp, d // 2) == 0.0).all()
+    touched = np.zeros(off.size, bool)
+    for name in ["wte", "wpe", "h0.b_p"] + [f"h{l}.b_o" for l in range(S.n_layer)]:
+        o, n = lay[name]
+        touched[o:o + n] = True
+    assert (diff[~touched] == 0.0).all()
