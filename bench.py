@@ -375,8 +375,21 @@ def long_context(g, torch, w, reps=20):
         us = 1e3 * e0.elapsed_time(e1) / reps
         by = step_bytes(s, "f32", p)
         out[f"p{p}"] = {"us_per_step": us, "GB_per_s": by / us * 1e-3, "bytes": by}
+    # the oracle's step at position 1023 on the cache the GPU built
+    # (single-threaded C on one host core): the long-context CPU baseline
+    row = g.cache_words_per_position(s)
+    cache = sess.read_cache()[:1023 * row]
     sess.close()
     model.close()
+    from oracle import Oracle
+    om = Oracle().model(s, w)
+    t0 = time.perf_counter()
+    st, lg, _ = om.cached_step(cache, int(toks[1023]), 1023)
+    dt = time.perf_counter() - t0
+    om.close()
+    assert st == "ok", st
+    out["oracle_p1023"] = {"tokens_per_s": 1.0 / dt, "s_per_step": dt, "cores": 1,
+                           "sample": "one cachedStep at position 1023 over the GPU-built 1023-position cache"}
     return out
 
 
@@ -525,6 +538,12 @@ def main():
         extra["prefill_f32"] = prefill_rate(g, torch, shape, w)
 
     cpu = None
+    if rank == 0 and not args.no_extra and args.quant == "f32":
+        # the int8 workload's CPU baseline: the oracle's int8 model, same sample
+        r8, dt8 = oracle_decode_rate(shape, w, toks, 1, 16)
+        extra["cpu_baseline_int8"] = {"value": r8, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                      "sample": f"16 int8 greedy decode steps at positions 16..31 after an untimed "
+                                                f"16-token prompt ({dt8:.1f} s)"}
     if rank == 0:
         n_dec = 16
         rate, dt = oracle_decode_rate(shape, w, toks, {"f32": 0, "int8": 1, "f16": 2, "int8_row": 3}[args.quant],

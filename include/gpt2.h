@@ -135,10 +135,11 @@ void gpt2_model_destroy(gpt2_model* model);
 gpt2_status gpt2_model_read_q8(gpt2_model* model, int index, int8_t* q_host, float* s_host);
 
 /* Which kernel runs this model's decode steps: 1 the cluster step kernel
- * (binary32 and binary16 models: thread-block clusters that complete each
- * projection's split-K partials in distributed shared memory), 0 the
- * per-phase step kernel (int8 models, or any model created while the
- * environment variable GPT2_STEP_KERNEL was "legacy").  For the cluster
+ * (thread-block clusters that complete each projection's split-K partials
+ * in distributed shared memory; binary32 and binary16 models created while
+ * the environment variable GPT2_STEP_KERNEL was "cluster"), 0 the per-phase
+ * step kernel (int8 models, and the others unless "cluster" was asked
+ * for; "phase" asks for it explicitly).  For the cluster
  * kernel *clusters and *cluster_size receive its grid (clusters x CTAs per
  * cluster); for the other they receive 0 and its CTA count.  Either pointer
  * may be NULL.  Returns -1 for a NULL model. */

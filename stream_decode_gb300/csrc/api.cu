@@ -66,6 +66,9 @@ struct gpt2_session {
 namespace {
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+// Whether binary32 and binary16 models step on the cluster kernel unless
+// GPT2_STEP_KERNEL says otherwise.
+constexpr bool kClusterStepDefault = false;
 
 size_t words_of(const gpt2_config* c) {
     size_t d = c->d_model, f = c->d_ff;
@@ -329,11 +332,12 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
             CK(cudaMalloc(&m->d_vocab, (uint64_t)cfg->vocab * rbd));
             CK(rows_to_f16(m->d_packed + m->wte_off, m->d_vocab, (size_t)cfg->vocab * D, 0));
         }
-        // decode steps: the cluster step kernel where it supports the shape
-        // and weight format (GPT2_STEP_KERNEL=legacy keeps step_kernel)
+        // decode steps: GPT2_STEP_KERNEL=cluster selects the cluster step
+        // kernel where it supports the shape and weight format, =phase the
+        // per-phase kernel; unset, kClusterStepDefault decides
         const char* sk = getenv("GPT2_STEP_KERNEL");
-        const bool legacy = sk && strcmp(sk, "legacy") == 0;
-        if (!legacy && cstep_supported(D, FF, D / (int)cfg->n_head, wfmt)) {
+        const bool want_cluster = sk ? strcmp(sk, "cluster") == 0 : kClusterStepDefault;
+        if (want_cluster && cstep_supported(D, FF, D / (int)cfg->n_head, wfmt)) {
             CK(cgeo_make(L, D, (int)cfg->n_head, FF, wfmt, grid_ctas, &m->cg));
             CK(cudaMalloc(&m->d_cstream, m->cg.layer_bytes * L));
             CK(cstream_build(m->d_wstream, m->layer_bytes, m->mat_off, L, D, (int)cfg->n_head, FF, wfmt, m->cg,

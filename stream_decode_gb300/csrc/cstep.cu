@@ -157,23 +157,26 @@ __host__ __device__ constexpr uint32_t unit_bytes() { return WF == kWF16 ? 8u : 
 template <int WF>
 __device__ __forceinline__ float chunk_rows(uint32_t w, int R, int W4, uint32_t x, int lane) {
     constexpr uint32_t UB = unit_bytes<WF>();
-    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    float a[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
     if (lane < R) {
         const uint32_t step = (uint32_t)R * UB;
-        uint32_t wa = w + (uint32_t)lane * UB;
+        uint32_t wa = w + (uint32_t)lane * UB, xa = x;
         int c = 0;
-        for (; c + 4 <= W4; c += 4, wa += 4 * step) {
-            const float4 w0 = ldsw<WF>(wa), w1 = ldsw<WF>(wa + step), w2 = ldsw<WF>(wa + 2 * step),
-                         w3 = ldsw<WF>(wa + 3 * step);
-            const uint32_t xa = x + 16u * (uint32_t)c;
-            a0 = dot4(a0, w0, lds4(xa));
-            a1 = dot4(a1, w1, lds4(xa + 16));
-            a2 = dot4(a2, w2, lds4(xa + 32));
-            a3 = dot4(a3, w3, lds4(xa + 48));
+        for (; c + 8 <= W4; c += 8, wa += 8 * step, xa += 128) {
+#pragma unroll
+            for (int h2 = 0; h2 < 8; h2 += 4) {
+                float4 wv[4], xv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) wv[u] = ldsw<WF>(wa + (h2 + u) * step);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) xv[u] = lds4(xa + 16u * (h2 + u));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) a[h2 + u] = dot4(a[h2 + u], wv[u], xv[u]);
+            }
         }
-        for (; c < W4; ++c, wa += step) a0 = dot4(a0, ldsw<WF>(wa), lds4(x + 16u * (uint32_t)c));
+        for (; c < W4; ++c, wa += step, xa += 16) a[0] = dot4(a[0], ldsw<WF>(wa), lds4(xa));
     }
-    return (a0 + a1) + (a2 + a3);
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
 // NR consecutive K-major rows (pitch pb bytes, W4 float4 columns each) in
@@ -566,6 +569,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     // Rows of a share against x4 (W4 float4 columns); row i's dot product to
     // out[i].  Chunk k is taken by warp k % 8.
     uint64_t prof_wait = 0, prof_total = 0;  // warp 0, last share: clock64 cycles waiting for chunks, in all
+    uint64_t prof_comb = 0;                  // thread 0: cycles of the last QKV combine
     // The chunks are taken in rounds of one per warp with a barrier between
     // rounds.  The ring's barriers are waited on by phase parity, which is
     // only unambiguous if the previous fill of a chunk's slot has landed;
@@ -612,57 +616,38 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         csync();
         return t;
     };
-    // Waits until every one of nw partial vectors (base + k * D, k < nw) has
-    // this slice's last word tagged `tag`: one lane of warp 0 per vector
-    // polls that sentinel, so a waiting CTA keeps nw loads in flight rather
-    // than one per word.  Called by every consumer thread; ends with an
+    // Adds the nw (<= 24) partial vectors base[k * D + col0 + e] (k < nw,
+    // tagged `tag`) and bias b to this slice of the residual, summed in
+    // vector order: xs[e] += (sum_k v_k) + b[e].  Thread e < SW polls its
+    // column's words, all loaded in one round trip per poll.  Ends with an
     // agreement barrier.
-    auto wait_sentinels = [&](const uint64_t* base, int nw, unsigned tag) -> bool {
+    constexpr int kMaxPollWords = 24;
+    auto gather_add = [&](const uint64_t* base, int nw, unsigned tag, const float* bias) -> bool {
         bool ok = true;
-        if (warp == 0) {
-            const uint64_t* sp = base + (size_t)lane * D + col0 + (SW - 1);
-            bool done = lane >= nw;
+        if (tid < SW) {
+            uint64_t w[kMaxPollWords];
+            uint32_t pending = (1u << nw) - 1u;
+            const uint64_t* p0 = base + col0 + tid;
+            const float bv = __ldg(bias + col0 + tid);
             uint64_t t0 = 0;
-            uint32_t spins = 0;
-            while (true) {
-                if (!done) done = tag_of(ld_tagged(sp)) == tag;
-                if (__all_sync(0xffffffffu, done)) break;
-                if ((++spins & 15) == 0) {
-                    const unsigned pend = __ballot_sync(0xffffffffu, !done);
-                    const int give = lane == 0 ? (int)timed_out(t0, 3, (uint64_t)pend) : 0;
-                    if (__shfl_sync(0xffffffffu, give, 0)) { ok = false; break; }
-                }
+            while (pending) {
+#pragma unroll
+                for (int i = 0; i < kMaxPollWords; ++i)
+                    if ((pending >> i) & 1u) w[i] = ld_tagged(p0 + (size_t)i * D);
+#pragma unroll
+                for (int i = 0; i < kMaxPollWords; ++i)
+                    if (((pending >> i) & 1u) && tag_of(w[i]) == tag) pending &= ~(1u << i);
+                if (pending && timed_out(t0, 3, pending)) { ok = false; break; }
+            }
+            if (ok) {
+                float y = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kMaxPollWords; ++i)
+                    if (i < nw) y += val_of(w[i]);
+                xs[tid] = __fadd_rn(xs[tid], __fadd_rn(y, bv));
             }
         }
         return agree(ok);
-    };
-    // The ordered sum of the nw tagged words base[k * D + col] (k < nw) of
-    // this thread's column, once their sentinels carry `tag` (words still in
-    // flight from the same stores are re-read).
-    auto gather_sum = [&](const uint64_t* base, int nw, int col, unsigned tag, float& sum) -> bool {
-        constexpr int B = 8;
-        sum = 0.0f;
-        uint64_t t0 = 0;
-        for (int k0 = 0; k0 < nw; k0 += B) {
-            uint64_t w[B];
-            uint32_t pending = 0;
-#pragma unroll
-            for (int i = 0; i < B; ++i)
-                if (k0 + i < nw) pending |= 1u << i;
-            while (pending) {
-#pragma unroll
-                for (int i = 0; i < B; ++i)
-                    if ((pending >> i) & 1u) w[i] = ld_tagged(base + (size_t)(k0 + i) * D + col);
-#pragma unroll
-                for (int i = 0; i < B; ++i)
-                    if (((pending >> i) & 1u) && tag_of(w[i]) == tag) pending &= ~(1u << i);
-                if (pending && timed_out(t0, 3)) return false;
-            }
-#pragma unroll
-            for (int i = 0; i < B; ++i)
-                if (k0 + i < nw) sum += val_of(w[i]);
-        }
-        return true;
     };
     // This slice's (mean, M2) of x - s (two passes over SW values), by warp 0, into dst[0..1].
     auto slice_stats = [&](float s, float* dst) {
@@ -684,18 +669,24 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             dst[1] = q;
         }
     };
-    // Merged (mean, M2) of CS slices whose stats sit at base + r' * stride.
+    // Mean and inverse deviation of the whole vector from the CS slices'
+    // (mean, M2) at base + r' * stride.  The slices have equal sizes, so the
+    // mean is the mean of the slice means and the sum of squares is
+    // sum M2_r + SW * sum (mean_r - mean)^2 (the pairwise update of Chan et
+    // al. with equal counts), with no cancellation.
     auto merge_stats = [&](const float* base, int stride, float& mean, float& rstd) {
-        float n = 0.0f, mu = 0.0f, m2 = 0.0f;
+        float mu = 0.0f;
+        for (int k = 0; k < CS; ++k) mu += base[k * stride];
+        mu = mu / (float)CS;
+        float m2 = 0.0f, sd = 0.0f;
         for (int k = 0; k < CS; ++k) {
-            const float nb = (float)SW, mb = base[k * stride], qb = base[k * stride + 1];
-            const float nn = n + nb, dl = mb - mu;
-            mu = mu + dl * (nb / nn);
-            m2 = m2 + qb + dl * dl * (n * nb / nn);
-            n = nn;
+            const float dl = base[k * stride] - mu;
+            m2 += base[k * stride + 1];
+            sd = fmaf(dl, dl, sd);
         }
+        m2 = fmaf((float)SW, sd, m2);
         mean = mu;
-        rstd = 1.0f / sqrtf(m2 / (float)D + kLnEps);
+        rstd = rsqrtf(m2 / (float)D + kLnEps);
     };
 
     // Greedy partials of the previous step (tag), reduced in every CTA; the
@@ -917,6 +908,19 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             const float g1 = tid < SW ? __ldg(P.packed + lp.ln1_g + col0 + tid) : 0.0f;
             const float g2 = tid < SW ? __ldg(P.packed + lp.ln2_g + col0 + tid) : 0.0f;
             float ln_shift = shift;  // shift of the LayerNorm being folded
+            // this layer's cached keys and values of this CTA's attention
+            // positions, prefetched into L2 while the block input forms
+            if (nh > 0) {
+                const int n = p + 1;
+                const int kk0 = (int)(((long long)r * n) / CS), kk1 = (int)(((long long)(r + 1) * n) / CS);
+                const int kk1c = kk1 < p ? kk1 : p;
+                for (int t = tid; t < (kk1c - kk0) * nh * 4; t += NT) {
+                    const int j = kk0 + t / (4 * nh), hs = (t / 4) % nh, part = t % 4;
+                    const float* row = P.cache + ((uint64_t)j * L + l) * 2 * D + (part >> 1) * D +
+                                       (c + hs * GG.NC) * DH + (part & 1) * (DH / 2);
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+                }
+            }
             // Micro-phases of the layer, one runtime loop so that each routine
             // (gather, dot products, all-gather, store) has one copy in the
             // binary: per head slot k of this cluster QKV (0), attention (1),
@@ -933,18 +937,13 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     const int q0 = (l > 0 && (kind == 0 || nh == 0)) ? 0 : 1, q1 = kind == 3 ? 1 : 0;
                     for (int q = q0; q <= q1 && alive; ++q) {
                         const uint64_t* src = q == 0 ? CP.partP + (size_t)((l - 1) & 1) * GG.NC * D : CP.partO;
-                        const int nw = q == 0 ? GG.NC : H;
-                        const unsigned tg = q == 0 ? tagA - 1u : tagA;
-                        const float bv = tid < SW ? __ldg(P.packed + (q == 0 ? P.lp[l - 1].b_p : lp.b_o) + col0 + tid) : 0.0f;
-                        if (!wait_sentinels(src, nw, tg)) { alive = false; break; }
-                        bool ok = true;
-                        if (tid < SW) {
-                            float y;
-                            ok = gather_sum(src + col0, nw, tid, tg, y);
-                            xs[tid] = __fadd_rn(xs[tid], __fadd_rn(y, bv));
+                        if (!gather_add(src, q == 0 ? GG.NC : H, q == 0 ? tagA - 1u : tagA,
+                                        P.packed + (q == 0 ? P.lp[l - 1].b_p : lp.b_o))) {
+                            alive = false;
+                            break;
                         }
-                        if (!agree(ok)) { alive = false; break; }
                         stamp(16 * l + (q == 0 ? 0 : 6));
+                        if (q == 0 && stamps && cur_step == 0 && tid == 0) stamps[16 * l + 15] = (uint64_t)clock64();
                         if (tr && c == 0) ctrace_copy(P.trace + (size_t)l * trace_layer + (q == 0 ? 0 : 6 * D) + col0, xs, SW, tid);
                     }
                     if (!alive) break;
@@ -981,8 +980,11 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     if (!agree(ok)) { alive = false; break; }
                     stamp(16 * l + (kind == 0 ? 1 : kind == 2 ? 5 : kind == 3 ? 7 : 9));
                 } else {
+                    const long long t_att = clock64();
                     attention(l, h, p);
                     csync();
+                    if (stamps && cur_step == 0 && tid == 0)
+                        stamps[16 * l + 14] = (prof_comb << 32) | ((uint64_t)(clock64() - t_att) & 0xFFFFFFFFull);
                     stamp(16 * l + 3);
                 }
                 // ---- the cluster all-gather (QKV partials, attention partials, FC partials)
@@ -1032,12 +1034,17 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     if (!gather_wait(bar, (uint32_t)(CS * nsend * 4), (u >> 1) & 1)) { alive = false; break; }
                     stamp(16 * l + (kind == 0 ? 2 : kind == 1 ? 4 : 8));
                     // ---- epilogues of the gathered values
+                    const long long t_epi = clock64();
                     if (kind == 0) {
                         float mean, rstd;
                         merge_stats(gbuf + 3 * DH, rowl, mean, rstd);
                         if (tid < 3 * DH) {
                             float a = 0.0f;
-                            for (int q = 0; q < CS; ++q) a += gbuf[(size_t)q * rowl + tid];
+                            float pv[16];
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) pv[q] = q < CS ? gbuf[(size_t)q * rowl + tid] : 0.0f;
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) if (q < CS) a += pv[q];
                             const float y = fmaf(rstd, fmaf(-mean, cj, a), dj);
                             qkv[tid] = y;
                             if (tid >= DH && (tid % CS) == r) {
@@ -1050,6 +1057,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                             ctrace_ln(P.trace + (size_t)l * trace_layer + D + col0, xs, ln_shift + mean, rstd,
                                       P.packed + lp.ln1_g + col0, P.packed + lp.ln1_b + col0, SW, tid);
                         if (k == nh - 1) shift = ln_shift + mean;
+                        if (stamps && cur_step == 0 && tid == 0) prof_comb = (uint64_t)(clock64() - t_epi);
                     } else if (kind == 1) {
                         if (tid < DH) {
                             float M = -INFINITY;
@@ -1071,7 +1079,11 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                         merge_stats(gbuf + nfc4, rowl, mean, rstd);
                         for (int j = tid; j < nfc; j += NT) {
                             float a = 0.0f;
-                            for (int q = 0; q < CS; ++q) a += gbuf[(size_t)q * rowl + j];
+                            float pv[16];
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) pv[q] = q < CS ? gbuf[(size_t)q * rowl + j] : 0.0f;
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) if (q < CS) a += pv[q];
                             float cc = cj, dd = dj;
                             if (j != tid) {
                                 cc = __ldg(fl + 6 * D + f0 + j);
@@ -1098,18 +1110,10 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         }
         if (!alive) break;
         // ================= final LayerNorm and the vocabulary rows
-        {
-            const unsigned tin = base + 2u * (unsigned)L;  // last layer's B
-            const uint64_t* src = CP.partP + (size_t)((L - 1) & 1) * GG.NC * D;
-            const float bp = tid < SW ? __ldg(P.packed + P.lp[L - 1].b_p + col0 + tid) : 0.0f;
-            if (!wait_sentinels(src, GG.NC, tin)) { alive = false; break; }
-            bool ok = true;
-            if (tid < SW) {
-                float y;
-                ok = gather_sum(src + col0, GG.NC, tid, tin, y);
-                xs[tid] = __fadd_rn(xs[tid], __fadd_rn(y, bp));
-            }
-            if (!agree(ok)) { alive = false; break; }
+        if (!gather_add(CP.partP + (size_t)((L - 1) & 1) * GG.NC * D, GG.NC, base + 2u * (unsigned)L,
+                        P.packed + P.lp[L - 1].b_p)) {
+            alive = false;
+            break;
         }
         stamp(16 * L + 0);
         bcast(xs, gX + col0, SW, &bars[6]);
@@ -1353,12 +1357,13 @@ cudaError_t cgeo_make(int L, int D, int H, int FF, int wf, int want_ctas, CGeo* 
     g.CS = CS;
     g.SW = D / CS;
     g.wb = wf == kWF16 ? 2 : 4;
-    if (g.SW > kCWarps * 32 || FF % 8 != 0 || DH % 8 != 0) return cudaErrorInvalidValue;
+    if (g.SW > kCWarps * 32 || FF % 8 != 0 || DH % 8 != 0 || H > 24) return cudaErrorInvalidValue;
     // clusters co-resident at one CTA per SM (the kernel's ring takes what
     // shared memory the rest leaves)
     int maxc = max_clusters(D, FF, DH, wf, CS, (uint32_t)kCMaxSmem);
     if (maxc <= 0) return cudaErrorInvalidConfiguration;
-    int NC = maxc < kCMaxClusters ? maxc : kCMaxClusters;
+    // at most 24 clusters: a CTA polls one word per cluster in one round trip
+    int NC = maxc < 24 ? maxc : 24;
     if (want_ctas > 0) {
         const int w = (want_ctas + CS - 1) / CS;
         if (w < NC) NC = w;
@@ -1371,8 +1376,10 @@ cudaError_t cgeo_make(int L, int D, int H, int FF, int wf, int want_ctas, CGeo* 
     // FC rows: head clusters carry 4 * DH * SW weights of attention per head
     // and CTA; an FC row costs 2 * SW weights per CTA (FC and MLP parts), so
     // equal bytes per CTA means nfc_c = base - 2 * DH * heads(c).  frac
-    // (GPT2_FC_BALANCE, default 1) scales that correction; 0 gives equal rows.
-    double frac = 1.0;
+    // (GPT2_FC_BALANCE) scales that correction; the default 0 gives equal
+    // rows, which measured faster (the stage that follows the FC rows waits
+    // for the slowest cluster).
+    double frac = 0.0;
     const char* env_bal = getenv("GPT2_FC_BALANCE");
     if (env_bal) frac = atof(env_bal);
     std::vector<int> nrow(NC);

@@ -28,7 +28,11 @@
 namespace gpt2 {
 
 constexpr int kCMaxClusters = 32;
-constexpr int kCWarps = 8;                       // consumer warps
+// Seven consumer warps plus the producer: at most two warps per SM
+// sub-partition, so every thread may use 255 registers (a third warp on one
+// sub-partition caps it at 168, and spills land in local memory, which has
+// little L1 left beside the ring).
+constexpr int kCWarps = 7;                       // consumer warps
 constexpr int kCThreads = (kCWarps + 1) * 32;    // + one producer warp
 constexpr int kCSlotBytes = 16384;               // one ring slot
 constexpr int kCMaxSlots = 16;

@@ -146,11 +146,13 @@ def checkpoint(s: Shape, seed: int, variant: str = "plain", block: int = 1 << 23
     trained GPT-2 models; used by the int8 scale-granularity ablation).
     ``offset_residual``: as rich, plus a residual stream that is hard on
     LayerNorm arithmetic: three fixed channels (5, d/3 + 7, 2d/3 + 11) of
-    every wte row are raised by 100, every wpe word by 3 (a nonzero residual
-    mean), every block's b_o by 0.25 (the mean drifts from layer to layer)
-    and channel d/2 of block 0's b_p by 100.  A variance formed as
+    every wpe row are raised by 100 and every other wpe word by 3 (a nonzero
+    residual mean), every block's b_o by 0.25 (the mean drifts from layer to
+    layer) and channel d/2 of block 0's b_p by 100.  A variance formed as
     E[x^2] - mean^2, or a LayerNorm folded without removing the common
-    offset first, loses most of its bits on such a stream.
+    offset first, loses most of its bits on such a stream.  wte (the tied
+    vocabulary matrix) is left as in rich, so the logits keep the magnitude
+    at which a binary32 tolerance of 2e-3 is meaningful.
     """
     if variant not in ("plain", "rich", "zero_blocks", "outlier_channels", "offset_residual"):
         raise ValueError(variant)
@@ -158,12 +160,11 @@ def checkpoint(s: Shape, seed: int, variant: str = "plain", block: int = 1 << 23
         out = checkpoint(s, seed, "rich", block)
         lay = layout(s)
         d = s.d_model
-        o, n = lay["wte"]
-        wte = out[o:o + n].reshape(s.vocab, d)
-        for ch in (5, d // 3 + 7, 2 * d // 3 + 11):
-            wte[:, ch] += np.float32(100.0)
         o, n = lay["wpe"]
-        out[o:o + n] += np.float32(3.0)
+        wpe = out[o:o + n].reshape(s.n_pos, d)
+        wpe += np.float32(3.0)
+        for ch in (5, d // 3 + 7, 2 * d // 3 + 11):
+            wpe[:, ch] += np.float32(97.0)
         for l in range(s.n_layer):
             o, n = lay[f"h{l}.b_o"]
             out[o:o + n] += np.float32(0.25)

@@ -23,6 +23,14 @@ def g():
     return gpt2
 
 
+@pytest.fixture(params=["phase", "cluster"])
+def kernel(request, monkeypatch):
+    """Runs a binary32 / binary16 test on each step kernel (the variable is
+    read when a model is created)."""
+    monkeypatch.setenv("GPT2_STEP_KERNEL", request.param)
+    return request.param
+
+
 @pytest.fixture(scope="module")
 def ref_f32(oracle, w124m):
     """The oracle's greedy session: 16 uniform random prompt tokens at
@@ -34,7 +42,7 @@ def ref_f32(oracle, w124m):
     return out
 
 
-def test_124m_f32_decode_128_positions(g, w124m, ref_f32):
+def test_124m_f32_decode_128_positions(g, w124m, ref_f32, kernel):
     s = synth.GPT2_124M
     seq, ref, ref_ch, ref_cache = ref_f32
     model = g.Model(s, w124m)
@@ -73,7 +81,7 @@ def test_124m_int8_decode_128_positions(g, oracle, w124m, ref_f32, quant):
           f"greedy agreement {greedy_agreement(ref, ch):.3f}")
 
 
-def test_124m_f16_decode_128_positions(g, oracle, w124m):
+def test_124m_f16_decode_128_positions(g, oracle, w124m, kernel):
     """Binary16 weight storage at full size: against the oracle's
     binary16-weight model, to the binary32 bar."""
     s = synth.GPT2_124M
@@ -99,7 +107,7 @@ def test_124m_projections_on_identical_inputs(g, oracle, w124m, quant):
 
 
 @pytest.mark.parametrize("p", [128, 512, 1023])
-def test_124m_long_context_positions(g, oracle, w124m, p):
+def test_124m_long_context_positions(g, oracle, w124m, p, kernel):
     """A seeded synthetic cache of p prior positions (keys/values ~ N(0, 0.25),
     the magnitude N(0,0.02) weights give), then one step at position p with
     token = the p-th uniform random token, on both sides."""
@@ -120,3 +128,54 @@ def test_124m_long_context_positions(g, oracle, w124m, p):
     out = sess.read_cache()
     assert np.array_equal(out[:p * row].view(np.uint32), cache.view(np.uint32))
     assert np.abs(out[p * row:] - ocache[p * row:]).max() <= LOGIT_TOL
+
+
+@pytest.fixture(scope="module")
+def ref_long(oracle, w124m):
+    """The long-context configuration as the workload defines it: 1024
+    uniform random tokens fed through the oracle's own cached steps, so its
+    cache of 1023 prior positions is the model's, not a synthetic one.
+    Returns (tokens, logits at positions 128, 512 and 1023, final cache)."""
+    s = synth.GPT2_124M_LONG
+    toks = [int(t) for t in synth.tokens(s.vocab, 1024, seed=1234)]
+    om = oracle.model(s, w124m)
+    logits, _, cache = om.session(toks, 1024)
+    om.close()
+    return toks, {p: logits[p].copy() for p in (128, 512, 1023)}, cache
+
+
+def test_124m_long_context_model_built_cache(g, w124m, ref_long, kernel):
+    """GPU and oracle are fed the same 1024 tokens (one launch on the GPU):
+    logits at positions 128, 512 and 1023 and every cache row agree."""
+    s = synth.GPT2_124M_LONG
+    toks, ref, ref_cache = ref_long
+    model = g.Model(s, w124m)
+    sess = g.Session(model)
+    logits, ch = run(sess, toks, 1024)
+    for p, ol in ref.items():
+        assert np.abs(logits[p] - ol).max() <= LOGIT_TOL, p
+        assert disagreements_are_near_ties(ol[None], ch[p:p + 1], LOGIT_TOL), p
+    cache = sess.read_cache()
+    assert cache.size == ref_cache.size and np.abs(cache - ref_cache).max() <= LOGIT_TOL
+    sess.close()
+    model.close()
+
+
+def test_124m_offset_residual_decode(g, oracle, kernel):
+    """GPT-2 124M on the offset_residual checkpoint (residual channels near
+    100, a drifting common offset): 32 positions teacher-forced on the
+    oracle's greedy sequence, to the binary32 bar."""
+    s = synth.GPT2_124M
+    w = synth.checkpoint(s, synth.SEED_124M, "offset_residual")
+    om = oracle.model(s, w)
+    seq, ref, ref_ch, ref_cache = oracle_greedy(om, synth.tokens(s.vocab, 8), 32)
+    om.close()
+    model = g.Model(s, w)
+    sess = g.Session(model)
+    logits, ch = run(sess, list(seq), 32)
+    assert np.abs(logits - ref).max() <= LOGIT_TOL, np.abs(logits - ref).max()
+    assert disagreements_are_near_ties(ref, ch, LOGIT_TOL)
+    cache = sess.read_cache()
+    assert np.abs(cache - ref_cache[:cache.size]).max() <= LOGIT_TOL
+    sess.close()
+    model.close()

@@ -151,3 +151,12 @@ def test_124m_long_context_batch(g, oracle, w124m):
     cached lengths 600, 900 and 1020 (seeded synthetic caches), two steps
     each, so the decode attention runs up to 64 passes of 16 keys."""
     _check_batch(g, oracle, synth.GPT2_124M_LONG, w124m, 3, 2, [600, 900, 1020])
+
+
+@pytest.mark.parametrize("B", [64, 256])
+def test_124m_batch_sizes_benched(g, oracle, w124m, B):
+    """GPT-2 124M at the batch sizes the benchmark times (64 and 256
+    sessions; two 128-row M tiles and four at 256), cached lengths 0..12, 3
+    steps each."""
+    p0s = [(7 * b) % 13 for b in range(B)]
+    _check_batch(g, oracle, synth.GPT2_124M, w124m, B, 3, p0s, seed=1700 + B)

@@ -30,6 +30,14 @@ def g():
     return gpt2
 
 
+@pytest.fixture(params=["phase", "cluster"])
+def kernel(request, monkeypatch):
+    """Runs a binary32 / binary16 test on each step kernel (the variable is
+    read when a model is created)."""
+    monkeypatch.setenv("GPT2_STEP_KERNEL", request.param)
+    return request.param
+
+
 def _session_case(g, oracle, shape, seed, variant, quant, grid, n_prompt=8):
     """The oracle runs its own greedy session from a seeded prompt; the GPU is
     fed that token sequence (one launch), and separately runs greedily on the
@@ -67,13 +75,24 @@ def _check_f32_session(out):
 
 
 @pytest.mark.parametrize("grid", [0, 1, 3, 7, 37])
-def test_tiny_f32_session(g, oracle, grid):
+def test_tiny_f32_session(g, oracle, grid, kernel):
     _check_f32_session(_session_case(g, oracle, synth.GPT2_TINY, synth.SEED_TINY, "rich", 0, grid))
 
 
 @pytest.mark.parametrize("grid", [0, 5])
-def test_small_shape_f32_session(g, oracle, grid):
+def test_small_shape_f32_session(g, oracle, grid, kernel):
     _check_f32_session(_session_case(g, oracle, P.SMALL, P.SEED_SMALL, "rich", 0, grid))
+
+
+@pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
+                         ids=["tiny", "small"])
+def test_offset_residual_f32_session(g, oracle, shape, seed, kernel):
+    """LayerNorm on a residual stream with channels near 100 and a common
+    offset that drifts from layer to layer (synthetic variant
+    offset_residual): the README applies LayerNorm to whatever the weights
+    make of the stream, and a variance formed as E[x^2] - mean^2 would lose
+    most of its bits here."""
+    _check_f32_session(_session_case(g, oracle, shape, seed, "offset_residual", 0, 0))
 
 
 def test_argmax_bit_exact(g, oracle):
@@ -142,23 +161,24 @@ def test_byte_level_validation_matches_oracle(g, oracle):
     P.check_validation(g)  # the pins' validation table, run against the GPU library
 
 
-@pytest.mark.parametrize("shape,quant,kind", [(synth.GPT2_TINY, 0, "cluster"), (synth.GPT2_TINY, 2, "cluster"),
-                                              (P.SMALL, 0, "cluster"), (synth.GPT2_TINY, 1, "phase"),
-                                              (synth.GPT2_TINY, 3, "phase")],
+@pytest.mark.parametrize("shape,quant", [(synth.GPT2_TINY, 0), (synth.GPT2_TINY, 2), (P.SMALL, 0), (synth.GPT2_TINY, 1),
+                                         (synth.GPT2_TINY, 3)],
                          ids=["tiny-f32", "tiny-f16", "small-f32", "tiny-int8", "tiny-int8row"])
-def test_step_kernel_in_use(g, shape, quant, kind):
-    """binary32 and binary16 models step on the cluster kernel (the session
-    tests above therefore test it); int8 models on the per-phase kernel."""
+def test_step_kernel_in_use(g, shape, quant, kernel):
+    """binary32 and binary16 models step on the kernel GPT2_STEP_KERNEL
+    names (so the session tests run on each); int8 models on the per-phase
+    kernel."""
     model = g.Model(shape, synth.checkpoint(shape, synth.SEED_TINY if shape is synth.GPT2_TINY else P.SEED_SMALL),
                     quant=quant)
     k, nc, cs = model.step_kernel
+    kind = kernel if quant in (0, 2) else "phase"
     assert k == kind
     if kind == "cluster":
         assert nc >= 1 and cs >= 1 and shape.d_model % cs == 0
     model.close()
 
 
-def test_step_apis_agree(g, oracle):
+def test_step_apis_agree(g, oracle, kernel):
     shape = synth.GPT2_TINY
     w = synth.checkpoint(shape, synth.SEED_TINY, "rich")
     toks = synth.tokens(shape.vocab, 6, seed=8)
@@ -182,7 +202,7 @@ def test_step_apis_agree(g, oracle):
     assert b.step(shape.vocab, d_logits, d_next) == "token"
 
 
-def test_run_host_matches_device_run(g):
+def test_run_host_matches_device_run(g, kernel):
     """gpt2_session_run_host (host token ids in, every step's logits and
     choices back in host memory) gives the device run's bits, with greedy
     feedback, and checks its host tokens before any launch."""
@@ -207,7 +227,7 @@ def test_run_host_matches_device_run(g):
     model.close()
 
 
-def test_greedy_token_without_history_is_an_error(g):
+def test_greedy_token_without_history_is_an_error(g, kernel):
     shape = synth.GPT2_TINY
     sess = g.Session(g.Model(shape, synth.checkpoint(shape, synth.SEED_TINY)))
     tin = dev_tokens([GREEDY, GREEDY])
@@ -215,7 +235,7 @@ def test_greedy_token_without_history_is_an_error(g):
     assert sess.sync() == "token"
 
 
-def test_nonfinite_logits_reported(g):
+def test_nonfinite_logits_reported(g, kernel):
     shape = synth.GPT2_TINY
     w = synth.checkpoint(shape, synth.SEED_TINY)
     lay = synth.layout(shape)
@@ -227,7 +247,7 @@ def test_nonfinite_logits_reported(g):
     assert (int(tout.cpu().numpy()[0]) & 0xFFFFFFFF) == 0xFFFFFFFF
 
 
-def test_stalled_phase_times_out_and_session_recovers(g):
+def test_stalled_phase_times_out_and_session_recovers(g, kernel):
     """A CTA that never publishes a phase makes the others' bounded waits
     expire: the run ends with 'timeout' (no hang, no fault) and the session is
     usable again after the status is read."""
@@ -242,7 +262,75 @@ def test_stalled_phase_times_out_and_session_recovers(g):
     assert np.isfinite(logits).all()
 
 
-def test_run_to_run_determinism(g):
+@pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
+                         ids=["tiny", "small"])
+def test_rewind_and_resume_are_bit_identical(g, shape, seed, kernel):
+    """The session recurrence (README cachedStep paragraph: each returned
+    cache is passed to the next position): rewinding to a position and
+    stepping again, or taking the cache at a position into a new session
+    and continuing there, gives the uninterrupted run's bits."""
+    w = synth.checkpoint(shape, seed, "rich")
+    model = g.Model(shape, w)
+    n, half = shape.max_pos, shape.max_pos // 2
+    toks = [int(t) for t in synth.tokens(shape.vocab, n, seed=21)]
+    full, full_ch = run(g.Session(model), toks, n)
+    # rewind: the second half again on the same session
+    a = g.Session(model)
+    run(a, toks, n)
+    assert a.rewind(half) == "ok" and a.position == half
+    again, again_ch = run(a, toks[half:], n - half)
+    assert np.array_equal(again.view(np.uint32), full[half:].view(np.uint32))
+    assert np.array_equal(again_ch, full_ch[half:])
+    # snapshot at half: the cache into a fresh session, then continue
+    b = g.Session(model)
+    run(b, toks[:half], half)
+    snap = b.read_cache()
+    c = g.Session(model)
+    assert c.load_cache(snap) == "ok" and c.position == half
+    cont, cont_ch = run(c, toks[half:], n - half)
+    assert np.array_equal(cont.view(np.uint32), full[half:].view(np.uint32))
+    assert np.array_equal(cont_ch, full_ch[half:])
+    assert np.array_equal(c.read_cache().view(np.uint32), a.read_cache().view(np.uint32))
+    for s_ in (a, b, c):
+        s_.close()
+    model.close()
+
+
+def test_writes_stay_inside_their_buffers(g, kernel):
+    """Canaries: a caller-owned cache filled with a pattern keeps it past
+    the positions stepped; logits written with a stride above vocab leave
+    the gaps between steps untouched; the choices buffer past the run is
+    untouched."""
+    shape = synth.GPT2_TINY
+    w = synth.checkpoint(shape, synth.SEED_TINY, "rich")
+    model = g.Model(shape, w)
+    V, row, n = shape.vocab, g.cache_words_per_position(shape), 5
+    canary = np.uint32(0x7FC0DEAD)  # a NaN payload no step can produce
+    cache = torch.tensor(np.full(shape.max_pos * row, canary, np.uint32).view(np.float32), device="cuda")
+    out = torch.empty(V, dtype=torch.float32, device="cuda")
+    for p, t in enumerate(synth.tokens(V, n, seed=3)):
+        assert model.cached_step_noalloc(cache, p, int(t), out) == "ok"
+    torch.cuda.synchronize()
+    c = cache.cpu().numpy().view(np.uint32)
+    assert (c[n * row:] == canary).all(), "a step wrote past its position's cache row"
+    assert not (c[:n * row] == canary).any()
+    stride = V + 37
+    lg = torch.tensor(np.full(n * stride + 11, canary, np.uint32).view(np.float32), device="cuda")
+    tout = torch.full((n + 9,), -12345, dtype=torch.int32, device="cuda")
+    sess = g.Session(model)
+    assert sess.run(dev_tokens(list(synth.tokens(V, n, seed=4))), n, lg, stride, tout) == "ok"
+    assert sess.sync() == "ok"
+    l = lg.cpu().numpy().view(np.uint32)
+    for s_ in range(n):
+        assert not (l[s_ * stride:s_ * stride + V] == canary).any()
+        assert (l[s_ * stride + V:(s_ + 1) * stride] == canary).all(), f"logits gap after step {s_}"
+    assert (l[n * stride:] == canary).all()
+    assert (tout.cpu().numpy()[n:] == -12345).all()
+    sess.close()
+    model.close()
+
+
+def test_run_to_run_determinism(g, kernel):
     shape = synth.GPT2_TINY
     w = synth.checkpoint(shape, synth.SEED_TINY, "rich")
     model = g.Model(shape, w)
@@ -386,7 +474,7 @@ def test_int8_session(g, oracle, shape, seed, quant):
     assert np.abs(cache - ref_cache).max() <= tol
 
 
-def test_f32_traced_stages_close_to_oracle(g, oracle):
+def test_f32_traced_stages_close_to_oracle(g, oracle, kernel):
     """Stage-by-stage binary32 check on the 192-wide shape from the trace."""
     shape = P.SMALL
     w = synth.checkpoint(shape, P.SEED_SMALL, "rich")
@@ -404,7 +492,7 @@ def test_f32_traced_stages_close_to_oracle(g, oracle):
 # ------------------------------------------------------------------ binary16 weights
 @pytest.mark.parametrize("shape,seed,grid", [(synth.GPT2_TINY, synth.SEED_TINY, 0), (synth.GPT2_TINY, synth.SEED_TINY, 7),
                                              (P.SMALL, P.SEED_SMALL, 0)], ids=["tiny", "tiny-grid7", "small"])
-def test_f16_session(g, oracle, shape, seed, grid):
+def test_f16_session(g, oracle, shape, seed, grid, kernel):
     """Binary16 weight storage: the oracle's binary16-weight model (binary32
     arithmetic on the rounded checkpoint) is matched to the binary32 bar."""
     _check_f32_session(_session_case(g, oracle, shape, seed, "rich", 2, grid))

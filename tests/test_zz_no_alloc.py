@@ -30,6 +30,14 @@ def g():
     return gpt2
 
 
+@pytest.fixture(params=["phase", "cluster"])
+def kernel(request, monkeypatch):
+    """Runs a binary32 / binary16 test on each step kernel (the variable is
+    read when a model is created)."""
+    monkeypatch.setenv("GPT2_STEP_KERNEL", request.param)
+    return request.param
+
+
 def _compare(g, shape, w, quant, n_calls=4):
     model = g.Model(shape, w, quant=quant)
     V, row = shape.vocab, g.cache_words_per_position(shape)
@@ -74,12 +82,12 @@ def _compare(g, shape, w, quant, n_calls=4):
     model.close()
 
 
-def test_noalloc_matches_session_step_tiny(g):
+def test_noalloc_matches_session_step_tiny(g, kernel):
     shape = synth.GPT2_TINY
     _compare(g, shape, synth.checkpoint(shape, synth.SEED_TINY, "rich"), g.F32)
 
 
-def test_noalloc_matches_session_step_124m(g, w124m):
+def test_noalloc_matches_session_step_124m(g, w124m, kernel):
     _compare(g, synth.GPT2_124M, w124m, g.F32, n_calls=3)
 
 
