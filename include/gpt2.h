@@ -300,7 +300,7 @@ gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
  * were stored; [7] clock64 when the phase's first weight chunk was known to
  * have landed.  Attention phases fill [0..6] only.
  * Models on the cluster step kernel (gpt2_model_step_kernel == 1) use
- * another layout: d_stamps holds 8 + grid_ctas * (16*n_layer + 4) u64.
+ * another layout: d_stamps holds 8 + grid_ctas * (16*n_layer + 8) u64.
  * Words 0..5 receive, when a bounded wait of the run gives up, the wait's
  * kind (1 ring chunk, 2 distributed-shared-memory gather, 3 tagged words,
  * 4 greedy partials), the CTA, the step, the layer and two words about what
@@ -313,7 +313,10 @@ gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
  * without a head leaves the second to sixth at 0); then for the QKV,
  * out-projection, FC and MLP shares of warp 0, (clock64 cycles waiting for
  * weight chunks << 32 | cycles in all); 2 words unused.  Then final input
- * formed, gathered, LN_f done, vocabulary rows done.  Pass NULL to stop. */
+ * formed, gathered, LN_f done, vocabulary rows done; then, if a wait of
+ * this CTA gave up, (kind | 0x100 if it left because another CTA had
+ * given up | thread index << 16), the step, the layer and what was
+ * awaited.  Pass NULL to stop. */
 gpt2_status gpt2_session_set_timing(gpt2_session* session, uint64_t* d_stamps);
 
 /* Debug/test: make the next run's CTA 0 skip publishing one phase so that

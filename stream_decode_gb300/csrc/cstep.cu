@@ -73,6 +73,18 @@ __device__ __forceinline__ void st_async4(uint32_t raddr, float4 v, uint32_t rba
                  : "memory");
 }
 
+// Orders this thread's earlier shared-memory writes before later bulk
+// (async-proxy) copies that read them.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
+// peer's (cluster address), completing on the peer's mbarrier.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -248,6 +260,24 @@ __device__ __noinline__ void cwait_gave_up(const StepPlan& P, int kind, int cta,
     crecord_error(P, kDevTimeout);
 }
 
+// The slow part of every bounded wait, out of line (it runs once per 20 us
+// of waiting): after `elapsed` ns, gives up if another CTA raised the abort
+// word or the wait limit has passed, noting where in `note` (this CTA's four
+// profiling words, when profiling).
+__device__ __noinline__ bool cwait_expired(const StepPlan& P, uint64_t elapsed, int kind, int cta, int step, int layer,
+                                           uint64_t what, uint64_t seen, uint64_t* note) {
+    const bool abort = ld_volatile_int(P.abort_flag) != 0;
+    if (!abort && elapsed <= P.wait_limit_ns) return false;
+    if (note) {
+        note[0] = (uint64_t)kind | (abort ? 0x100ull : 0ull) | ((uint64_t)threadIdx.x << 16);
+        note[1] = (uint64_t)step;
+        note[2] = (uint64_t)layer;
+        note[3] = what;
+    }
+    if (!abort) cwait_gave_up(P, kind, cta, step, layer, what, seen);
+    return true;
+}
+
 // Activation trace (step 0 of a traced run): copies, and a LayerNorm output
 // (x - mean) * rstd * g + b of a slice; out of line, off the hot path.
 __device__ __noinline__ void ctrace_copy(float* dst, const float* src, int n, int tid) {
@@ -312,6 +342,10 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     const int f0 = GG.fc0[c], nfc = GG.fc0[c + 1] - GG.fc0[c];
     const int nfc4 = (nfc + 3) & ~3;
     const int col0 = r * SW;
+    // rank r appends rows [kv_lo, kv_hi) of a head's 3 DH q/k/v rows (its
+    // keys and values) to the KV cache
+    const int kv_per = (2 * DH + CS - 1) / CS;
+    const int kv_lo = DH + r * kv_per, kv_hi = min(3 * DH, kv_lo + kv_per);
     constexpr int NT = kCWarps * 32;
     const uint64_t head_bytes = cg_head_bytes(GG, DH);
     const uint32_t wb = (uint32_t)GG.wb;
@@ -376,13 +410,29 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     auto part_base = [&](int l) -> const uint8_t* {
         return CP.cstream + (uint64_t)l * GG.layer_bytes + GG.seg[c] + (uint64_t)r * GG.cta_bytes[c];
     };
-    auto share_qkv = [&](int l, int k) { return make_share(part_base(l) + k * head_bytes, (uint32_t)SW * wb, 3 * DH); };
-    auto share_wo = [&](int l, int k) {
-        return make_share(part_base(l) + k * head_bytes + (uint64_t)3 * DH * SW * wb, (uint32_t)DH * wb, SW);
-    };
-    auto share_fc = [&](int l) { return make_share(part_base(l) + nh * head_bytes, (uint32_t)SW * wb, nfc); };
-    auto share_wp = [&](int l) {
-        return make_share(part_base(l) + nh * head_bytes + (uint64_t)nfc * SW * wb, (uint32_t)nfc * wb, SW);
+    // Share j of layer l (j < 2 * nh + 2): for head slot k = j / 2 its QKV
+    // part (j even) and out-projection part (j odd); then FC (j = 2 nh) and
+    // MLP (j = 2 nh + 1).  One routine for every share keeps one copy of it
+    // in the binary.
+    auto share_at = [&](int l, int j) -> Share {
+        uint64_t off;
+        uint32_t pb;
+        int n;
+        if (j < 2 * nh) {
+            const bool wo = (j & 1) != 0;
+            off = (uint64_t)(j >> 1) * head_bytes + (wo ? (uint64_t)3 * DH * SW * wb : 0ull);
+            pb = (uint32_t)(wo ? DH : SW) * wb;
+            n = wo ? SW : 3 * DH;
+        } else if (j == 2 * nh) {
+            off = (uint64_t)nh * head_bytes;
+            pb = (uint32_t)SW * wb;
+            n = nfc;
+        } else {
+            off = (uint64_t)nh * head_bytes + (uint64_t)nfc * SW * wb;
+            pb = (uint32_t)nfc * wb;
+            n = SW;
+        }
+        return make_share(part_base(l) + off, pb, n);
     };
     const int V = P.V;
     const int v0 = (int)(((long long)cta * V) / GG.G), v1 = (int)(((long long)(cta + 1) * V) / GG.G);
@@ -448,16 +498,13 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     ++gi;
                 }
             };
+            // per step: the layers' shares in order, then the vocabulary rows
+            // (layer index L), from one issue site
             for (int s = 0; s < P.n_steps && !stop; ++s) {
-                for (int l = 0; l < L && !stop; ++l) {
-                    for (int k = 0; k < nh; ++k) {
-                        issue(share_qkv(l, k), true);
-                        issue(share_wo(l, k), true);
-                    }
-                    issue(share_fc(l), true);
-                    issue(share_wp(l), true);
+                for (int l = 0; l <= L && !stop; ++l) {
+                    const int nj = l < L ? 2 * nh + 2 : 1;
+                    for (int j = 0; j < nj && !stop; ++j) issue(l < L ? share_at(l, j) : share_vocab(), l < L);
                 }
-                issue(share_vocab(), false);
             }
             // every issued copy lands before this thread leaves
             const uint32_t nslot = gi < (uint32_t)NSL ? gi : (uint32_t)NSL;
@@ -501,27 +548,12 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         csync();
         return *slot == 0;
     };
-    auto note_give_up = [&](int kind, bool abort, uint64_t what) {
-        if (stamps) {
-            stamps[16 * L + 4] = (uint64_t)kind | (abort ? 0x100ull : 0ull) | ((uint64_t)threadIdx.x << 16);
-            stamps[16 * L + 5] = (uint64_t)cur_step;
-            stamps[16 * L + 6] = (uint64_t)cur_layer;
-            stamps[16 * L + 7] = what;
-        }
-    };
     auto timed_out = [&](uint64_t& t0, int kind, uint64_t what = 0, uint64_t seen = 0) -> bool {
         const uint64_t now = globaltimer_ns();
         if (t0 == 0) { t0 = now; return false; }
-        if (now - t0 > kCAbortCheckNs && ld_volatile_int(P.abort_flag)) {
-            note_give_up(kind, true, what);
-            return true;
-        }
-        if (now - t0 > P.wait_limit_ns) {
-            note_give_up(kind, false, what);
-            cwait_gave_up(P, kind, cta, cur_step, cur_layer, what, seen);
-            return true;
-        }
-        return false;
+        if (now - t0 <= kCAbortCheckNs) return false;
+        return cwait_expired(P, now - t0, kind, cta, cur_step, cur_layer, what, seen,
+                             stamps ? stamps + 16 * L + 4 : nullptr);
     };
     // Warp-uniform bounded wait for ring chunk cc.
     auto wait_chunk = [&](uint32_t cc) -> bool {
@@ -549,13 +581,16 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     // n floats (n % 4 == 0) at src into this CTA's row `dst` of a gather
     // buffer in every CTA of the cluster (same offset), completing on each
     // peer's mbarrier bar.
+    // One bulk copy per peer, issued by lanes 0..CS-1 of warp 0; the writers
+    // of src fenced their writes for the async proxy before the caller's
+    // barrier.  The issuing lanes wait until the copies have read src, so
+    // src may be rewritten after the next barrier.
     auto bcast = [&](const float* src, const float* dst, int n, uint64_t* bar) {
-        const int nv = n >> 2;
-        const uint32_t la = smem_addr(dst), lb = smem_addr(bar);
-        for (int k = tid; k < nv * CS; k += NT) {
-            const int dr = k / nv, v = k - dr * nv;
-            st_async4(mapa(la + 16u * (uint32_t)v, (uint32_t)dr), reinterpret_cast<const float4*>(src)[v],
-                      mapa(lb, (uint32_t)dr));
+        if (warp == 0 && lane < CS) {
+            bulk_to_peer(mapa(smem_addr(dst), (uint32_t)lane), smem_addr(src), (uint32_t)n * 4u,
+                         mapa(smem_addr(bar), (uint32_t)lane));
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         }
     };
     // Waits (bounded) for a gather of `bytes` on this CTA's mbarrier (armed
@@ -646,21 +681,31 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     if (i < nw) y += val_of(w[i]);
                 xs[tid] = __fadd_rn(xs[tid], __fadd_rn(y, bv));
             }
+            fence_async_smem();
         }
         return agree(ok);
     };
-    // This slice's (mean, M2) of x - s (two passes over SW values), by warp 0, into dst[0..1].
+    // This slice's (mean, M2) of x - s (two passes over SW values), by the
+    // last consumer warp (the one without a chunk in most shares), into
+    // dst[0..1].
     auto slice_stats = [&](float s, float* dst) {
-        if (warp != 0) return;
+        if (warp != kCWarps - 1) return;
+        const float4* x4 = reinterpret_cast<const float4*>(xs);
         float a = 0.0f;
-        for (int e = lane; e < SW; e += 32) a += xs[e] - s;
+#pragma unroll 1
+        for (int e = lane; e < SW / 4; e += 32) {
+            const float4 v = x4[e];
+            a += ((v.x - s) + (v.y - s)) + ((v.z - s) + (v.w - s));
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        const float mean = a / (float)SW;
+        const float mean = a * (1.0f / (float)SW);
         float q = 0.0f;
-        for (int e = lane; e < SW; e += 32) {
-            const float d = (xs[e] - s) - mean;
-            q = fmaf(d, d, q);
+#pragma unroll 1
+        for (int e = lane; e < SW / 4; e += 32) {
+            const float4 v = x4[e];
+            const float d0 = (v.x - s) - mean, d1 = (v.y - s) - mean, d2 = (v.z - s) - mean, d3 = (v.w - s) - mean;
+            q = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, q))));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
@@ -758,9 +803,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             }
         }
     };
-    auto attention = [&](int l, int h, int p) {
-        const int n = p + 1;
-        const int k0 = (int)(((long long)r * n) / CS), k1 = (int)(((long long)(r + 1) * n) / CS);
+    auto attention = [&](int l, int h, int p, int k0, int k1) {
         const float* kv0 = P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL;
         const float den = sqrtf((float)DH);
         const float4* q4 = reinterpret_cast<const float4*>(qkv + dc * DPL);
@@ -878,6 +921,9 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             publish_choice(s - 1, prev_choice, nf);
             if (nf) { alive = false; break; }
         }
+        // this CTA's keys [att_k0, att_k1) of positions 0..p (cached ones below att_k1c)
+        const int att_k0 = (int)(((long long)r * (p + 1)) / CS), att_k1 = (int)(((long long)(r + 1) * (p + 1)) / CS);
+        const int att_k1c = att_k1 < p ? att_k1 : p;
         unsigned tok = P.tokens_in ? P.tokens_in[s] : P.token0;
         if (tok == 0xFFFFFFFFu) tok = prev_choice;
         if (tok >= (unsigned)V) {
@@ -910,14 +956,14 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             float ln_shift = shift;  // shift of the LayerNorm being folded
             // this layer's cached keys and values of this CTA's attention
             // positions, prefetched into L2 while the block input forms
-            if (nh > 0) {
-                const int n = p + 1;
-                const int kk0 = (int)(((long long)r * n) / CS), kk1 = (int)(((long long)(r + 1) * n) / CS);
-                const int kk1c = kk1 < p ? kk1 : p;
-                for (int t = tid; t < (kk1c - kk0) * nh * 4; t += NT) {
-                    const int j = kk0 + t / (4 * nh), hs = (t / 4) % nh, part = t % 4;
-                    const float* row = P.cache + ((uint64_t)j * L + l) * 2 * D + (part >> 1) * D +
-                                       (c + hs * GG.NC) * DH + (part & 1) * (DH / 2);
+            // (four 128-byte lines per position and head: key and value halves)
+#pragma unroll 1
+            for (int hs = 0; hs < nh; ++hs) {
+                const float* hrow = P.cache + (uint64_t)l * 2 * D + (c + hs * GG.NC) * DH;
+#pragma unroll 1
+                for (int t = tid; t < (att_k1c - att_k0) * 4; t += NT) {
+                    const float* row = hrow + (uint64_t)(att_k0 + (t >> 2)) * L * 2 * D + ((t >> 1) & 1) * D +
+                                       (t & 1) * (DH / 2);
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
                 }
             }
@@ -961,18 +1007,19 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     Share sh;
                     const float* xv;
                     int W4;
-                    if (kind == 0) { sh = share_qkv(l, k); xv = xin; W4 = SW / 4; }
-                    else if (kind == 2) { sh = share_wo(l, k); xv = oh; W4 = DH / 4; }
-                    else if (kind == 3) { sh = share_fc(l); xv = xin; W4 = SW / 4; }
-                    else { sh = share_wp(l); xv = uu; W4 = nfc4 / 4; }
+                    sh = share_at(l, kind == 0 ? 2 * k : kind == 2 ? 2 * k + 1 : kind == 3 ? 2 * nh : 2 * nh + 1);
+                    if (kind == 0 || kind == 3) { xv = xin; W4 = SW / 4; }
+                    else if (kind == 2) { xv = oh; W4 = DH / 4; }
+                    else { xv = uu; W4 = nfc4 / 4; }
                     const bool ok = run_share(sh, xv, W4, pa);
-                    if (tid == 0 && (kind == 0 || kind == 3)) {
+                    if (warp == kCWarps - 1 && lane == 0 && (kind == 0 || kind == 3)) {
                         const int n0 = kind == 0 ? 3 * DH : nfc4;
                         pa[n0] = s_st[0];
                         pa[n0 + 1] = s_st[1];
                         pa[n0 + 2] = 0.0f;
                         pa[n0 + 3] = 0.0f;
                     }
+                    if (kind == 0 || kind == 3) fence_async_smem();
                     if (stamps && cur_step == 0 && tid == 0) {
                         const int sl = 16 * l + 10 + (kind == 0 ? 0 : kind == 2 ? 1 : kind == 3 ? 2 : 3) * 1;
                         stamps[sl] = (prof_wait << 32) | (prof_total & 0xFFFFFFFFull);
@@ -981,7 +1028,8 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     stamp(16 * l + (kind == 0 ? 1 : kind == 2 ? 5 : kind == 3 ? 7 : 9));
                 } else {
                     const long long t_att = clock64();
-                    attention(l, h, p);
+                    attention(l, h, p, att_k0, att_k1);
+                    fence_async_smem();
                     csync();
                     if (stamps && cur_step == 0 && tid == 0)
                         stamps[16 * l + 14] = (prof_comb << 32) | ((uint64_t)(clock64() - t_att) & 0xFFFFFFFFull);
@@ -1016,49 +1064,18 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     // loaded while the gather completes: the first keys of this
                     // CTA's attention share, and this thread's fold constants
                     float cj = 0.0f, dj = 0.0f;
-                    int J = 0;
-                    if (kind == 0) {
-                        const int n = p + 1;
-                        const int kk0 = (int)(((long long)r * n) / CS), kk1 = (int)(((long long)(r + 1) * n) / CS);
-                        fetch(P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL, kk0 + warp * KPW + ks, kk1, p, ka, va);
-                        if (tid < 3 * DH) {
-                            J = (tid / DH) * D + h * DH + (tid % DH);
-                            cj = __ldg(fl + J);
-                            dj = __ldg(fl + 3 * D + J);
-                        }
-                    } else if (kind == 3 && tid < nfc) {
-                        J = f0 + tid;
-                        cj = __ldg(fl + 6 * D + J);
-                        dj = __ldg(fl + 6 * D + FF + J);
+                    if (kind == 0)
+                        fetch(P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL, att_k0 + warp * KPW + ks, att_k1, p, ka, va);
+                    if ((kind == 0 && tid < 3 * DH) || (kind == 3 && tid < nfc)) {
+                        const int Jt = kind == 0 ? (tid / DH) * D + h * DH + (tid % DH) : 6 * D + f0 + tid;
+                        cj = __ldg(fl + Jt);
+                        dj = __ldg(fl + Jt + (kind == 0 ? 3 * D : FF));
                     }
                     if (!gather_wait(bar, (uint32_t)(CS * nsend * 4), (u >> 1) & 1)) { alive = false; break; }
                     stamp(16 * l + (kind == 0 ? 2 : kind == 1 ? 4 : 8));
                     // ---- epilogues of the gathered values
                     const long long t_epi = clock64();
-                    if (kind == 0) {
-                        float mean, rstd;
-                        merge_stats(gbuf + 3 * DH, rowl, mean, rstd);
-                        if (tid < 3 * DH) {
-                            float a = 0.0f;
-                            float pv[16];
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) pv[q] = q < CS ? gbuf[(size_t)q * rowl + tid] : 0.0f;
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) if (q < CS) a += pv[q];
-                            const float y = fmaf(rstd, fmaf(-mean, cj, a), dj);
-                            qkv[tid] = y;
-                            if (tid >= DH && (tid % CS) == r) {
-                                const int off = tid < 2 * DH ? h * DH + (tid - DH) : D + h * DH + (tid - 2 * DH);
-                                P.cache[((uint64_t)p * L + l) * 2 * D + off] = y;
-                            }
-                            if (tr && r == 0) P.trace[(size_t)l * trace_layer + 2 * D + J] = y;
-                        }
-                        if (tr && c == 0 && k == 0)
-                            ctrace_ln(P.trace + (size_t)l * trace_layer + D + col0, xs, ln_shift + mean, rstd,
-                                      P.packed + lp.ln1_g + col0, P.packed + lp.ln1_b + col0, SW, tid);
-                        if (k == nh - 1) shift = ln_shift + mean;
-                        if (stamps && cur_step == 0 && tid == 0) prof_comb = (uint64_t)(clock64() - t_epi);
-                    } else if (kind == 1) {
+                    if (kind == 1) {
                         if (tid < DH) {
                             float M = -INFINITY;
                             for (int q = 0; q < CS; ++q) M = fmaxf(M, gbuf[(size_t)q * rowl]);
@@ -1075,28 +1092,43 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                             if (tr && r == 0) P.trace[(size_t)l * trace_layer + 5 * D + h * DH + tid] = o;
                         }
                     } else {
+                        // QKV (0) or FC (3): the CS slice partials summed in
+                        // rank order, the LayerNorm fold, then q/k/v (and the
+                        // KV append) or the GELU output
+                        const bool qk = kind == 0;
+                        const int nrow = qk ? 3 * DH : nfc;
                         float mean, rstd;
-                        merge_stats(gbuf + nfc4, rowl, mean, rstd);
-                        for (int j = tid; j < nfc; j += NT) {
+                        merge_stats(gbuf + (qk ? 3 * DH : nfc4), rowl, mean, rstd);
+#pragma unroll 1
+                        for (int j = tid; j < nrow; j += NT) {
                             float a = 0.0f;
                             float pv[16];
 #pragma unroll
                             for (int q = 0; q < 16; ++q) pv[q] = q < CS ? gbuf[(size_t)q * rowl + j] : 0.0f;
 #pragma unroll
                             for (int q = 0; q < 16; ++q) if (q < CS) a += pv[q];
+                            const int Jr = qk ? (j / DH) * D + h * DH + (j % DH) : 6 * D + f0 + j;
                             float cc = cj, dd = dj;
                             if (j != tid) {
-                                cc = __ldg(fl + 6 * D + f0 + j);
-                                dd = __ldg(fl + 6 * D + FF + f0 + j);
+                                cc = __ldg(fl + Jr);
+                                dd = __ldg(fl + Jr + (qk ? 3 * D : FF));
                             }
-                            const float uv = cgelu(fmaf(rstd, fmaf(-mean, cc, a), dd));
-                            uu[j] = uv;
-                            if (tr && r == 0) P.trace[(size_t)l * trace_layer + 8 * D + f0 + j] = uv;
+                            float y = fmaf(rstd, fmaf(-mean, cc, a), dd);
+                            if (qk) {
+                                qkv[j] = y;
+                                if (j >= kv_lo && j < kv_hi) P.cache[((uint64_t)p * L + l) * 2 * D + (Jr - D)] = y;
+                            } else {
+                                y = cgelu(y);
+                                uu[j] = y;
+                            }
+                            if (tr && r == 0) P.trace[(size_t)l * trace_layer + (qk ? 2 * D + Jr : 8 * D + f0 + j)] = y;
                         }
-                        if (tr && c == 0)
-                            ctrace_ln(P.trace + (size_t)l * trace_layer + 7 * D + col0, xs, ln_shift + mean, rstd,
-                                      P.packed + lp.ln2_g + col0, P.packed + lp.ln2_b + col0, SW, tid);
-                        shift = ln_shift + mean;
+                        if (tr && c == 0 && (!qk || k == 0))
+                            ctrace_ln(P.trace + (size_t)l * trace_layer + (qk ? D : 7 * D) + col0, xs, ln_shift + mean,
+                                      rstd, P.packed + (qk ? lp.ln1_g : lp.ln2_g) + col0,
+                                      P.packed + (qk ? lp.ln1_b : lp.ln2_b) + col0, SW, tid);
+                        if (!qk || k == nh - 1) shift = ln_shift + mean;
+                        if (qk && stamps && cur_step == 0 && tid == 0) prof_comb = (uint64_t)(clock64() - t_epi);
                     }
                     csync();
                 } else {

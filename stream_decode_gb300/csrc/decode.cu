@@ -1073,6 +1073,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     // thread r runs row r's epilogue.
     float* fpart = reinterpret_cast<float*>(smem + lay.fpart);
     int fast_no = 0;
+    // int8 models trace step 0 from the fast path itself, in every CTA: the
+    // vectors the fast path quantizes (CTA 0; every CTA forms the same ones)
+    // and each CTA's own QKV rows.  (binary32 / binary16 traced steps take
+    // the general path in CTA 0.)
+    bool q8_trace_now = false;
     // With from_vin the input is the vector already formed in vin (the
     // LayerNorm output or merged attention heads of the general path) and
     // the epilogue adds the plain bias.
@@ -1219,6 +1224,20 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 #pragma unroll
                 for (int e = 0; e < 4 * Q::NC; ++e) x[e] = fmaf((x[e] - mean) * rstd, gq[e], bq[e]);
             }
+            if (q8_trace_now && cta == 0) {
+                // trace offsets per layer: x 0, LN1 D, attention output 5D, x_mid 6D, LN2 7D, GELU output 8D
+                const size_t tb = (size_t)l * (8 * D + FF);
+                const int oin = kind == kPhQKV ? D : kind == kPhO ? 5 * D : kind == kPhFC ? 7 * D : 8 * D;
+#pragma unroll
+                for (int cc = 0; cc < Q::NC; ++cc) {
+                    const int col = tid + Q::NT * cc;
+                    if (col < Q::NV)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) P.trace[tb + oin + 4 * col + e] = x[4 * cc + e];
+                }
+                if (kLnWidth && has_ln)
+                    for (int i = tid; i < D; i += NT) P.trace[tb + (kind == kPhQKV ? 0 : 6 * D) + i] = xs[i];
+            }
             quantize_quads<KK>(x, vq, vs, tid);
             consumers_sync();
             if (!(kLnWidth && has_ln) && *slot != 0) return false;
@@ -1242,6 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             if (kind == kPhQKV) {
                 st_tagged(P.qkv + j, tg, y);
                 if (j >= D) P.cache[((uint64_t)p * L + l) * 2 * D + (j - D)] = y;
+                if (Q8 && q8_trace_now) P.trace[(size_t)l * (8 * D + FF) + 2 * D + j] = y;
             } else if (kind == kPhFC) {
                 st_tagged(P.u + j, tg, gelu_tanh(y));
             } else {
@@ -1477,7 +1497,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     for (; s < P.n_steps && alive; ++s) {
         const int p = P.p0 + s;
         const unsigned base = P.epoch + (unsigned)s * per_step;
-        const bool trace_step = tracer && s == 0;
+        const bool trace_step = tracer && s == 0 && !Q8;
+        q8_trace_now = Q8 && P.trace != nullptr && s == 0;
         if (s > 0) {
             if (!reduce_choice(base)) { alive = false; break; }
             prev_choice = *s_tok;
@@ -1651,8 +1672,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 }
             }
             // ---- activation trace (step 0, CTA 0): per layer x, LN_1(x), qkv,
-            // attention output, x_mid, LN_2(x_mid), GELU output; then x_final, LN_f(x_final)
-            if (trace_step) {
+            // attention output, x_mid, LN_2(x_mid), GELU output; then x_final, LN_f(x_final).
+            // int8 models trace here only the vocabulary phase (the layers
+            // trace from the fast path).
+            if (trace_step || (q8_trace_now && tracer && kind == kPhVocab)) {
                 const int tb = l * trace_layer;
                 if (kind == kPhO) {
                     float qv[2 * PPQ];

@@ -1,0 +1,185 @@
+"""int8 decode (quantized GPT-2 abstract: int8 weights and projection
+inputs, scales per 64 consecutive coordinates, nearest-even rounding,
+saturation, int32 accumulation, a fixed rescale order, binary32 elsewhere):
+checks that accept every correct int8 realization and reject a binary32
+answer.
+
+Two correct int8 realizations may differ where a binary32 rounding
+difference before a quantizer moves a code by one step (a quotient within
+an ulp or two of a half-integer).  A GPT-2 124M step quantizes about 65,000
+values, so a few such flips per step are expected; most move the logits by
+far less than the binary32 bar, some by a few hundredths.  Quantization
+error itself is larger: on a checkpoint whose activations carry a few large
+channels (synthetic variant outlier_channels, the shape of trained GPT-2's
+activation outliers) the int8 answer is far from the binary32 one, so:
+- over all compared logits, the RMS distance from the GPU to the int8
+  oracle is at most half the binary32 oracle's (a binary32 answer has
+  ratio 1 by definition, so the check rejects it);
+- no compared step is further from the int8 oracle than the binary32
+  oracle is at its furthest (a flipped code is one quantization step, an
+  error the method accepts);
+- greedy agreement with the int8 oracle is at least 99% on whole sessions.
+Whole sessions carry a flip into the cache and every later step, so they
+are compared on small seeded cases; at 124M each sampled step starts from
+the GPU's own cache prefix, so a flip stays in its step.
+The projections of a traced step are also recomputed by the oracle's int8
+projection from the step kernel's own traced inputs, bit for bit: the
+quantizer, the dp4a group sums and the ordered rescale as the step kernel
+wires them (which vector, which scale slot, after which LayerNorm)."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+from gpu_util import AGREE_MIN, LOGIT_TOL, greedy_agreement, run  # noqa: E402
+from stream_decode_gb300 import synth  # noqa: E402
+
+import oracle_pins as P  # noqa: E402
+
+RMS_FRAC = 0.5  # rms |gpu - int8 oracle| <= RMS_FRAC * rms |binary32 oracle - int8 oracle|
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from stream_decode_gb300 import gpt2
+    return gpt2
+
+
+def _int8_session_case(g, oracle, shape, seed, quant, n, n_prompt=8):
+    w = synth.checkpoint(shape, seed, "outlier_channels")
+    toks = [int(t) for t in synth.tokens(shape.vocab, n_prompt, seed=11)]
+    oq = oracle.model(shape, w, quant=quant)
+    ref, ref_ch, _ = oq.session(toks + [-1] * (n - n_prompt), n)
+    oq.close()
+    seq = toks + [int(c) for c in ref_ch[n_prompt - 1:n - 1]]
+    of = oracle.model(shape, w)
+    ref32, _, _ = of.session(seq, n)
+    of.close()
+    model = g.Model(shape, w, quant=quant)
+    logits, ch = run(g.Session(model), seq, n)
+    model.close()
+    return logits, ch, ref, ref32
+
+
+def _check(logits, ch, ref, ref32, agree_min=AGREE_MIN):
+    scale = np.maximum(1.0, np.abs(ref).max(axis=1))
+    d32 = np.abs(ref32 - ref).max(axis=1)
+    dg = np.abs(logits - ref).max(axis=1)
+    rms32 = float(np.sqrt(np.mean((ref32 - ref) ** 2)))
+    rmsg = float(np.sqrt(np.mean((logits - ref) ** 2)))
+    exact = dg <= LOGIT_TOL * scale
+    print(f"int8 vs binary32 oracle: rms {rms32:.4g}, per-step max {d32.min():.4g}..{d32.max():.4g}; "
+          f"gpu vs int8 oracle: rms {rmsg:.4g}, max {dg.max():.4g}, steps within the binary32 bar "
+          f"{int(exact.sum())}/{exact.size}; agreement {greedy_agreement(ref, ch):.3f}")
+    # the binary32 answer is far from the int8 one at every step
+    assert np.all(d32 > LOGIT_TOL * scale), d32
+    assert rmsg <= RMS_FRAC * rms32, (rmsg, rms32)
+    assert dg.max() <= d32.max(), (dg.max(), d32.max())
+    assert greedy_agreement(ref, ch) >= agree_min
+
+
+@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+@pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
+                         ids=["tiny", "small"])
+def test_int8_session_is_int8_not_binary32(g, oracle, shape, seed, quant):
+    _check(*_int8_session_case(g, oracle, shape, seed, quant, shape.max_pos))
+
+
+@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+def test_124m_int8_steps_are_int8_not_binary32(g, oracle, quant):
+    """GPT-2 124M: the GPU runs 64 positions in one launch; at 8 sampled
+    positions the oracle takes the same step (int8, and binary32) from the
+    GPU's own cache prefix, so the comparison sees only the code flips of
+    that one step, not the flips accumulated in the cache."""
+    s = synth.GPT2_124M
+    w = synth.checkpoint(s, synth.SEED_124M, "outlier_channels")
+    toks = [int(t) for t in synth.tokens(s.vocab, 64, seed=17)]
+    model = g.Model(s, w, quant=quant)
+    sess = g.Session(model)
+    logits, ch = run(sess, toks, 64)
+    cache = sess.read_cache()
+    sess.close()
+    model.close()
+    row = g.cache_words_per_position(s)
+    oq, of = oracle.model(s, w, quant=quant), oracle.model(s, w)
+    ps = [1, 9, 17, 25, 33, 41, 52, 63]
+    ref, ref32 = [], []
+    for p in ps:
+        st, lq, _ = oq.cached_step(cache[:p * row], toks[p], p)
+        st32, l32, _ = of.cached_step(cache[:p * row], toks[p], p)
+        assert st == st32 == "ok"
+        ref.append(lq)
+        ref32.append(l32)
+    oq.close()
+    of.close()
+    # greedy choices: a flipped step may pick another near-tied token
+    _check(logits[ps], np.asarray(ch)[ps], np.stack(ref), np.stack(ref32), agree_min=0.75)
+
+
+@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+@pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
+                         ids=["tiny", "small"])
+def test_int8_traced_projections_bit_exact(g, oracle, shape, seed, quant):
+    """A step at position 5 (after a teacher-forced prefix) with the
+    activation trace on: every projection output the trace holds equals the
+    oracle's int8 projection of the traced input, bit for bit (qkv from
+    LN_1(x); the attention residual from the head outputs; the block output
+    from the GELU outputs; the logits from LN_f(x_final)), and the GELU
+    outputs equal the oracle's GELU of the oracle's FC projection of the
+    traced LN_2 output to a few ulp (the tanh of the two libraries may
+    differ in the last bits)."""
+    w = synth.checkpoint(shape, seed, "outlier_channels")
+    om = oracle.model(shape, w, quant=quant)
+    model = g.Model(shape, w, quant=quant)
+    sess = g.Session(model)
+    toks = [int(t) for t in synth.tokens(shape.vocab, 6, seed=13)]
+    run(sess, toks[:5], 5)
+    tr = torch.zeros(g.trace_words(shape), dtype=torch.float32, device="cuda")
+    sess.set_trace(tr)
+    logits, _ = run(sess, toks[5:6], 1)
+    t = tr.cpu().numpy()
+    d, F, L = shape.d_model, shape.d_ff, shape.n_layer
+    lay = synth.layout(shape)
+    per = 8 * d + F
+
+    def par(name):
+        o, n = lay[name]
+        return w[o:o + n]
+
+    def same(a, b):
+        return np.array_equal(np.asarray(a, np.float32).view(np.uint32), np.asarray(b, np.float32).view(np.uint32))
+
+    for l in range(L):
+        base = l * per
+        x, ln1 = t[base:base + d], t[base + d:base + 2 * d]
+        qkv, o_ = t[base + 2 * d:base + 5 * d], t[base + 5 * d:base + 6 * d]
+        xm, ln2, u = t[base + 6 * d:base + 7 * d], t[base + 7 * d:base + 8 * d], t[base + 8 * d:base + 8 * d + F]
+        x_next = t[(l + 1) * per:(l + 1) * per + d] if l + 1 < L else t[L * per:L * per + d]
+        q, s = om.q8_matrix(4 * l)
+        assert same(qkv, oracle.linear_q8(ln1, q, s, par(f"h{l}.b_qkv"))), f"qkv, layer {l}"
+        q, s = om.q8_matrix(4 * l + 1)
+        y = oracle.linear_q8(o_, q, s, par(f"h{l}.b_o"))
+        assert same(xm, (x + y).astype(np.float32)), f"attention residual, layer {l}"
+        q, s = om.q8_matrix(4 * l + 2)
+        pre = oracle.linear_q8(ln2, q, s, par(f"h{l}.b_fc"))
+        ref_u = np.array([oracle.gelu(float(v)) for v in pre], np.float32)
+        assert np.abs(u - ref_u).max() <= 4 * np.spacing(np.abs(ref_u).max()), f"gelu, layer {l}"
+        q, s = om.q8_matrix(4 * l + 3)
+        y = oracle.linear_q8(u, q, s, par(f"h{l}.b_p"))
+        assert same(x_next, (xm + y).astype(np.float32)), f"block output, layer {l}"
+        # the LayerNorm outputs the kernel quantized are those of its residual, to rounding
+        for xx, lnv, gn, bn in ((x, ln1, f"h{l}.ln1_g", f"h{l}.ln1_b"), (xm, ln2, f"h{l}.ln2_g", f"h{l}.ln2_b")):
+            ref_ln = oracle.layernorm(xx, par(gn), par(bn))
+            assert np.abs(lnv - ref_ln).max() <= 1e-5 * max(1.0, float(np.abs(ref_ln).max())), f"LN, layer {l}"
+    xf, lnf = t[L * per:L * per + d], t[L * per + d:L * per + 2 * d]
+    q, s = om.q8_matrix(4 * L)
+    assert same(logits[0], oracle.linear_q8(lnf, q, s, None)), "logits"
+    assert np.abs(lnf - oracle.layernorm(xf, par("lnf_g"), par("lnf_b"))).max() <= 1e-5 * max(
+        1.0, float(np.abs(lnf).max()))
+    sess.close()
+    model.close()
+    om.close()
