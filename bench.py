@@ -56,7 +56,7 @@ def step_bytes(shape, quant: str, p: int) -> int:
     if quant in ("f32", "f16"):
         mats = L * (d * 3 * d + d * d + d * F + F * d) + V * d
         weights = (4 if quant == "f32" else 2) * mats + 4 * params
-    elif quant == "int8_row":
+    elif quant in ("int8_row", "int8_row_act"):
         rb = lambda K: K + 4  # one scale per row (the device copy repeats it per group)
         mats = L * (3 * d * rb(d) + d * rb(d) + F * rb(d) + d * rb(F)) + V * rb(d)
         weights = mats + 4 * params
@@ -162,7 +162,7 @@ def reference_arm(args, shape, w, toks):
     ws, rank, _ = dist_info()
     if rank != 0:
         return
-    quant = {"f32": 0, "int8": 1, "f16": 2, "int8_row": 3}[args.quant]
+    quant = {"f32": 0, "int8": 1, "f16": 2, "int8_row": 3, "int8_row_act": 4}[args.quant]
     per_step = 2
     from oracle import Oracle
     om = Oracle().model(shape, w, quant=quant)
@@ -259,7 +259,7 @@ def prefill_rate(g, torch, shape, w, n: int = 128, reps: int = 10):
 
 def measure_decode(g, torch, shape, w, toks, quant: str, args, rank_sync):
     """Returns (ms per bench step, launches, session) after W warm-ups and K timed steps."""
-    q = {"f32": g.F32, "int8": g.INT8_G64, "f16": g.F16, "int8_row": g.INT8_ROW}[quant]
+    q = {"f32": g.F32, "int8": g.INT8_G64, "f16": g.F16, "int8_row": g.INT8_ROW, "int8_row_act": g.INT8_ROW_ACT}[quant]
     model = g.Model(shape, w, quant=q)
     sess = g.Session(model)
     V = shape.vocab
@@ -452,7 +452,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--quant", choices=["f32", "int8", "f16", "int8_row"], default="f32")
+    ap.add_argument("--quant", choices=["f32", "int8", "f16", "int8_row", "int8_row_act"], default="f32")
     ap.add_argument("--no-extra", action="store_true", help="skip the int8, binary16, long-context and prefill extras")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the 128-token prefill leg (3 warm-up calls, --steps timed calls); prints its JSON")
@@ -533,6 +533,14 @@ def main():
                                         "weights": "int8, one scale per output row; group-64 activation scales"}
             sr.close()
             mr.close()
+            msa, _, ma, sa, _, _ = measure_decode(g, torch, shape, w, toks, "int8_row_act", args, lambda: None)
+            extra["int8_row_act_decode"] = {"tokens_per_s": DECODE / (msa * 1e-3), "ms_per_step": msa,
+                                            "GB_per_s": br / (msa * 1e-3) / 1e9,
+                                            "frac_of_peak": br / (msa * 1e-3) / 1e9 / peak,
+                                            "weights": "int8, one scale per output row; one scale per "
+                                                       "activation vector"}
+            sa.close()
+            ma.close()
         extra["long_context_f32"] = long_context(g, torch, w)
         extra["batched_f32"] = [batched_decode(g, torch, shape, w, B) for B in (16, 64, 256)]
         extra["prefill_f32"] = prefill_rate(g, torch, shape, w)
@@ -546,7 +554,8 @@ def main():
                                                 f"16-token prompt ({dt8:.1f} s)"}
     if rank == 0:
         n_dec = 16
-        rate, dt = oracle_decode_rate(shape, w, toks, {"f32": 0, "int8": 1, "f16": 2, "int8_row": 3}[args.quant],
+        rate, dt = oracle_decode_rate(shape, w, toks, {"f32": 0, "int8": 1, "f16": 2, "int8_row": 3,
+                                                       "int8_row_act": 4}[args.quant],
                                       n_dec)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n_dec} greedy decode steps at positions 16..31 after an untimed 16-token prompt "

@@ -63,9 +63,12 @@ typedef enum gpt2_quant {
     GPT2_F16 = 2,      /* the 48 block matrices and the tied embedding stored as binary16 (rounded to
                           nearest-even at load), widened to binary32 before every multiply-add;
                           everything else binary32 (the gpt2.s page's half-precision weight option) */
-    GPT2_INT8_ROW = 3  /* as GPT2_INT8_G64, but one weight scale per output row (maxabs over the whole
+    GPT2_INT8_ROW = 3, /* as GPT2_INT8_G64, but one weight scale per output row (maxabs over the whole
                           row / 127); the rescale keeps the grouped order with the row's scale in every
                           group's place; projection inputs keep their group-64 scales */
+    GPT2_INT8_ROW_ACT = 4 /* as GPT2_INT8_ROW, and every projection input quantized with one scale for
+                             the whole vector (maxabs / 127) in every group's place: the per-activation-row
+                             design the quantized GPT-2 abstract measured and rejected */
 } gpt2_quant;
 
 /* In a device token array: use the previous step's greedy choice. */
@@ -120,8 +123,9 @@ gpt2_status gpt2_cached_step(const gpt2_config* cfg, const void* weights_host, s
 
 /* Uploads the packed checkpoint and builds the device weight streams
  * (K-major copies of the block matrices; for GPT2_INT8_G64 the int8 copies
- * of the 48 block matrices and the tied wte with their group scales; for
- * GPT2_F16 binary16 copies of both).
+ * of the 48 block matrices and the tied wte with their group scales, for
+ * GPT2_INT8_ROW and GPT2_INT8_ROW_ACT with their row scales; for GPT2_F16
+ * binary16 copies of both).
  * grid_ctas: CTAs of the persistent step kernel, 0 = one per SM.
  * Synchronous.  Checks weights_len, the shape and the quantization. */
 gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights_host, size_t weights_len, int quant,

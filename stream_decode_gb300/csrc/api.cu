@@ -24,7 +24,7 @@ cudaError_t quantize_rows(const float* src_out_in, uint8_t* dst, int K, int N, b
 cudaError_t fold_rows(const uint8_t* rows, int K, int N, int wf, const float* g, const float* b, const float* bias,
                       float* c, float* d, cudaStream_t st);
 cudaError_t launch_project(const uint8_t* rows, int K, int N, int wq, const float* x, const float* bias, float* y,
-                           int stream, cudaStream_t st);
+                           int stream, int act_row, cudaStream_t st);
 cudaError_t launch_argmax(const float* v, unsigned n, uint32_t* idx, int* nonfinite, cudaStream_t st);
 bool cstep_supported(int D, int FF, int DH, int wf);
 cudaError_t cgeo_make(int L, int D, int H, int FF, int wf, int want_ctas, CGeo* out);
@@ -141,6 +141,7 @@ void fill_plan(const gpt2_session* s, StepPlan& P) {
     P.stall_phase = -1;
     P.prefetch_chunks = 0;
     P.pace_ns = kDefaultPaceNs;
+    P.act_row = m->quant == GPT2_INT8_ROW_ACT;
 }
 
 unsigned phases_per_step(const gpt2_model* m) {
@@ -248,14 +249,14 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
     if (!out) return GPT2_ERR_ARG;
     *out = nullptr;
     if (!config_ok(cfg) || (quant != GPT2_F32 && quant != GPT2_INT8_G64 && quant != GPT2_F16 &&
-                            quant != GPT2_INT8_ROW))
+                            quant != GPT2_INT8_ROW && quant != GPT2_INT8_ROW_ACT))
         return GPT2_ERR_CONFIG;
     if (!weights || weights_len != words_of(cfg) * 4) return GPT2_ERR_WEIGHTS_LEN;
     const int D = (int)cfg->d_model, FF = (int)cfg->d_ff, L = (int)cfg->n_layer;
     // the weight format of the device streams: per-row int8 scales use the
     // grouped layout with the row's scale in every group slot
-    const int wfmt = quant == GPT2_INT8_ROW ? kWQ8 : quant;
-    const bool q8 = wfmt == kWQ8, per_row = quant == GPT2_INT8_ROW;
+    const int wfmt = (quant == GPT2_INT8_ROW || quant == GPT2_INT8_ROW_ACT) ? kWQ8 : quant;
+    const bool q8 = wfmt == kWQ8, per_row = quant == GPT2_INT8_ROW || quant == GPT2_INT8_ROW_ACT;
     const int maxc = step_max_ctas(D, FF, D / (int)cfg->n_head, wfmt, (int)cfg->max_pos);
     if (maxc <= 0) return GPT2_ERR_CUDA;
     if (grid_ctas < 0 || grid_ctas > maxc) return GPT2_ERR_CONFIG;
@@ -619,7 +620,8 @@ gpt2_status gpt2_debug_project(gpt2_model* m, int index, const float* d_x, float
         bias = m->d_packed + b;
     }
     // the path the step kernel takes for this matrix at one CTA per SM: streaming for the vocabulary
-    return cuda_status(launch_project(rows, K, N, m->wfmt, d_x, bias, d_y, index == 4 * L ? 1 : 0, (cudaStream_t)stream));
+    return cuda_status(launch_project(rows, K, N, m->wfmt, d_x, bias, d_y, index == 4 * L ? 1 : 0,
+                                      m->quant == GPT2_INT8_ROW_ACT, (cudaStream_t)stream));
 }
 
 gpt2_status gpt2_debug_argmax(const float* d_values, uint32_t n, uint32_t* d_index, int* d_nonfinite,

@@ -585,12 +585,17 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     // of src fenced their writes for the async proxy before the caller's
     // barrier.  The issuing lanes wait until the copies have read src, so
     // src may be rewritten after the next barrier.
-    auto bcast = [&](const float* src, const float* dst, int n, uint64_t* bar) {
+    // With wait_now the issuing lanes wait until the copies have read src;
+    // otherwise only until the previous call's copies have (so a caller
+    // alternates between two source buffers, and a buffer is rewritten only
+    // after the barrier that follows the next call).
+    auto bcast = [&](const float* src, const float* dst, int n, uint64_t* bar, bool wait_now) {
         if (warp == 0 && lane < CS) {
             bulk_to_peer(mapa(smem_addr(dst), (uint32_t)lane), smem_addr(src), (uint32_t)n * 4u,
                          mapa(smem_addr(bar), (uint32_t)lane));
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            if (wait_now) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            else asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         }
     };
     // Waits (bounded) for a gather of `bytes` on this CTA's mbarrier (armed
@@ -803,7 +808,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             }
         }
     };
-    auto attention = [&](int l, int h, int p, int k0, int k1) {
+    auto attention = [&](int l, int h, int p, int k0, int k1, float* pw) {
         const float* kv0 = P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL;
         const float den = sqrtf((float)DH);
         const float4* q4 = reinterpret_cast<const float4*>(qkv + dc * DPL);
@@ -891,12 +896,12 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     O = fmaf(st[2 + d], cw, O);
                 }
             }
-            pa[4 + tid] = O;
+            pw[4 + tid] = O;
             if (tid == 0) {
-                pa[0] = M;
-                pa[1] = Z;
-                pa[2] = 0.0f;
-                pa[3] = 0.0f;
+                pw[0] = M;
+                pw[1] = Z;
+                pw[2] = 0.0f;
+                pw[3] = 0.0f;
             }
         }
     };
@@ -906,6 +911,8 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     unsigned prev_choice = *P.last_token;
     bool alive = !*s_abort;
     uint32_t useA = 0, useT = 0, useB = 0;  // uses of the double-buffered gathers
+    uint32_t n_bcast = 0;                     // all-gathers issued from the partials buffers
+    const int prow = (int)lay.prow;
     float* s_st = s_stA;                      // this slice's (mean, M2) of the LayerNorm input
     int s = 0;
     for (; s < P.n_steps && alive; ++s) {
@@ -976,6 +983,11 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                 const int kind = mp < 3 * nh ? mp % 3 : 3 + (mp - 3 * nh);
                 const int k = mp < 3 * nh ? mp / 3 : 0;
                 const int h = c + k * GG.NC;
+                // this micro-phase's partials: the all-gathered ones (QKV,
+                // attention, FC) alternate between two buffers, so that a
+                // buffer's copies to the peers complete while the next
+                // micro-phase fills the other
+                float* pw = (kind == 2 || kind == 4) ? pa : pa + (1 + (n_bcast & 1)) * prow;
                 // ---- the residual slice a LayerNorm of this micro-phase reads
                 if ((kind == 0 && k == 0) || kind == 3) {
                     // q = 0: the previous layer's MLP partials (block input);
@@ -1011,13 +1023,13 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     if (kind == 0 || kind == 3) { xv = xin; W4 = SW / 4; }
                     else if (kind == 2) { xv = oh; W4 = DH / 4; }
                     else { xv = uu; W4 = nfc4 / 4; }
-                    const bool ok = run_share(sh, xv, W4, pa);
+                    const bool ok = run_share(sh, xv, W4, pw);
                     if (warp == kCWarps - 1 && lane == 0 && (kind == 0 || kind == 3)) {
                         const int n0 = kind == 0 ? 3 * DH : nfc4;
-                        pa[n0] = s_st[0];
-                        pa[n0 + 1] = s_st[1];
-                        pa[n0 + 2] = 0.0f;
-                        pa[n0 + 3] = 0.0f;
+                        pw[n0] = s_st[0];
+                        pw[n0 + 1] = s_st[1];
+                        pw[n0 + 2] = 0.0f;
+                        pw[n0 + 3] = 0.0f;
                     }
                     if (kind == 0 || kind == 3) fence_async_smem();
                     if (stamps && cur_step == 0 && tid == 0) {
@@ -1028,7 +1040,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     stamp(16 * l + (kind == 0 ? 1 : kind == 2 ? 5 : kind == 3 ? 7 : 9));
                 } else {
                     const long long t_att = clock64();
-                    attention(l, h, p, att_k0, att_k1);
+                    attention(l, h, p, att_k0, att_k1, pw);
                     fence_async_smem();
                     csync();
                     if (stamps && cur_step == 0 && tid == 0)
@@ -1060,7 +1072,8 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                         gbuf = gB + (size_t)(u & 1) * CS * rowl;
                         bar = &bars[4 + (u & 1)];
                     }
-                    bcast(pa, gbuf + (size_t)r * rowl, nsend, bar);
+                    bcast(pw, gbuf + (size_t)r * rowl, nsend, bar, false);
+                    ++n_bcast;
                     // loaded while the gather completes: the first keys of this
                     // CTA's attention share, and this thread's fold constants
                     float cj = 0.0f, dj = 0.0f;
@@ -1136,7 +1149,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     uint64_t* dst = kind == 2 ? CP.partO + (size_t)h * D + col0
                                               : CP.partP + ((size_t)(l & 1) * GG.NC + c) * D + col0;
                     const unsigned tg = out_tag(kind == 2 ? tagA : tagB);
-                    for (int e = tid; e < SW; e += NT) st_tagged(dst + e, tg, pa[e]);
+                    for (int e = tid; e < SW; e += NT) st_tagged(dst + e, tg, pw[e]);
                 }
             }
         }
@@ -1148,7 +1161,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             break;
         }
         stamp(16 * L + 0);
-        bcast(xs, gX + col0, SW, &bars[6]);
+        bcast(xs, gX + col0, SW, &bars[6], true);
         {
             if (!gather_wait(&bars[6], (uint32_t)(D * 4), (uint32_t)s & 1)) { alive = false; break; }
         }
@@ -1230,6 +1243,9 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         if (reduce_choice(P.epoch + (unsigned)P.n_steps * per_step)) publish_choice(s - 1, *s_tok, *s_nf);
     }
     if (tid == 0) *s_abort = 1;  // the producer stops issuing
+    // this CTA's copies into its peers have landed before any CTA of the
+    // cluster leaves (a run that stopped early may have some in flight)
+    if (warp == 0 && lane < CS) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     cluster_barrier();
 }
 

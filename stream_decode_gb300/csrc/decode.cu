@@ -220,10 +220,31 @@ __device__ __forceinline__ void arg_warp_reduce(ArgBest& b) {
 // Quantize v[0..N) per group of 64 into q/s (int8 path).  Warp w owns groups
 // w, w + warps, ...; its groups are loaded, reduced and quantized together so
 // the shuffles and divisions of different groups overlap.
+// With row set, one scale for the whole vector instead (the largest |v| of
+// all N, reduced through red[kConsumerWarps] with one consumer barrier),
+// written to every group's slot.
+__device__ __forceinline__ float row_absmax(float m, float* red, int warp, int lane) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    consumers_sync();
+    float r = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) r = fmaxf(r, red[w]);
+    return r;
+}
+
 template <int N>
-__device__ __forceinline__ void quantize_vec(const float* v, int8_t* q, float* s, int warp, int lane) {
+__device__ __forceinline__ void quantize_vec(const float* v, int8_t* q, float* s, int warp, int lane, bool row,
+                                             float* red) {
     constexpr int NG = N / kGroup;
     constexpr int GPW = (NG + kConsumerWarps - 1) / kConsumerWarps;  // groups per warp (at most)
+    float mrow = 0.0f;
+    if (row) {
+        float m = 0.0f;
+        for (int i = warp * 32 + lane; i < N; i += kConsumerWarps * 32) m = fmaxf(m, fabsf(v[i]));
+        mrow = row_absmax(m, red, warp, lane);
+    }
     float a[GPW], b[GPW], m[GPW];
 #pragma unroll
     for (int k = 0; k < GPW; ++k) {
@@ -241,7 +262,7 @@ __device__ __forceinline__ void quantize_vec(const float* v, int8_t* q, float* s
     for (int k = 0; k < GPW; ++k) {
         const int gi = warp + kConsumerWarps * k;
         if (gi < NG) {
-            const float sc = __fdiv_rn(m[k], 127.0f), inv = __frcp_rn(sc);
+            const float sc = __fdiv_rn(row ? mrow : m[k], 127.0f), inv = __frcp_rn(sc);
             q[gi * kGroup + lane] = (int8_t)quantize_fast(a[k], sc, inv);
             q[gi * kGroup + 32 + lane] = (int8_t)quantize_fast(b[k], sc, inv);
             if (lane == 0) s[gi] = sc;
@@ -257,17 +278,29 @@ __device__ __forceinline__ void quantize_vec(const float* v, int8_t* q, float* s
 template <int K>
 __device__ __forceinline__ void quantize_quads(const float (&x)[4 * ((K / 4 + kConsumerWarps * 32 - 1) /
                                                                       (kConsumerWarps * 32))],
-                                               int8_t* q, float* s, int tid) {
+                                               int8_t* q, float* s, int tid, bool row, float* red) {
     constexpr int NT = kConsumerWarps * 32, NV = K / 4, NC = (NV + NT - 1) / NT;
     static_assert(K % kGroup == 0 && NT % 16 == 0, "groups are whole half-warps");
+    auto absmax4 = [&](int cc) {
+        // max of |v| starting from 0; NaN never wins a comparison
+        return fmaxf(fmaxf(fmaxf(fabsf(x[4 * cc]), fabsf(x[4 * cc + 1])), fmaxf(fabsf(x[4 * cc + 2]), fabsf(x[4 * cc + 3]))),
+                     0.0f);
+    };
+    float mrow = 0.0f;
+    if (row) {
+        float m = 0.0f;
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc)
+            if (tid + NT * cc < NV) m = fmaxf(m, absmax4(cc));
+        mrow = row_absmax(m, red, tid >> 5, tid & 31);
+    }
 #pragma unroll
     for (int cc = 0; cc < NC; ++cc) {
         const int col = tid + NT * cc;
-        // max of |v| starting from 0; NaN never wins a comparison
-        float m = fmaxf(fmaxf(fmaxf(fabsf(x[4 * cc]), fabsf(x[4 * cc + 1])), fmaxf(fabsf(x[4 * cc + 2]), fabsf(x[4 * cc + 3]))),
-                        0.0f);
+        float m = absmax4(cc);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (row) m = mrow;
         if (col < NV) {
             const float sc = __fdiv_rn(m, 127.0f), inv = __frcp_rn(sc);
             const uint32_t b0 = (uint32_t)(uint8_t)(int8_t)quantize_fast(x[4 * cc], sc, inv);
@@ -1238,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 if (kLnWidth && has_ln)
                     for (int i = tid; i < D; i += NT) P.trace[tb + (kind == kPhQKV ? 0 : 6 * D) + i] = xs[i];
             }
-            quantize_quads<KK>(x, vq, vs, tid);
+            quantize_quads<KK>(x, vq, vs, tid, P.act_row != 0, red);
             consumers_sync();
             if (!(kLnWidth && has_ln) && *slot != 0) return false;
             y = coop_q8<KK>(ring, gi, g.nrows, vq, vs, rsc, tid);
@@ -1666,8 +1699,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             if constexpr (Q8) {
                 // a streamed share's input (a spread share quantizes in its phase)
                 if (!spread) {
-                    if (kind == kPhP) quantize_vec<FF>(vin, vq, vs, warp, lane);
-                    else quantize_vec<D>(vin, vq, vs, warp, lane);
+                    if (kind == kPhP) quantize_vec<FF>(vin, vq, vs, warp, lane, P.act_row != 0, red);
+                    else quantize_vec<D>(vin, vq, vs, warp, lane, P.act_row != 0, red);
                     consumers_sync();
                 }
             }
@@ -1776,7 +1809,8 @@ template <int K, int WQ>
 __global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint8_t* __restrict__ rows, int N,
                                                                       const float* __restrict__ x,
                                                                       const float* __restrict__ bias,
-                                                                      float* __restrict__ y, int stream) {
+                                                                      float* __restrict__ y, int stream,
+                                                                      int act_row) {
     using H = HookGeo<K, WQ>;
     constexpr bool Q8 = H::Q8;
     extern __shared__ __align__(128) uint8_t sm[];
@@ -1797,7 +1831,7 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) project_kernel(const uint
     }
     for (int i = tid; i < K; i += blockDim.x) vin[i] = x[i];
     __syncthreads();
-    if constexpr (Q8) quantize_vec<K>(vin, vq, vs, warp, lane);
+    if constexpr (Q8) quantize_vec<K>(vin, vq, vs, warp, lane, act_row != 0, scratch);
     __syncthreads();
     auto out = [&](int j, float v) { y[j] = bias ? __fadd_rn(v, bias[j]) : v; };
     if (!stream) {
@@ -1853,23 +1887,23 @@ __global__ void __launch_bounds__(kConsumerWarps * 32) argmax_kernel(const float
 
 template <int K, int WQ>
 static cudaError_t project_t(const uint8_t* rows, int N, const float* x, const float* bias, float* y, int stream,
-                             cudaStream_t st) {
+                             int act_row, cudaStream_t st) {
     using H = HookGeo<K, WQ>;
     const int per_block = stream ? H::CHUNKS_STREAM * H::RPC : H::ROWS_SPREAD;
     cudaError_t e = cudaFuncSetAttribute(project_kernel<K, WQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)H::SMEM);
     if (e != cudaSuccess) return e;
     project_kernel<K, WQ><<<(N + per_block - 1) / per_block, kConsumerWarps * 32, H::SMEM, st>>>(rows, N, x, bias, y,
-                                                                                               stream);
+                                                                                               stream, act_row);
     return cudaGetLastError();
 }
 
 cudaError_t launch_project(const uint8_t* rows, int K, int N, int wq, const float* x, const float* bias, float* y,
-                           int stream, cudaStream_t st) {
+                           int stream, int act_row, cudaStream_t st) {
 #define GPT2_PROJ(KK)                                                                                        \
     if (K == KK)                                                                                             \
-        return wq == kWQ8    ? project_t<KK, kWQ8>(rows, N, x, bias, y, stream, st)                          \
-               : wq == kWF16 ? project_t<KK, kWF16>(rows, N, x, bias, y, stream, st)                         \
-                             : project_t<KK, kWF32>(rows, N, x, bias, y, stream, st);
+        return wq == kWQ8    ? project_t<KK, kWQ8>(rows, N, x, bias, y, stream, act_row, st)                 \
+               : wq == kWF16 ? project_t<KK, kWF16>(rows, N, x, bias, y, stream, act_row, st)                \
+                             : project_t<KK, kWF32>(rows, N, x, bias, y, stream, act_row, st);
     GPT2_PROJ(64) GPT2_PROJ(192) GPT2_PROJ(256) GPT2_PROJ(384) GPT2_PROJ(768) GPT2_PROJ(3072)
 #undef GPT2_PROJ
     return cudaErrorInvalidValue;

@@ -127,6 +127,7 @@ struct StepPlan {
     int stall_phase;            // test: CTA 0 skips publishing this phase (-1 = none)
     int prefetch_chunks;        // L2 bulk prefetch distance in chunks (0 = off)
     uint32_t pace_ns;           // least interval between block-weight chunk issues (0 = unpaced)
+    int act_row;                // int8: one activation scale per projection input vector (else per 64)
 };
 
 // LayerNorm folded into the projection that follows it (binary32 models):

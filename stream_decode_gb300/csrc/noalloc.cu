@@ -146,6 +146,7 @@ extern "C" gpt2_status gpt2_cached_step_noalloc(const gpt2_model* m, float* d_ca
     P.stall_phase = -1;
     P.prefetch_chunks = 0;
     P.pace_ns = kDefaultPaceNs;
+    P.act_row = m->quant == GPT2_INT8_ROW_ACT;
     if (m->ckern) {
         // the cluster step kernel: the same plan, its geometry and exchange words
         CPlan C;

@@ -21,7 +21,7 @@ if not os.path.exists(_LIB_PATH):
 lib = C.CDLL(_LIB_PATH)
 
 GREEDY = 0xFFFFFFFF
-F32, INT8_G64, F16, INT8_ROW = 0, 1, 2, 3
+F32, INT8_G64, F16, INT8_ROW, INT8_ROW_ACT = 0, 1, 2, 3, 4
 STATUS = {0: "ok", 1: "weights_len", 2: "token", 3: "position", 4: "cache_len", 5: "tokens_len",
           6: "nonfinite", 7: "config", 8: "nomem", 9: "timeout", 10: "cuda", 11: "arg", 12: "scratch"}
 

@@ -99,7 +99,7 @@ def test_124m_f16_decode_128_positions(g, oracle, w124m, kernel):
     assert np.abs(cache - ref_cache).max() <= LOGIT_TOL
 
 
-@pytest.mark.parametrize("quant", [0, 1, 2, 3], ids=["f32", "int8", "f16", "int8_row"])
+@pytest.mark.parametrize("quant", [0, 1, 2, 3, 4], ids=["f32", "int8", "f16", "int8_row", "int8_row_act"])
 def test_124m_projections_on_identical_inputs(g, oracle, w124m, quant):
     from test_gpu_decode import check_projections
     L = 12

@@ -379,9 +379,10 @@ def check_projections(g, oracle, shape, w, quant, indices, seed=31):
     bit for bit against the oracle's int8 projection (codes, int32 group
     sums, fixed-order rescale, bias); binary32 models within 1e-5, and
     binary16-weight models within 1e-5 of the binary32 projection with the
-    oracle's rounded weights."""
+    oracle's rounded weights.  quant 4 quantizes the input with one scale
+    for the whole vector."""
     model = g.Model(shape, w, quant=quant)
-    q8 = quant in (1, 3)
+    q8 = quant in (1, 3, 4)
     om = oracle.model(shape, w, quant=quant) if q8 else None
     p = None
     for idx in indices:
@@ -406,7 +407,7 @@ def check_projections(g, oracle, shape, w, quant, indices, seed=31):
         y = dy.cpu().numpy()
         b = _matrix_bias(shape, w, idx)
         if q8:
-            ref = oracle.linear_q8(x, q, s, b)
+            ref = oracle.linear_q8(x, q, s, b, per_row_x=quant == 4)
             assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), f"matrix {idx}"
         else:
             ref = oracle.linear_f32(x, wm.astype(np.float32), b)
@@ -418,7 +419,7 @@ def check_projections(g, oracle, shape, w, quant, indices, seed=31):
 
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
-@pytest.mark.parametrize("quant", [0, 1, 2, 3], ids=["f32", "int8", "f16", "int8_row"])
+@pytest.mark.parametrize("quant", [0, 1, 2, 3, 4], ids=["f32", "int8", "f16", "int8_row", "int8_row_act"])
 def test_projections_on_identical_inputs(g, oracle, shape, seed, quant):
     w = synth.checkpoint(shape, seed, "rich")
     check_projections(g, oracle, shape, w, quant, range(4 * shape.n_layer + 1))
@@ -462,7 +463,7 @@ def test_int8_activation_codes_near_ties(g, oracle):
 
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
-@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+@pytest.mark.parametrize("quant", [1, 3, 4], ids=["group64", "per_row", "per_row_act"])
 def test_int8_session(g, oracle, shape, seed, quant):
     logits, ch, ref, ref_ch, cache, ref_cache, greedy_ch, seq = _session_case(g, oracle, shape, seed, "rich", quant,
                                                                                0)

@@ -82,14 +82,14 @@ def _check(logits, ch, ref, ref32, agree_min=AGREE_MIN):
     assert greedy_agreement(ref, ch) >= agree_min
 
 
-@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+@pytest.mark.parametrize("quant", [1, 3, 4], ids=["group64", "per_row", "per_row_act"])
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
 def test_int8_session_is_int8_not_binary32(g, oracle, shape, seed, quant):
     _check(*_int8_session_case(g, oracle, shape, seed, quant, shape.max_pos))
 
 
-@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+@pytest.mark.parametrize("quant", [1, 3, 4], ids=["group64", "per_row", "per_row_act"])
 def test_124m_int8_steps_are_int8_not_binary32(g, oracle, quant):
     """GPT-2 124M: the GPU runs 64 positions in one launch; at 8 sampled
     positions the oracle takes the same step (int8, and binary32) from the
@@ -120,7 +120,7 @@ def test_124m_int8_steps_are_int8_not_binary32(g, oracle, quant):
     _check(logits[ps], np.asarray(ch)[ps], np.stack(ref), np.stack(ref32), agree_min=0.75)
 
 
-@pytest.mark.parametrize("quant", [1, 3], ids=["group64", "per_row"])
+@pytest.mark.parametrize("quant", [1, 3, 4], ids=["group64", "per_row", "per_row_act"])
 @pytest.mark.parametrize("shape,seed", [(synth.GPT2_TINY, synth.SEED_TINY), (P.SMALL, P.SEED_SMALL)],
                          ids=["tiny", "small"])
 def test_int8_traced_projections_bit_exact(g, oracle, shape, seed, quant):
@@ -143,6 +143,7 @@ def test_int8_traced_projections_bit_exact(g, oracle, shape, seed, quant):
     logits, _ = run(sess, toks[5:6], 1)
     t = tr.cpu().numpy()
     d, F, L = shape.d_model, shape.d_ff, shape.n_layer
+    rx = quant == 4  # one activation scale per vector
     lay = synth.layout(shape)
     per = 8 * d + F
 
@@ -160,16 +161,16 @@ def test_int8_traced_projections_bit_exact(g, oracle, shape, seed, quant):
         xm, ln2, u = t[base + 6 * d:base + 7 * d], t[base + 7 * d:base + 8 * d], t[base + 8 * d:base + 8 * d + F]
         x_next = t[(l + 1) * per:(l + 1) * per + d] if l + 1 < L else t[L * per:L * per + d]
         q, s = om.q8_matrix(4 * l)
-        assert same(qkv, oracle.linear_q8(ln1, q, s, par(f"h{l}.b_qkv"))), f"qkv, layer {l}"
+        assert same(qkv, oracle.linear_q8(ln1, q, s, par(f"h{l}.b_qkv"), per_row_x=rx)), f"qkv, layer {l}"
         q, s = om.q8_matrix(4 * l + 1)
-        y = oracle.linear_q8(o_, q, s, par(f"h{l}.b_o"))
+        y = oracle.linear_q8(o_, q, s, par(f"h{l}.b_o"), per_row_x=rx)
         assert same(xm, (x + y).astype(np.float32)), f"attention residual, layer {l}"
         q, s = om.q8_matrix(4 * l + 2)
-        pre = oracle.linear_q8(ln2, q, s, par(f"h{l}.b_fc"))
+        pre = oracle.linear_q8(ln2, q, s, par(f"h{l}.b_fc"), per_row_x=rx)
         ref_u = np.array([oracle.gelu(float(v)) for v in pre], np.float32)
         assert np.abs(u - ref_u).max() <= 4 * np.spacing(np.abs(ref_u).max()), f"gelu, layer {l}"
         q, s = om.q8_matrix(4 * l + 3)
-        y = oracle.linear_q8(u, q, s, par(f"h{l}.b_p"))
+        y = oracle.linear_q8(u, q, s, par(f"h{l}.b_p"), per_row_x=rx)
         assert same(x_next, (xm + y).astype(np.float32)), f"block output, layer {l}"
         # the LayerNorm outputs the kernel quantized are those of its residual, to rounding
         for xx, lnv, gn, bn in ((x, ln1, f"h{l}.ln1_g", f"h{l}.ln1_b"), (xm, ln2, f"h{l}.ln2_g", f"h{l}.ln2_b")):
@@ -177,7 +178,7 @@ def test_int8_traced_projections_bit_exact(g, oracle, shape, seed, quant):
             assert np.abs(lnv - ref_ln).max() <= 1e-5 * max(1.0, float(np.abs(ref_ln).max())), f"LN, layer {l}"
     xf, lnf = t[L * per:L * per + d], t[L * per + d:L * per + 2 * d]
     q, s = om.q8_matrix(4 * L)
-    assert same(logits[0], oracle.linear_q8(lnf, q, s, None)), "logits"
+    assert same(logits[0], oracle.linear_q8(lnf, q, s, None, per_row_x=rx)), "logits"
     assert np.abs(lnf - oracle.layernorm(xf, par("lnf_g"), par("lnf_b"))).max() <= 1e-5 * max(
         1.0, float(np.abs(lnf).max()))
     sess.close()

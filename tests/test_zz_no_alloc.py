@@ -91,7 +91,7 @@ def test_noalloc_matches_session_step_124m(g, w124m, kernel):
     _compare(g, synth.GPT2_124M, w124m, g.F32, n_calls=3)
 
 
-@pytest.mark.parametrize("fmt", ["INT8_G64", "F16", "INT8_ROW"])
+@pytest.mark.parametrize("fmt", ["INT8_G64", "F16", "INT8_ROW", "INT8_ROW_ACT"])
 def test_noalloc_matches_session_step_other_formats(g, fmt):
     shape = synth.GPT2_TINY
     _compare(g, shape, synth.checkpoint(shape, synth.SEED_TINY, "rich"), getattr(g, fmt))
