@@ -334,7 +334,10 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
-    const int CS = GG.CS, SW = GG.SW, NSL = GG.slots;
+    // the cluster size and slice width are constants of the instantiation
+    // (the host builds the geometry with the same function)
+    constexpr int CS = cluster_size_for(D), SW = D / CS;
+    const int NSL = GG.slots;
     const int r = (int)cluster_rank();
     const int c = cta / CS;
     const int L = P.L, H = P.H;
@@ -915,19 +918,23 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     const int prow = (int)lay.prow;
     float* s_st = s_stA;                      // this slice's (mean, M2) of the LayerNorm input
     int s = 0;
-    for (; s < P.n_steps && alive; ++s) {
+    // s = n_steps only reduces the last step's greedy choice (in CTA 0, which
+    // reports it), so that the reduction has one copy in the binary
+    for (; s <= P.n_steps && alive; ++s) {
         const int p = P.p0 + s;
         const unsigned base = P.epoch + (unsigned)s * per_step;
         const bool tr = tracing && s == 0;
         cur_step = s;
         cur_layer = 0;
         if (s > 0) {
+            if (s == P.n_steps && cta != 0) break;
             if (!reduce_choice(base)) { alive = false; break; }
             prev_choice = *s_tok;
             const int nf = *s_nf;
             publish_choice(s - 1, prev_choice, nf);
             if (nf) { alive = false; break; }
         }
+        if (s == P.n_steps) break;
         // this CTA's keys [att_k0, att_k1) of positions 0..p (cached ones below att_k1c)
         const int att_k0 = (int)(((long long)r * (p + 1)) / CS), att_k1 = (int)(((long long)(r + 1) * (p + 1)) / CS);
         const int att_k1c = att_k1 < p ? att_k1 : p;
@@ -1108,8 +1115,16 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                         // QKV (0) or FC (3): the CS slice partials summed in
                         // rank order, the LayerNorm fold, then q/k/v (and the
                         // KV append) or the GELU output
+                        // (the loop's per-kind choices are selects, so that
+                        // the compiler keeps one copy of its body)
                         const bool qk = kind == 0;
                         const int nrow = qk ? 3 * DH : nfc;
+                        float* dstv = qk ? qkv : uu;
+                        const int klo = qk ? kv_lo : 0, khi = qk ? kv_hi : 0;
+                        float* kvrow = P.cache + ((uint64_t)p * L + l) * 2 * D - D;
+                        float* trp = (tr && r == 0) ? P.trace + (size_t)l * trace_layer + (qk ? 2 * D : 8 * D + f0)
+                                                    : nullptr;
+                        const int dstride = qk ? 3 * D : FF;
                         float mean, rstd;
                         merge_stats(gbuf + (qk ? 3 * DH : nfc4), rowl, mean, rstd);
 #pragma unroll 1
@@ -1124,17 +1139,13 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                             float cc = cj, dd = dj;
                             if (j != tid) {
                                 cc = __ldg(fl + Jr);
-                                dd = __ldg(fl + Jr + (qk ? 3 * D : FF));
+                                dd = __ldg(fl + Jr + dstride);
                             }
-                            float y = fmaf(rstd, fmaf(-mean, cc, a), dd);
-                            if (qk) {
-                                qkv[j] = y;
-                                if (j >= kv_lo && j < kv_hi) P.cache[((uint64_t)p * L + l) * 2 * D + (Jr - D)] = y;
-                            } else {
-                                y = cgelu(y);
-                                uu[j] = y;
-                            }
-                            if (tr && r == 0) P.trace[(size_t)l * trace_layer + (qk ? 2 * D + Jr : 8 * D + f0 + j)] = y;
+                            const float y0 = fmaf(rstd, fmaf(-mean, cc, a), dd);
+                            const float y = qk ? y0 : cgelu(y0);
+                            dstv[j] = y;
+                            if (j >= klo && j < khi) kvrow[Jr] = y;
+                            if (trp) trp[qk ? Jr : j] = y;
                         }
                         if (tr && c == 0 && (!qk || k == 0))
                             ctrace_ln(P.trace + (size_t)l * trace_layer + (qk ? D : 7 * D) + col0, xs, ln_shift + mean,
@@ -1237,10 +1248,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                 st_tagged_release(ap, tag_pack(tg, b.v));
             }
         }
-    }
-    // The last step's greedy choice (CTA 0 reports it).
-    if (alive && s == P.n_steps && cta == 0) {
-        if (reduce_choice(P.epoch + (unsigned)P.n_steps * per_step)) publish_choice(s - 1, *s_tok, *s_nf);
     }
     if (tid == 0) *s_abort = 1;  // the producer stops issuing
     // this CTA's copies into its peers have landed before any CTA of the
@@ -1374,12 +1381,6 @@ int max_clusters(int D, int FF, int DH, int wf, int CS, uint32_t smem) {
 
 // Cluster size per model width: a slice of 128 floats (one warp of float4
 // columns) where the width allows.
-int preferred_cs(int D) {
-    if (D % 128 == 0 && D / 128 <= 8) return D / 128;
-    if (D % 32 == 0 && D / 32 <= 8) return D / 32;
-    return 1;
-}
-
 }  // namespace
 
 bool cstep_supported(int D, int FF, int DH, int wf) {
@@ -1398,9 +1399,7 @@ cudaError_t cgeo_make(int L, int D, int H, int FF, int wf, int want_ctas, CGeo* 
     const int DH = D / H;
     CGeo g;
     memset(&g, 0, sizeof(g));
-    int CS = preferred_cs(D);
-    const char* env_cs = getenv("GPT2_CLUSTER_SIZE");
-    if (env_cs) CS = atoi(env_cs);
+    const int CS = cluster_size_for(D);
     if (CS < 1 || CS > 16 || D % CS != 0 || (D / CS) % 8 != 0) return cudaErrorInvalidValue;
     g.CS = CS;
     g.SW = D / CS;

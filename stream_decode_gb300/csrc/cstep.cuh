@@ -73,6 +73,13 @@ struct CPlan {
     uint64_t* partP;            // [2][NC][D] MLP-projection partials of each cluster, by layer parity (tagged words)
 };
 
+// Cluster size for width D: CS = D / 128 when that is at most 8 (GPT-2
+// 124M: 6, one warp of float4 columns per CTA), else D / 32; a constant of
+// the kernel's instantiation.
+__host__ __device__ constexpr int cluster_size_for(int D) {
+    return (D % 128 == 0 && D / 128 <= 8) ? D / 128 : (D % 32 == 0 && D / 32 <= 8) ? D / 32 : 1;
+}
+
 // Stamps per CTA in the timing buffer of the cluster kernel.
 __host__ __device__ inline int cstamps_per_cta(int L) { return 16 * L + 8; }
 
