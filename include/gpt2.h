@@ -314,10 +314,8 @@ gpt2_status gpt2_session_set_trace(gpt2_session* session, float* d_trace);
  * QKV partials done, q/k/v gathered, attention done, head outputs gathered,
  * out-projection partials stored, attention residual formed, FC partials
  * done, GELU outputs gathered, MLP partials stored (a CTA of a cluster
- * without a head leaves the second to sixth at 0); then for the QKV,
- * out-projection, FC and MLP shares of warp 0, (clock64 cycles waiting for
- * weight chunks << 32 | cycles in all); 2 words unused.  Then final input
- * formed, gathered, LN_f done, vocabulary rows done; then, if a wait of
+ * without a head leaves the second to sixth at 0); 6 words unused.  Then
+ * final input formed, gathered, LN_f done, vocabulary rows done; then, if a wait of
  * this CTA gave up, (kind | 0x100 if it left because another CTA had
  * given up | thread index << 16), the step, the layer and what was
  * awaited.  Pass NULL to stop. */

@@ -73,6 +73,13 @@ __device__ __forceinline__ void st_async4(uint32_t raddr, float4 v, uint32_t rba
                  : "memory");
 }
 
+// 4 bytes into a peer's shared memory, completing on the peer's mbarrier.
+__device__ __forceinline__ void st_async1(uint32_t raddr, float v, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(raddr), "f"(v),
+                 "r"(rbar)
+                 : "memory");
+}
+
 // Orders this thread's earlier shared-memory writes before later bulk
 // (async-proxy) copies that read them.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -390,11 +397,11 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         // always before a peer can send that next use's data: a barrier is
         // never armed after data for its phase has arrived.
         {
-            const int nfc4_ = ((plan.g.fc0[blockIdx.x / plan.g.CS + 1] - plan.g.fc0[blockIdx.x / plan.g.CS]) + 3) & ~3;
+            const int nfc_ = plan.g.fc0[blockIdx.x / plan.g.CS + 1] - plan.g.fc0[blockIdx.x / plan.g.CS];
             for (int i = 0; i < 2; ++i) {
-                mbar_arrive_expect_tx(&bars[0 + i], (uint32_t)(plan.g.CS * (3 * DH + 4) * 4));
-                mbar_arrive_expect_tx(&bars[2 + i], (uint32_t)(plan.g.CS * (DH + 4) * 4));
-                mbar_arrive_expect_tx(&bars[4 + i], (uint32_t)(plan.g.CS * (nfc4_ + 4) * 4));
+                mbar_arrive_expect_tx(&bars[0 + i], (uint32_t)(plan.g.CS * (3 * DH + 2) * 4));
+                mbar_arrive_expect_tx(&bars[2 + i], (uint32_t)(plan.g.CS * (DH + 2) * 4));
+                mbar_arrive_expect_tx(&bars[4 + i], (uint32_t)(plan.g.CS * (nfc_ + 2) * 4));
             }
             mbar_arrive_expect_tx(&bars[6], (uint32_t)(D * 4));
         }
@@ -601,41 +608,51 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             else asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         }
     };
+    // One value to the same offset (local address a) of every CTA of the
+    // cluster, this one included, completing 4 bytes on each one's mbarrier
+    // (local address bar).  The all-gathers of partials are made of these:
+    // each value leaves the thread that computed it, with no staging copy
+    // and no barrier before the send.
+    auto send_all = [&](uint32_t a, float v, uint32_t bar) {
+#pragma unroll
+        for (int q = 0; q < CS; ++q) st_async1(mapa(a, (uint32_t)q), v, mapa(bar, (uint32_t)q));
+    };
     // Waits (bounded) for a gather of `bytes` on this CTA's mbarrier (armed
     // in advance), agrees on the outcome, and re-arms the barrier for its
     // next use.  Contains an agreement barrier.
-    auto gather_wait = [&](uint64_t* bar, uint32_t bytes, uint32_t par) -> bool {
-        const bool ok = agree(wait_bar(bar, par));
+    auto gather_wait = [&](uint64_t* bar, uint32_t bytes, uint32_t par, bool ok_in) -> bool {
+        const bool ok = agree(ok_in && wait_bar(bar, par));
         if (ok && tid == 0) mbar_arrive_expect_tx(bar, bytes);
         return ok;
     };
     // Rows of a share against x4 (W4 float4 columns); row i's dot product to
     // out[i].  Chunk k is taken by warp k % 8.
-    uint64_t prof_wait = 0, prof_total = 0;  // warp 0, last share: clock64 cycles waiting for chunks, in all
-    uint64_t prof_comb = 0;                  // thread 0: cycles of the last QKV combine
     // The chunks are taken in rounds of one per warp with a barrier between
     // rounds.  The ring's barriers are waited on by phase parity, which is
     // only unambiguous if the previous fill of a chunk's slot has landed;
     // the rounds keep every warp within one round of the others, so the
     // previous fill of any slot this round uses (kCWarps <= slots) was
     // consumed in an earlier round.
-    auto run_share = [&](const Share& sh, const float* x, int W4, float* out) -> bool {
+    // With row_s != 0 each row's result is sent to offset 4 * row of row_s
+    // (a gather row, local address) in every CTA of the cluster, completing
+    // on bar_s; otherwise it is stored to out.
+    auto run_share = [&](const Share& sh, const float* x, int W4, float* out, uint32_t row_s, uint32_t bar_s) -> bool {
         bool ok = true;
         const uint32_t x_s = smem_addr(x);
-        const long long t_in = clock64();
-        long long t_wait = 0;
         for (int k0 = 0; k0 < sh.nch; k0 += kCWarps) {
             const int k = k0 + warp;
             if (ok && k < sh.nch) {
                 const uint32_t cc = gi + (uint32_t)k;
-                const long long tw = clock64();
                 ok = wait_chunk(cc);
-                t_wait += clock64() - tw;
                 if (ok) {
                     const uint32_t w = ring_s + (cc % (uint32_t)NSL) * (uint32_t)kCSlotBytes;
                     const int n = min(sh.rpc, sh.n - k * sh.rpc);
                     const float v = chunk_rows<WF>(w, n, W4, x_s, lane);
-                    if (lane < n) out[k * sh.rpc + lane] = v;
+                    if (lane < n) {
+                        const int i = k * sh.rpc + lane;
+                        if (row_s) send_all(row_s + 4u * (uint32_t)i, v, bar_s);
+                        else out[i] = v;
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[cc % (uint32_t)NSL]);
                 }
@@ -643,8 +660,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             if (k0 + kCWarps < sh.nch) csync();
         }
         gi += (uint32_t)sh.nch;
-        prof_wait = (uint64_t)t_wait;
-        prof_total = (uint64_t)(clock64() - t_in);
         return ok;
     };
     // Deterministic block sum over the consumer threads (same value in all).
@@ -790,8 +805,9 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     };
 
     // Attention of head h (layer l, position p) over this CTA's keys
-    // [k0, k1) of 0..p: (max, sum, unnormalised weighted values) into
-    // pa[0], pa[1], pa[4 .. 4 + DH).  LPK lanes per key, DPL dims per lane;
+    // [k0, k1) of 0..p: (max, sum, unnormalised weighted values) sent to
+    // words 0, 1 and 4 .. 4 + DH of gather row row_s in every CTA of the
+    // cluster.  LPK lanes per key, DPL dims per lane;
     // the current position's key and value come from qkv (this step's).
     constexpr int LPK = DH >= 32 ? 8 : 4;
     constexpr int KPW = 32 / LPK;
@@ -811,7 +827,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             }
         }
     };
-    auto attention = [&](int l, int h, int p, int k0, int k1, float* pw) {
+    auto attention = [&](int l, int h, int p, int k0, int k1, uint32_t row_s, uint32_t bar_s) {
         const float* kv0 = P.cache + (uint64_t)l * 2 * D + h * DH + dc * DPL;
         const float den = sqrtf((float)DH);
         const float4* q4 = reinterpret_cast<const float4*>(qkv + dc * DPL);
@@ -860,7 +876,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             }
         }
         // merge the key slots of the warp (lanes with the same dc)
-#pragma unroll
+#pragma unroll 1
         for (int o = LPK; o < 32; o <<= 1) {
             const float om = __shfl_xor_sync(0xffffffffu, m, o);
             const float oz = __shfl_xor_sync(0xffffffffu, z, o);
@@ -890,7 +906,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, stage[(w * LPK + cq) * (2 + DPL)]);
             float Z = 0.0f, O = 0.0f;
             if (M != -INFINITY) {
-#pragma unroll
+#pragma unroll 1
                 for (int w = 0; w < kCWarps; ++w) {
                     const float* st = stage + (w * LPK + cq) * (2 + DPL);
                     if (st[0] == -INFINITY) continue;
@@ -899,12 +915,10 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     O = fmaf(st[2 + d], cw, O);
                 }
             }
-            pw[4 + tid] = O;
+            send_all(row_s + 4u * (uint32_t)(4 + tid), O, bar_s);
             if (tid == 0) {
-                pw[0] = M;
-                pw[1] = Z;
-                pw[2] = 0.0f;
-                pw[3] = 0.0f;
+                send_all(row_s, M, bar_s);
+                send_all(row_s + 4u, Z, bar_s);
             }
         }
     };
@@ -914,8 +928,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     unsigned prev_choice = *P.last_token;
     bool alive = !*s_abort;
     uint32_t useA = 0, useT = 0, useB = 0;  // uses of the double-buffered gathers
-    uint32_t n_bcast = 0;                     // all-gathers issued from the partials buffers
-    const int prow = (int)lay.prow;
     float* s_st = s_stA;                      // this slice's (mean, M2) of the LayerNorm input
     int s = 0;
     // s = n_steps only reduces the last step's greedy choice (in CTA 0, which
@@ -990,11 +1002,35 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                 const int kind = mp < 3 * nh ? mp % 3 : 3 + (mp - 3 * nh);
                 const int k = mp < 3 * nh ? mp / 3 : 0;
                 const int h = c + k * GG.NC;
-                // this micro-phase's partials: the all-gathered ones (QKV,
-                // attention, FC) alternate between two buffers, so that a
-                // buffer's copies to the peers complete while the next
-                // micro-phase fills the other
-                float* pw = (kind == 2 || kind == 4) ? pa : pa + (1 + (n_bcast & 1)) * prow;
+                // the cluster all-gather of this micro-phase (QKV partials,
+                // attention partials, FC partials): use u of a double-buffered
+                // gather buffer of CS rows of rowl floats, nval values per row
+                const bool gat = kind == 0 || kind == 1 || kind == 3;
+                uint32_t u = 0;
+                int rowl = 0, nval = 0;
+                float* gbuf = nullptr;
+                uint64_t* bar = nullptr;
+                if (kind == 0) {
+                    u = useA++;
+                    rowl = 3 * DH + 4;
+                    nval = 3 * DH + 2;
+                    gbuf = gA + (size_t)(u & 1) * CS * rowl;
+                    bar = &bars[0 + (u & 1)];
+                } else if (kind == 1) {
+                    u = useT++;
+                    rowl = DH + 4;
+                    nval = DH + 2;
+                    gbuf = gT + (size_t)(u & 1) * CS * rowl;
+                    bar = &bars[2 + (u & 1)];
+                } else if (kind == 3) {
+                    u = useB++;
+                    rowl = GG.nfc_max + 4;
+                    nval = nfc + 2;
+                    gbuf = gB + (size_t)(u & 1) * CS * rowl;
+                    bar = &bars[4 + (u & 1)];
+                }
+                const uint32_t row_s = gat ? smem_addr(gbuf + (size_t)r * rowl) : 0u;
+                const uint32_t bar_s = gat ? smem_addr(bar) : 0u;
                 // ---- the residual slice a LayerNorm of this micro-phase reads
                 if ((kind == 0 && k == 0) || kind == 3) {
                     // q = 0: the previous layer's MLP partials (block input);
@@ -1008,7 +1044,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                             break;
                         }
                         stamp(16 * l + (q == 0 ? 0 : 6));
-                        if (q == 0 && stamps && cur_step == 0 && tid == 0) stamps[16 * l + 15] = (uint64_t)clock64();
                         if (tr && c == 0) ctrace_copy(P.trace + (size_t)l * trace_layer + (q == 0 ? 0 : 6 * D) + col0, xs, SW, tid);
                     }
                     if (!alive) break;
@@ -1022,6 +1057,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     slice_stats(ln_shift, s_st);
                 }
                 // ---- dot products of this micro-phase's share (attention has none)
+                bool ok_share = true;
                 if (kind != 1) {
                     Share sh;
                     const float* xv;
@@ -1030,57 +1066,22 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     if (kind == 0 || kind == 3) { xv = xin; W4 = SW / 4; }
                     else if (kind == 2) { xv = oh; W4 = DH / 4; }
                     else { xv = uu; W4 = nfc4 / 4; }
-                    const bool ok = run_share(sh, xv, W4, pw);
-                    if (warp == kCWarps - 1 && lane == 0 && (kind == 0 || kind == 3)) {
-                        const int n0 = kind == 0 ? 3 * DH : nfc4;
-                        pw[n0] = s_st[0];
-                        pw[n0 + 1] = s_st[1];
-                        pw[n0 + 2] = 0.0f;
-                        pw[n0 + 3] = 0.0f;
+                    if (gat && warp == kCWarps - 1 && lane == 0) {
+                        // this slice's LayerNorm statistics go with the partials
+                        const uint32_t n0 = (uint32_t)(kind == 0 ? 3 * DH : nfc4);
+                        send_all(row_s + 4u * n0, s_st[0], bar_s);
+                        send_all(row_s + 4u * (n0 + 1u), s_st[1], bar_s);
                     }
-                    if (kind == 0 || kind == 3) fence_async_smem();
-                    if (stamps && cur_step == 0 && tid == 0) {
-                        const int sl = 16 * l + 10 + (kind == 0 ? 0 : kind == 2 ? 1 : kind == 3 ? 2 : 3) * 1;
-                        stamps[sl] = (prof_wait << 32) | (prof_total & 0xFFFFFFFFull);
-                    }
-                    if (!agree(ok)) { alive = false; break; }
+                    ok_share = run_share(sh, xv, W4, pa, row_s, bar_s);
+                    // the out-projection and MLP partials are stored from pa by other threads
+                    if (!gat && !agree(ok_share)) { alive = false; break; }
                     stamp(16 * l + (kind == 0 ? 1 : kind == 2 ? 5 : kind == 3 ? 7 : 9));
                 } else {
-                    const long long t_att = clock64();
-                    attention(l, h, p, att_k0, att_k1, pw);
-                    fence_async_smem();
-                    csync();
-                    if (stamps && cur_step == 0 && tid == 0)
-                        stamps[16 * l + 14] = (prof_comb << 32) | ((uint64_t)(clock64() - t_att) & 0xFFFFFFFFull);
+                    attention(l, h, p, att_k0, att_k1, row_s, bar_s);
                     stamp(16 * l + 3);
                 }
-                // ---- the cluster all-gather (QKV partials, attention partials, FC partials)
-                if (kind == 0 || kind == 1 || kind == 3) {
-                    uint32_t u;
-                    int rowl, nsend;
-                    float* gbuf;
-                    uint64_t* bar;
-                    if (kind == 0) {
-                        u = useA++;
-                        rowl = 3 * DH + 4;
-                        nsend = rowl;
-                        gbuf = gA + (size_t)(u & 1) * CS * rowl;
-                        bar = &bars[0 + (u & 1)];
-                    } else if (kind == 1) {
-                        u = useT++;
-                        rowl = DH + 4;
-                        nsend = rowl;
-                        gbuf = gT + (size_t)(u & 1) * CS * rowl;
-                        bar = &bars[2 + (u & 1)];
-                    } else {
-                        u = useB++;
-                        rowl = GG.nfc_max + 4;
-                        nsend = nfc4 + 4;
-                        gbuf = gB + (size_t)(u & 1) * CS * rowl;
-                        bar = &bars[4 + (u & 1)];
-                    }
-                    bcast(pw, gbuf + (size_t)r * rowl, nsend, bar, false);
-                    ++n_bcast;
+                // ---- the cluster all-gather completes, then its epilogue
+                if (gat) {
                     // loaded while the gather completes: the first keys of this
                     // CTA's attention share, and this thread's fold constants
                     float cj = 0.0f, dj = 0.0f;
@@ -1091,15 +1092,15 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                         cj = __ldg(fl + Jt);
                         dj = __ldg(fl + Jt + (kind == 0 ? 3 * D : FF));
                     }
-                    if (!gather_wait(bar, (uint32_t)(CS * nsend * 4), (u >> 1) & 1)) { alive = false; break; }
+                    if (!gather_wait(bar, (uint32_t)(CS * nval * 4), (u >> 1) & 1, ok_share)) { alive = false; break; }
                     stamp(16 * l + (kind == 0 ? 2 : kind == 1 ? 4 : 8));
                     // ---- epilogues of the gathered values
-                    const long long t_epi = clock64();
                     if (kind == 1) {
                         if (tid < DH) {
                             float M = -INFINITY;
                             for (int q = 0; q < CS; ++q) M = fmaxf(M, gbuf[(size_t)q * rowl]);
                             float Z = 0.0f, O = 0.0f;
+#pragma unroll 1
                             for (int q = 0; q < CS; ++q) {
                                 const float* row = gbuf + (size_t)q * rowl;
                                 if (row[0] == -INFINITY) continue;
@@ -1152,7 +1153,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                                       rstd, P.packed + (qk ? lp.ln1_g : lp.ln2_g) + col0,
                                       P.packed + (qk ? lp.ln1_b : lp.ln2_b) + col0, SW, tid);
                         if (!qk || k == nh - 1) shift = ln_shift + mean;
-                        if (qk && stamps && cur_step == 0 && tid == 0) prof_comb = (uint64_t)(clock64() - t_epi);
                     }
                     csync();
                 } else {
@@ -1160,7 +1160,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     uint64_t* dst = kind == 2 ? CP.partO + (size_t)h * D + col0
                                               : CP.partP + ((size_t)(l & 1) * GG.NC + c) * D + col0;
                     const unsigned tg = out_tag(kind == 2 ? tagA : tagB);
-                    for (int e = tid; e < SW; e += NT) st_tagged(dst + e, tg, pw[e]);
+                    for (int e = tid; e < SW; e += NT) st_tagged(dst + e, tg, pa[e]);
                 }
             }
         }
@@ -1174,7 +1174,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         stamp(16 * L + 0);
         bcast(xs, gX + col0, SW, &bars[6], true);
         {
-            if (!gather_wait(&bars[6], (uint32_t)(D * 4), (uint32_t)s & 1)) { alive = false; break; }
+            if (!gather_wait(&bars[6], (uint32_t)(D * 4), (uint32_t)s & 1, true)) { alive = false; break; }
         }
         stamp(16 * L + 1);
         // LN_f over the whole vector: mean, then squares around it (the oracle's two passes)
@@ -1253,6 +1253,10 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     // this CTA's copies into its peers have landed before any CTA of the
     // cluster leaves (a run that stopped early may have some in flight)
     if (warp == 0 && lane < CS) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    // A run that stopped early may also leave values of an all-gather in
+    // flight towards a peer that will not wait for them; they land within
+    // microseconds, so the CTA lingers 20 us before the cluster leaves.
+    if (!alive) __nanosleep(20000);
     cluster_barrier();
 }
 

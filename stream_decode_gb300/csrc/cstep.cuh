@@ -103,7 +103,6 @@ __host__ __device__ inline CScratch cscratch_layout(int D, int H, int NC, int G)
 // Shared-memory layout of the cluster step kernel (byte offsets).
 struct CSmem {
     uint32_t ring, full, empty, bars, gA, gT, gB, gX, pa, qkv, oh, uu, xs, xin, xf, stage, misc, plan, total;
-    uint32_t prow;  // floats per partials buffer (pa holds three)
 };
 
 __host__ __device__ constexpr uint32_t calign16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -122,8 +121,7 @@ __host__ __device__ inline CSmem csmem_layout(int D, int DH, int CS, int SW, int
     s.gT = o; o = calign16(o + 2u * CS * (DH + 4) * 4);           // [2][CS][DH + 4]
     s.gB = o; o = calign16(o + 2u * CS * (nfc_max + 4) * 4);      // [2][CS][nfc_max + 4]
     s.gX = o; o = calign16(o + (uint32_t)D * 4);                  // all-gathered vector of the cluster
-    s.prow = (uint32_t)calign16((uint32_t)mrow * 4) / 4;
-    s.pa = o; o += 3u * s.prow * 4;                                 // this CTA's partials (+ stats): [3][prow]
+    s.pa = o; o = calign16(o + (uint32_t)mrow * 4);               // this CTA's out-projection / MLP partials
     s.qkv = o; o = calign16(o + 3u * DH * 4);
     s.oh = o; o = calign16(o + (uint32_t)DH * 4);
     s.uu = o; o = calign16(o + (uint32_t)(nfc_max + 4) * 4);
