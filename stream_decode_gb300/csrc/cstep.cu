@@ -384,6 +384,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     float* s_red = reinterpret_cast<float*>(smem + lay.misc) + 8;   // [warps] block reductions
     float* s_arg = reinterpret_cast<float*>(smem + lay.misc) + 24;  // [warps][3]
     float* s_stA = reinterpret_cast<float*>(smem + lay.misc) + 48;  // stage A slice (mean, M2)
+    CShareRow* shares = reinterpret_cast<CShareRow*>(smem + lay.shares);
 
     if (tid == 0) {
         for (int i = 0; i < NSL; ++i) {
@@ -409,6 +410,29 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         s_fail[0] = 0;
         s_fail[1] = 0;
         fence_mbar_init();
+        // this CTA's shares of a layer: for head slot k its QKV part (2k) and
+        // out-projection part (2k + 1); then FC (2 nh) and MLP (2 nh + 1)
+        for (int j = 0; j < 2 * nh + 2; ++j) {
+            uint64_t off;
+            uint32_t pb;
+            int n;
+            if (j < 2 * nh) {
+                const bool wo = (j & 1) != 0;
+                off = (uint64_t)(j >> 1) * head_bytes + (wo ? (uint64_t)3 * DH * SW * wb : 0ull);
+                pb = (uint32_t)(wo ? DH : SW) * wb;
+                n = wo ? SW : 3 * DH;
+            } else if (j == 2 * nh) {
+                off = (uint64_t)nh * head_bytes;
+                pb = (uint32_t)SW * wb;
+                n = nfc;
+            } else {
+                off = (uint64_t)nh * head_bytes + (uint64_t)nfc * SW * wb;
+                pb = (uint32_t)nfc * wb;
+                n = SW;
+            }
+            const Share sh = make_share(nullptr, pb, n);
+            shares[j] = CShareRow{(uint32_t)off, pb, n, sh.rpc, sh.nch, 0, 0, 0};
+        }
     }
     __syncthreads();
     // every CTA's barriers are initialised before any peer writes into them
@@ -417,32 +441,19 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     // The share sequence of a step, identical on both sides of the ring:
     // per layer, per head slot k: QKV part, out-projection part; then the
     // FC part and the MLP part; then the vocabulary rows.
-    auto part_base = [&](int l) -> const uint8_t* {
-        return CP.cstream + (uint64_t)l * GG.layer_bytes + GG.seg[c] + (uint64_t)r * GG.cta_bytes[c];
-    };
-    // Share j of layer l (j < 2 * nh + 2): for head slot k = j / 2 its QKV
-    // part (j even) and out-projection part (j odd); then FC (j = 2 nh) and
-    // MLP (j = 2 nh + 1).  One routine for every share keeps one copy of it
-    // in the binary.
+    // this CTA's part of layer 0 of the stream; layer l's is layer_bytes further
+    const uint8_t* part0 = CP.cstream + GG.seg[c] + (uint64_t)r * GG.cta_bytes[c];
+    // Share j of layer l, from the table the prologue built (one routine
+    // for every share keeps one copy of it in the binary).
     auto share_at = [&](int l, int j) -> Share {
-        uint64_t off;
-        uint32_t pb;
-        int n;
-        if (j < 2 * nh) {
-            const bool wo = (j & 1) != 0;
-            off = (uint64_t)(j >> 1) * head_bytes + (wo ? (uint64_t)3 * DH * SW * wb : 0ull);
-            pb = (uint32_t)(wo ? DH : SW) * wb;
-            n = wo ? SW : 3 * DH;
-        } else if (j == 2 * nh) {
-            off = (uint64_t)nh * head_bytes;
-            pb = (uint32_t)SW * wb;
-            n = nfc;
-        } else {
-            off = (uint64_t)nh * head_bytes + (uint64_t)nfc * SW * wb;
-            pb = (uint32_t)nfc * wb;
-            n = SW;
-        }
-        return make_share(part_base(l) + off, pb, n);
+        const CShareRow t = shares[j];
+        Share sh;
+        sh.base = part0 + (uint64_t)l * GG.layer_bytes + t.off;
+        sh.pb = t.pb;
+        sh.n = t.n;
+        sh.rpc = t.rpc;
+        sh.nch = t.nch;
+        return sh;
     };
     const int V = P.V;
     const int v0 = (int)(((long long)cta * V) / GG.G), v1 = (int)(((long long)(cta + 1) * V) / GG.G);
@@ -1424,6 +1435,7 @@ cudaError_t cgeo_make(int L, int D, int H, int FF, int wf, int want_ctas, CGeo* 
     g.NC = NC;
     g.G = NC * CS;
     g.HPC = (H + NC - 1) / NC;
+    if (g.HPC > kCMaxHeadSlots) return cudaErrorInvalidValue;
     // FC rows: head clusters carry 4 * DH * SW weights of attention per head
     // and CTA; an FC row costs 2 * SW weights per CTA (FC and MLP parts), so
     // equal bytes per CTA means nfc_c = base - 2 * DH * heads(c).  frac

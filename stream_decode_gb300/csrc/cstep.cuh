@@ -102,7 +102,15 @@ __host__ __device__ inline CScratch cscratch_layout(int D, int H, int NC, int G)
 
 // Shared-memory layout of the cluster step kernel (byte offsets).
 struct CSmem {
-    uint32_t ring, full, empty, bars, gA, gT, gB, gX, pa, qkv, oh, uu, xs, xin, xf, stage, misc, plan, total;
+    uint32_t ring, full, empty, bars, gA, gT, gB, gX, pa, qkv, oh, uu, xs, xin, xf, stage, misc, shares, plan, total;
+};
+
+// Head slots per cluster at most (a layer has 2 * heads + 2 shares per CTA).
+constexpr int kCMaxHeadSlots = 8;
+// A CTA's share j of every layer, relative to its part of the layer.
+struct CShareRow {
+    uint32_t off, pb;
+    int n, rpc, nch, pad0, pad1, pad2;
 };
 
 __host__ __device__ constexpr uint32_t calign16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -130,6 +138,7 @@ __host__ __device__ inline CSmem csmem_layout(int D, int DH, int CS, int SW, int
     s.xf = o; o = calign16(o + (uint32_t)D * 4);
     s.stage = o; o = calign16(o + 768u * 4);
     s.misc = o; o = calign16(o + 64u * 4);
+    s.shares = o; o = calign16(o + (uint32_t)(2 * kCMaxHeadSlots + 2) * (uint32_t)sizeof(CShareRow));
     s.plan = o; o = calign16(o + (uint32_t)sizeof(CPlan));
     s.total = o;
     return s;
