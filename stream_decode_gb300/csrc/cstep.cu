@@ -917,7 +917,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, stage[(w * LPK + cq) * (2 + DPL)]);
             float Z = 0.0f, O = 0.0f;
             if (M != -INFINITY) {
-#pragma unroll 1
+#pragma unroll
                 for (int w = 0; w < kCWarps; ++w) {
                     const float* st = stage + (w * LPK + cq) * (2 + DPL);
                     if (st[0] == -INFINITY) continue;
@@ -1111,7 +1111,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                             float M = -INFINITY;
                             for (int q = 0; q < CS; ++q) M = fmaxf(M, gbuf[(size_t)q * rowl]);
                             float Z = 0.0f, O = 0.0f;
-#pragma unroll 1
+#pragma unroll
                             for (int q = 0; q < CS; ++q) {
                                 const float* row = gbuf + (size_t)q * rowl;
                                 if (row[0] == -INFINITY) continue;
