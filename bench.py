@@ -142,20 +142,22 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def oracle_decode_rate(shape, w, toks, quant: int, n_decode: int):
+def oracle_decode_rate(shape, w, toks, quant: int, n_decode: int, passes: int = 1):
     """Times the oracle (single-threaded C) on the decode workload: the prompt
-    cache is built untimed, then n_decode teacher-forced steps are timed."""
+    cache is built untimed, then `passes` runs of n_decode greedy steps from
+    it are timed."""
     from oracle import Oracle
     om = Oracle().model(shape, w, quant=quant)
-    _, ch, cache = om.session(list(toks), PROMPT)
-    tok = int(ch[-1])
+    _, ch, cache0 = om.session(list(toks), PROMPT)
     t0 = time.perf_counter()
-    for i in range(n_decode):
-        st, lg, cache = om.cached_step(cache, tok, PROMPT + i)
-        tok = int(np.argmax(lg))
+    for _ in range(passes):
+        cache, tok = cache0, int(ch[-1])
+        for i in range(n_decode):
+            st, lg, cache = om.cached_step(cache, tok, PROMPT + i)
+            tok = int(np.argmax(lg))
     dt = time.perf_counter() - t0
     om.close()
-    return n_decode / dt, dt
+    return passes * n_decode / dt, dt
 
 
 def reference_arm(args, shape, w, toks):
@@ -216,9 +218,14 @@ def traffic_from_profiles(kernel_src_hash: str, quant: str):
     return None
 
 
-def kernel_hash():
+# Sources of each step kernel (the traffic record is keyed by their hash).
+KERNEL_SOURCES = {"cluster": ("cstep.cu", "cstep.cuh", "gpt2_dev.cuh"), "phase": ("decode.cu", "gpt2_dev.cuh")}
+KERNEL_NAMES = {"cluster": "cstep_kernel", "phase": "step_kernel"}
+
+
+def kernel_hash(kind: str = "phase"):
     h = hashlib.sha256()
-    for name in ("decode.cu", "gpt2_dev.cuh"):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "stream_decode_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -356,13 +363,18 @@ def long_context(g, torch, w, reps=20):
     d = torch.tensor(toks.astype(np.int32), device="cuda")
     assert sess.run(d, 1023, None, 0, None) == "ok"
     assert sess.sync() == "ok"
+    row = g.cache_words_per_position(s)
+    cache = sess.read_cache()  # positions 0..1022, for the oracle's step below
+    assert cache.size == 1023 * row
     out = {}
     stream = torch.cuda.current_stream()
-    for p in (128, 512, 1023):
+    # a session rewinds only backwards: the positions are timed in descending
+    # order (a step at p rewrites row p with the same token's key and value)
+    for p in (1023, 512, 128):
         tin = d[p:p + 1]
         for _ in range(3):
-            sess.rewind(p)
-            sess.run(tin, 1, None, 0, None, stream)
+            assert sess.rewind(p) == "ok"
+            assert sess.run(tin, 1, None, 0, None, stream) == "ok"
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -377,8 +389,6 @@ def long_context(g, torch, w, reps=20):
         out[f"p{p}"] = {"us_per_step": us, "GB_per_s": by / us * 1e-3, "bytes": by}
     # the oracle's step at position 1023 on the cache the GPU built
     # (single-threaded C on one host core): the long-context CPU baseline
-    row = g.cache_words_per_position(s)
-    cache = sess.read_cache()[:1023 * row]
     sess.close()
     model.close()
     from oracle import Oracle
@@ -499,8 +509,10 @@ def main():
     peak, peak_kind = _peaks()
     launch_bytes = sum(step_bytes(shape, args.quant, p) for p in range(PROMPT, PROMPT + DECODE))
     achieved = launch_bytes / (ms * 1e-3) / 1e9
-    # the committed record is of one 112-step launch (positions 16..127)
-    traffic = traffic_from_profiles(kernel_hash(), args.quant) if DECODE == 112 else None
+    # which step kernel the model runs, and the committed traffic record of
+    # one 112-step launch (positions 16..127) if it was taken on that source
+    kkind = model.step_kernel[0]
+    traffic = traffic_from_profiles(kernel_hash(kkind), args.quant) if DECODE == 112 else None
 
     e2e_rate, _ = measure_e2e(g, sess, shape, first, 5)
     e2e_tok_rate, _ = measure_e2e_per_token(g, sess, shape, first, 2)
@@ -548,18 +560,18 @@ def main():
     cpu = None
     if rank == 0 and not args.no_extra and args.quant == "f32":
         # the int8 workload's CPU baseline: the oracle's int8 model, same sample
-        r8, dt8 = oracle_decode_rate(shape, w, toks, 1, 16)
+        r8, dt8 = oracle_decode_rate(shape, w, toks, 1, DECODE, 2)
         extra["cpu_baseline_int8"] = {"value": r8, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                      "sample": f"16 int8 greedy decode steps at positions 16..31 after an untimed "
-                                                f"16-token prompt ({dt8:.1f} s)"}
+                                      "sample": f"two runs of the workload's {DECODE} int8 greedy decode steps "
+                                                f"(positions 16..127) after an untimed 16-token prompt ({dt8:.1f} s)"}
     if rank == 0:
-        n_dec = 16
         rate, dt = oracle_decode_rate(shape, w, toks, {"f32": 0, "int8": 1, "f16": 2, "int8_row": 3,
                                                        "int8_row_act": 4}[args.quant],
-                                      n_dec)
+                                      DECODE, 2)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n_dec} greedy decode steps at positions 16..31 after an untimed 16-token prompt "
-                         f"({dt:.1f} s of single-threaded C on {cpu_cores()} available host cores)"}
+               "sample": f"two runs of the workload's {DECODE} greedy decode steps (positions 16..127) after an "
+                         f"untimed 16-token prompt ({dt:.1f} s of single-threaded C on {cpu_cores()} available "
+                         f"host cores)"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -567,7 +579,7 @@ def main():
                 "vs_baseline": None, "dtype": args.quant, "data": "synthetic (seeded N(0,0.02) weights, "
                 "uniform random prompt tokens)", "config": workload_config(args),
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                             "frac": achieved / peak, "traffic": traffic,
+                             "frac": achieved / peak, "traffic": traffic, "kernel": KERNEL_NAMES[kkind],
                              "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                              "algorithmic_bytes_per_launch": launch_bytes},
                 "cpu_baseline": cpu,

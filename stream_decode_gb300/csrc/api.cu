@@ -68,7 +68,7 @@ namespace {
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 // Whether binary32 and binary16 models step on the cluster kernel unless
 // GPT2_STEP_KERNEL says otherwise.
-constexpr bool kClusterStepDefault = false;
+constexpr bool kClusterStepDefault = true;
 
 size_t words_of(const gpt2_config* c) {
     size_t d = c->d_model, f = c->d_ff;

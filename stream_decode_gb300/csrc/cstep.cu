@@ -369,7 +369,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     float* gT = reinterpret_cast<float*>(smem + lay.gT);
     float* gB = reinterpret_cast<float*>(smem + lay.gB);
     float* gX = reinterpret_cast<float*>(smem + lay.gX);
-    float* pa = reinterpret_cast<float*>(smem + lay.pa);
     float* qkv = reinterpret_cast<float*>(smem + lay.qkv);
     float* oh = reinterpret_cast<float*>(smem + lay.oh);
     float* uu = reinterpret_cast<float*>(smem + lay.uu);
@@ -646,8 +645,10 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     // consumed in an earlier round.
     // With row_s != 0 each row's result is sent to offset 4 * row of row_s
     // (a gather row, local address) in every CTA of the cluster, completing
-    // on bar_s; otherwise it is stored to out.
-    auto run_share = [&](const Share& sh, const float* x, int W4, float* out, uint32_t row_s, uint32_t bar_s) -> bool {
+    // on bar_s; otherwise it is published as the tagged word gdst[row].
+    // Either way it leaves the lane that computed it.
+    auto run_share = [&](const Share& sh, const float* x, int W4, uint32_t row_s, uint32_t bar_s, uint64_t* gdst,
+                         unsigned gtag) -> bool {
         bool ok = true;
         const uint32_t x_s = smem_addr(x);
         for (int k0 = 0; k0 < sh.nch; k0 += kCWarps) {
@@ -662,7 +663,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     if (lane < n) {
                         const int i = k * sh.rpc + lane;
                         if (row_s) send_all(row_s + 4u * (uint32_t)i, v, bar_s);
-                        else out[i] = v;
+                        else st_tagged(gdst + i, gtag, v);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[cc % (uint32_t)NSL]);
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     auto merge_stats = [&](const float* base, int stride, float& mean, float& rstd) {
         float mu = 0.0f;
         for (int k = 0; k < CS; ++k) mu += base[k * stride];
-        mu = mu / (float)CS;
+        mu = mu * (1.0f / (float)CS);
         float m2 = 0.0f, sd = 0.0f;
         for (int k = 0; k < CS; ++k) {
             const float dl = base[k * stride] - mu;
@@ -765,7 +766,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         }
         m2 = fmaf((float)SW, sd, m2);
         mean = mu;
-        rstd = rsqrtf(m2 / (float)D + kLnEps);
+        rstd = rsqrtf(fmaf(m2, 1.0f / (float)D, kLnEps));
     };
 
     // Greedy partials of the previous step (tag), reduced in every CTA; the
@@ -887,7 +888,7 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             }
         }
         // merge the key slots of the warp (lanes with the same dc)
-#pragma unroll 1
+#pragma unroll
         for (int o = LPK; o < 32; o <<= 1) {
             const float om = __shfl_xor_sync(0xffffffffu, m, o);
             const float oz = __shfl_xor_sync(0xffffffffu, z, o);
@@ -1083,8 +1084,11 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                         send_all(row_s + 4u * n0, s_st[0], bar_s);
                         send_all(row_s + 4u * (n0 + 1u), s_st[1], bar_s);
                     }
-                    ok_share = run_share(sh, xv, W4, pa, row_s, bar_s);
-                    // the out-projection and MLP partials are stored from pa by other threads
+                    // out-projection (2) or MLP (4) partials of this CTA's output
+                    // rows, published as tagged words
+                    uint64_t* gdst = kind == 2 ? CP.partO + (size_t)h * D + col0
+                                   : kind == 4 ? CP.partP + ((size_t)(l & 1) * GG.NC + c) * D + col0 : nullptr;
+                    ok_share = run_share(sh, xv, W4, row_s, bar_s, gdst, out_tag(kind == 2 ? tagA : tagB));
                     if (!gat && !agree(ok_share)) { alive = false; break; }
                     stamp(16 * l + (kind == 0 ? 1 : kind == 2 ? 5 : kind == 3 ? 7 : 9));
                 } else {
@@ -1166,12 +1170,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                         if (!qk || k == nh - 1) shift = ln_shift + mean;
                     }
                     csync();
-                } else {
-                    // ---- out-projection (2) or MLP (4) partials of this CTA's output rows
-                    uint64_t* dst = kind == 2 ? CP.partO + (size_t)h * D + col0
-                                              : CP.partP + ((size_t)(l & 1) * GG.NC + c) * D + col0;
-                    const unsigned tg = out_tag(kind == 2 ? tagA : tagB);
-                    for (int e = tid; e < SW; e += NT) st_tagged(dst + e, tg, pa[e]);
                 }
             }
         }

@@ -102,7 +102,7 @@ __host__ __device__ inline CScratch cscratch_layout(int D, int H, int NC, int G)
 
 // Shared-memory layout of the cluster step kernel (byte offsets).
 struct CSmem {
-    uint32_t ring, full, empty, bars, gA, gT, gB, gX, pa, qkv, oh, uu, xs, xin, xf, stage, misc, shares, plan, total;
+    uint32_t ring, full, empty, bars, gA, gT, gB, gX, qkv, oh, uu, xs, xin, xf, stage, misc, shares, plan, total;
 };
 
 // Head slots per cluster at most (a layer has 2 * heads + 2 shares per CTA).
@@ -117,9 +117,6 @@ __host__ __device__ constexpr uint32_t calign16(uint32_t x) { return (x + 15u) &
 
 __host__ __device__ inline CSmem csmem_layout(int D, int DH, int CS, int SW, int nfc_max, int slots) {
     CSmem s{};
-    int mrow = 3 * DH > nfc_max ? 3 * DH : nfc_max;
-    if (SW > mrow) mrow = SW;
-    mrow += 4;
     uint32_t o = 0;
     s.ring = o; o += (uint32_t)slots * kCSlotBytes;
     s.full = o; o += (uint32_t)slots * 8;
@@ -129,7 +126,6 @@ __host__ __device__ inline CSmem csmem_layout(int D, int DH, int CS, int SW, int
     s.gT = o; o = calign16(o + 2u * CS * (DH + 4) * 4);           // [2][CS][DH + 4]
     s.gB = o; o = calign16(o + 2u * CS * (nfc_max + 4) * 4);      // [2][CS][nfc_max + 4]
     s.gX = o; o = calign16(o + (uint32_t)D * 4);                  // all-gathered vector of the cluster
-    s.pa = o; o = calign16(o + (uint32_t)mrow * 4);               // this CTA's out-projection / MLP partials
     s.qkv = o; o = calign16(o + 3u * DH * 4);
     s.oh = o; o = calign16(o + (uint32_t)DH * 4);
     s.uu = o; o = calign16(o + (uint32_t)(nfc_max + 4) * 4);
