@@ -472,7 +472,8 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     if (warp == kCWarps) {
         if (lane == 0 && !*s_abort) {
             const uint64_t pol = policy_evict_first();
-            uint32_t gi = 0;
+            uint32_t gi = 0;                // chunks issued
+            uint32_t pslot = 0, pfill = 0;  // slot of the next chunk, and how often the ring has wrapped
             bool stop = false;
             // Pacing: the block-matrix chunks are issued at least pace_ns per
             // 12 KB apart (scaled by the chunk's bytes).  Without it, the
@@ -482,8 +483,8 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             uint64_t next_issue = 0;
             auto issue = [&](const Share& sh, bool paced) {
                 for (int k = 0; k < sh.nch && !stop; ++k) {
-                    const int slot = (int)(gi % (uint32_t)NSL);
-                    const uint32_t fill = gi / (uint32_t)NSL;
+                    const int slot = (int)pslot;
+                    const uint32_t fill = pfill;
                     if (fill > 0) {
                         uint64_t t0 = 0;
                         uint32_t spins = 0;
@@ -516,6 +517,10 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                     mbar_arrive_expect_tx(&full[slot], bytes);
                     bulk_load(ring + (size_t)slot * kCSlotBytes, sh.base + (uint64_t)r0 * sh.pb, bytes, &full[slot], pol);
                     ++gi;
+                    if (++pslot == (uint32_t)NSL) {
+                        pslot = 0;
+                        ++pfill;
+                    }
                 }
             };
             // per step: the layers' shares in order, then the vocabulary rows
@@ -548,7 +553,6 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     }
 
     // ================================================= consumer warps
-    uint32_t gi = 0;  // chunks consumed
     // Profiling (step 0) and the location of a wait that gave up.
     uint64_t* stamps = P.timing ? P.timing + 8 + (size_t)cta * cstamps_per_cta(L) : nullptr;
     int cur_step = 0, cur_layer = 0;
@@ -576,18 +580,28 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                              stamps ? stamps + 16 * L + 4 : nullptr);
     };
     // Warp-uniform bounded wait for ring chunk cc.
-    auto wait_chunk = [&](uint32_t cc) -> bool {
-        const int slot = (int)(cc % (uint32_t)NSL);
-        const uint32_t par = (cc / (uint32_t)NSL) & 1;
+    auto wait_chunk = [&](uint32_t slot, uint32_t par) -> bool {
         uint64_t t0 = 0;
         uint32_t spins = 0;
         while (!__all_sync(0xffffffffu, mbar_try_wait(&full[slot], par))) {
             if ((++spins & 63) == 0) {
-                int give_up = lane == 0 ? (int)timed_out(t0, 1, cc) : 0;
+                int give_up = lane == 0 ? (int)timed_out(t0, 1, slot | (par << 8)) : 0;
                 if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
             }
         }
         return true;
+    };
+    // The consumers' ring cursor: the slot of the next chunk to consume and
+    // the parity of its fill (no division on the way).  Chunk k < slots
+    // ahead of the cursor is in slot_of(k) with parity par_of(k).
+    uint32_t rslot = 0, rpar = 0;
+    auto ring_advance = [&](int n) {
+        uint32_t t = rslot + (uint32_t)n;
+        while (t >= (uint32_t)NSL) {
+            t -= (uint32_t)NSL;
+            rpar ^= 1u;
+        }
+        rslot = t;
     };
     // Bounded wait for one phase of a local mbarrier that peers complete.
     auto wait_bar = [&](uint64_t* bar, uint32_t par) -> bool {
@@ -653,11 +667,16 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
         const uint32_t x_s = smem_addr(x);
         for (int k0 = 0; k0 < sh.nch; k0 += kCWarps) {
             const int k = k0 + warp;
+            // this warp's chunk of the round: warp < kCWarps <= slots ahead of the cursor
+            uint32_t slot = rslot + (uint32_t)warp, par = rpar;
+            if (slot >= (uint32_t)NSL) {
+                slot -= (uint32_t)NSL;
+                par ^= 1u;
+            }
             if (ok && k < sh.nch) {
-                const uint32_t cc = gi + (uint32_t)k;
-                ok = wait_chunk(cc);
+                ok = wait_chunk(slot, par);
                 if (ok) {
-                    const uint32_t w = ring_s + (cc % (uint32_t)NSL) * (uint32_t)kCSlotBytes;
+                    const uint32_t w = ring_s + slot * (uint32_t)kCSlotBytes;
                     const int n = min(sh.rpc, sh.n - k * sh.rpc);
                     const float v = chunk_rows<WF>(w, n, W4, x_s, lane);
                     if (lane < n) {
@@ -666,12 +685,12 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                         else st_tagged(gdst + i, gtag, v);
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[cc % (uint32_t)NSL]);
+                    if (lane == 0) mbar_arrive(&empty[slot]);
                 }
             }
+            ring_advance(min(kCWarps, sh.nch - k0));
             if (k0 + kCWarps < sh.nch) csync();
         }
-        gi += (uint32_t)sh.nch;
         return ok;
     };
     // Deterministic block sum over the consumer threads (same value in all).
@@ -1218,11 +1237,15 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
             // rounds of one chunk per warp, as in run_share
             for (int k0 = 0; k0 < sh.nch; k0 += kCWarps) {
                 const int kc = k0 + warp;
+                uint32_t slot = rslot + (uint32_t)warp, par = rpar;
+                if (slot >= (uint32_t)NSL) {
+                    slot -= (uint32_t)NSL;
+                    par ^= 1u;
+                }
                 if (ok && kc < sh.nch) {
-                    const uint32_t cc = gi + (uint32_t)kc;
-                    ok = wait_chunk(cc);
+                    ok = wait_chunk(slot, par);
                     if (ok) {
-                        const uint32_t w = ring_s + (cc % (uint32_t)NSL) * (uint32_t)kCSlotBytes;
+                        const uint32_t w = ring_s + slot * (uint32_t)kCSlotBytes;
                         const int n = min(sh.rpc, sh.n - kc * sh.rpc);
                         const float v = long_rows<kVocabRows, D / 4, WF>(w, sh.pb, n, xf_s, lane);
                         if (lane < n) {
@@ -1231,12 +1254,12 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
                             best_update(best, v, (unsigned)j);
                         }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[cc % (uint32_t)NSL]);
+                        if (lane == 0) mbar_arrive(&empty[slot]);
                     }
                 }
+                ring_advance(min(kCWarps, sh.nch - k0));
                 if (k0 + kCWarps < sh.nch) csync();
             }
-            gi += (uint32_t)sh.nch;
             best_warp(best);
             if (lane == 0) {
                 s_arg[warp * 3 + 0] = best.v;
