@@ -200,14 +200,15 @@ __device__ __forceinline__ float chunk_rows(uint32_t w, int R, int W4, uint32_t 
 
 // NR consecutive K-major rows (pitch pb bytes, W4 float4 columns each) in
 // shared memory against x (W4 float4s): lanes stride the columns, then one
-// transpose-reduction; lane i < n returns row i's total.  For the long
-// vocabulary rows.
+// transpose-reduction (over NR rounded up to a power of two, the extra rows
+// zero); lane i < n returns row i's total.  For the long vocabulary rows.
 template <int NR, int W4, int WF>
 __device__ __forceinline__ float long_rows(uint32_t w, uint32_t pb, int n, uint32_t x, int lane) {
     constexpr uint32_t UB = unit_bytes<WF>();
-    float acc[NR];
+    constexpr int NP = NR <= 1 ? 1 : NR <= 2 ? 2 : NR <= 4 ? 4 : NR <= 8 ? 8 : NR <= 16 ? 16 : 32;
+    float acc[NP];
 #pragma unroll
-    for (int i = 0; i < NR; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < NP; ++i) acc[i] = 0.0f;
 #pragma unroll
     for (int t = 0; t < (W4 + 31) / 32; ++t) {
         const int cc = lane + 32 * t;
@@ -218,7 +219,7 @@ __device__ __forceinline__ float long_rows(uint32_t w, uint32_t pb, int n, uint3
                 if (i < n) acc[i] = dot4(acc[i], ldsw<WF>(w + (uint32_t)i * pb + UB * (uint32_t)cc), xv);
         }
     }
-    return transpose_sum<NR>(acc, lane);
+    return transpose_sum<NP>(acc, lane);
 }
 
 __device__ __forceinline__ void crecord_error(const StepPlan& P, int code) {
@@ -458,9 +459,9 @@ __global__ void __launch_bounds__(kCThreads, 1) cstep_kernel(const __grid_consta
     const int v0 = (int)(((long long)cta * V) / GG.G), v1 = (int)(((long long)(cta + 1) * V) / GG.G);
     const uint32_t rbv = (uint32_t)row_bytes(D, WF);
     // vocabulary rows per chunk: a power of two (its transpose-reduction), at most 32
+    // vocabulary rows per chunk: as many as a slot holds, at most 32
     constexpr int kVocabFit = kCSlotBytes / row_bytes(D, WF);
-    constexpr int kVocabRows = kVocabFit >= 32 ? 32 : kVocabFit >= 16 ? 16 : kVocabFit >= 8 ? 8 : kVocabFit >= 4 ? 4
-                                                                                              : kVocabFit >= 2 ? 2 : 1;
+    constexpr int kVocabRows = kVocabFit >= 32 ? 32 : kVocabFit;
     auto share_vocab = [&]() {
         Share sh = make_share(P.vocab + (uint64_t)v0 * rbv, rbv, v1 - v0);
         sh.rpc = kVocabRows < sh.n ? kVocabRows : (sh.n > 0 ? sh.n : 1);
