@@ -182,16 +182,14 @@ __device__ __forceinline__ float chunk_rows(uint32_t w, int R, int W4, uint32_t 
         uint32_t wa = w + (uint32_t)lane * UB, xa = x;
         int c = 0;
         for (; c + 8 <= W4; c += 8, wa += 8 * step, xa += 128) {
+            // all sixteen loads of eight units in flight before the first multiply-add
+            float4 wv[8], xv[8];
 #pragma unroll
-            for (int h2 = 0; h2 < 8; h2 += 4) {
-                float4 wv[4], xv[4];
+            for (int u = 0; u < 8; ++u) wv[u] = ldsw<WF>(wa + u * step);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) wv[u] = ldsw<WF>(wa + (h2 + u) * step);
+            for (int u = 0; u < 8; ++u) xv[u] = lds4(xa + 16u * u);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) xv[u] = lds4(xa + 16u * (h2 + u));
-#pragma unroll
-                for (int u = 0; u < 4; ++u) a[h2 + u] = dot4(a[h2 + u], wv[u], xv[u]);
-            }
+            for (int u = 0; u < 8; ++u) a[u] = dot4(a[u], wv[u], xv[u]);
         }
         for (; c < W4; ++c, wa += step, xa += 16) a[0] = dot4(a[0], ldsw<WF>(wa), lds4(xa));
     }
