@@ -338,8 +338,14 @@ gpt2_status gpt2_model_create(const gpt2_config* cfg, const void* weights, size_
         // per-phase kernel; unset, kClusterStepDefault decides
         const char* sk = getenv("GPT2_STEP_KERNEL");
         const bool want_cluster = sk ? strcmp(sk, "cluster") == 0 : kClusterStepDefault;
-        if (want_cluster && cstep_supported(D, FF, D / (int)cfg->n_head, wfmt)) {
-            CK(cgeo_make(L, D, (int)cfg->n_head, FF, wfmt, grid_ctas, &m->cg));
+        // (a geometry the GPU cannot hold, e.g. too few co-resident
+        // clusters, leaves the model on the per-phase kernel)
+        bool use_cluster = want_cluster && cstep_supported(D, FF, D / (int)cfg->n_head, wfmt);
+        if (use_cluster && cgeo_make(L, D, (int)cfg->n_head, FF, wfmt, grid_ctas, &m->cg) != cudaSuccess) {
+            use_cluster = false;
+            (void)cudaGetLastError();  // an occupancy query that failed leaves no error behind
+        }
+        if (use_cluster) {
             CK(cudaMalloc(&m->d_cstream, m->cg.layer_bytes * L));
             CK(cstream_build(m->d_wstream, m->layer_bytes, m->mat_off, L, D, (int)cfg->n_head, FF, wfmt, m->cg,
                              m->d_cstream, 0));
