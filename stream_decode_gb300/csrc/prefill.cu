@@ -352,8 +352,10 @@ bool tc_ready() {
         cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
         if (g_sms <= 0) g_sms = 1;
     }
-    return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)tc::kTcSmem) == cudaSuccess;
+    return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)tc::tc_smem(64)) == cudaSuccess &&
+           cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)tc::tc_smem(128)) == cudaSuccess;
 }
 
 int tc_sm_count() { return g_sms; }
@@ -361,17 +363,25 @@ int tc_sm_count() { return g_sms; }
 cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W, const float* Wlo, int w_rows, int K,
                     int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st) {
     if (K % tc::kBlockK || N % tc::kTileN || w_rows > N || m_rows <= 0) return cudaErrorInvalidValue;
+    // 128 output features per tile for up to 64 rows where N allows (half
+    // the activation reads of the 64-wide tile; measured faster for 16 and
+    // 64 sessions, slower for the 128-row prefill), else 64
+    const int TN = (N % 128 == 0 && m_rows <= tc::kTileM / 2) ? 128 : 64;
     tc::TcMaps maps;
     const int a_rows = m_rows <= tc::kTileM / 2 ? tc::kTileM / 2 : tc::kTileM;  // A rows loaded per tile
     if (!kmajor_map(&maps.a_hi, A, K, m_rows, a_rows) || !kmajor_map(&maps.a_lo, Alo, K, m_rows, a_rows) ||
-        !kmajor_map(&maps.b_hi, W, K, w_rows, tc::kTileN) || !kmajor_map(&maps.b_lo, Wlo, K, w_rows, tc::kTileN))
+        !kmajor_map(&maps.b_hi, W, K, w_rows, TN) || !kmajor_map(&maps.b_lo, Wlo, K, w_rows, TN))
         return cudaErrorInvalidValue;
-    const int m_tiles = (m_rows + tc::kTileM - 1) / tc::kTileM, n_tiles = N / tc::kTileN;
+    const int m_tiles = (m_rows + tc::kTileM - 1) / tc::kTileM, n_tiles = N / TN;
     int splits = choose_splits(m_tiles, n_tiles, K);
     if (splits > max_splits) splits = max_splits < 1 ? 1 : max_splits;
     *splits_out = splits;
-    tc::tf32x3_gemm_kernel<<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::kTcSmem, st>>>(
-        maps, K, N, m_rows, splits, part, status, (int)kDevTimeout, a_rows);
+    if (TN == 128)
+        tc::tf32x3_gemm_kernel<128><<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::tc_smem(128), st>>>(
+            maps, K, N, m_rows, splits, part, status, (int)kDevTimeout, a_rows);
+    else
+        tc::tf32x3_gemm_kernel<64><<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::tc_smem(64), st>>>(
+            maps, K, N, m_rows, splits, part, status, (int)kDevTimeout, a_rows);
     return cudaGetLastError();
 }
 

@@ -1,9 +1,11 @@
 // tc_gemm.cuh -- the prefill projections on the 5th-generation tensor cores.
 //
 // C_part[split][m][n] = sum over this split's K range of A[m][k] * B[n][k]
-// for one 128 x 64 output tile per CTA (rows m of the prompt, output
-// features n), with both operands K-major in global memory (activations
-// [n_tok][K]; weights [N][K], the device layout of every block matrix).
+// for one 128 x TN output tile per CTA (rows m of the prompt, TN = 64 or
+// 128 output features n), with both operands K-major in global memory
+// (activations [n_tok][K]; weights [N][K], the device layout of every block
+// matrix).  The wider tile reads each activation tile for twice as many
+// output features (half the activation traffic from L2) at one stage less.
 //
 // binary32 accuracy from TF32 tensor cores ("3xTF32"): each operand x is
 // split as x = hi + lo with hi = x with its low 13 mantissa bits cleared
@@ -14,8 +16,8 @@
 //
 // Pipeline per CTA (128 threads): warp 0 lane 0 issues TMA tile loads (128 B
 // swizzle) of A_hi, A_lo, B_hi, B_lo for each 32-wide K block into a ring of
-// kTcStages stages (mbarriers full/empty); warp 1 lane 0 issues
-// tcgen05.mma (M=128, N=64, K=8, kind::tf32, accumulator in TMEM) and
+// tc_stages(TN) stages (mbarriers full/empty); warp 1 lane 0 issues
+// tcgen05.mma (M=128, N=TN, K=8, kind::tf32, accumulator in TMEM) and
 // commits each stage back to its producer; after the last block all four
 // warps read the accumulator rows (tcgen05.ld 32x32b) and store the fp32
 // partial tile.  Every wait is bounded; on expiry the CTA records an error,
@@ -30,17 +32,20 @@ namespace gpt2 {
 namespace tc {
 
 constexpr int kTileM = 128;            // prompt rows per tile (the MMA's M)
-constexpr int kTileN = 64;             // output features per tile (the MMA's N)
+constexpr int kTileN = 64;             // the narrow tile's output features (the MMA's N); a shape multiple
 constexpr int kBlockK = 32;            // K per stage: one 128-byte swizzle row of fp32
 constexpr int kMmaK = 8;               // K per tcgen05.mma of kind::tf32
-constexpr int kTcStages = 4;
 constexpr int kTcThreads = 128;
 constexpr uint32_t kABytes = kTileM * kBlockK * 4;  // 16 KB per A tile (hi or lo)
-constexpr uint32_t kBBytes = kTileN * kBlockK * 4;  // 8 KB per B tile (hi or lo)
-constexpr uint32_t kStageBytes = 2 * kABytes + 2 * kBBytes;
-constexpr uint32_t kTmemCols = 64;     // fp32 accumulator columns (= kTileN)
-constexpr uint32_t kTcSmem = kTcStages * kStageBytes + 1024 /* alignment slack */ + 256 /* barriers */;
-static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "tiles stay 1024-byte aligned for the swizzle atoms");
+// per tile width TN (64 or 128): B tile bytes, stage bytes, stages, dynamic shared memory
+__host__ __device__ constexpr uint32_t tc_bbytes(int TN) { return (uint32_t)TN * kBlockK * 4; }
+__host__ __device__ constexpr uint32_t tc_stage_bytes(int TN) { return 2 * kABytes + 2 * tc_bbytes(TN); }
+__host__ __device__ constexpr int tc_stages(int TN) { return TN <= 64 ? 4 : 3; }
+__host__ __device__ constexpr uint32_t tc_smem(int TN) {
+    return (uint32_t)tc_stages(TN) * tc_stage_bytes(TN) + 1024 /* alignment slack */ + 256 /* barriers */;
+}
+static_assert(kABytes % 1024 == 0 && tc_bbytes(64) % 1024 == 0, "tiles stay 1024-byte aligned for the swizzle atoms");
+static_assert(tc_smem(128) <= 232448, "the wide tile's stages fit in shared memory");
 
 struct TcMaps {
     CUtensorMap a_hi, a_lo, b_hi, b_lo;  // A: dims {K, rows}; B: dims {K, N}; boxes {32, 128} / {32, 64}
@@ -63,9 +68,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor: fp32 accumulator, TF32 A and B, both K-major,
-// N = kTileN, M = kTileM.
-__host__ __device__ constexpr uint32_t instr_desc() {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+// N = TN, M = kTileM.
+__host__ __device__ constexpr uint32_t instr_desc(int TN) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_mbar_init(uint64_t* b, uint32_t n) {
@@ -116,9 +121,13 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // depends only on A row r, so the unloaded upper half of the A tiles only
 // feeds accumulator rows that are never stored.  err: set to
 // err_code (if still 0) when any wait expires.
+template <int TN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ TcMaps maps, int K, int N, int m_rows, int splits, float* part,
                        int* err, int err_code, int a_rows) {
+    constexpr int kTcStages = tc_stages(TN);
+    constexpr uint32_t kBBytes = tc_bbytes(TN), kStageBytes = tc_stage_bytes(TN);
+    constexpr uint32_t kTmemCols = (uint32_t)TN;  // fp32 accumulator columns
     extern __shared__ uint8_t tc_smem_raw[];
     // 1024-byte aligned stage area (swizzle atoms), barriers after it
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -129,7 +138,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile int* s_bad = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileN;
+    const int n0 = blockIdx.x * TN;
     const int split = blockIdx.y;
     const int m0 = blockIdx.z * kTileM;
     const int nkb = K / kBlockK;
@@ -180,7 +189,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
-        const uint32_t idesc = instr_desc();
+        const uint32_t idesc = instr_desc(TN);
         bool any = false;
         for (int kb = kb0; kb < kb1; ++kb) {
             const int i = kb - kb0, s = i % kTcStages;
@@ -211,7 +220,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = m0 + warp * 32 + lane;
     float* dst = part + ((size_t)split * m_rows + row) * N + n0;
 #pragma unroll
-    for (int c0 = 0; c0 < kTileN; c0 += 16) {
+    for (int c0 = 0; c0 < TN; c0 += 16) {
         uint32_t v[16];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
