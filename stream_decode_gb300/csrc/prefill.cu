@@ -354,7 +354,7 @@ bool tc_ready() {
     }
     return cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)tc::tc_smem(64)) == cudaSuccess &&
-           cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+           cudaFuncSetAttribute(tc::tf32x3_gemm_kernel<128, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)tc::tc_smem(128)) == cudaSuccess;
 }
 
@@ -376,8 +376,8 @@ cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W
     int splits = choose_splits(m_tiles, n_tiles, K);
     if (splits > max_splits) splits = max_splits < 1 ? 1 : max_splits;
     *splits_out = splits;
-    if (TN == 128)
-        tc::tf32x3_gemm_kernel<128><<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::tc_smem(128), st>>>(
+    if (TN == 128)  // (only for up to 64 rows: 64-row A tiles)
+        tc::tf32x3_gemm_kernel<128, 64><<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::tc_smem(128), st>>>(
             maps, K, N, m_rows, splits, part, status, (int)kDevTimeout, a_rows);
     else
         tc::tf32x3_gemm_kernel<64><<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::tc_smem(64), st>>>(

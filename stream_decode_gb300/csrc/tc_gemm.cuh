@@ -16,7 +16,7 @@
 //
 // Pipeline per CTA (128 threads): warp 0 lane 0 issues TMA tile loads (128 B
 // swizzle) of A_hi, A_lo, B_hi, B_lo for each 32-wide K block into a ring of
-// tc_stages(TN) stages (mbarriers full/empty); warp 1 lane 0 issues
+// as many stages as the shared stage area holds (mbarriers full/empty); warp 1 lane 0 issues
 // tcgen05.mma (M=128, N=TN, K=8, kind::tf32, accumulator in TMEM) and
 // commits each stage back to its producer; after the last block all four
 // warps read the accumulator rows (tcgen05.ld 32x32b) and store the fp32
@@ -39,10 +39,10 @@ constexpr int kTcThreads = 128;
 constexpr uint32_t kABytes = kTileM * kBlockK * 4;  // 16 KB per A tile (hi or lo)
 // per tile width TN (64 or 128): B tile bytes, stage bytes, stages, dynamic shared memory
 __host__ __device__ constexpr uint32_t tc_bbytes(int TN) { return (uint32_t)TN * kBlockK * 4; }
-__host__ __device__ constexpr uint32_t tc_stage_bytes(int TN) { return 2 * kABytes + 2 * tc_bbytes(TN); }
-__host__ __device__ constexpr int tc_stages(int TN) { return TN <= 64 ? 4 : 3; }
+// the stage area every instantiation shares: four 128 x 64 stages
+constexpr uint32_t kTcArea = 4 * (2 * kABytes + 2 * 64 * kBlockK * 4);
 __host__ __device__ constexpr uint32_t tc_smem(int TN) {
-    return (uint32_t)tc_stages(TN) * tc_stage_bytes(TN) + 1024 /* alignment slack */ + 256 /* barriers */;
+    return kTcArea + 1024 /* alignment slack */ + 256 /* barriers */;
 }
 static_assert(kABytes % 1024 == 0 && tc_bbytes(64) % 1024 == 0, "tiles stay 1024-byte aligned for the swizzle atoms");
 static_assert(tc_smem(128) <= 232448, "the wide tile's stages fit in shared memory");
@@ -121,17 +121,22 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // depends only on A row r, so the unloaded upper half of the A tiles only
 // feeds accumulator rows that are never stored.  err: set to
 // err_code (if still 0) when any wait expires.
-template <int TN>
+template <int TN, int AR = kTileM>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tf32x3_gemm_kernel(const __grid_constant__ TcMaps maps, int K, int N, int m_rows, int splits, float* part,
                        int* err, int err_code, int a_rows) {
-    constexpr int kTcStages = tc_stages(TN);
-    constexpr uint32_t kBBytes = tc_bbytes(TN), kStageBytes = tc_stage_bytes(TN);
+    // AR: rows of each stored A tile (64 when the tile has at most 64 valid
+    // rows: the stage is smaller and the area holds more stages; the MMA
+    // still reads 128 rows of A, rows 64..127 being the bytes that follow in
+    // the stage, which feed only accumulator rows that are never stored)
+    constexpr uint32_t kABytes = (uint32_t)AR * kBlockK * 4;
+    constexpr uint32_t kBBytes = tc_bbytes(TN), kStageBytes = 2 * kABytes + 2 * kBBytes;
+    constexpr int kTcStages = (int)(kTcArea / kStageBytes) < 6 ? (int)(kTcArea / kStageBytes) : 6;
     constexpr uint32_t kTmemCols = (uint32_t)TN;  // fp32 accumulator columns
     extern __shared__ uint8_t tc_smem_raw[];
     // 1024-byte aligned stage area (swizzle atoms), barriers after it
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(base + kTcStages * kStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + kTcArea);
     uint64_t* empty = full + kTcStages;
     uint64_t* done = empty + kTcStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
