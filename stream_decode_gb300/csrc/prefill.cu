@@ -329,12 +329,13 @@ bool kmajor_map(CUtensorMap* map, const float* base, int K, int rows, int box_ro
 }
 
 // K splits for an (m tiles x n tiles) grid.
-int choose_splits(int m_tiles, int n_tiles, int K) {
+int choose_splits(int m_tiles, int n_tiles, int K, int TN) {
     const int nkb = K / tc::kBlockK;
     const int tiles = m_tiles * n_tiles;
     // about two thirds of the SMs: longer K ranges per CTA keep its 4-stage
-    // pipeline full (measured best between 36 and 300 CTAs on 152 SMs)
-    const int want = (2 * g_sms + 2) / 3;
+    // pipeline full (measured best between 36 and 300 CTAs on 152 SMs); the
+    // 128-wide tiles of the batched step measured best on every SM
+    const int want = TN == 128 ? g_sms : (2 * g_sms + 2) / 3;
     int s = (want + tiles / 2) / tiles;
     if (s < 1) s = 1;
     if (s > nkb) s = nkb;
@@ -373,7 +374,7 @@ cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W
         !kmajor_map(&maps.b_hi, W, K, w_rows, TN) || !kmajor_map(&maps.b_lo, Wlo, K, w_rows, TN))
         return cudaErrorInvalidValue;
     const int m_tiles = (m_rows + tc::kTileM - 1) / tc::kTileM, n_tiles = N / TN;
-    int splits = choose_splits(m_tiles, n_tiles, K);
+    int splits = choose_splits(m_tiles, n_tiles, K, TN);
     if (splits > max_splits) splits = max_splits < 1 ? 1 : max_splits;
     *splits_out = splits;
     if (TN == 128)  // (only for up to 64 rows: 64-row A tiles)
