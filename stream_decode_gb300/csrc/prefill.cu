@@ -332,10 +332,12 @@ bool kmajor_map(CUtensorMap* map, const float* base, int K, int rows, int box_ro
 int choose_splits(int m_tiles, int n_tiles, int K, int TN) {
     const int nkb = K / tc::kBlockK;
     const int tiles = m_tiles * n_tiles;
-    // about two thirds of the SMs: longer K ranges per CTA keep its 4-stage
-    // pipeline full (measured best between 36 and 300 CTAs on 152 SMs); the
-    // 128-wide tiles of the batched step measured best on every SM
-    const int want = TN == 128 ? g_sms : (2 * g_sms + 2) / 3;
+    // about two thirds of the SMs for one row tile of 64-wide tiles: longer K
+    // ranges per CTA keep its 4-stage pipeline full (measured best between
+    // 36 and 300 CTAs on 152 SMs for the 128-row prefill); every SM for the
+    // 128-wide tiles of up to 64 rows and for several row tiles (the batched
+    // step at 16, 64 and 256 sessions measured best so)
+    const int want = (TN == 128 || m_tiles > 1) ? g_sms : (2 * g_sms + 2) / 3;
     int s = (want + tiles / 2) / tiles;
     if (s < 1) s = 1;
     if (s > nkb) s = nkb;
