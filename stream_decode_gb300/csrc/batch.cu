@@ -38,6 +38,7 @@ __global__ void batch_embed_kernel(const float* __restrict__ packed, uint64_t wt
                                    const uint32_t* __restrict__ tokens_in, const int* __restrict__ step,
                                    const uint32_t* __restrict__ last, const int* __restrict__ pos, int D,
                                    uint32_t vocab, float* __restrict__ X, int* status) {
+    chain_enter();
     const int b = blockIdx.x, B = gridDim.x;
     uint32_t t = tokens_in[(size_t)(*step) * B + b];
     if (t == 0xFFFFFFFFu) t = last[b];
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kBAttnThreads) batch_attention_kernel(const fl
     static_assert(DPL >= 2 && DPL % 2 == 0, "head width");
     __shared__ float sm[kKeySlots], sz[kKeySlots];
     __shared__ float so[kKeySlots][DH];
+    chain_enter();
     const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
     const int slot = t / kLanesPerKey, e8 = t % kLanesPerKey;
     const int p = pos[b];
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(kBChoiceThreads) batch_logits_kernel(
     __shared__ float s_v[kBChoiceThreads / 32];
     __shared__ unsigned s_i[kBChoiceThreads / 32];
     __shared__ int s_nf[kBChoiceThreads / 32];
+    chain_enter();
     const int c = blockIdx.x, C = gridDim.x, b = blockIdx.y, B = gridDim.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float* o = out ? out + (size_t)(*step) * stride + (size_t)b * V : nullptr;
@@ -246,6 +249,7 @@ __global__ void batch_pick_kernel(const float* __restrict__ cand_v, const unsign
                                   const int* __restrict__ cand_nf, int C, uint32_t* __restrict__ tokens_out,
                                   uint32_t* __restrict__ last, int* __restrict__ pos, int* step, int* status) {
     __shared__ int s_step;
+    chain_enter();
     const int b = threadIdx.x, B = blockDim.x;
     if (b == 0) s_step = *step;
     __syncthreads();
@@ -314,7 +318,10 @@ namespace {
 
 constexpr int kBatchMaxSplits = 16;
 
-// Every launch of one batched step on stream st.
+// Every launch of one batched step on stream st.  Each kernel after the
+// first is a programmatic dependent launch (chain.cuh): 16 / 64 / 256
+// sessions measured 593 / 735 / 1,373 against 617 / 778 / 1,432 us per step
+// with plain launches.
 cudaError_t batch_launches(gpt2_batch* bt, const uint32_t* d_tokens_in, float* d_logits, size_t stride,
                            uint32_t* d_tokens_out, cudaStream_t st) {
     gpt2_model* m = bt->m;
@@ -329,24 +336,24 @@ cudaError_t batch_launches(gpt2_batch* bt, const uint32_t* d_tokens_in, float* d
         const uint64_t off = (uint64_t)l * m->layer_bytes + m->mat_off[mat];
         const float* W = reinterpret_cast<const float*>(m->d_wstream + off);
         const float* Wlo = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(m->d_wlo) + off);
-        return tc_gemm(A, Alo, B, W, Wlo, N, K, N, kBatchMaxSplits, sp, bt->part, status, st);
+        return tc_gemm(A, Alo, B, W, Wlo, N, K, N, kBatchMaxSplits, sp, bt->part, status, st, true);
     };
     auto reduce = [&](int splits, int N, uint64_t bias_off, int kind, float* out, float* out_lo, int l) {
         const size_t total = (size_t)B * N;
         const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-        reduce_kernel<<<blocks, 256, 0, st>>>(bt->part, splits, B, N, P + bias_off, kind, out, out_lo, bt->X,
-                                              bt->d_cache, L, l, D, bt->d_pos, bt->session_words);
-        return cudaGetLastError();
+        return chain_launch(true, reduce_kernel, dim3(blocks), dim3(256), 0, st, (const float*)bt->part, splits, B, N,
+                            P + bias_off, kind, out, out_lo, bt->X, bt->d_cache, L, l, D, (const int*)bt->d_pos,
+                            bt->session_words);
     };
     auto ln = [&](uint64_t g_off, uint64_t b_off, int splits, uint64_t bias_off) {
-        ln_split_kernel<<<B, kLnThreads, 0, st>>>(bt->X, P + g_off, P + b_off, D, bt->A, bt->Alo,
-                                                  splits ? bt->part : nullptr, splits, B, P + bias_off);
-        return cudaGetLastError();
+        return chain_launch(true, ln_split_kernel, dim3(B), dim3(kLnThreads), 0, st, bt->X, P + g_off, P + b_off, D,
+                            bt->A, bt->Alo, (const float*)(splits ? bt->part : nullptr), splits, B, P + bias_off);
     };
 
-    batch_embed_kernel<<<B, 256, 0, st>>>(P, m->wte_off, m->wpe_off, d_tokens_in, bt->d_words + 1, bt->d_last,
-                                          bt->d_pos, D, c.vocab, bt->X, status);
-    e = cudaGetLastError();
+    // the first kernel of the chain: a plain launch after the previous step
+    e = chain_launch(false, batch_embed_kernel, dim3(B), dim3(256), 0, st, P, m->wte_off, m->wpe_off, d_tokens_in,
+                     (const int*)(bt->d_words + 1), (const uint32_t*)bt->d_last, (const int*)bt->d_pos, D, c.vocab,
+                     bt->X, status);
     if (e == cudaSuccess) e = ln(m->lp[0].ln1_g, m->lp[0].ln1_b, 0, 0);
     int sp = 1;
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
@@ -354,16 +361,12 @@ cudaError_t batch_launches(gpt2_batch* bt, const uint32_t* d_tokens_in, float* d
         if ((e = gemm(bt->A, bt->Alo, D, 3 * D, l, kQKV, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, 3 * D, lp.b_qkv, kRedQKV, bt->QKV, nullptr, l)) != cudaSuccess) break;
         const dim3 agrid(H, B);
-        if (DH == 64)
-            batch_attention_kernel<64><<<agrid, kBAttnThreads, 0, st>>>(bt->QKV, bt->d_cache, bt->session_words,
-                                                                       bt->d_pos, L, l, D, bt->A, bt->Alo);
-        else if (DH == 32)
-            batch_attention_kernel<32><<<agrid, kBAttnThreads, 0, st>>>(bt->QKV, bt->d_cache, bt->session_words,
-                                                                       bt->d_pos, L, l, D, bt->A, bt->Alo);
-        else
-            batch_attention_kernel<16><<<agrid, kBAttnThreads, 0, st>>>(bt->QKV, bt->d_cache, bt->session_words,
-                                                                       bt->d_pos, L, l, D, bt->A, bt->Alo);
-        if ((e = cudaGetLastError()) != cudaSuccess) break;
+        auto attn = DH == 64 ? batch_attention_kernel<64> : DH == 32 ? batch_attention_kernel<32>
+                                                                     : batch_attention_kernel<16>;
+        if ((e = chain_launch(true, attn, agrid, dim3(kBAttnThreads), 0, st, (const float*)bt->QKV,
+                              (const float*)bt->d_cache, bt->session_words, (const int*)bt->d_pos, L, l, D, bt->A,
+                              bt->Alo)) != cudaSuccess)
+            break;
         if ((e = gemm(bt->A, bt->Alo, D, D, l, kO, &sp)) != cudaSuccess) break;
         if ((e = ln(lp.ln2_g, lp.ln2_b, sp, lp.b_o)) != cudaSuccess) break;  // residual + LN2
         if ((e = gemm(bt->A, bt->Alo, D, FF, l, kFC, &sp)) != cudaSuccess) break;
@@ -376,17 +379,17 @@ cudaError_t batch_launches(gpt2_batch* bt, const uint32_t* d_tokens_in, float* d
     // tied vocabulary projection: logits[b][n] = wte[n] . LN_f(x_b), one split
     int vs = 1;
     e = tc_gemm(bt->A, bt->Alo, B, P + m->wte_off, m->d_wte_lo, (int)c.vocab, D, bt->v_pad, 1, &vs, bt->vpart,
-                status, st);
+                status, st, true);
     if (e != cudaSuccess) return e;
     const int C = (bt->v_pad + kChoiceChunk - 1) / kChoiceChunk;
     float* cv = bt->cand;
     unsigned* ci = reinterpret_cast<unsigned*>(bt->cand + (size_t)B * C);
     int* cnf = reinterpret_cast<int*>(bt->cand + 2 * (size_t)B * C);
-    batch_logits_kernel<<<dim3(C, B), kBChoiceThreads, 0, st>>>(bt->vpart, vs, bt->v_pad, (int)c.vocab, d_logits,
-                                                                stride, bt->d_words + 1, cv, ci, cnf);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    batch_pick_kernel<<<1, B, 0, st>>>(cv, ci, cnf, C, d_tokens_out, bt->d_last, bt->d_pos, bt->d_words + 1, status);
-    return cudaGetLastError();
+    e = chain_launch(true, batch_logits_kernel, dim3(C, B), dim3(kBChoiceThreads), 0, st, (const float*)bt->vpart, vs,
+                     bt->v_pad, (int)c.vocab, d_logits, stride, (const int*)(bt->d_words + 1), cv, ci, cnf);
+    if (e != cudaSuccess) return e;
+    return chain_launch(true, batch_pick_kernel, dim3(1), dim3(B), 0, st, (const float*)cv, (const unsigned*)ci,
+                        (const int*)cnf, C, d_tokens_out, bt->d_last, bt->d_pos, bt->d_words + 1, status);
 }
 
 gpt2_status batch_status(cudaError_t e) {

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attention_kernel(const float*
     __shared__ __align__(16) float vs[kKeyTile][DH];
     __shared__ float qs[kAttnRows][DH];
     __shared__ float ps[kAttnWarps][kKeyTile];
+    chain_enter();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x, r0 = blockIdx.y * kAttnRows;
     const size_t N3 = 3 * (size_t)D;
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kChoiceThreads) choice_kernel(const float* __r
     __shared__ float s_v[kChoiceThreads / 32];
     __shared__ unsigned s_i[kChoiceThreads / 32];
     __shared__ int s_nf[kChoiceThreads / 32];
+    chain_enter();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float bv = -INFINITY;
     unsigned bi = 0xFFFFFFFFu;
@@ -233,6 +235,7 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float* __restr
     static_assert(D <= 1024, "row width");
     __shared__ __align__(16) float xs[D];
     __shared__ float red[kHeadThreads / 32];
+    chain_enter();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float* x = X + (size_t)last * D;
     float s = 0.0f;
@@ -364,7 +367,7 @@ bool tc_ready() {
 int tc_sm_count() { return g_sms; }
 
 cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W, const float* Wlo, int w_rows, int K,
-                    int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st) {
+                    int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st, bool pdl) {
     if (K % tc::kBlockK || N % tc::kTileN || w_rows > N || m_rows <= 0) return cudaErrorInvalidValue;
     // 128 output features per tile for up to 64 rows where N allows (half
     // the activation reads of the 64-wide tile; measured faster for 16 and
@@ -379,13 +382,10 @@ cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W
     int splits = choose_splits(m_tiles, n_tiles, K, TN);
     if (splits > max_splits) splits = max_splits < 1 ? 1 : max_splits;
     *splits_out = splits;
-    if (TN == 128)  // (only for up to 64 rows: 64-row A tiles)
-        tc::tf32x3_gemm_kernel<128, 64><<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::tc_smem(128), st>>>(
-            maps, K, N, m_rows, splits, part, status, (int)kDevTimeout, a_rows);
-    else
-        tc::tf32x3_gemm_kernel<64><<<dim3(n_tiles, splits, m_tiles), tc::kTcThreads, tc::tc_smem(64), st>>>(
-            maps, K, N, m_rows, splits, part, status, (int)kDevTimeout, a_rows);
-    return cudaGetLastError();
+    // (128-wide tiles only for up to 64 rows: 64-row A tiles)
+    return chain_launch(pdl, TN == 128 ? tc::tf32x3_gemm_kernel<128, 64> : tc::tf32x3_gemm_kernel<64>,
+                        dim3(n_tiles, splits, m_tiles), dim3(tc::kTcThreads), tc::tc_smem(TN), st, maps, K, N, m_rows,
+                        splits, part, status, (int)kDevTimeout, a_rows);
 }
 
 cudaError_t split_lo(const float* w, float* lo, size_t n, cudaStream_t st) {
@@ -458,6 +458,11 @@ bool prefill_shape_supported(const gpt2_config& c) {
 
 namespace {
 
+// The prefill's kernels are plain stream-ordered launches: programmatic
+// dependent launches (chain.cuh) measured slower here, 0.937 against 0.852
+// ms per 128-token prefill (the batched step's chain gains from them).
+constexpr bool kPrefillPdl = false;
+
 // Every launch of one prefill, enqueued on stream st.
 cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok, int n, float* cache, float* logits,
                              int* status, uint32_t* d_choice, uint32_t* d_next, cudaStream_t st) {
@@ -471,26 +476,25 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
         const uint64_t off = (uint64_t)l * m->layer_bytes + m->mat_off[mat];
         const float* W = reinterpret_cast<const float*>(m->d_wstream + off);
         const float* Wlo = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(m->d_wlo) + off);
-        return tc_gemm(A, Alo, n, W, Wlo, N, K, N, kPrefillMaxSplits, splits_out, w->part, status, st);
+        return tc_gemm(A, Alo, n, W, Wlo, N, K, N, kPrefillMaxSplits, splits_out, w->part, status, st, kPrefillPdl);
     };
     auto reduce = [&](int splits, int N, uint64_t bias_off, int kind, float* out, float* out_lo, int l) {
         const size_t total = (size_t)n * N;
         const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-        reduce_kernel<<<blocks, 256, 0, st>>>(w->part, splits, n, N, P + bias_off, kind, out, out_lo, w->X, cache, L,
-                                              l, D, nullptr, 0);
-        return cudaGetLastError();
+        return chain_launch(kPrefillPdl, reduce_kernel, dim3(blocks), dim3(256), 0, st, (const float*)w->part, splits, n, N,
+                            P + bias_off, kind, out, out_lo, w->X, cache, L, l, D, (const int*)nullptr, (size_t)0);
     };
 
     // LayerNorm of the residual rows into A (+ remainder); with a projection's
     // partials, the residual add of that projection first (one kernel)
     auto ln = [&](uint64_t g_off, uint64_t b_off, int splits, uint64_t bias_off) {
-        ln_split_kernel<<<n, kLnThreads, 0, st>>>(w->X, P + g_off, P + b_off, D, w->A, w->Alo,
-                                                  splits ? w->part : nullptr, splits, n, P + bias_off);
-        return cudaGetLastError();
+        return chain_launch(kPrefillPdl, ln_split_kernel, dim3(n), dim3(kLnThreads), 0, st, w->X, P + g_off, P + b_off, D,
+                            w->A, w->Alo, (const float*)(splits ? w->part : nullptr), splits, n, P + bias_off);
     };
 
-    embed_kernel<<<n, 256, 0, st>>>(P, m->wte_off, m->wpe_off, d_tok, D, c.vocab, w->X, status);
-    e = cudaGetLastError();
+    // the first kernel of the chain: a plain launch
+    e = chain_launch(false, embed_kernel, dim3(n), dim3(256), 0, st, P, m->wte_off, m->wpe_off, d_tok, D, c.vocab,
+                     w->X, status);
     if (e == cudaSuccess) e = ln(m->lp[0].ln1_g, m->lp[0].ln1_b, 0, 0);
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
         const LayerParams& lp = m->lp[l];
@@ -498,9 +502,10 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
         if ((e = gemm(w->A, w->Alo, D, 3 * D, l, kQKV, &sp)) != cudaSuccess) break;
         if ((e = reduce(sp, 3 * D, lp.b_qkv, kRedQKV, w->QKV, nullptr, l)) != cudaSuccess) break;
         const dim3 agrid(H, (n + kAttnRows - 1) / kAttnRows);
-        if (DH == 64) attention_kernel<64><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
-        else if (DH == 32) attention_kernel<32><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
-        else attention_kernel<16><<<agrid, kAttnWarps * 32, 0, st>>>(w->QKV, n, D, w->A, w->Alo);
+        auto attn = DH == 64 ? attention_kernel<64> : DH == 32 ? attention_kernel<32> : attention_kernel<16>;
+        if ((e = chain_launch(kPrefillPdl, attn, agrid, dim3(kAttnWarps * 32), 0, st, (const float*)w->QKV, n, D, w->A,
+                              w->Alo)) != cudaSuccess)
+            break;
         if ((e = gemm(w->A, w->Alo, D, D, l, kO, &sp)) != cudaSuccess) break;
         if ((e = ln(lp.ln2_g, lp.ln2_b, sp, lp.b_o)) != cudaSuccess) break;  // residual + LN2
         if ((e = gemm(w->A, w->Alo, D, FF, l, kFC, &sp)) != cudaSuccess) break;
@@ -514,12 +519,13 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
     const float* lb = P + m->lnf_b;
     const float* wte = P + m->wte_off;
     const int hb = 2 * tc_sm_count();  // two blocks per SM
-    if (D == 768) head_kernel<192><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
-    else if (D == 192) head_kernel<48><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
-    else if (D == 64) head_kernel<16><<<hb, kHeadThreads, 0, st>>>(w->X, n - 1, lg, lb, wte, (int)c.vocab, logits);
-    else return cudaErrorInvalidValue;
-    choice_kernel<<<1, kChoiceThreads, 0, st>>>(logits, c.vocab, d_choice, d_next, status);
-    return cudaGetLastError();
+    if (D != 768 && D != 192 && D != 64) return cudaErrorInvalidValue;
+    auto head = D == 768 ? head_kernel<192> : D == 192 ? head_kernel<48> : head_kernel<16>;
+    e = chain_launch(kPrefillPdl, head, dim3(hb), dim3(kHeadThreads), 0, st, (const float*)w->X, n - 1, lg, lb, wte,
+                     (int)c.vocab, logits);
+    if (e != cudaSuccess) return e;
+    return chain_launch(kPrefillPdl, choice_kernel, dim3(1), dim3(kChoiceThreads), 0, st, (const float*)logits, c.vocab,
+                        d_choice, d_next, status);
 }
 
 }  // namespace

@@ -45,9 +45,10 @@ int tc_sm_count();
 // their TF32 remainders Alo, Wlo beside them.  W has w_rows <= N rows; the
 // columns n >= w_rows read zeros.  K a multiple of 32, N of 64; base
 // addresses 16-byte aligned.  *splits_out = the number of K splits chosen
-// (at most max_splits); part holds splits x m_rows x N floats.
+// (at most max_splits); part holds splits x m_rows x N floats.  pdl: a
+// programmatic dependent launch (chain.cuh) after the kernel before it on st.
 cudaError_t tc_gemm(const float* A, const float* Alo, int m_rows, const float* W, const float* Wlo, int w_rows, int K,
-                    int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st);
+                    int N, int max_splits, int* splits_out, float* part, int* status, cudaStream_t st, bool pdl);
 // lo[i] = w[i] - (w[i] with its low 13 mantissa bits cleared), i < n.
 cudaError_t split_lo(const float* w, float* lo, size_t n, cudaStream_t st);
 // The model's block-matrix TF32 remainders (made once, on stream st).

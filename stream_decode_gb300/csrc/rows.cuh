@@ -8,6 +8,7 @@
 
 #include <cstdint>
 
+#include "chain.cuh"
 #include "gpt2_dev.cuh"
 
 namespace gpt2 {
@@ -42,6 +43,7 @@ __global__ void split_lo_kernel(const float* __restrict__ w, float* __restrict__
 __global__ void embed_kernel(const float* __restrict__ packed, uint64_t wte_off, uint64_t wpe_off,
                              const uint32_t* __restrict__ tok, int D, uint32_t vocab, float* __restrict__ X,
                              int* status) {
+    chain_enter();
     const int i = blockIdx.x;
     const uint32_t t = tok[i];
     if (t >= vocab) {
@@ -66,6 +68,7 @@ __global__ void __launch_bounds__(kLnThreads) ln_split_kernel(float* __restrict_
                                                              const float* __restrict__ part, int splits, int n,
                                                              const float* __restrict__ bias) {
     __shared__ float red[kLnThreads / 32];
+    chain_enter();
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float* x = X + (size_t)row * D;
     float v[8];
@@ -159,6 +162,7 @@ __global__ void reduce_kernel(const float* __restrict__ part, int splits, int n,
                               const float* __restrict__ bias, int kind, float* __restrict__ out,
                               float* __restrict__ out_lo, float* __restrict__ X, float* __restrict__ cache, int L,
                               int l, int D, const int* __restrict__ pos, size_t session_words) {
+    chain_enter();
     const size_t total = (size_t)n * N;
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
          idx += (size_t)gridDim.x * blockDim.x) {

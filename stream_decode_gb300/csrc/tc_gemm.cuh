@@ -28,6 +28,8 @@
 
 #include <cstdint>
 
+#include "chain.cuh"
+
 namespace gpt2 {
 namespace tc {
 
@@ -169,6 +171,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
+    // everything above touched shared and tensor memory only; the A tiles
+    // and the partials are the neighbouring kernels' data
+    chain_enter();
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer
