@@ -13,7 +13,8 @@
 // zero rows), and the greedy choice (chunks of each row in parallel, then
 // one thread per session, which also advances the positions).  A step is
 // one CUDA graph (captured once per set of output buffers) replayed once
-// per step.
+// per step; every kernel after the step's first is a programmatic
+// dependent launch (chain.cuh).
 #include <cuda_runtime.h>
 
 #include <cmath>
