@@ -1,7 +1,8 @@
-// chain.cuh -- programmatic dependent launch for the kernel chain of the
+// chain.cuh -- programmatic dependent launch for the kernel chains of the
 // batched decode step (one CUDA graph per step, 113 short kernels in stream
-// order).  The prompt prefill's kernels carry the same hooks but are
-// launched plainly: programmatic launches measured slower there.
+// order; every kernel after the first is chained) and of the prompt prefill
+// (one graph, 112 kernels; only its GEMMs are chained, the rest measured
+// slower chained).
 //
 // A kernel launched with the programmatic-serialization attribute may be
 // scheduled while the kernel before it in the stream is still running: its
@@ -16,6 +17,8 @@
 //     most two kernels of the chain are resident at a time, and a kernel
 //     completes only after its predecessor did (which makes the ordering
 //     transitive: a kernel also sees the writes of every earlier kernel).
+//     A chain may mix chained and plain launches: a plain launch waits for
+//     its predecessor's completion as usual, which keeps the same order.
 // Without the attribute (the first kernel of a chain, or GPT2_PDL=0 in the
 // environment) both instructions are no-ops and the launches are plain
 // stream-ordered launches.

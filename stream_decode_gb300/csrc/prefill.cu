@@ -458,9 +458,14 @@ bool prefill_shape_supported(const gpt2_config& c) {
 
 namespace {
 
-// The prefill's kernels are plain stream-ordered launches: programmatic
-// dependent launches (chain.cuh) measured slower here, 0.937 against 0.852
-// ms per 128-token prefill (the batched step's chain gains from them).
+// Programmatic dependent launches (chain.cuh) in the prefill: for the
+// GEMMs only, whose CTAs then initialise their barriers and tensor memory
+// while the kernel before them drains.  Per 128-token prefill, same box:
+// 0.817 ms with the GEMMs chained, 0.854 with plain launches, 0.94 with
+// every kernel chained and 0.98 with every kernel but the GEMMs chained.
+// The other kernels' successors are plain launches, so each GEMM still
+// completes before the kernel after it starts.
+constexpr bool kPrefillGemmPdl = true;
 constexpr bool kPrefillPdl = false;
 
 // Every launch of one prefill, enqueued on stream st.
@@ -476,7 +481,7 @@ cudaError_t prefill_launches(gpt2_model* m, PrefillWs* w, const uint32_t* d_tok,
         const uint64_t off = (uint64_t)l * m->layer_bytes + m->mat_off[mat];
         const float* W = reinterpret_cast<const float*>(m->d_wstream + off);
         const float* Wlo = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(m->d_wlo) + off);
-        return tc_gemm(A, Alo, n, W, Wlo, N, K, N, kPrefillMaxSplits, splits_out, w->part, status, st, kPrefillPdl);
+        return tc_gemm(A, Alo, n, W, Wlo, N, K, N, kPrefillMaxSplits, splits_out, w->part, status, st, kPrefillGemmPdl);
     };
     auto reduce = [&](int splits, int N, uint64_t bias_off, int kind, float* out, float* out_lo, int l) {
         const size_t total = (size_t)n * N;
