@@ -55,6 +55,20 @@ MUTANTS = [
      "linear_q8(x, q->q, q->s, b, n_in, n_out, y, 0);"),
     ("token_bound_off_by_one", "if (token >= c->vocab) return REF_ERR_TOKEN;",
      "if (token > c->vocab) return REF_ERR_TOKEN;"),
+    ("attention_residual_dropped",
+     "project(m, 4 * l + 1, o, b->w_o, b->b_o, d, d, y);\n        for (int i = 0; i < d; i++) x[i] = x[i] + y[i];",
+     "project(m, 4 * l + 1, o, b->w_o, b->b_o, d, d, y);\n        for (int i = 0; i < d; i++) x[i] = y[i];"),
+    ("ln1_takes_ln2_parameters", "ref_layernorm(x, b->ln1_g, b->ln1_b, d, a);",
+     "ref_layernorm(x, b->ln2_g, b->ln2_b, d, a);"),
+    ("final_layernorm_dropped", "ref_layernorm(x, m->lnf_g, m->lnf_b, d, a);", "memcpy(a, x, sizeof(float) * d);"),
+    ("out_projection_bias_dropped", "project(m, 4 * l + 1, o, b->w_o, b->b_o, d, d, y);",
+     "project(m, 4 * l + 1, o, b->w_o, NULL, d, d, y);"),
+    ("fc_bias_dropped", "project(m, 4 * l + 2, a, b->w_fc, b->b_fc, d, f, u);",
+     "project(m, 4 * l + 2, a, b->w_fc, NULL, d, f, u);"),
+    ("current_position_not_attended", "ref_attention_head(qkv + h * dh, k0, v0, (int)pos + 1, dh, row, o + h * dh, NULL);",
+     "ref_attention_head(qkv + h * dh, k0, v0, pos ? (int)pos : 1, dh, row, o + h * dh, NULL);"),
+    ("values_read_at_key_offset", "const float *v0 = cache + (size_t)l * 2 * d + d + h * dh;",
+     "const float *v0 = cache + (size_t)l * 2 * d + h * dh;"),
 ]
 
 
