@@ -69,6 +69,13 @@ MUTANTS = [
      "ref_attention_head(qkv + h * dh, k0, v0, pos ? (int)pos : 1, dh, row, o + h * dh, NULL);"),
     ("values_read_at_key_offset", "const float *v0 = cache + (size_t)l * 2 * d + d + h * dh;",
      "const float *v0 = cache + (size_t)l * 2 * d + h * dh;"),
+    ("signed_group_maximum", "float a = fabsf(x[i]);", "float a = x[i];"),
+    ("activation_scale_dropped", "sum += ((float)acc[g] * xs[g]) * ws[(size_t)j * ng + g];",
+     "sum += (float)acc[g] * ws[(size_t)j * ng + g];"),
+    ("group_dot_skips_first_term", "for (int i = g * REF_GROUP; i < (g + 1) * REF_GROUP; i++) a +=",
+     "for (int i = g * REF_GROUP + 1; i < (g + 1) * REF_GROUP; i++) a +="),
+    ("int8_bias_dropped", "y[j] = b ? sum + b[j] : sum;", "y[j] = sum;"),
+    ("negative_saturation_at_128", "if (r < -127.0f) r = -127.0f;", "if (r < -128.0f) r = -128.0f;"),
 ]
 
 
