@@ -327,6 +327,15 @@ def check_validation(o, shape=synth.GPT2_TINY, seed=synth.SEED_TINY):
         (w, ok_cache[:-1], 1, 3, "cache_len"),
         (w, np.zeros(4 * row, np.float32), 1, 3, "cache_len"),
     ]
+    # several invalid inputs at once: the first condition in the order the
+    # README's cachedStep paragraph names them (weight length, token,
+    # position, cache length) decides the status; the outputs are empty in
+    # every case (reading R17)
+    bad += [
+        (w[:-1], np.zeros(shape.max_pos * row + 1, np.float32), shape.vocab, shape.max_pos + 1, "weights_len"),
+        (w, np.zeros(shape.max_pos * row + 1, np.float32), shape.vocab, shape.max_pos + 1, "token"),
+        (w, ok_cache, 1, shape.max_pos, "position"),
+    ]
     for ww, cc, t, pos, want in bad:
         st, lg, co = o.cached_step(shape, ww, cc, t, pos)
         assert st == want and lg.size == 0 and co.size == 0, (want, st)
@@ -338,6 +347,10 @@ def check_validation(o, shape=synth.GPT2_TINY, seed=synth.SEED_TINY):
         (w, toks.astype("<u4").tobytes()[:-1], "tokens_len"),
         (w, np.zeros(shape.max_pos + 1, "<u4").tobytes(), "tokens_len"),
         (w, np.array([1, shape.vocab], "<u4").tobytes(), "token"),
+        # several at once (infer paragraph: weight length, then the token
+        # array, its length before its entries; reading R17)
+        (w[:-1], np.array([shape.vocab], "<u4").tobytes()[:-1], "weights_len"),
+        (w, np.array([shape.vocab], "<u4").tobytes() + b"\x00", "tokens_len"),
     ]
     for ww, tb, want in bad_inf:
         st, lg = o.infer(shape, ww, tb)

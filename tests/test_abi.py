@@ -64,6 +64,8 @@ def test_validation_needs_no_gpu(lib, oracle):
         (w, np.zeros(s.max_pos * row, np.float32), 1, s.max_pos),
         (w, np.zeros(3 * row - 1, np.float32), 1, 3),
         (w[:-1], np.zeros(3 * row - 1, np.float32), s.vocab, s.max_pos),
+        (w, np.zeros(3 * row - 1, np.float32), s.vocab, s.max_pos),
+        (w, np.zeros(3 * row, np.float32), 1, s.max_pos),
     ]
     for ww, cc, t, p in cases:
         st, lg, co = lib.cached_step(s, ww, cc, t, p)
@@ -71,7 +73,7 @@ def test_validation_needs_no_gpu(lib, oracle):
         assert st == ost and lg.size == 0 and co.size == 0, (st, ost)
     toks = synth.tokens(s.vocab, 4)
     for tb in (b"", toks.astype("<u4").tobytes()[:-2], np.zeros(s.max_pos + 1, "<u4").tobytes(),
-               np.array([3, s.vocab], "<u4").tobytes()):
+               np.array([3, s.vocab], "<u4").tobytes(), np.array([s.vocab], "<u4").tobytes() + b"\x00"):
         st, lg = lib.infer(s, w, tb)
         ost, _ = oracle.infer(s, w, tb)
         assert st == ost and lg.size == 0

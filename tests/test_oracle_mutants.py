@@ -76,6 +76,15 @@ MUTANTS = [
      "for (int i = g * REF_GROUP + 1; i < (g + 1) * REF_GROUP; i++) a +="),
     ("int8_bias_dropped", "y[j] = b ? sum + b[j] : sum;", "y[j] = sum;"),
     ("negative_saturation_at_128", "if (r < -127.0f) r = -127.0f;", "if (r < -128.0f) r = -128.0f;"),
+    ("position_checked_before_token",
+     "    if (token >= c->vocab) return REF_ERR_TOKEN;\n    if (position >= c->max_pos) return REF_ERR_POSITION;",
+     "    if (position >= c->max_pos) return REF_ERR_POSITION;\n    if (token >= c->vocab) return REF_ERR_TOKEN;"),
+    ("cache_length_checked_before_position",
+     "    if (position >= c->max_pos) return REF_ERR_POSITION;\n    size_t row = ref_cache_words_per_position(c);\n"
+     "    if (cache_len != (size_t)position * row * 4) return REF_ERR_CACHE_LEN;",
+     "    size_t row = ref_cache_words_per_position(c);\n"
+     "    if (cache_len != (size_t)position * row * 4) return REF_ERR_CACHE_LEN;\n"
+     "    if (position >= c->max_pos) return REF_ERR_POSITION;"),
 ]
 
 
