@@ -85,6 +85,8 @@ MUTANTS = [
      "    size_t row = ref_cache_words_per_position(c);\n"
      "    if (cache_len != (size_t)position * row * 4) return REF_ERR_CACHE_LEN;\n"
      "    if (position >= c->max_pos) return REF_ERR_POSITION;"),
+    ("softmax_without_max_shift", "e[j] = expf(e[j] - m);", "e[j] = expf(e[j]);"),
+    ("infer_returns_first_row", "t + 1 == n ? logits_out : NULL", "t == 0 ? logits_out : NULL"),
 ]
 
 
