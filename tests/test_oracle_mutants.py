@@ -112,3 +112,41 @@ def test_pins_catch_mutant(source, name, old, new):
             except (AssertionError, ValueError, RuntimeError) as e:  # noqa: PERF203
                 caught.append(check.__name__)
         assert caught, f"no pin caught mutant {name}"
+
+
+def _round_f16_mutants():
+    """Plausible mistakes in the binary16-weight checkpoint (oracle.round_f16,
+    gpt2.s page, half-precision weight paragraph), built around the real
+    function: rounding toward zero instead of to nearest, rounding every
+    tensor (LayerNorm parameters and biases too), leaving wte in binary32."""
+    import numpy as np
+    import oracle
+    from stream_decode_gb300 import synth
+    real = oracle.round_f16
+
+    def toward_zero(shape, weights):
+        w = np.asarray(weights, np.float32)
+        r = real(shape, weights)
+        away = np.abs(r) > np.abs(w)
+        r[away] = np.nextafter(r[away].astype(np.float16), np.float16(0)).astype(np.float32)
+        return r
+
+    def every_tensor(shape, weights):
+        return np.asarray(weights, np.float32).astype(np.float16).astype(np.float32)
+
+    def wte_kept(shape, weights):
+        r = real(shape, weights)
+        off, n = synth.layout(shape)["wte"]
+        r[off:off + n] = np.asarray(weights, np.float32)[off:off + n]
+        return r
+
+    return [("round_toward_zero", toward_zero), ("every_tensor_rounded", every_tensor), ("wte_not_rounded", wte_kept)]
+
+
+@pytest.mark.parametrize("name,fn", _round_f16_mutants(), ids=[m[0] for m in _round_f16_mutants()])
+def test_round_f16_pin_catches_mutant(monkeypatch, name, fn):
+    import oracle
+    monkeypatch.setattr(oracle, "round_f16", fn)
+    o = Oracle(oracle.build())
+    with pytest.raises(AssertionError):
+        P.check_round_f16(o)
